@@ -1,0 +1,157 @@
+"""GB300-native fused exact attention: a thin ctypes binding over libfa.so.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+only marshals arguments (torch tensors -> device pointers, the current CUDA
+stream) and turns status codes into exceptions.  It never falls back to any
+other implementation: if ``lib/libfa.so`` is missing, every call raises.
+
+Build the library with ``python -m attention_blackwell_gb300.build``.
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = ["fwd", "exp2_emu", "set_tuning", "device_status", "num_sms", "FAError", "library_path", "lib"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "lib", "libfa.so")
+_lib = None
+
+HEAD_DIM = 128
+
+
+class FAError(RuntimeError):
+    """A libfa call returned a non-zero status."""
+
+    def __init__(self, code, what):
+        self.code = code
+        super().__init__("%s: %s (%d)" % (what, _status_string(code), code))
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded libfa.so (ctypes.CDLL); raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError("libfa.so is not built (%s); run `python -m attention_blackwell_gb300.build`"
+                               % _LIB_PATH)
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i, f, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int64
+        L.fa_status_string.restype = ctypes.c_char_p
+        L.fa_status_string.argtypes = [i]
+        L.fa_num_sms.restype = i
+        L.fa_num_sms.argtypes = []
+        L.fa_set_tuning.restype = i
+        L.fa_set_tuning.argtypes = [i, f]
+        L.fa_fwd.restype = i
+        L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp]
+        L.fa_get_device_status.restype = i
+        L.fa_get_device_status.argtypes = [vp, vp]
+        L.fa_exp2_emu.restype = i
+        L.fa_exp2_emu.argtypes = [vp, vp, i64, vp]
+        _lib = L
+    return _lib
+
+
+def _status_string(code):
+    try:
+        return lib().fa_status_string(int(code)).decode()
+    except Exception:  # library missing while formatting an error
+        return "status"
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise FAError(rc, what)
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _need(t, name, dtype):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def num_sms():
+    n = lib().fa_num_sms()
+    if n < 0:
+        raise FAError(n, "fa_num_sms")
+    return n
+
+
+def set_tuning(exp2_emu_eighths=0, tau=8.0):
+    """Process-wide forward tuning (share of exp2 on the FMA pipe, rescale tau)."""
+    _check(lib().fa_set_tuning(int(exp2_emu_eighths), float(tau)), "fa_set_tuning")
+
+
+def fwd(q, k, v, causal=False, alpha=None, cu_seqlens=None, max_seqlen=None, out=None, lse=None, stream=None):
+    """Forward attention.  Returns (o, lse).
+
+    Fixed length: q [B,N,Hq,128], k/v [B,N,Hkv,128] bf16 -> o like q,
+    lse float32 [B,Hq,N].  Varlen: q [T,Hq,128], k/v [T,Hkv,128],
+    cu_seqlens int32 [B+1] on the device, max_seqlen -> o [T,Hq,128],
+    lse [Hq,T].
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16)
+    varlen = cu_seqlens is not None
+    if varlen:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        if q.dim() != 3:
+            raise ValueError("varlen q must be [T, Hq, d]")
+        T, Hq, d = q.shape
+        Hkv = k.shape[1]
+        B, N = cu_seqlens.numel() - 1, T
+        if max_seqlen is None:
+            raise ValueError("varlen needs max_seqlen")
+        lse_shape = (Hq, T)
+    else:
+        if q.dim() != 4:
+            raise ValueError("q must be [B, N, Hq, d]")
+        B, N, Hq, d = q.shape
+        Hkv = k.shape[2]
+        max_seqlen = N
+        lse_shape = (B, Hq, N)
+    if k.shape != v.shape or k.shape[:-2] != q.shape[:-2]:
+        raise ValueError("k and v must match q's leading shape")
+    if alpha is None:
+        alpha = 1.0 / (d ** 0.5)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    rc = lib().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d, float(alpha),
+                      1 if causal else 0, _ptr(cu_seqlens), int(max_seqlen), _stream(stream))
+    _check(rc, "fa_fwd")
+    return out, lse
+
+
+def device_status(workspace=None, stream=None):
+    """Synchronise the stream and return (and clear) the device status code."""
+    return lib().fa_get_device_status(_ptr(workspace), _stream(stream))
+
+
+def exp2_emu(x, stream=None):
+    """The forward kernel's FMA-pipe 2^x on a float32 CUDA tensor."""
+    _need(x, "x", torch.float32)
+    y = torch.empty_like(x)
+    _check(lib().fa_exp2_emu(_ptr(x), _ptr(y), x.numel(), _stream(stream)), "fa_exp2_emu")
+    return y

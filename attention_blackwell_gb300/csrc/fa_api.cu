@@ -1,0 +1,206 @@
+// fa_api.cu -- the C ABI of libfa.so (declared in include/fa.h): argument
+// validation, TMA tensor-map construction, persistent-grid sizing, the device
+// status word, and the kernel launches.  No device memory is allocated here.
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace fa {
+
+// One status word per device the library runs on (static device storage).
+__device__ DevStatus g_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int num_sms = 0;
+    int l2_bytes = 0;
+    DevStatus* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int g_emu_eighths = 0;         // share of exp2 pairs on the FMA pipe (eighths)
+float g_tau = 8.0f;            // conditional-rescale threshold, log2(256)
+
+int current_device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_LAUNCH;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FA_ERR_LAUNCH;
+        if (cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return FA_ERR_LAUNCH;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return FA_ERR_LAUNCH;
+        d.status = static_cast<DevStatus*>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return FA_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// bf16 tensor [T, H, 128] -> 3-D map {128, H, T}, box {64, 1, 128}, 128-B swizzle.
+// Rows past T read as zero.
+int make_map(CUtensorMap* map, const void* ptr, int H, long long T) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return FA_ERR_LAUNCH;
+    cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)H * kHeadDim * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)kTileM};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_INVALID;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+DevStatus* device_status_ptr() {
+    DeviceInfo* d = nullptr;
+    return current_device_info(&d) == FA_OK ? d->status : nullptr;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID: return "FA_ERR_INVALID: invalid argument";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: configuration not supported by this build";
+        case FA_ERR_ALIGN: return "FA_ERR_ALIGN: tensor not 16-byte aligned";
+        case FA_ERR_LAUNCH: return "FA_ERR_LAUNCH: CUDA launch error";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a device-side wait gave up";
+        case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing or too small";
+        default: return "FA_ERR_UNKNOWN";
+    }
+}
+
+int fa_num_sms(void) {
+    DeviceInfo* d = nullptr;
+    int rc = current_device_info(&d);
+    return rc == FA_OK ? d->num_sms : rc;
+}
+
+int fa_set_tuning(int exp2_emu_eighths, float tau) {
+    if (exp2_emu_eighths < 0 || exp2_emu_eighths > 2) return FA_ERR_UNSUPPORTED;
+    if (!(tau >= 0.0f) || !(tau <= 64.0f)) return FA_ERR_INVALID;
+    g_emu_eighths = exp2_emu_eighths;
+    g_tau = tau;
+    return FA_OK;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int N, int d,
+           float alpha, int causal, const int* cu_seqlens, int max_seqlen, cudaStream_t stream) {
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID;
+    if (B < 1 || N < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return FA_ERR_INVALID;
+    if (!(alpha > 0.0f) || !isfinite(alpha)) return FA_ERR_INVALID;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID;
+    if (d != kHeadDim) return FA_ERR_UNSUPPORTED;
+    const bool varlen = cu_seqlens != nullptr;
+    if (varlen) {
+        if (max_seqlen < 1) return FA_ERR_INVALID;
+        if (B > kMaxVarlenSeqs || (max_seqlen + kUnitRows - 1) / kUnitRows > kMaxUnitLevels)
+            return FA_ERR_UNSUPPORTED;
+    }
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGN;
+    if (varlen && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FA_ERR_ALIGN;
+    const long long T = varlen ? (long long)N : (long long)B * N;
+    if (T == 0) return FA_OK;
+    if (T > 0x7fffffffLL || (long long)Hq * T > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+
+    DeviceInfo* dev = nullptr;
+    int rc = current_device_info(&dev);
+    if (rc != FA_OK) return rc;
+
+    FwdLaunch L;
+    if ((rc = make_map(&L.tq, q, Hq, T)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tk, k, Hkv, T)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tv, v, Hkv, T)) != FA_OK) return rc;
+    L.a.o = o;
+    L.a.lse = lse;
+    L.a.cu_seqlens = cu_seqlens;
+    L.a.status = dev->status;
+    L.a.B = B;
+    L.a.Hq = Hq;
+    L.a.Hkv = Hkv;
+    L.a.N = N;
+    L.a.causal = causal;
+    L.a.varlen = varlen ? 1 : 0;
+    L.a.max_seqlen = varlen ? max_seqlen : N;
+    // Causal fixed length: (batch, head) pairs per L2 section so that the K/V
+    // of one section (2 * N * 128 * 2 bytes per key/value head) fill about
+    // half of L2; pairs of one group share their K/V head.
+    {
+        const long long kv_bytes = 512LL * (N > 0 ? N : 1);
+        long long sec = (long long)(Hq / Hkv) * ((long long)dev->l2_bytes / 2) / kv_bytes;
+        if (sec < 1) sec = 1;
+        if (sec > (long long)B * Hq) sec = (long long)B * Hq;
+        L.a.l2_section = (int)sec;
+    }
+    L.a.scale_log2 = alpha * 1.4426950408889634f;
+    L.a.tau = g_tau;
+    L.emu_eighths = g_emu_eighths;
+    L.num_sms = dev->num_sms;
+    cudaError_t e = launch_fwd(L, stream);
+    return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_get_device_status(const void* workspace, cudaStream_t stream) {
+    (void)workspace;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_LAUNCH;
+    DeviceInfo* dev = nullptr;
+    int rc = current_device_info(&dev);
+    if (rc != FA_OK) return rc;
+    DevStatus s;
+    if (cudaMemcpy(&s, dev->status, sizeof s, cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_LAUNCH;
+    if (s.code != 0) {
+        if (getenv("FA_LOG"))
+            fprintf(stderr, "fa: device status %d at wait site %d (block %d)\n", s.code, s.where, s.block);
+        DevStatus z = {0, 0, 0, 0};
+        if (cudaMemcpy(dev->status, &z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_LAUNCH;
+        return s.code;
+    }
+    return FA_OK;
+}
+
+int fa_exp2_emu(const float* x, float* y, int64_t n, cudaStream_t stream) {
+    if (n < 0 || (n > 0 && (!x || !y))) return FA_ERR_INVALID;
+    return launch_exp2_emu(x, y, n, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // extern "C"

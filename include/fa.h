@@ -1,0 +1,121 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) fused exact attention library (libfa.so).
+ *
+ * The operation (FlashAttention-4 blog, opening section and "Forward pass"
+ * section; FlashAttention-4 paper summary, notation table):
+ *
+ *   S = alpha * Q K^T  (+ causal mask: key j visible to query i iff j <= i)
+ *   P = softmax(S) row-wise,   O = P V,   LSE_i = ln sum_j exp(S_ij)
+ *
+ * and its gradients (FlashAttention-4 blog, "Backward pass" section: the five
+ * products S, dP, dV, dK, dQ plus the elementwise work for P and dS):
+ *
+ *   dV = P^T dO,  dP = dO V^T,  D_i = sum_j P_ij dP_ij,  dS = P * (dP - D),
+ *   dQ = alpha dS K,  dK = alpha dS^T Q.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Element types: q, k, v, o, do, dq, dk, dv are bfloat16 (raw 16-bit
+ *   storage, passed as void*); lse is float32; cu_seqlens is int32.
+ * - Head dimension d must be 128.  Hq must be a multiple of Hkv; query head
+ *   h reads key/value head h / (Hq / Hkv).
+ * - Fixed-length layout (cu_seqlens == NULL): q, o, do, dq are [B, N, Hq, d]
+ *   row-major, k, v, dk, dv are [B, N, Hkv, d]; lse is [B, Hq, N].
+ * - Variable-length layout (cu_seqlens != NULL): B sequences packed along
+ *   the token axis; N is then the TOTAL token count T; q, o are [T, Hq, d],
+ *   k, v are [T, Hkv, d], lse is [Hq, T].  cu_seqlens is a DEVICE array of
+ *   B+1 non-decreasing offsets with cu_seqlens[0] = 0 and cu_seqlens[B] = T;
+ *   max_seqlen is an upper bound on every sequence length.
+ * - Causal masks are top-left aligned within each sequence (query and key
+ *   lengths are equal).
+ * - Pointers are device pointers owned by the caller; the library allocates
+ *   no device memory.  Every tensor must be 16-byte aligned and contiguous.
+ * - Calls are asynchronous: they validate arguments on the host, enqueue
+ *   kernels on `stream` and return.  They never synchronise (except
+ *   fa_get_device_status).  No exception crosses the ABI.
+ * - Return value: FA_OK, or a negative fa_status for invalid arguments
+ *   (nothing is launched) or a launch error.  Device-side faults of the
+ *   pipeline's own bounded waits are reported through fa_get_device_status.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID = -1,      /* null pointer, bad size, bad scale           */
+    FA_ERR_UNSUPPORTED = -2,  /* legal but not built: d != 128, ...         */
+    FA_ERR_ALIGN = -3,        /* a tensor is not 16-byte aligned            */
+    FA_ERR_LAUNCH = -4,       /* CUDA reported an error at launch           */
+    FA_ERR_TIMEOUT = -5,      /* a device-side wait gave up (see status)    */
+    FA_ERR_WORKSPACE = -6     /* backward workspace missing or too small    */
+} fa_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *fa_status_string(int status);
+
+/* Number of streaming multiprocessors the kernels size their persistent
+ * grids by on the current device (>0), or a negative fa_status. */
+int fa_num_sms(void);
+
+/*
+ * Process-wide tuning of the forward kernel (affects later fa_fwd calls):
+ *   exp2_emu_eighths: share of the softmax exponentials evaluated on the FMA
+ *     pipe by the polynomial (fa_exp2_emu) instead of MUFU.EX2, in eighths
+ *     (0, 1 or 2; FlashAttention-4 paper summary §3.1.3 uses 10-25 %).
+ *   tau: conditional-rescale threshold in log2 units, 0 <= tau <= 64
+ *     (default log2(256) = 8; tau = 0 rescales whenever the max grows).
+ * Every setting gives the same attention up to rounding.  Not thread-safe
+ * with concurrent fa_fwd calls.  Errors: FA_ERR_UNSUPPORTED, FA_ERR_INVALID.
+ */
+int fa_set_tuning(int exp2_emu_eighths, float tau);
+
+/*
+ * Forward: O and LSE of exact attention (FlashAttention-4 blog, "Forward
+ * pass: a new softmax pipeline with conditional rescaling").
+ *
+ * q [B,N,Hq,128], k/v [B,N,Hkv,128] bf16 in; o [B,N,Hq,128] bf16 out,
+ * lse [B,Hq,N] float32 out (natural log, includes alpha).  Varlen: see
+ * above.  alpha > 0 is the logit scale (normally 1/sqrt(128)).
+ * causal: 0 or 1.  N == 0 (or T == 0) is a no-op returning FA_OK.
+ * Errors: FA_ERR_INVALID (null pointer, B<1, N<0, Hq/Hkv<1, Hq % Hkv,
+ * alpha not finite and > 0, varlen without max_seqlen>0),
+ * FA_ERR_UNSUPPORTED (d != 128), FA_ERR_ALIGN, FA_ERR_LAUNCH.
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+           int B, int Hq, int Hkv, int N, int d, float alpha, int causal,
+           const int *cu_seqlens, int max_seqlen, cudaStream_t stream);
+
+/*
+ * Reads (and clears) the library's device status word on the current
+ * device after synchronising `stream`: FA_OK, or FA_ERR_TIMEOUT when a
+ * kernel's bounded wait gave up (the kernel then skipped its remaining work,
+ * drained its own copies, freed its tensor memory and returned).
+ * `workspace` may be NULL; when it is a backward workspace its status word
+ * is read (and cleared) too.
+ */
+int fa_get_device_status(const void *workspace, cudaStream_t stream);
+
+/*
+ * The forward kernel's FMA-pipe exponential, exposed for testing: y[i] =
+ * 2^x[i] by Cody-Waite range reduction (n = floor(x), f = x - n) and a
+ * degree-3 Horner polynomial in f with p0 = 1, scaled by adding n to the
+ * exponent bits (FlashAttention-4 blog, "Faster exponential" section;
+ * paper summary §3.1.3: max relative error 8.77e-5 on [0,1)).  Inputs below
+ * -127 (and -inf) give 0 or a value below 2^-126.  x, y: device float32
+ * arrays of n elements.  Errors: FA_ERR_INVALID, FA_ERR_LAUNCH.
+ */
+int fa_exp2_emu(const float *x, float *y, int64_t n, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,79 @@
+"""The C-ABI library builds, loads without a GPU, exports every function that
+include/*.h declares, and rejects bad arguments before touching the GPU.
+CPU only: no compute call is made."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(fa_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_blackwell_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert {"fa_fwd", "fa_get_device_status", "fa_status_string", "fa_exp2_emu"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    lib.fa_status_string.restype = ctypes.c_char_p
+    assert lib.fa_status_string(0) == b"FA_OK"
+    for code in range(-1, -7, -1):
+        assert lib.fa_status_string(code).startswith(b"FA_ERR_")
+
+
+def test_fwd_rejects_bad_arguments_on_the_host(lib):
+    f = lib.fa_fwd
+    vp, i, fl = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    f.restype = i
+    f.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, fl, i, vp, i, vp]
+    P = 0x10000  # never dereferenced: every call below fails validation first
+    ok = dict(q=P, k=P, v=P, o=P, lse=P, B=1, Hq=2, Hkv=2, N=128, d=128, alpha=0.1, causal=0, cu=None, ms=0)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["N"], a["d"],
+                 a["alpha"], a["causal"], a["cu"], a["ms"], None)
+
+    assert call(q=None) == -1
+    assert call(B=0) == -1
+    assert call(N=-1) == -1
+    assert call(Hq=3) == -1            # Hq % Hkv
+    assert call(alpha=0.0) == -1
+    assert call(alpha=float("inf")) == -1
+    assert call(causal=2) == -1
+    assert call(d=64) == -2
+    assert call(cu=P, ms=0) == -1      # varlen without max_seqlen
+    assert call(cu=P, ms=1 << 20) == -2
+    assert call(B=5000, cu=P, ms=128) == -2
+    assert call(o=P + 8) == -3
+
+
+def test_set_tuning_validation(lib):
+    lib.fa_set_tuning.argtypes = [ctypes.c_int, ctypes.c_float]
+    assert lib.fa_set_tuning(7, 8.0) == -2
+    assert lib.fa_set_tuning(0, -1.0) == -1
+    assert lib.fa_set_tuning(0, 8.0) == 0

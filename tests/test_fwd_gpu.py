@@ -1,0 +1,208 @@
+"""Forward parity: the CUDA kernel (through the C ABI) vs the fp64 CPU oracle.
+
+Tolerances (stated for the forward pass): O max |err| <= 2e-2 and mean |err|
+<= 1e-3; LSE abs err <= 1e-3.  Inputs come from the seeded generators in
+attention_blackwell_gb300.workloads; the oracle sees the same bf16 values
+upcast exactly to float64.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from attention_blackwell_gb300 import workloads as W
+from oracle import attention as A
+from oracle import exp2_poly as E
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_ABS = 2e-2, 1e-3, 1e-3
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import attention_blackwell_gb300 as fa
+    fa.lib()
+    fa.set_tuning(0, 8.0)
+    yield fa
+    fa.set_tuning(0, 8.0)
+
+
+def _gpu(t):
+    return t.cuda() if t is not None else None
+
+
+def run(fa, inp, causal, alpha=None):
+    q, k, v = _gpu(inp["q"]), _gpu(inp["k"]), _gpu(inp["v"])
+    cu = _gpu(inp.get("cu_seqlens"))
+    ms = max(inp["lengths"]) if cu is not None else None
+    o, lse = fa.fwd(q, k, v, causal=causal, alpha=alpha, cu_seqlens=cu, max_seqlen=ms)
+    assert fa.device_status() == 0
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def check(o, lse, o_ref, lse_ref):
+    err = np.abs(o - o_ref)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert err.max() <= O_MAX, err.max()
+    assert err.mean() <= O_MEAN, err.mean()
+    assert np.abs(lse - lse_ref).max() <= LSE_ABS, np.abs(lse - lse_ref).max()
+
+
+def small_inputs(B, N, Hq, Hkv, q_std=1.0, seed=0, lengths=None):
+    if lengths is not None:
+        cu = W.cu_seqlens_of(lengths)
+        T = int(cu[-1])
+        shp_q, shp_k = (T, Hq, 128), (T, Hkv, 128)
+    else:
+        cu, T = None, B * N
+        shp_q, shp_k = (B, N, Hq, 128), (B, N, Hkv, 128)
+        lengths = [N] * B
+    return {"q": W.normal_bf16(shp_q, seed, q_std), "k": W.normal_bf16(shp_k, seed + 1),
+            "v": W.normal_bf16(shp_k, seed + 2), "cu_seqlens": cu, "lengths": lengths, "T": T}
+
+
+def oracle(inp, causal, alpha=1 / math.sqrt(128)):
+    return A.forward(inp["q"], inp["k"], inp["v"], alpha, causal, cu_seqlens=inp.get("cu_seqlens"))
+
+
+def test_tiny_workload(fa):
+    w = W.WORKLOADS["tiny"]
+    inp = W.make_inputs(w)
+    o, lse = run(fa, inp, w.causal)
+    check(o, lse, *oracle(inp, w.causal))
+
+
+@pytest.mark.parametrize("N", [1, 100, 128, 129, 255, 256, 383, 640, 1000])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_lengths(fa, N, causal):
+    inp = small_inputs(2, N, 2, 2, seed=N)
+    o, lse = run(fa, inp, causal)
+    check(o, lse, *oracle(inp, causal))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (8, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_heads(fa, Hq, Hkv, causal):
+    inp = small_inputs(2, 300, Hq, Hkv, seed=7)
+    o, lse = run(fa, inp, causal)
+    check(o, lse, *oracle(inp, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_small(fa, causal):
+    inp = small_inputs(0, 0, 4, 1, seed=11, lengths=[1, 130, 257, 0, 700, 5, 256])
+    o, lse = run(fa, inp, causal)
+    check(o, lse, *oracle(inp, causal))
+
+
+def test_alpha_other_than_default(fa):
+    inp = small_inputs(1, 200, 2, 2, seed=13)
+    o, lse = run(fa, inp, True, alpha=0.05)
+    check(o, lse, *oracle(inp, True, alpha=0.05))
+
+
+@pytest.mark.parametrize("tau", [0.0, 8.0, 64.0])
+def test_conditional_rescale_identity(fa, tau):
+    """Skipping rescales (tau = 8) or never rescaling after the first tile
+    (tau = 64) gives the tau = 0 result up to rounding."""
+    inp = small_inputs(1, 1024, 2, 2, q_std=3.0, seed=17)
+    fa.set_tuning(0, tau)
+    try:
+        o, lse = run(fa, inp, True)
+    finally:
+        fa.set_tuning(0, 8.0)
+    o_ref, lse_ref = oracle(inp, True)
+    check(o, lse, o_ref, lse_ref)
+    fa.set_tuning(0, 0.0)
+    try:
+        o0, _ = run(fa, inp, True)
+    finally:
+        fa.set_tuning(0, 8.0)
+    assert np.abs(o - o0).max() <= 2e-2
+
+
+@pytest.mark.parametrize("emu", [1, 2])
+def test_exp2_split_parity(fa, emu):
+    inp = small_inputs(2, 513, 2, 2, seed=19)
+    fa.set_tuning(emu, 8.0)
+    try:
+        o, lse = run(fa, inp, True)
+    finally:
+        fa.set_tuning(0, 8.0)
+    check(o, lse, *oracle(inp, True))
+
+
+def test_exp2_emu_kernel_error_bound(fa):
+    """The kernel's FMA exp2 meets the pages' 8.77e-5 bound on [0,1) (every
+    2^8-th float32 there) and on a wide random range, and agrees with the
+    oracle's independent float32 evaluation to within 1 ulp."""
+    bits = np.arange(0, 0x3F800000, 256, dtype=np.uint32)
+    x01 = bits.view(np.float32)
+    xr = np.random.default_rng(3).uniform(-126, 127.9, 1 << 20).astype(np.float32)
+    for x in (x01, xr):
+        y = fa.exp2_emu(torch.from_numpy(x).cuda()).cpu().numpy()
+        exact = np.exp2(x.astype(np.float64))
+        assert (np.abs(y - exact) / exact).max() <= 8.77e-5
+        yo = E.exp2_poly(x)
+        ulp = np.abs(y.view(np.int32).astype(np.int64) - yo.view(np.int32).astype(np.int64))
+        assert ulp.max() <= 1
+    special = fa.exp2_emu(torch.tensor([-math.inf, -500.0, -127.0, 0.0, 8.0], device="cuda")).cpu().tolist()
+    assert special[:3] == [0.0, 0.0, 0.0] and special[3] == 1.0 and special[4] == 256.0
+
+
+def test_repeatable_bitwise(fa):
+    inp = small_inputs(2, 700, 4, 2, seed=23)
+    o1, l1 = run(fa, inp, True)
+    o2, l2 = run(fa, inp, True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ----------------------------------------------- full-size workloads (sampled)
+
+def _sample_picks(rng, B, Hq, lengths, n):
+    picks = []
+    for _ in range(n):
+        b = int(rng.integers(B))
+        L = lengths[b]
+        i = int(rng.choice([0, L - 1, int(rng.integers(L))]))
+        picks.append((b, int(rng.integers(Hq)), i))
+    return picks
+
+
+@pytest.mark.parametrize("name", ["large", "causal", "varlen"])
+def test_full_size_sampled(fa, name):
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w)
+    o, lse = run(fa, inp, w.causal)
+    rng = np.random.default_rng(5)
+    picks = _sample_picks(rng, w.B, w.Hq, inp["lengths"], 96)
+    ro, rl = A.forward_rows(inp["q"], inp["k"], inp["v"], w.alpha, w.causal, picks,
+                            cu_seqlens=inp["cu_seqlens"])
+    cu = inp["cu_seqlens"]
+    for n, (b, h, i) in enumerate(picks):
+        if cu is None:
+            go, gl = o[b, i, h], lse[b, h, i]
+        else:
+            go, gl = o[int(cu[b]) + i, h], lse[h, int(cu[b]) + i]
+        assert np.abs(go - ro[n]).max() <= O_MAX
+        assert abs(gl - rl[n]) <= LSE_ABS
+    # properties at full size: finite everywhere, |O| bounded by max |V|
+    vmax = float(inp["v"].float().abs().max())
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert np.abs(o).max() <= vmax * (1 + 1e-2)
+
+
+def test_status_and_bad_arguments(fa):
+    L = fa.lib()
+    q = torch.zeros(1, 128, 2, 128, dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty(1, 2, 128, device="cuda")
+    p = lambda t: t.data_ptr()
+    s = torch.cuda.current_stream().cuda_stream
+    assert L.fa_fwd(p(q), p(q), p(q), p(o), p(lse), 1, 2, 2, 128, 64, 0.1, 0, None, 0, s) == -2  # d != 128
+    assert L.fa_fwd(p(q), p(q), p(q), p(o), p(lse), 1, 3, 2, 128, 128, 0.1, 0, None, 0, s) == -1  # Hq % Hkv
+    assert L.fa_fwd(p(q) + 2, p(q), p(q), p(o), p(lse), 1, 2, 2, 128, 128, 0.1, 0, None, 0, s) == -3
+    assert L.fa_fwd(p(q), p(q), p(q), p(o), p(lse), 1, 2, 2, 0, 128, 0.1, 0, None, 0, s) == 0  # empty
+    assert fa.device_status() == 0
