@@ -1,0 +1,407 @@
+"""Throughput of the fused attention hot path on GB300: one JSON line.
+
+Default (our arm): ``python bench.py [--gpus N --steps K --warmup W]``.
+A step is one pass of the hot path over one batch of the headline workload
+(B=4, Hq=Hkv=16, N=4096, d=128, non-causal, bf16, synthetic N(0,1) inputs):
+the forward kernel, then (once built) the backward chain (preprocess,
+main kernel, dQ postprocess) on the same batch.  FLOPs credited:
+4*B*Hq*N^2*d for the forward, 2.5x that for the backward.
+
+Timing: W untimed steps, then K steps bracketed by a barrier and
+torch.cuda.synchronize(), timed with CUDA events on the launching stream; the
+inputs (Q, K, V, dO: 64 MiB each) exceed the 126 MB L2, so no flush is done
+between steps.  Per-kernel durations come from CUDA events recorded between
+the launches of every timed step.  SM clocks and throttle reasons are sampled
+with nvidia-smi during the timed region.
+
+``--impl reference`` times the CPU oracle (float64, the machine's host cores) on a
+bounded sample of the same workload and prints the same line with
+"impl": "reference".  Under torchrun every rank runs the workload on its own
+GPU (replicas; attention has no exchange step) and rank 0 prints the line.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOPs/s (BF16, d=128) and % of 2.25 PFLOPS dense peak"
+PEAK_NOMINAL_TFLOPS = 2250.0
+WORKLOAD = "large"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-bwd", action="store_true", help="time the forward only")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
+    return ap.parse_args()
+
+
+def dist_init(n):
+    rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("FA_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device=None):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples taken in a thread."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.samples = []
+        self.proc = None
+        self.index = index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 5:
+            time.sleep(0.01)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        win = [p for (t, p) in self.samples if t0 <= t <= t1] or [p for (_, p) in self.samples[-3:]]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [num(p[0]) for p in win if num(p[0]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[3 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(win[0][1]),
+                "power_w_max": max((num(p[2]) or 0.0) for p in win), "reasons": reasons, "samples": len(win)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def kernel_traffic(name):
+    """dram bytes per launch from the committed ncu summary, or None when the
+    kernel's source changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        rec = json.load(open(path)).get(name)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return rec["dram_bytes_per_launch"] if sha == rec["source_sha"] else None
+
+
+def cpu_baseline(w, inp, with_bwd, budget_s):
+    """The float64 oracle, as it stands, on whole (batch, head) slices of the
+    same workload until ``budget_s`` seconds have been spent (at least one)."""
+    import numpy as np
+
+    from attention_blackwell_gb300 import workloads as W
+    from oracle import attention as A
+
+    q = inp["q"].float().numpy().astype(np.float64)
+    k = inp["k"].float().numpy().astype(np.float64)
+    v = inp["v"].float().numpy().astype(np.float64)
+    do = inp["do"].float().numpy().astype(np.float64) if with_bwd else None
+    g = w.Hq // w.Hkv
+    done, flops, t0 = 0, 0.0, time.perf_counter()
+    while True:
+        b, h = divmod(done % (w.B * w.Hq), w.Hq)
+        A.head_forward(q[b, :, h], k[b, :, h // g], v[b, :, h // g], w.alpha, w.causal)
+        flops += W.attention_flops(1, [w.N], w.causal)
+        if with_bwd:
+            A.head_backward(q[b, :, h], k[b, :, h // g], v[b, :, h // g], do[b, :, h], w.alpha, w.causal)
+            flops += W.attention_flops(1, [w.N], w.causal, backward=True)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "%d of %d (batch, head) slices of the %s workload, %s, float64 NumPy, %.1f s"
+                      % (done, w.B * w.Hq, w.name, "forward+backward" if with_bwd else "forward", dt)}
+
+
+def build_step(fa, w, dev_t, has_bwd):
+    """[(name, launch callable, credited FLOPs, launches)] for one step."""
+    from attention_blackwell_gb300 import workloads as W
+    q, k, v, o, lse = dev_t["q"], dev_t["k"], dev_t["v"], dev_t["o"], dev_t["lse"]
+    ks = [("fwd", lambda: fa.fwd(q, k, v, causal=w.causal, out=o, lse=lse),
+           W.attention_flops(w.Hq, [w.N] * w.B, w.causal), 1)]
+    if has_bwd:
+        do, dq, dk, dv, ws = dev_t["do"], dev_t["dq"], dev_t["dk"], dev_t["dv"], dev_t["ws"]
+        ks.append(("bwd_pre", lambda: fa.bwd_preprocess(o, do, lse, ws, causal=w.causal), 0.0, 1))
+        ks.append(("bwd", lambda: fa.bwd_main(q, k, v, do, ws, dk=dk, dv=dv, causal=w.causal),
+                   W.attention_flops(w.Hq, [w.N] * w.B, w.causal, backward=True), 1))
+        ks.append(("bwd_post", lambda: fa.bwd_postprocess(ws, dq, causal=w.causal), 0.0, 1))
+    return ks
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import attention_blackwell_gb300 as fa
+    from attention_blackwell_gb300 import workloads as W
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[WORKLOAD]
+    has_bwd = hasattr(fa, "bwd_main") and not args.no_bwd
+    inp = W.make_inputs(w, with_grad=True)
+    t = {n: inp[n].to(dev) for n in ("q", "k", "v", "do")}
+    t["o"] = torch.empty_like(t["q"])
+    t["lse"] = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+    if has_bwd:
+        t["dq"], t["dk"], t["dv"] = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+        t["ws"] = fa.bwd_workspace(w.B, w.Hq, w.N, deterministic=False, device=dev)
+    kernels = build_step(fa, w, t, has_bwd)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        for i, (_, fn, _, _) in enumerate(kernels):
+            if ev is not None:
+                ev[i][0].record(stream)
+            fn()
+            if ev is not None:
+                ev[i][1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if fa.device_status() != 0:
+        raise RuntimeError("device status reported a timeout during warm-up")
+
+    K = args.steps
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in kernels]
+           for _ in range(K)]
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t_start.record(stream)
+    for s in range(K):
+        step(evs[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(world)
+    if clocks:
+        clocks.stop()
+    if fa.device_status() != 0:
+        raise RuntimeError("device status reported a timeout in the timed region")
+    ms_local = t_start.elapsed_time(t_end)
+    ms = max_over_ranks(ms_local, world, dev)
+    per_kernel = []
+    for i, (name, _, fl, nl) in enumerate(kernels):
+        d = [evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(K)]
+        per_kernel.append({"kernel": name, "avg_ms": sum(d) / K, "flops": fl, "launches_per_step": nl})
+    flops_step = sum(k[2] for k in kernels)
+    value = flops_step * K * world / (ms / 1e3) / 1e12
+
+    # End to end through the public API with host buffers: every step copies
+    # the step's inputs from pinned host memory and reads its results back.
+    host = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
+    outs = ["o", "lse"] + (["dq", "dk", "dv"] if has_bwd else [])
+    host_out = {n: torch.empty(t[n].shape, dtype=t[n].dtype, pin_memory=True) for n in outs}
+    ins = ["q", "k", "v"] + (["do"] if has_bwd else [])
+    h2d = sum(host[n].numel() * host[n].element_size() for n in ins)
+    d2h = sum(host_out[n].numel() * host_out[n].element_size() for n in outs)
+    E = max(3, args.e2e_steps)
+
+    def e2e_step():
+        for n in ins:
+            t[n].copy_(host[n], non_blocking=True)
+        step()
+        for n in outs:
+            host_out[n].copy_(t[n], non_blocking=True)
+        stream.synchronize()
+
+    e2e_step()
+    barrier(world)
+    e0 = time.perf_counter()
+    for _ in range(E):
+        e2e_step()
+    e2e_ms = max_over_ranks((time.perf_counter() - e0) * 1e3, world, dev)
+    e2e_value = flops_step * E * world / (e2e_ms / 1e3) / 1e12
+    return locals()
+
+
+def emit(line):
+    print(json.dumps(line), flush=True)
+
+
+def main_ours(args):
+    rank, world = dist_init(args.gpus)
+    r = run_ours(args, rank, world)
+    if rank != 0:
+        return
+    w, K, kernels, per_kernel = r["w"], r["K"], r["kernels"], r["per_kernel"]
+    peaks = measured_peaks()
+    dom = max(per_kernel, key=lambda p: p["avg_ms"] * p["launches_per_step"])
+    achieved = dom["flops"] / (dom["avg_ms"] / 1e3) / 1e12 if dom["flops"] else None
+    if peaks and peaks.get("bf16_tflops"):
+        peak, peak_src = float(peaks["bf16_tflops"]), "measured burst cuBLAS bf16 (MEASURED_PEAKS.json)"
+    else:
+        peak, peak_src = 1900.0, "fallback 1.9 PFLOP/s bf16"
+    clk = r["clocks"].summary(r["wall0"], r["wall1"]) if r["clocks"] else None
+    step_name = "+".join(p["kernel"] for p in per_kernel)
+    line = {
+        "metric": METRIC,
+        "value": round(r["value"], 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": round(r["ms"] / K, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "%s: B=%d Hq=%d Hkv=%d N=%d d=%d %s" % (
+            w.name, w.B, w.Hq, w.Hkv, w.N, w.d, "causal" if w.causal else "non-causal"),
+            "step": step_name, "global_batch": w.B * world, "seq_len": w.N,
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": "no flush: Q, K, V, dO are 64 MiB each (> 126 MB L2 together)"},
+        "pct_of_2.25PF": round(100.0 * r["value"] / PEAK_NOMINAL_TFLOPS, 2),
+        "breakdown": [{"kernel": p["kernel"], "avg_ms": round(p["avg_ms"], 4),
+                       "tflops": round(p["flops"] / (p["avg_ms"] / 1e3) / 1e12, 1) if p["flops"] else None}
+                      for p in per_kernel],
+        "roofline": {"kernel": dom["kernel"], "bound": "tensor",
+                     "achieved": round(achieved, 1) if achieved else None, "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4) if achieved else None,
+                     "peak_source": peak_src,
+                     "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4)
+                     if achieved and peaks and peaks.get("bf16_tflops_sustained") else None,
+                     "traffic": kernel_traffic(dom["kernel"])},
+        "e2e": {"value": round(r["e2e_value"], 2), "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"], "steps": r["E"]},
+        "gpu_launches": K * sum(p["launches_per_step"] for p in per_kernel),
+        "clocks": clk,
+    }
+    line["cpu_baseline"] = cpu_baseline(w, r["inp"], r["has_bwd"], args.cpu_seconds)
+    emit(line)
+
+
+def main_reference(args):
+    """The CPU oracle as the reference arm (rank 0 only)."""
+    rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import numpy as np
+
+    from attention_blackwell_gb300 import workloads as W
+    from oracle import attention as A
+
+    w = W.WORKLOADS[WORKLOAD]
+    with_bwd = not args.no_bwd
+    inp = W.make_inputs(w, with_grad=True)
+    q = inp["q"].float().numpy().astype(np.float64)
+    k = inp["k"].float().numpy().astype(np.float64)
+    v = inp["v"].float().numpy().astype(np.float64)
+    do = inp["do"].float().numpy().astype(np.float64)
+
+    def step(s):  # one (batch, head) slice of the workload per step
+        b, h = divmod(s % (w.B * w.Hq), w.Hq)
+        hk = h // (w.Hq // w.Hkv)
+        A.head_forward(q[b, :, h], k[b, :, hk], v[b, :, hk], w.alpha, w.causal)
+        f = W.attention_flops(1, [w.N], w.causal)
+        if with_bwd:
+            A.head_backward(q[b, :, h], k[b, :, hk], v[b, :, hk], do[b, :, h], w.alpha, w.causal)
+            f += W.attention_flops(1, [w.N], w.causal, backward=True)
+        return f
+
+    for s in range(max(1, args.warmup)):
+        step(s)
+    t0 = time.perf_counter()
+    flops = sum(step(s) for s in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = "one (batch, head) slice of the %s workload per step (%s), float64 NumPy" % (
+        w.name, "forward+backward" if with_bwd else "forward")
+    emit({"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "TFLOP/s", "n_gpus": world,
+          "steps": args.steps, "warmup": max(1, args.warmup), "ms_per_step": round(dt * 1e3 / args.steps, 2),
+          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+          "config": {"workload": "%s: B=%d Hq=%d Hkv=%d N=%d d=%d %s" % (
+              w.name, w.B, w.Hq, w.Hkv, w.N, w.d, "causal" if w.causal else "non-causal"),
+              "step": "oracle slice"},
+          "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                           "sample": sample},
+          "e2e": {"value": round(value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}})
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        main_reference(a)
+    else:
+        main_ours(a)
