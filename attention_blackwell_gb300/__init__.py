@@ -12,7 +12,7 @@ import os
 
 import torch
 
-__all__ = ["fwd", "exp2_emu", "set_tuning", "device_status", "num_sms", "FAError", "library_path", "lib"]
+__all__ = ["fwd", "bwd", "bwd_workspace", "exp2_emu", "set_tuning", "device_status", "num_sms", "FAError", "library_path", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libfa.so")
@@ -50,6 +50,13 @@ def lib():
         L.fa_set_tuning.argtypes = [i, f]
         L.fa_fwd.restype = i
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp]
+        sz = ctypes.c_size_t
+        L.fa_bwd_workspace_size.restype = sz
+        L.fa_bwd_workspace_size.argtypes = [i, i, i, i, i, i]
+        L.fa_bwd_stages.restype = i
+        L.fa_bwd_stages.argtypes = [i] + [vp] * 9 + [i, i, i, i, i, f, i, vp, i, i, vp, sz, vp]
+        L.fa_bwd.restype = i
+        L.fa_bwd.argtypes = [vp] * 9 + [i, i, i, i, i, f, i, vp, i, i, vp, sz, vp]
         L.fa_get_device_status.restype = i
         L.fa_get_device_status.argtypes = [vp, vp]
         L.fa_exp2_emu.restype = i
@@ -142,6 +149,55 @@ def fwd(q, k, v, causal=False, alpha=None, cu_seqlens=None, max_seqlen=None, out
                       1 if causal else 0, _ptr(cu_seqlens), int(max_seqlen), _stream(stream))
     _check(rc, "fa_fwd")
     return out, lse
+
+
+def _shapes(q, k, cu_seqlens, max_seqlen):
+    if cu_seqlens is not None:
+        T, Hq, d = q.shape
+        return cu_seqlens.numel() - 1, T, Hq, k.shape[1], d, max_seqlen
+    B, N, Hq, d = q.shape
+    return B, N, Hq, k.shape[2], d, N
+
+
+def bwd_workspace(B, Hq, N, deterministic=False, varlen=False, device=None):
+    """A uint8 CUDA tensor large enough for fa_bwd (N = total tokens if varlen)."""
+    n = lib().fa_bwd_workspace_size(int(B), int(Hq), int(N), HEAD_DIM, int(bool(deterministic)), int(bool(varlen)))
+    if n == 0:
+        raise ValueError("invalid sizes for the backward workspace")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def bwd(q, k, v, o, lse, do, causal=False, alpha=None, cu_seqlens=None, max_seqlen=None, deterministic=False,
+        workspace=None, dq=None, dk=None, dv=None, stages=7, stream=None):
+    """Backward attention.  Returns (dq, dk, dv); layouts as in fwd.
+
+    ``stages`` selects the launches (1 preprocess, 2 main, 4 postprocess);
+    the default runs all three.
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _need(t, n, torch.bfloat16)
+    _need(lse, "lse", torch.float32)
+    varlen = cu_seqlens is not None
+    if varlen:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        if max_seqlen is None:
+            raise ValueError("varlen needs max_seqlen")
+    B, N, Hq, Hkv, d, ms = _shapes(q, k, cu_seqlens, max_seqlen)
+    if alpha is None:
+        alpha = 1.0 / (d ** 0.5)
+    if workspace is None:
+        workspace = bwd_workspace(B, Hq, N, deterministic, varlen, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _need(t, n, torch.bfloat16)
+    rc = lib().fa_bwd_stages(int(stages), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
+                             _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, float(alpha), 1 if causal else 0,
+                             _ptr(cu_seqlens), int(ms), int(bool(deterministic)), _ptr(workspace),
+                             workspace.numel(), _stream(stream))
+    _check(rc, "fa_bwd")
+    return dq, dk, dv
 
 
 def device_status(workspace=None, stream=None):

@@ -180,22 +180,103 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+static int read_and_clear(DevStatus* where) {
+    DevStatus s;
+    if (cudaMemcpy(&s, where, sizeof s, cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_LAUNCH;
+    if (s.code == 0) return FA_OK;
+    if (getenv("FA_LOG"))
+        fprintf(stderr, "fa: device status %d at wait site %d (block %d)\n", s.code, s.where, s.block);
+    DevStatus z = {0, 0, 0, 0};
+    if (cudaMemcpy(where, &z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_LAUNCH;
+    return s.code;
+}
+
 int fa_get_device_status(const void* workspace, cudaStream_t stream) {
-    (void)workspace;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_LAUNCH;
     DeviceInfo* dev = nullptr;
     int rc = current_device_info(&dev);
     if (rc != FA_OK) return rc;
-    DevStatus s;
-    if (cudaMemcpy(&s, dev->status, sizeof s, cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_LAUNCH;
-    if (s.code != 0) {
-        if (getenv("FA_LOG"))
-            fprintf(stderr, "fa: device status %d at wait site %d (block %d)\n", s.code, s.where, s.block);
-        DevStatus z = {0, 0, 0, 0};
-        if (cudaMemcpy(dev->status, &z, sizeof z, cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_LAUNCH;
-        return s.code;
+    int a = read_and_clear(dev->status);
+    int b = workspace ? read_and_clear(&static_cast<BwdHeader*>(const_cast<void*>(workspace))->status) : FA_OK;
+    return a != FA_OK ? a : b;
+}
+
+size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, int deterministic, int varlen) {
+    if (B < 1 || Hq < 1 || N < 0 || d != kHeadDim) return 0;
+    const long long T = varlen ? (long long)N : (long long)B * N;
+    return ws_layout(T, B, Hq, deterministic ? 1 : 0, varlen ? 1 : 0).total;
+}
+
+int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, float alpha,
+                  int causal, const int* cu_seqlens, int max_seqlen, int deterministic, void* workspace,
+                  size_t workspace_bytes, cudaStream_t stream) {
+    if (stages < 1 || stages > 7) return FA_ERR_INVALID;
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID;
+    if (B < 1 || N < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return FA_ERR_INVALID;
+    if (!(alpha > 0.0f) || !isfinite(alpha)) return FA_ERR_INVALID;
+    if ((causal != 0 && causal != 1) || (deterministic != 0 && deterministic != 1)) return FA_ERR_INVALID;
+    if (d != kHeadDim) return FA_ERR_UNSUPPORTED;
+    const bool varlen = cu_seqlens != nullptr;
+    if (varlen) {
+        if (max_seqlen < 1) return FA_ERR_INVALID;
+        if (B > kMaxVarlenSeqs || max_seqlen > 131072) return FA_ERR_UNSUPPORTED;
     }
-    return FA_OK;
+    const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return FA_ERR_ALIGN;
+    if (varlen && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FA_ERR_ALIGN;
+    const long long T = varlen ? (long long)N : (long long)B * N;
+    if (T == 0) return FA_OK;
+    if (T > 0x7fffffffLL || (long long)Hq * T > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    const WsLayout w = ws_layout(T, B, Hq, deterministic, varlen ? 1 : 0);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
+        return FA_ERR_WORKSPACE;
+
+    DeviceInfo* dev = nullptr;
+    int rc = current_device_info(&dev);
+    if (rc != FA_OK) return rc;
+    BwdLaunch L;
+    if ((rc = make_map(&L.tq, q, Hq, T)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tk, k, Hkv, T)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tv, v, Hkv, T)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tdo, dout, Hq, T)) != FA_OK) return rc;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    BwdArgs& a = L.a;
+    a.o = o;
+    a.dO = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.cu_seqlens = cu_seqlens;
+    a.hdr = reinterpret_cast<BwdHeader*>(ws);
+    a.D = reinterpret_cast<float*>(ws + w.d_off);
+    a.dqacc = reinterpret_cast<float*>(ws + w.dq_off);
+    a.sem = reinterpret_cast<int*>(ws + w.sem_off);
+    a.units = reinterpret_cast<int4*>(ws + w.unit_off);
+    a.sem_stride = w.sem_stride;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.N = N;
+    a.T = T;
+    a.causal = causal;
+    a.varlen = varlen ? 1 : 0;
+    a.deterministic = deterministic;
+    a.max_seqlen = varlen ? max_seqlen : N;
+    a.alpha = alpha;
+    a.scale_log2 = alpha * 1.4426950408889634f;
+    L.num_sms = dev->num_sms;
+    cudaError_t e = launch_bwd(L, stages, stream);
+    return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+           void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, float alpha, int causal, const int* cu_seqlens,
+           int max_seqlen, int deterministic, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return fa_bwd_stages(7, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, alpha, causal, cu_seqlens,
+                         max_seqlen, deterministic, workspace, workspace_bytes, stream);
 }
 
 int fa_exp2_emu(const float* x, float* y, int64_t n, cudaStream_t stream) {

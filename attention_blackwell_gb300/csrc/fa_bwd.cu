@@ -1,0 +1,689 @@
+// fa_bwd.cu -- backward attention for sm_103a (tcgen05 / TMEM / TMA).
+//
+// Gradients of O = softmax(alpha Q K^T [+ causal]) V for d = 128
+// (FlashAttention-4 blog, "Backward pass" section): with upstream dO,
+//   D_i = sum_d dO_id O_id,  P = exp(alpha Q K^T - LSE),
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),
+//   dK = alpha dS^T Q,  dQ = alpha dS K.
+//
+// Three stages on the caller's stream:
+//   1. preprocess: D (one warp per query row and head), dQacc := 0,
+//      semaphores := 0, and for varlen a work list in longest-first order;
+//   2. main kernel: one persistent CTA per SM; a work unit is one 128-key
+//      tile of one (sequence, key/value head); the CTA keeps K, V and the dK,
+//      dV accumulators resident and streams the query tiles of every query
+//      head of the group.  It recomputes S and P transposed (keys on the
+//      TMEM lanes) so that P^T sits in TMEM exactly as operand A of the dV
+//      product (FlashAttention-4 blog, "Backward pass": transposed
+//      recompute, P^T/dS^T resident as operand A), runs the five UMMAs per
+//      tile and adds dQ into an fp32 accumulator in global memory with
+//      vector reductions -- in a fixed order behind per-tile semaphores in
+//      deterministic mode (blog, "Deterministic mode");
+//   3. postprocess: dq = bf16(alpha * dQacc).
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kLevelsMax = 1024;  // key-tile levels of the varlen plan (max_seqlen <= 131072)
+
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// ---------------------------------------------------------------- stage 1
+
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long rows = a.T * a.Hq;
+    for (long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < rows; w += nwarps) {
+        const long long tok = w / a.Hq;
+        const int h = (int)(w - tok * a.Hq);
+        const size_t off = ((size_t)tok * a.Hq + h) * kHeadDim;
+        const uint2 ov = reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.o) + off)[lane];
+        const uint2 dv = reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.dO) + off)[lane];
+        float s = bf16lo(ov.x) * bf16lo(dv.x) + bf16hi(ov.x) * bf16hi(dv.x) + bf16lo(ov.y) * bf16lo(dv.y) +
+                  bf16hi(ov.y) * bf16hi(dv.y);
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+        const size_t r = (size_t)h * a.T + tok;
+        if (lane == 0) a.D[r] = s;
+        reinterpret_cast<float4*>(a.dqacc + r * kHeadDim)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (a.deterministic) {
+        const long long n = (long long)a.Hq * a.sem_stride;
+        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+             i += (long long)gridDim.x * blockDim.x)
+            a.sem[i] = 0;
+    }
+}
+
+// Varlen work list: units (sequence, key/value head, key tile k) ordered by
+// k ascending (longest remaining query range first under a causal mask, and
+// the order the deterministic semaphores need), sequences within a level by
+// key-tile count, descending.  One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a) {
+    __shared__ int s_cu[kMaxVarlenSeqs + 1], s_order[kMaxVarlenSeqs], s_pref[kLevelsMax + 1];
+    __shared__ int s_maxk;
+    const int tid = threadIdx.x, B = a.B;
+    for (int i = tid; i <= B; i += blockDim.x) {
+        const int c = a.cu_seqlens[i];
+        s_cu[i] = c < 0 ? 0 : (c > a.N ? a.N : c);
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int i = 1; i <= B; ++i) s_cu[i] = s_cu[i] > s_cu[i - 1] ? s_cu[i] : s_cu[i - 1];
+    __syncthreads();
+    auto nkv = [&](int s) { return (s_cu[s + 1] - s_cu[s] + kTileN - 1) / kTileN; };
+    for (int i = tid; i < B; i += blockDim.x) {
+        const int ni = nkv(i);
+        int rank = 0;
+        for (int j = 0; j < B; ++j) {
+            const int nj = nkv(j);
+            rank += (nj > ni) || (nj == ni && j < i);
+        }
+        s_order[rank] = i;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int maxk = B > 0 ? nkv(s_order[0]) : 0;
+        if (maxk > kLevelsMax) {
+            if (atomicCAS(&a.hdr->status.code, 0, -1) == 0) a.hdr->status.where = 200;
+            maxk = 0;
+        }
+        int acc = 0, p = B;
+        for (int k = 0; k < maxk; ++k) {
+            while (p > 0 && nkv(s_order[p - 1]) <= k) --p;   // sequences with more than k key tiles
+            s_pref[k] = acc;
+            acc += p * a.Hkv;
+        }
+        s_pref[maxk] = acc;
+        s_maxk = maxk;
+        a.hdr->total_units = acc;
+    }
+    __syncthreads();
+    const int maxk = s_maxk, total = s_pref[maxk];
+    for (int u = tid; u < total; u += blockDim.x) {
+        int lo = 0, hi = maxk;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (s_pref[mid + 1] > u) hi = mid; else lo = mid + 1;
+        }
+        const int r = u - s_pref[lo];
+        a.units[u] = make_int4(s_order[r / a.Hkv], r % a.Hkv, lo, 0);
+    }
+}
+
+// ---------------------------------------------------------------- stage 3
+
+__global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const long long rows = a.T * a.Hq;
+    for (long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < rows; w += nwarps) {
+        const long long tok = w / a.Hq;
+        const int h = (int)(w - tok * a.Hq);
+        const float4 g = reinterpret_cast<const float4*>(a.dqacc + ((size_t)h * a.T + tok) * kHeadDim)[lane];
+        uint2 o;
+        o.x = pack_bf16x2(g.x * a.alpha, g.y * a.alpha);
+        o.y = pack_bf16x2(g.z * a.alpha, g.w * a.alpha);
+        reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.dq) + ((size_t)tok * a.Hq + h) * kHeadDim)[lane] = o;
+    }
+}
+
+// ---------------------------------------------------------------- stage 2
+//
+// Warp roles (384 threads):
+//   warps 0-3   "softmax" warpgroup, one thread per KEY row (TMEM lane):
+//               P^T = 2^(alpha log2e S^T - LSE log2e) -> bf16 into TMEM
+//               (operand A of dV += P^T dO); dS^T = P^T (dP^T - D) -> bf16 into
+//               shared memory in the 128-B swizzled layout both the dK and the
+//               dQ UMMAs read (K-major for dK, MN-major for dQ);
+//   warps 4-7   dQ warpgroup, one thread per QUERY row: drains dQ_i from TMEM
+//               into the fp32 accumulator (vector reductions), then at the end
+//               of a unit stores dK (x alpha) and dV in bf16;
+//   warp  8     loader: K, V once per unit (TMA), then Q_i, dO_i (TMA) and
+//               LSE_i, D_i (plain loads) into a two-stage ring;
+//   warp  9     UMMA issuer (one thread);  warps 10-11 idle.
+//
+// Tensor memory (512 columns): dK acc 0-127, dV acc 128-255,
+//   R0 256-383: S^T, then P^T (bf16, first 64 columns);
+//   R1 384-511: dP^T, then dQ_i (the paper's 1-CTA sharing of dP/dS/dQ columns).
+// Per query tile the UMMA order is dV, dK, S(next), dQ, dP(next): the next
+// tile's S^T is in flight while dQ of this tile drains (FlashAttention-4 blog,
+// "Backward pass": dK/dQ of tile j-1 overlap the elementwise work of tile j).
+//
+// Shared memory (dynamic, 1024-aligned, 232448 bytes):
+//   K 32K | V 32K | Q[2] 2x32K | dO[2] 2x32K | dS 32K | lse2[2][128], D[2][128] | barriers
+constexpr int kBwdThreads = 384;
+constexpr uint32_t kT32 = 32768, kBox = 16384;
+constexpr uint32_t kOffK = 0, kOffV = kT32, kOffQ = 2 * kT32, kOffDO = 4 * kT32, kOffDS = 6 * kT32;
+constexpr uint32_t kOffStat = 7 * kT32;                 // lse2[2][128], D[2][128] floats
+constexpr uint32_t kOffBar = kOffStat + 4 * 128 * 4;
+constexpr uint32_t kBwdSmem = kOffBar + 1024;           // 232448
+
+struct BwdShared {
+    uint64_t kv_full, kv_empty, q_full[2], q_empty[2];
+    uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dq_full, dq_free, dkdv_done, acc_free, drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int total;
+};
+static_assert(sizeof(BwdShared) <= 1024, "barrier block");
+
+constexpr uint32_t kColDK = 0, kColDV = 128, kColR0 = 256, kColR1 = 384;
+
+enum : int { kBSiteKvEmpty = 11, kBSiteQEmpty, kBSiteKvFull, kBSiteAcc, kBSiteQFull, kBSiteP, kBSiteDs,
+             kBSiteDqFree, kBSiteS, kBSiteDp, kBSiteDsFree, kBSiteDq, kBSiteDkdv, kBSiteSem };
+
+struct BUnit {
+    int seq, hk, k, tok0, len, n, nq, i0;
+};
+
+// Decode unit u: fixed length -> key tile k = u / (B*Hkv) (all first key
+// tiles before any second one: the order the deterministic semaphores and the
+// causal longest-first rule both want); varlen -> the planned work list.
+__device__ __forceinline__ bool bwd_unit(const BwdArgs& a, int total, int u, BUnit& U) {
+    if (u >= total) return false;
+    if (!a.varlen) {
+        const int bh = a.B * a.Hkv;
+        U.k = u / bh;
+        const int r = u - U.k * bh;
+        U.seq = r / a.Hkv;
+        U.hk = r - U.seq * a.Hkv;
+        U.tok0 = U.seq * a.N;
+        U.len = a.N;
+    } else {
+        const int4 e = a.units[u];
+        U.seq = e.x;
+        U.hk = e.y;
+        U.k = e.z;
+        int c0 = a.cu_seqlens[U.seq], c1 = a.cu_seqlens[U.seq + 1];
+        c0 = c0 < 0 ? 0 : (c0 > a.N ? a.N : c0);
+        c1 = c1 < c0 ? c0 : (c1 > a.N ? a.N : c1);
+        U.tok0 = c0;
+        U.len = c1 - c0;
+    }
+    U.nq = (U.len + kTileM - 1) / kTileM;
+    U.i0 = a.causal ? U.k : 0;
+    U.n = (a.Hq / a.Hkv) * (U.nq - U.i0);
+    return true;
+}
+
+// A 128x128x128 product with both operands K-major in shared memory
+// (S^T = K Q^T and dP^T = V dO^T).
+__device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a_smem, uint32_t b_smem) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+    const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, 16, 1024);
+#pragma unroll 1
+    for (uint32_t k = 0; k < 8; ++k) {
+        const uint32_t off = ((k >> 2) * kBox + (k & 3) * 32) >> 4;
+        umma_ss(d, ad + off, bd + off, idesc, k > 0);
+    }
+}
+
+// D (+)= A[tmem] B, B MN-major in shared memory (dV += P^T dO).
+__device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b_smem, uint32_t acc) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+    const uint64_t bd = sdesc_sw128(b_smem, kBox, 1024);
+#pragma unroll 1
+    for (uint32_t k = 0; k < 8; ++k) umma_ts(d, a_tmem + k * 8, bd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
+}
+
+// D (+)= A B with A K-major and B MN-major in shared memory (dK += dS^T Q).
+__device__ __forceinline__ void mma_kn(uint32_t d, uint32_t a_smem, uint32_t b_smem, uint32_t acc) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+    const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, kBox, 1024);
+#pragma unroll 1
+    for (uint32_t k = 0; k < 8; ++k)
+        umma_ss(d, ad + (((k >> 2) * kBox + (k & 3) * 32) >> 4), bd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
+}
+
+// D = A B with A and B both MN-major in shared memory (dQ = dS K: dS^T is
+// stored key-major, i.e. queries contiguous = M contiguous).
+__device__ __forceinline__ void mma_nn(uint32_t d, uint32_t a_smem, uint32_t b_smem) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 1, 1);
+    const uint64_t ad = sdesc_sw128(a_smem, kBox, 1024), bd = sdesc_sw128(b_smem, kBox, 1024);
+#pragma unroll 1
+    for (uint32_t k = 0; k < 8; ++k) umma_ss(d, ad + ((k * 2048) >> 4), bd + ((k * 2048) >> 4), idesc, k > 0);
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Named barrier that also ORs a predicate over its threads (uniform result).
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(n) : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(kBwdThreads, 1)
+bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+           const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const BwdArgs a) {
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t base = smem_u32(dsm);
+    if (base & 1023u) {  // the swizzled tiles need a 1024-byte aligned window
+        if (tid == 0 && atomicCAS(&a.hdr->status.code, 0, -1) == 0) a.hdr->status.where = 300;
+        return;
+    }
+    BwdShared& sh = *reinterpret_cast<BwdShared*>(dsm + kOffBar);
+    float* s_lse = reinterpret_cast<float*>(dsm + kOffStat);  // [2][128], LSE * log2(e)
+    float* s_D = s_lse + 256;                                 // [2][128]
+    const uint32_t sK = base + kOffK, sV = base + kOffV, sDS = base + kOffDS;
+
+    if (tid == 0) {
+        mbar_init(&sh.kv_full, 1);
+        mbar_init(&sh.kv_empty, 1);
+        for (int s = 0; s < 2; ++s) { mbar_init(&sh.q_full[s], 1); mbar_init(&sh.q_empty[s], 1); }
+        mbar_init(&sh.s_full, 1);
+        mbar_init(&sh.dp_full, 1);
+        mbar_init(&sh.p_ready, 128);
+        mbar_init(&sh.ds_ready, 128);
+        mbar_init(&sh.ds_free, 1);
+        mbar_init(&sh.dq_full, 1);
+        mbar_init(&sh.dq_free, 128);
+        mbar_init(&sh.dkdv_done, 1);
+        mbar_init(&sh.acc_free, 128);
+        mbar_init(&sh.drain, 1);
+        sh.abort_flag = 0;
+        sh.total = a.varlen ? a.hdr->total_units : a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN);
+        fence_mbar_init();
+    }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+        tma_prefetch_desc(&tdo);
+    }
+    if (warp == 0) {
+        tmem_alloc(&sh.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const WaitCtx wc{&sh.abort_flag, &a.hdr->status};
+    const uint32_t tmem = sh.tmem_base;
+    const int total = sh.total;
+    const int g = a.Hq / a.Hkv;
+    const float scale = a.scale_log2;
+
+    // Register split (launch 384 x 168 = 64512): key-row warpgroup 232 (a
+    // 128-float P row), dQ warpgroup keeps 168, loader/UMMA warpgroup 56:
+    // 128 * (232 + 168 + 56) = 58368.
+    if (warp >= 8) {
+        regs_dec<56>();
+        if (warp == 8) {
+            // ------------------------------------------------------------ loader
+            uint32_t jj = 0, uc = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok; u += gridDim.x) {
+                BUnit U;
+                if (!bwd_unit(a, total, u, U)) break;
+                if (lane == 0) ok = mbar_wait(&sh.kv_empty, (uc & 1) ^ 1, wc, kBSiteKvEmpty);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&sh.kv_full, 2 * kT32);
+                    for (int c = 0; c < 2; ++c) {
+                        tma_load_3d(sK + c * kBox, &tk, &sh.kv_full, c * 64, U.hk, U.tok0 + U.k * kTileN);
+                        tma_load_3d(sV + c * kBox, &tv, &sh.kv_full, c * 64, U.hk, U.tok0 + U.k * kTileN);
+                    }
+                }
+                const int span = U.nq - U.i0;
+                for (int t = 0; t < U.n; ++t, ++jj) {
+                    const int st = jj & 1, h = U.hk * g + t / span, i = U.i0 + t % span;
+                    if (lane == 0) ok = mbar_wait(&sh.q_empty[st], ((jj >> 1) & 1) ^ 1, wc, kBSiteQEmpty);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int row = 4 * lane + e, q = i * kTileM + row;
+                        float l2 = 0.f, dd = 0.f;
+                        if (q < U.len) {
+                            const size_t li = a.varlen ? (size_t)h * a.T + U.tok0 + q
+                                                       : ((size_t)U.seq * a.Hq + h) * a.N + q;
+                            l2 = a.lse[li] * 1.4426950408889634f;
+                            dd = a.D[(size_t)h * a.T + U.tok0 + q];
+                        }
+                        s_lse[st * 128 + row] = l2;
+                        s_D[st * 128 + row] = dd;
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&sh.q_full[st], 2 * kT32);
+                        for (int c = 0; c < 2; ++c) {
+                            tma_load_3d(base + kOffQ + st * kT32 + c * kBox, &tq, &sh.q_full[st], c * 64, h,
+                                        U.tok0 + i * kTileM);
+                            tma_load_3d(base + kOffDO + st * kT32 + c * kBox, &tdo, &sh.q_full[st], c * 64, h,
+                                        U.tok0 + i * kTileM);
+                        }
+                    }
+                }
+                ++uc;
+            }
+            if (lane == 0) {  // drain this thread's copies before teardown
+                const uint64_t t0 = globaltimer_ns();
+                for (uint32_t d = (jj > 2 ? jj - 2 : 0); d < jj; ++d)
+                    while (!mbar_try_wait(smem_u32(&sh.q_full[d & 1]), (d >> 1) & 1) &&
+                           globaltimer_ns() - t0 < kWaitLimitNs) {}
+                if (uc > 0)
+                    while (!mbar_try_wait(smem_u32(&sh.kv_full), (uc - 1) & 1) &&
+                           globaltimer_ns() - t0 < kWaitLimitNs) {}
+            }
+            __syncwarp();
+        } else if (warp == 9) {
+            // ------------------------------------------------------- UMMA issuer
+            if (lane == 0) {
+                uint32_t jj = 0, uc = 0;
+                bool ok = true;
+                for (int u = blockIdx.x; ok; u += gridDim.x) {
+                    BUnit U;
+                    if (!bwd_unit(a, total, u, U)) break;
+                    if (!(ok = mbar_wait(&sh.kv_full, uc & 1, wc, kBSiteKvFull))) break;
+                    if (!(ok = mbar_wait(&sh.acc_free, (uc & 1) ^ 1, wc, kBSiteAcc))) break;
+                    if (!(ok = mbar_wait(&sh.q_full[jj & 1], (jj >> 1) & 1, wc, kBSiteQFull))) break;
+                    tc_fence_after();
+                    mma_kk(tmem + kColR0, sK, base + kOffQ + (jj & 1) * kT32);
+                    umma_commit(&sh.s_full);
+                    if (jj > 0) {
+                        if (!(ok = mbar_wait(&sh.dq_free, (jj - 1) & 1, wc, kBSiteDqFree))) break;
+                        tc_fence_after();
+                    }
+                    mma_kk(tmem + kColR1, sV, base + kOffDO + (jj & 1) * kT32);
+                    umma_commit(&sh.dp_full);
+                    for (int t = 0; t < U.n; ++t, ++jj) {
+                        const uint32_t st = jj & 1, st2 = (jj + 1) & 1;
+                        const bool more = t + 1 < U.n;
+                        if (!(ok = mbar_wait(&sh.p_ready, jj & 1, wc, kBSiteP))) break;
+                        tc_fence_after();
+                        mma_tn(tmem + kColDV, tmem + kColR0, base + kOffDO + st * kT32, t > 0);
+                        if (!(ok = mbar_wait(&sh.ds_ready, jj & 1, wc, kBSiteDs))) break;
+                        tc_fence_after();
+                        mma_kn(tmem + kColDK, sDS, base + kOffQ + st * kT32, t > 0);
+                        if (more) {
+                            if (!(ok = mbar_wait(&sh.q_full[st2], ((jj + 1) >> 1) & 1, wc, kBSiteQFull))) break;
+                            tc_fence_after();
+                            mma_kk(tmem + kColR0, sK, base + kOffQ + st2 * kT32);
+                            umma_commit(&sh.s_full);
+                        }
+                        mma_nn(tmem + kColR1, sDS, sK);
+                        umma_commit(&sh.dq_full);
+                        umma_commit(&sh.ds_free);
+                        umma_commit(&sh.q_empty[st]);
+                        if (more) {
+                            if (!(ok = mbar_wait(&sh.dq_free, jj & 1, wc, kBSiteDqFree))) break;
+                            tc_fence_after();
+                            mma_kk(tmem + kColR1, sV, base + kOffDO + st2 * kT32);
+                            umma_commit(&sh.dp_full);
+                        }
+                    }
+                    umma_commit(&sh.dkdv_done);
+                    umma_commit(&sh.kv_empty);
+                    ++uc;
+                }
+                umma_commit(&sh.drain);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(smem_u32(&sh.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+            }
+            __syncwarp();
+        }
+    } else if (warp < 4) {
+        regs_inc<232>();
+        // ------------------------------------------------ P^T and dS^T (key rows)
+        const int r = tid;                                   // key row in the tile == TMEM lane
+        const uint32_t lb = (uint32_t)(warp * 32) << 16;
+        const uint32_t tR0 = tmem + lb + kColR0, tR1 = tmem + lb + kColR1;
+        uint8_t* ds_row = dsm + kOffDS + r * 128;
+        const int sw = r & 7;
+        uint32_t jj = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok; u += gridDim.x) {
+            BUnit U;
+            if (!bwd_unit(a, total, u, U)) break;
+            const int key = U.k * kTileN + r;
+            const int span = U.nq - U.i0;
+            for (int t = 0; t < U.n; ++t, ++jj) {
+                const int st = jj & 1, i = U.i0 + t % span;
+                if (!(ok = mbar_wait(&sh.q_full[st], (jj >> 1) & 1, wc, kBSiteQFull))) break;
+                if (!(ok = mbar_wait(&sh.s_full, jj & 1, wc, kBSiteS))) break;
+                tc_fence_after();
+                float p[128];
+                {
+                    uint32_t* pu = reinterpret_cast<uint32_t*>(p);
+                    tmem_ld32(tR0 + 0, *reinterpret_cast<uint32_t(*)[32]>(pu + 0));
+                    tmem_ld32(tR0 + 32, *reinterpret_cast<uint32_t(*)[32]>(pu + 32));
+                    tmem_ld32(tR0 + 64, *reinterpret_cast<uint32_t(*)[32]>(pu + 64));
+                    tmem_ld32(tR0 + 96, *reinterpret_cast<uint32_t(*)[32]>(pu + 96));
+                    tmem_wait_ld();
+                }
+                // visible columns c: query 128 i + c < len, key < len, and key <= query if causal
+                int c_lo = a.causal ? key - i * kTileM : 0;
+                int c_hi = U.len - i * kTileM;
+                if (key >= U.len) c_hi = 0;
+                const float4* l2v = reinterpret_cast<const float4*>(s_lse + st * 128);
+#pragma unroll
+                for (int c4 = 0; c4 < 32; ++c4) {
+                    const float4 l4 = l2v[c4];
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = 4 * c4 + e;
+                        const float pe = ex2_mufu(fmaf(p[c], scale, -lv[e]));
+                        p[c] = (c >= c_lo && c < c_hi) ? pe : 0.f;
+                    }
+                }
+#pragma unroll
+                for (int stg = 0; stg < 4; ++stg) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) pk[m] = pack_bf16x2(p[stg * 32 + 2 * m], p[stg * 32 + 2 * m + 1]);
+                    tmem_st16(tR0 + stg * 16, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&sh.p_ready);
+
+                if (!(ok = mbar_wait(&sh.dp_full, jj & 1, wc, kBSiteDp))) break;
+                if (!(ok = mbar_wait(&sh.ds_free, (jj & 1) ^ 1, wc, kBSiteDsFree))) break;
+                tc_fence_after();
+                const float4* dv4 = reinterpret_cast<const float4*>(s_D + st * 128);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t dp[32];
+                    tmem_ld32(tR1 + cc * 32, dp);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        const float4 d4 = dv4[cc * 8 + m];
+                        const int c = cc * 32 + 4 * m;
+                        pk[2 * m] = pack_bf16x2(p[c] * (__uint_as_float(dp[4 * m]) - d4.x),
+                                                p[c + 1] * (__uint_as_float(dp[4 * m + 1]) - d4.y));
+                        pk[2 * m + 1] = pack_bf16x2(p[c + 2] * (__uint_as_float(dp[4 * m + 2]) - d4.z),
+                                                    p[c + 3] * (__uint_as_float(dp[4 * m + 3]) - d4.w));
+                    }
+                    // 32 queries = four 16-byte chunks; chunk q of the row holds
+                    // queries 8q..8q+7: box q/8, position (q%8) ^ (row%8).
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const int q = cc * 4 + m;
+                        *reinterpret_cast<uint4*>(ds_row + (q >> 3) * kBox + (((q & 7) ^ sw) << 4)) =
+                            make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
+                    }
+                }
+                fence_async_smem();
+                tc_fence_before();
+                mbar_arrive(&sh.ds_ready);
+            }
+        }
+    } else {
+        // -------------------------------------------- dQ drain, dK/dV epilogue
+        const int r = tid - 128;                             // query row (dQ) / key row (dK, dV)
+        const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tR1 = tmem + lb + kColR1;
+        uint32_t jj = 0, uc = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok; u += gridDim.x) {
+            BUnit U;
+            if (!bwd_unit(a, total, u, U)) break;
+            const int span = U.nq - U.i0;
+            for (int t = 0; t < U.n; ++t, ++jj) {
+                const int h = U.hk * g + t / span, i = U.i0 + t % span;
+                const int row = i * kTileM + r;
+                ok = mbar_wait(&sh.dq_full, jj & 1, wc, kBSiteDq);
+                // Deterministic mode uses named barriers below: every thread of
+                // the warpgroup must take the same path, so agree on aborts.
+                if (a.deterministic) ok = !named_bar_or(1, 128, !ok);
+                if (!ok) break;
+                tc_fence_after();
+                int* sem = a.deterministic ? a.sem + (size_t)h * a.sem_stride + U.seq + (U.tok0 + i * kTileM) / kTileN
+                                           : nullptr;
+                if (sem) {
+                    // Key tiles add into this query tile in ascending order;
+                    // wait (bounded) until the previous one has released it.
+                    bool gave_up = false;
+                    if (r == 0) {
+                        const uint64_t t0 = globaltimer_ns();
+                        uint32_t spins = 0;
+                        while (ld_acquire(sem) != U.k) {
+                            if ((++spins & 255u) == 0 &&
+                                (*(volatile int*)&sh.abort_flag || globaltimer_ns() - t0 > kWaitLimitNs)) {
+                                if (atomicCAS(&a.hdr->status.code, 0, kStatusTimeout) == 0) {
+                                    a.hdr->status.where = kBSiteSem;
+                                    a.hdr->status.block = blockIdx.x;
+                                }
+                                *(volatile int*)&sh.abort_flag = 1;
+                                gave_up = true;
+                                break;
+                            }
+                        }
+                    }
+                    if (named_bar_or(1, 128, gave_up)) { ok = false; break; }
+                }
+                float* dst = a.dqacc + ((size_t)h * a.T + U.tok0 + row) * kHeadDim;
+                const bool valid = row < U.len;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(tR1 + cc * 32, v);
+                    tmem_wait_ld();
+                    if (valid) {
+#pragma unroll
+                        for (int m = 0; m < 8; ++m)
+                            red_add_v4(dst + cc * 32 + 4 * m, __uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
+                                       __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&sh.dq_free);
+                if (sem) {
+                    __threadfence();
+                    named_bar(1, 128);
+                    if (r == 0) red_release_add(sem, 1);
+                }
+            }
+            if (!ok) break;
+            if (!(ok = mbar_wait(&sh.dkdv_done, uc & 1, wc, kBSiteDkdv))) break;
+            ++uc;
+            tc_fence_after();
+            const int key = U.k * kTileN + r;
+            const bool kvalid = key < U.len;
+            const size_t orow = ((size_t)(U.tok0 + key) * a.Hkv + U.hk) * kHeadDim;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t tacc = tmem + lb + (which ? kColDV : kColDK);
+                const float mul = which ? 1.f : a.alpha;
+                uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which ? a.dv : a.dk) + orow);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(tacc + cc * 32, v);
+                    tmem_wait_ld();
+                    if (kvalid) {
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const float* f = reinterpret_cast<const float*>(v + 8 * m);
+                            out[cc * 4 + m] = make_uint4(pack_bf16x2(f[0] * mul, f[1] * mul), pack_bf16x2(f[2] * mul, f[3] * mul),
+                                                         pack_bf16x2(f[4] * mul, f[5] * mul), pack_bf16x2(f[6] * mul, f[7] * mul));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&sh.acc_free);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+__global__ void bwd_reset_status_kernel(BwdHeader* hdr) {
+    hdr->status.code = 0;
+    hdr->status.where = 0;
+    hdr->status.block = 0;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdLaunch& L, int stages, cudaStream_t stream) {
+    const BwdArgs& a = L.a;
+    const int ew_grid = L.num_sms * 8;
+    if (stages & 1) {
+        bwd_reset_status_kernel<<<1, 1, 0, stream>>>(a.hdr);
+        bwd_pre_kernel<<<ew_grid, 256, 0, stream>>>(a);
+        if (a.varlen) bwd_plan_kernel<<<1, 1024, 0, stream>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (stages & 2) {
+        cudaError_t e0 = cudaFuncSetAttribute(bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdSmem);
+        if (e0 != cudaSuccess) return e0;
+        long long units = a.varlen ? (long long)a.Hkv * ((a.T + kTileN - 1) / kTileN + a.B)
+                                   : (long long)a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN);
+        int grid = (int)(units < L.num_sms ? units : L.num_sms);
+        if (grid < 1) grid = 1;
+        bwd_kernel<<<grid, kBwdThreads, kBwdSmem, stream>>>(L.tq, L.tk, L.tv, L.tdo, a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (stages & 4) {
+        bwd_post_kernel<<<ew_grid, 256, 0, stream>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace fa

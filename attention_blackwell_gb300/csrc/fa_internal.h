@@ -38,6 +38,71 @@ struct FwdLaunch {
     int num_sms;
 };
 
+// ---------------------------------------------------------------- backward
+//
+// Workspace layout (caller-allocated, sized by fa_bwd_workspace_size):
+//   [0, 256)           BwdHeader (status word, unit count)
+//   D                  float [Hq][T]            rowsum(dO * O)
+//   dQacc              float [Hq][T][128]       fp32 dQ accumulator
+//   semaphores         int   [Hq][T/128 + B + 1] (deterministic mode)
+//   units              int4  [Hkv * (T/128 + B)] (varlen work list)
+// T = B*N for fixed length, the packed token count for varlen.
+struct BwdHeader {
+    DevStatus status;
+    int total_units;   // varlen: written by the plan kernel
+    int pad[59];
+};
+
+struct WsLayout {
+    size_t d_off, dq_off, sem_off, unit_off, total;
+    long long sem_stride;  // semaphores per query head
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+inline WsLayout ws_layout(long long T, int B, int Hq, int deterministic, int varlen) {
+    WsLayout w;
+    const long long tiles = (T + kTileN - 1) / kTileN;
+    w.sem_stride = tiles + B + 1;
+    w.d_off = align256(sizeof(BwdHeader));
+    w.dq_off = align256(w.d_off + (size_t)Hq * T * 4);
+    w.sem_off = align256(w.dq_off + (size_t)Hq * T * kHeadDim * 4);
+    w.unit_off = align256(w.sem_off + (deterministic ? (size_t)Hq * w.sem_stride * 4 : 0));
+    w.total = align256(w.unit_off + (varlen ? (size_t)Hq * (tiles + B) * 16 : 0));
+    return w;
+}
+
+struct BwdArgs {
+    const void* o;           // bf16 [T, Hq, 128] (forward output)
+    const void* dO;          // bf16 [T, Hq, 128]
+    const float* lse;        // forward LSE: [B, Hq, N] or varlen [Hq, T]
+    void* dq;                // bf16 [T, Hq, 128]
+    void* dk;                // bf16 [T, Hkv, 128]
+    void* dv;                // bf16 [T, Hkv, 128]
+    const int* cu_seqlens;   // device int32[B+1] or nullptr
+    BwdHeader* hdr;
+    float* D;
+    float* dqacc;
+    int* sem;
+    int4* units;
+    long long sem_stride;
+    int B, Hq, Hkv;
+    int N;                   // fixed: sequence length; varlen: T
+    long long T;
+    int causal, varlen, deterministic, max_seqlen;
+    float alpha, scale_log2;
+};
+
+struct BwdLaunch {
+    CUtensorMap tq, tk, tv, tdo;
+    BwdArgs a;
+    int num_sms;
+};
+
+// Backward stages (fa_bwd.cu): 1 = preprocess (D, zero dQacc/semaphores,
+// varlen plan), 2 = main kernel (dK, dV, dQacc), 4 = dQ postprocess.
+cudaError_t launch_bwd(const BwdLaunch& L, int stages, cudaStream_t stream);
+
 // Launch the forward kernel (fa_fwd.cu).  Returns a cudaError_t.
 cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream);
 

@@ -195,10 +195,12 @@ def build_step(fa, w, dev_t, has_bwd):
            W.attention_flops(w.Hq, [w.N] * w.B, w.causal), 1)]
     if has_bwd:
         do, dq, dk, dv, ws = dev_t["do"], dev_t["dq"], dev_t["dk"], dev_t["dv"], dev_t["ws"]
-        ks.append(("bwd_pre", lambda: fa.bwd_preprocess(o, do, lse, ws, causal=w.causal), 0.0, 1))
-        ks.append(("bwd", lambda: fa.bwd_main(q, k, v, do, ws, dk=dk, dv=dv, causal=w.causal),
-                   W.attention_flops(w.Hq, [w.N] * w.B, w.causal, backward=True), 1))
-        ks.append(("bwd_post", lambda: fa.bwd_postprocess(ws, dq, causal=w.causal), 0.0, 1))
+        def stage(s):
+            return lambda: fa.bwd(q, k, v, o, lse, do, causal=w.causal, workspace=ws, dq=dq, dk=dk, dv=dv, stages=s)
+        pre_launches = 2  # status reset + preprocess (fixed length: no varlen plan)
+        ks.append(("bwd_pre", stage(1), 0.0, pre_launches))
+        ks.append(("bwd", stage(2), W.attention_flops(w.Hq, [w.N] * w.B, w.causal, backward=True), 1))
+        ks.append(("bwd_post", stage(4), 0.0, 1))
     return ks
 
 
@@ -212,7 +214,7 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = W.WORKLOADS[WORKLOAD]
-    has_bwd = hasattr(fa, "bwd_main") and not args.no_bwd
+    has_bwd = hasattr(fa, "bwd") and not args.no_bwd
     inp = W.make_inputs(w, with_grad=True)
     t = {n: inp[n].to(dev) for n in ("q", "k", "v", "do")}
     t["o"] = torch.empty_like(t["q"])
@@ -234,7 +236,7 @@ def run_ours(args, rank, world):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
-    if fa.device_status() != 0:
+    if fa.device_status(t.get("ws")) != 0:
         raise RuntimeError("device status reported a timeout during warm-up")
 
     K = args.steps
@@ -256,7 +258,7 @@ def run_ours(args, rank, world):
     barrier(world)
     if clocks:
         clocks.stop()
-    if fa.device_status() != 0:
+    if fa.device_status(t.get("ws")) != 0:
         raise RuntimeError("device status reported a timeout in the timed region")
     ms_local = t_start.elapsed_time(t_end)
     ms = max_over_ranks(ms_local, world, dev)

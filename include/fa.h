@@ -94,6 +94,48 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            const int *cu_seqlens, int max_seqlen, cudaStream_t stream);
 
 /*
+ * Bytes of device workspace fa_bwd needs (the library allocates none):
+ * D (rowsum(dO*O), fp32), the fp32 dQ accumulator, the deterministic-mode
+ * semaphores and the varlen work list.  N is the sequence length (fixed
+ * length) or the total token count T (varlen = 1).  Returns 0 for invalid
+ * sizes.  About 516 * Hq * T bytes.
+ */
+size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, int deterministic, int varlen);
+
+/*
+ * Backward: dQ, dK, dV of exact attention (FlashAttention-4 blog, "Backward
+ * pass", "Deterministic mode").  Inputs q, k, v, the forward's o and lse,
+ * and the upstream gradient dout (layouts as in fa_fwd); outputs dq like q,
+ * dk and dv like k (bf16; for Hkv < Hq, dk/dv sum over the query heads of
+ * each group).  deterministic = 1 adds dQ contributions in a fixed order
+ * (bit-identical across runs); 0 uses unordered fp32 reductions.
+ * workspace: device memory of at least fa_bwd_workspace_size(...) bytes,
+ * 256-byte aligned, owned by the caller; its contents need no
+ * initialisation and are overwritten.  Calls that share a workspace must not
+ * overlap on the GPU.
+ * Errors: as fa_fwd, plus FA_ERR_WORKSPACE (NULL, misaligned or too small)
+ * and FA_ERR_UNSUPPORTED (varlen with max_seqlen > 131072 or B > 1024).
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dout, void *dq, void *dk, void *dv,
+           int B, int Hq, int Hkv, int N, int d, float alpha, int causal,
+           const int *cu_seqlens, int max_seqlen, int deterministic,
+           void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * fa_bwd split into its three launches, for callers that time or schedule
+ * them separately: stages is a bit mask, 1 = preprocess (D, zero the dQ
+ * accumulator and semaphores, varlen work list), 2 = main kernel (dK, dV and
+ * the dQ accumulator), 4 = dQ postprocess (dq = bf16(alpha * accumulator)).
+ * Stages must run in this order on one workspace; fa_bwd == stages 7.
+ */
+int fa_bwd_stages(int stages, const void *q, const void *k, const void *v, const void *o,
+                  const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                  int B, int Hq, int Hkv, int N, int d, float alpha, int causal,
+                  const int *cu_seqlens, int max_seqlen, int deterministic,
+                  void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Reads (and clears) the library's device status word on the current
  * device after synchronising `stream`: FA_OK, or FA_ERR_TIMEOUT when a
  * kernel's bounded wait gave up (the kernel then skipped its remaining work,

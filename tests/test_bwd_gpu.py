@@ -1,0 +1,138 @@
+"""Backward parity: dQ, dK, dV from the CUDA path (C ABI) vs the fp64 oracle.
+
+Tolerance (stated for the backward): for each of dQ, dK, dV,
+max |err| <= 2e-2 * max |grad_oracle|.  The kernel consumes the GPU
+forward's own O and LSE, as in real use; the oracle recomputes everything
+from Q, K, V in float64.  Deterministic mode must be bit-identical across 10
+runs.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from attention_blackwell_gb300 import workloads as W
+from oracle import attention as A
+
+pytestmark = pytest.mark.gpu
+
+REL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import attention_blackwell_gb300 as fa
+    fa.lib()
+    fa.set_tuning(0, 8.0)
+    return fa
+
+
+def inputs(B, N, Hq, Hkv, seed=0, lengths=None, q_std=1.0):
+    if lengths is not None:
+        cu = W.cu_seqlens_of(lengths)
+        T = int(cu[-1])
+        sq, sk = (T, Hq, 128), (T, Hkv, 128)
+    else:
+        cu, lengths = None, [N] * B
+        sq, sk = (B, N, Hq, 128), (B, N, Hkv, 128)
+    return {"q": W.normal_bf16(sq, seed, q_std), "k": W.normal_bf16(sk, seed + 1), "v": W.normal_bf16(sk, seed + 2),
+            "do": W.normal_bf16(sq, seed + 3), "cu_seqlens": cu, "lengths": lengths}
+
+
+def gpu_grads(fa, inp, causal, deterministic=False, repeats=1):
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    cu = inp["cu_seqlens"].cuda() if inp["cu_seqlens"] is not None else None
+    ms = max(inp["lengths"]) if cu is not None else None
+    o, lse = fa.fwd(q, k, v, causal=causal, cu_seqlens=cu, max_seqlen=ms)
+    B, Hq = len(inp["lengths"]), q.shape[-2]
+    N = q.shape[0] if cu is not None else q.shape[1]
+    ws = fa.bwd_workspace(B, Hq, N, deterministic, cu is not None)
+    outs = []
+    for _ in range(repeats):
+        dq, dk, dv = fa.bwd(q, k, v, o, lse, do, causal=causal, cu_seqlens=cu, max_seqlen=ms,
+                            deterministic=deterministic, workspace=ws)
+        assert fa.device_status(ws) == 0
+        outs.append(tuple(t.float().cpu().numpy() for t in (dq, dk, dv)))
+    return outs
+
+
+def check(got, ref):
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        scale = np.abs(r).max()
+        err = np.abs(g - r).max()
+        assert np.isfinite(g).all(), name
+        assert err <= REL * scale, (name, err, scale)
+
+
+def oracle(inp, causal):
+    return A.backward(inp["q"], inp["k"], inp["v"], inp["do"], 1 / math.sqrt(128), causal,
+                      cu_seqlens=inp["cu_seqlens"])
+
+
+@pytest.mark.parametrize("N", [128, 200, 256, 513])
+@pytest.mark.parametrize("causal", [False, True])
+def test_small(fa, N, causal):
+    inp = inputs(2, N, 2, 2, seed=N)
+    check(gpu_grads(fa, inp, causal)[0], oracle(inp, causal))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (8, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_heads(fa, Hq, Hkv, causal):
+    inp = inputs(1, 300, Hq, Hkv, seed=5)
+    check(gpu_grads(fa, inp, causal)[0], oracle(inp, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen(fa, causal):
+    inp = inputs(0, 0, 4, 2, seed=9, lengths=[130, 1, 0, 300, 64, 257])
+    check(gpu_grads(fa, inp, causal)[0], oracle(inp, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_deterministic_small(fa, causal):
+    inp = inputs(2, 640, 4, 2, seed=13)
+    runs = gpu_grads(fa, inp, causal, deterministic=True, repeats=10)
+    for r in runs[1:]:
+        for a, b in zip(runs[0], r):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    check(runs[0], oracle(inp, causal))
+
+
+def test_large_q_logits(fa):
+    inp = inputs(1, 384, 2, 2, seed=17, q_std=3.0)
+    check(gpu_grads(fa, inp, True)[0], oracle(inp, True))
+
+
+# --------------------------------------------- full-size causal backward
+
+@pytest.fixture(scope="module")
+def full(fa):
+    w = W.WORKLOADS["causal_bwd"]
+    inp = W.make_inputs(w)
+    atomic = gpu_grads(fa, inp, True, deterministic=False)[0]
+    det = gpu_grads(fa, inp, True, deterministic=True, repeats=10)
+    return w, inp, atomic, det
+
+
+def _head_ref(inp, w, b, h):
+    q, k, v, do = (inp[n][b, :, h].float().numpy().astype(np.float64) for n in ("q", "k", "v", "do"))
+    return A.head_backward(q, k, v, do, w.alpha, True)
+
+
+@pytest.mark.parametrize("b,h", [(0, 0), (1, 15)])
+def test_full_size_atomic_and_deterministic(full, b, h):
+    w, inp, atomic, det = full
+    ref = _head_ref(inp, w, b, h)
+    for got in (atomic, det[0]):
+        check([g[b, :, h] for g in got], ref)
+
+
+def test_full_size_deterministic_bit_identical(full):
+    _, _, atomic, det = full
+    for r in det[1:]:
+        for a, b in zip(det[0], r):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    for a, b in zip(det[0], atomic):  # the two modes agree up to summation order
+        assert np.abs(a - b).max() <= 1e-2 * max(np.abs(b).max(), 1e-6)
