@@ -136,6 +136,35 @@ int fa_bwd_stages(int stages, const void *q, const void *k, const void *v, const
                   void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * fa_bwd without a workspace argument, for callers that cannot allocate
+ * device memory when they need gradients (for example code running under a
+ * framework that owns every device allocation, or a plugin whose host
+ * application forbids allocation after start-up).  The FlashAttention-4 pages
+ * have no counterpart: this is a library convenience.
+ *
+ * It computes exactly what fa_bwd computes (same arguments, minus the
+ * workspace) and allocates nothing: its scratch is a 64 MiB array of static
+ * device storage inside the library, reserved on every GPU that loads the
+ * library until the process exits.  Sizes whose workspace
+ * (fa_bwd_workspace_size) exceeds 64 MiB -- about Hq * T > 130000 -- are
+ * rejected with FA_ERR_WORKSPACE before anything is launched; other errors
+ * as fa_bwd.
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * - All calls on a device share the one scratch array, which keeps the last
+ *   call's contents (each call re-zeroes what must start at zero).  Calls
+ *   that overlap on the GPU (different streams, or concurrent host threads)
+ *   race on it and produce wrong gradients: serialise them.
+ * - A device-side wait timeout is recorded in the scratch area's own status
+ *   word, which callers cannot read; fa_get_device_status does not see it.
+ */
+int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                   const void *dout, void *dq, void *dk, void *dv,
+                   int B, int Hq, int Hkv, int N, int d, float alpha, int causal,
+                   const int *cu_seqlens, int max_seqlen, int deterministic, cudaStream_t stream);
+
+/*
  * Reads (and clears) the library's device status word on the current
  * device after synchronising `stream`: FA_OK, or FA_ERR_TIMEOUT when a
  * kernel's bounded wait gave up (the kernel then skipped its remaining work,
