@@ -40,10 +40,12 @@ WORKLOAD = "large"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-bwd", action="store_true", help="time the forward only")
+    ap.add_argument("--workload", default=WORKLOAD, help="large (default), tiny, causal, varlen, causal_bwd")
+    ap.add_argument("--deterministic", action="store_true", help="backward in deterministic mode")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
     return ap.parse_args()
@@ -157,49 +159,60 @@ def kernel_traffic(name):
     return rec["dram_bytes_per_launch"] if sha == rec["source_sha"] else None
 
 
-def cpu_baseline(w, inp, with_bwd, budget_s):
-    """The float64 oracle, as it stands, on whole (batch, head) slices of the
-    same workload until ``budget_s`` seconds have been spent (at least one)."""
+def _slice(inp, w, b):
+    """Rows of sequence b: (q, k, v, do) float64 arrays [L, H, d]."""
     import numpy as np
+    cu = inp["cu_seqlens"]
+    out = []
+    for n in ("q", "k", "v", "do"):
+        t = inp[n]
+        t = t[b] if cu is None else t[int(cu[b]):int(cu[b + 1])]
+        out.append(t.float().numpy().astype(np.float64))
+    return out
 
+
+def cpu_baseline(w, inp, with_bwd, budget_s):
+    """The float64 oracle, as it stands, on whole (sequence, head) slices of
+    the same workload until ``budget_s`` seconds have been spent (at least one)."""
     from attention_blackwell_gb300 import workloads as W
     from oracle import attention as A
 
-    q = inp["q"].float().numpy().astype(np.float64)
-    k = inp["k"].float().numpy().astype(np.float64)
-    v = inp["v"].float().numpy().astype(np.float64)
-    do = inp["do"].float().numpy().astype(np.float64) if with_bwd else None
     g = w.Hq // w.Hkv
     done, flops, t0 = 0, 0.0, time.perf_counter()
     while True:
         b, h = divmod(done % (w.B * w.Hq), w.Hq)
-        A.head_forward(q[b, :, h], k[b, :, h // g], v[b, :, h // g], w.alpha, w.causal)
-        flops += W.attention_flops(1, [w.N], w.causal)
+        q, k, v, do = _slice(inp, w, b)
+        L = q.shape[0]
+        A.head_forward(q[:, h], k[:, h // g], v[:, h // g], w.alpha, w.causal)
+        flops += W.attention_flops(1, [L], w.causal)
         if with_bwd:
-            A.head_backward(q[b, :, h], k[b, :, h // g], v[b, :, h // g], do[b, :, h], w.alpha, w.causal)
-            flops += W.attention_flops(1, [w.N], w.causal, backward=True)
+            A.head_backward(q[:, h], k[:, h // g], v[:, h // g], do[:, h], w.alpha, w.causal)
+            flops += W.attention_flops(1, [L], w.causal, backward=True)
         done += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": "%d of %d (batch, head) slices of the %s workload, %s, float64 NumPy, %.1f s"
-                      % (done, w.B * w.Hq, w.name, "forward+backward" if with_bwd else "forward", dt)}
+            "sample": "%d (sequence, head) slices of the %s workload (%d in total), %s, float64 NumPy, %.1f s"
+                      % (done, w.name, w.B * w.Hq, "forward+backward" if with_bwd else "forward", dt)}
 
 
-def build_step(fa, w, dev_t, has_bwd):
+def build_step(fa, w, dev_t, has_bwd, deterministic):
     """[(name, launch callable, credited FLOPs, launches)] for one step."""
     from attention_blackwell_gb300 import workloads as W
     q, k, v, o, lse = dev_t["q"], dev_t["k"], dev_t["v"], dev_t["o"], dev_t["lse"]
-    ks = [("fwd", lambda: fa.fwd(q, k, v, causal=w.causal, out=o, lse=lse),
-           W.attention_flops(w.Hq, [w.N] * w.B, w.causal), 1)]
+    cu, ms, lens = dev_t["cu"], dev_t["max_seqlen"], dev_t["lengths"]
+    ks = [("fwd", lambda: fa.fwd(q, k, v, causal=w.causal, cu_seqlens=cu, max_seqlen=ms, out=o, lse=lse),
+           W.attention_flops(w.Hq, lens, w.causal), 1)]
     if has_bwd:
         do, dq, dk, dv, ws = dev_t["do"], dev_t["dq"], dev_t["dk"], dev_t["dv"], dev_t["ws"]
+
         def stage(s):
-            return lambda: fa.bwd(q, k, v, o, lse, do, causal=w.causal, workspace=ws, dq=dq, dk=dk, dv=dv, stages=s)
-        pre_launches = 2  # status reset + preprocess (fixed length: no varlen plan)
-        ks.append(("bwd_pre", stage(1), 0.0, pre_launches))
-        ks.append(("bwd", stage(2), W.attention_flops(w.Hq, [w.N] * w.B, w.causal, backward=True), 1))
+            return lambda: fa.bwd(q, k, v, o, lse, do, causal=w.causal, cu_seqlens=cu, max_seqlen=ms,
+                                  deterministic=deterministic, workspace=ws, dq=dq, dk=dk, dv=dv, stages=s)
+        # status reset + preprocess (+ the varlen work-list plan)
+        ks.append(("bwd_pre", stage(1), 0.0, 2 + (cu is not None)))
+        ks.append(("bwd", stage(2), W.attention_flops(w.Hq, lens, w.causal, backward=True), 1))
         ks.append(("bwd_post", stage(4), 0.0, 1))
     return ks
 
@@ -213,16 +226,25 @@ def run_ours(args, rank, world):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = W.WORKLOADS[WORKLOAD]
+    w = W.WORKLOADS[args.workload]
     has_bwd = hasattr(fa, "bwd") and not args.no_bwd
     inp = W.make_inputs(w, with_grad=True)
     t = {n: inp[n].to(dev) for n in ("q", "k", "v", "do")}
     t["o"] = torch.empty_like(t["q"])
-    t["lse"] = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+    t["lengths"] = inp["lengths"]
+    if w.varlen:
+        t["cu"], t["max_seqlen"] = inp["cu_seqlens"].to(dev), max(inp["lengths"])
+        t["lse"] = torch.empty((w.Hq, inp["T"]), dtype=torch.float32, device=dev)
+        n_rows = inp["T"]
+    else:
+        t["cu"], t["max_seqlen"] = None, None
+        t["lse"] = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+        n_rows = w.N
     if has_bwd:
         t["dq"], t["dk"], t["dv"] = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
-        t["ws"] = fa.bwd_workspace(w.B, w.Hq, w.N, deterministic=False, device=dev)
-    kernels = build_step(fa, w, t, has_bwd)
+        t["ws"] = fa.bwd_workspace(w.B, w.Hq, n_rows, deterministic=args.deterministic, varlen=w.varlen,
+                                   device=dev)
+    kernels = build_step(fa, w, t, has_bwd, args.deterministic)
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
@@ -297,6 +319,13 @@ def run_ours(args, rank, world):
     return locals()
 
 
+def describe(w, inp):
+    head = "%s: B=%d Hq=%d Hkv=%d d=%d %s" % (w.name, w.B, w.Hq, w.Hkv, w.d, "causal" if w.causal else "non-causal")
+    if w.varlen:
+        return head + " varlen T=%d lengths U[%d,%d] seed %d" % (inp["T"], w.len_range[0], w.len_range[1], 4)
+    return head + " N=%d" % w.N
+
+
 def emit(line):
     print(json.dumps(line), flush=True)
 
@@ -329,11 +358,12 @@ def main_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "%s: B=%d Hq=%d Hkv=%d N=%d d=%d %s" % (
-            w.name, w.B, w.Hq, w.Hkv, w.N, w.d, "causal" if w.causal else "non-causal"),
-            "step": step_name, "global_batch": w.B * world, "seq_len": w.N,
+        "config": {"workload": describe(w, r["inp"]),
+            "step": step_name, "global_batch": w.B * world, "seq_len": w.N or max(r["inp"]["lengths"]),
+            "deterministic_bwd": bool(args.deterministic),
             "parallelism": "replicas" if world > 1 else "single",
-            "l2": "no flush: Q, K, V, dO are 64 MiB each (> 126 MB L2 together)"},
+            "l2": "no flush: the step's inputs (%.0f MiB) exceed the 126 MB L2" % (
+                sum(r["t"][n].numel() * 2 for n in ("q", "k", "v", "do")) / 2 ** 20)},
         "pct_of_2.25PF": round(100.0 * r["value"] / PEAK_NOMINAL_TFLOPS, 2),
         "breakdown": [{"kernel": p["kernel"], "avg_ms": round(p["avg_ms"], 4),
                        "tflops": round(p["flops"] / (p["avg_ms"] / 1e3) / 1e12, 1) if p["flops"] else None}
@@ -364,22 +394,20 @@ def main_reference(args):
     from attention_blackwell_gb300 import workloads as W
     from oracle import attention as A
 
-    w = W.WORKLOADS[WORKLOAD]
+    w = W.WORKLOADS[args.workload]
     with_bwd = not args.no_bwd
     inp = W.make_inputs(w, with_grad=True)
-    q = inp["q"].float().numpy().astype(np.float64)
-    k = inp["k"].float().numpy().astype(np.float64)
-    v = inp["v"].float().numpy().astype(np.float64)
-    do = inp["do"].float().numpy().astype(np.float64)
 
-    def step(s):  # one (batch, head) slice of the workload per step
+    def step(s):  # one (sequence, head) slice of the workload per step
         b, h = divmod(s % (w.B * w.Hq), w.Hq)
         hk = h // (w.Hq // w.Hkv)
-        A.head_forward(q[b, :, h], k[b, :, hk], v[b, :, hk], w.alpha, w.causal)
-        f = W.attention_flops(1, [w.N], w.causal)
+        q, k, v, do = _slice(inp, w, b)
+        L = q.shape[0]
+        A.head_forward(q[:, h], k[:, hk], v[:, hk], w.alpha, w.causal)
+        f = W.attention_flops(1, [L], w.causal)
         if with_bwd:
-            A.head_backward(q[b, :, h], k[b, :, hk], v[b, :, hk], do[b, :, h], w.alpha, w.causal)
-            f += W.attention_flops(1, [w.N], w.causal, backward=True)
+            A.head_backward(q[:, h], k[:, hk], v[:, hk], do[:, h], w.alpha, w.causal)
+            f += W.attention_flops(1, [L], w.causal, backward=True)
         return f
 
     for s in range(max(1, args.warmup)):
@@ -388,14 +416,12 @@ def main_reference(args):
     flops = sum(step(s) for s in range(args.steps))
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
-    sample = "one (batch, head) slice of the %s workload per step (%s), float64 NumPy" % (
+    sample = "one (sequence, head) slice of the %s workload per step (%s), float64 NumPy" % (
         w.name, "forward+backward" if with_bwd else "forward")
     emit({"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "TFLOP/s", "n_gpus": world,
           "steps": args.steps, "warmup": max(1, args.warmup), "ms_per_step": round(dt * 1e3 / args.steps, 2),
           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-          "config": {"workload": "%s: B=%d Hq=%d Hkv=%d N=%d d=%d %s" % (
-              w.name, w.B, w.Hq, w.Hkv, w.N, w.d, "causal" if w.causal else "non-causal"),
-              "step": "oracle slice"},
+          "config": {"workload": describe(w, inp), "step": "oracle slice"},
           "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                            "sample": sample},
           "e2e": {"value": round(value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}})
