@@ -218,7 +218,7 @@ __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a_smem, uint32_t b_s
 #pragma unroll 1
     for (uint32_t k = 0; k < 8; ++k) {
         const uint32_t off = ((k >> 2) * kBox + (k & 3) * 32) >> 4;
-        umma_ss(d, ad + off, bd + off, idesc, k > 0);
+        umma_ss_w(d, ad + off, bd + off, idesc, k > 0);
     }
 }
 
@@ -227,7 +227,7 @@ __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b_s
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
     const uint64_t bd = sdesc_sw128(b_smem, kBox, 1024);
 #pragma unroll 1
-    for (uint32_t k = 0; k < 8; ++k) umma_ts(d, a_tmem + k * 8, bd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
+    for (uint32_t k = 0; k < 8; ++k) umma_ts_w(d, a_tmem + k * 8, bd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
 }
 
 // D (+)= A B with A K-major and B MN-major in shared memory (dK += dS^T Q).
@@ -236,7 +236,7 @@ __device__ __forceinline__ void mma_kn(uint32_t d, uint32_t a_smem, uint32_t b_s
     const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, kBox, 1024);
 #pragma unroll 1
     for (uint32_t k = 0; k < 8; ++k)
-        umma_ss(d, ad + (((k >> 2) * kBox + (k & 3) * 32) >> 4), bd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
+        umma_ss_w(d, ad + (((k >> 2) * kBox + (k & 3) * 32) >> 4), bd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
 }
 
 // D = A B with A and B both MN-major in shared memory (dQ = dS K: dS^T is
@@ -245,7 +245,7 @@ __device__ __forceinline__ void mma_nn(uint32_t d, uint32_t a_smem, uint32_t b_s
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 1, 1);
     const uint64_t ad = sdesc_sw128(a_smem, kBox, 1024), bd = sdesc_sw128(b_smem, kBox, 1024);
 #pragma unroll 1
-    for (uint32_t k = 0; k < 8; ++k) umma_ss(d, ad + ((k * 2048) >> 4), bd + ((k * 2048) >> 4), idesc, k > 0);
+    for (uint32_t k = 0; k < 8; ++k) umma_ss_w(d, ad + ((k * 2048) >> 4), bd + ((k * 2048) >> 4), idesc, k > 0);
 }
 
 __device__ __forceinline__ void fence_async_smem() {
@@ -402,55 +402,55 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             __syncwarp();
         } else if (warp == 9) {
             // ------------------------------------------------------- UMMA issuer
-            if (lane == 0) {
+            {   // the whole warp runs the issue loop (see umma_ss_w)
                 uint32_t jj = 0, uc = 0;
                 bool ok = true;
                 for (int u = blockIdx.x; ok; u += gridDim.x) {
                     BUnit U;
                     if (!bwd_unit(a, total, u, U)) break;
-                    if (!(ok = mbar_wait(&sh.kv_full, uc & 1, wc, kBSiteKvFull))) break;
-                    if (!(ok = mbar_wait(&sh.acc_free, (uc & 1) ^ 1, wc, kBSiteAcc))) break;
-                    if (!(ok = mbar_wait(&sh.q_full[jj & 1], (jj >> 1) & 1, wc, kBSiteQFull))) break;
+                    if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, kBSiteKvFull))) break;
+                    if (!(ok = mbar_wait_w(&sh.acc_free, (uc & 1) ^ 1, wc, kBSiteAcc))) break;
+                    if (!(ok = mbar_wait_w(&sh.q_full[jj & 1], (jj >> 1) & 1, wc, kBSiteQFull))) break;
                     tc_fence_after();
                     mma_kk(tmem + kColR0, sK, base + kOffQ + (jj & 1) * kT32);
-                    umma_commit(&sh.s_full);
+                    umma_commit_w(&sh.s_full);
                     if (jj > 0) {
-                        if (!(ok = mbar_wait(&sh.dq_free, (jj - 1) & 1, wc, kBSiteDqFree))) break;
+                        if (!(ok = mbar_wait_w(&sh.dq_free, (jj - 1) & 1, wc, kBSiteDqFree))) break;
                         tc_fence_after();
                     }
                     mma_kk(tmem + kColR1, sV, base + kOffDO + (jj & 1) * kT32);
-                    umma_commit(&sh.dp_full);
+                    umma_commit_w(&sh.dp_full);
                     for (int t = 0; t < U.n; ++t, ++jj) {
                         const uint32_t st = jj & 1, st2 = (jj + 1) & 1;
                         const bool more = t + 1 < U.n;
-                        if (!(ok = mbar_wait(&sh.p_ready, jj & 1, wc, kBSiteP))) break;
+                        if (!(ok = mbar_wait_w(&sh.p_ready, jj & 1, wc, kBSiteP))) break;
                         tc_fence_after();
                         mma_tn(tmem + kColDV, tmem + kColR0, base + kOffDO + st * kT32, t > 0);
-                        if (!(ok = mbar_wait(&sh.ds_ready, jj & 1, wc, kBSiteDs))) break;
+                        if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, kBSiteDs))) break;
                         tc_fence_after();
                         mma_kn(tmem + kColDK, sDS, base + kOffQ + st * kT32, t > 0);
                         if (more) {
-                            if (!(ok = mbar_wait(&sh.q_full[st2], ((jj + 1) >> 1) & 1, wc, kBSiteQFull))) break;
+                            if (!(ok = mbar_wait_w(&sh.q_full[st2], ((jj + 1) >> 1) & 1, wc, kBSiteQFull))) break;
                             tc_fence_after();
                             mma_kk(tmem + kColR0, sK, base + kOffQ + st2 * kT32);
-                            umma_commit(&sh.s_full);
+                            umma_commit_w(&sh.s_full);
                         }
                         mma_nn(tmem + kColR1, sDS, sK);
-                        umma_commit(&sh.dq_full);
-                        umma_commit(&sh.ds_free);
-                        umma_commit(&sh.q_empty[st]);
+                        umma_commit_w(&sh.dq_full);
+                        umma_commit_w(&sh.ds_free);
+                        umma_commit_w(&sh.q_empty[st]);
                         if (more) {
-                            if (!(ok = mbar_wait(&sh.dq_free, jj & 1, wc, kBSiteDqFree))) break;
+                            if (!(ok = mbar_wait_w(&sh.dq_free, jj & 1, wc, kBSiteDqFree))) break;
                             tc_fence_after();
                             mma_kk(tmem + kColR1, sV, base + kOffDO + st2 * kT32);
-                            umma_commit(&sh.dp_full);
+                            umma_commit_w(&sh.dp_full);
                         }
                     }
-                    umma_commit(&sh.dkdv_done);
-                    umma_commit(&sh.kv_empty);
+                    umma_commit_w(&sh.dkdv_done);
+                    umma_commit_w(&sh.kv_empty);
                     ++uc;
                 }
-                umma_commit(&sh.drain);
+                umma_commit_w(&sh.drain);
                 const uint64_t t0 = globaltimer_ns();
                 while (!mbar_try_wait(smem_u32(&sh.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
             }

@@ -153,7 +153,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
 #pragma unroll 1
     for (uint32_t k = 0; k < 8; ++k) {
         const uint32_t off = ((k >> 2) * kBoxBytes + (k & 3) * 32) >> 4;  // 16-byte units
-        umma_ss(d_tmem, qd + off, kd + off, idesc, k > 0);
+        umma_ss_w(d_tmem, qd + off, kd + off, idesc, k > 0);
     }
 }
 
@@ -164,7 +164,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
     const uint64_t vd = sdesc_sw128(v_smem, kBoxBytes, 1024);
 #pragma unroll 1
     for (uint32_t k = 0; k < 8; ++k)
-        umma_ts(d_tmem, p_tmem + k * 8, vd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
+        umma_ts_w(d_tmem, p_tmem + k * 8, vd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
 }
 
 template <int kEmuEighths>
@@ -327,63 +327,63 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         __syncwarp();
       } else if (warp == 9) {
         // ------------------------------------------------------- UMMA issuer
-        if (lane == 0) {
+        {   // the whole warp runs the issue loop (see umma_ss_w)
             uint32_t it = 0, uc = 0, pc[2] = {0, 0};
             bool ok = true;
             for (int u = blockIdx.x; ok; u += gridDim.x) {
                 Unit U;
                 if (!sched.get(u, U)) break;
                 const int n0 = kv_tiles(U, 0, a.causal), n1 = kv_tiles(U, 1, a.causal);
-                if (!(ok = mbar_wait(&sh.q_full, uc & 1, wc, kSiteQFull))) break;
+                if (!(ok = mbar_wait_w(&sh.q_full, uc & 1, wc, kSiteQFull))) break;
                 tc_fence_after();
                 uint32_t slot_k = it % kStages;
-                if (!(ok = mbar_wait(&sh.full[slot_k], (it / kStages) & 1, wc, kSiteRingFull))) break;
+                if (!(ok = mbar_wait_w(&sh.full[slot_k], (it / kStages) & 1, wc, kSiteRingFull))) break;
                 tc_fence_after();
                 ++it;
                 issue_qk(tmem + col_s(0), sQ, sRing + slot_k * kTileBytes);
-                umma_commit(&sh.s_full[0]);
+                umma_commit_w(&sh.s_full[0]);
                 issue_qk(tmem + col_s(1), sQ + kTileBytes, sRing + slot_k * kTileBytes);
-                umma_commit(&sh.s_full[1]);
-                umma_commit(&sh.empty[slot_k]);
+                umma_commit_w(&sh.s_full[1]);
+                umma_commit_w(&sh.empty[slot_k]);
                 for (int j = 0; j < n1; ++j) {
                     const uint32_t slot_v = it % kStages;
-                    if (!(ok = mbar_wait(&sh.full[slot_v], (it / kStages) & 1, wc, kSiteRingFull))) break;
+                    if (!(ok = mbar_wait_w(&sh.full[slot_v], (it / kStages) & 1, wc, kSiteRingFull))) break;
                     ++it;
                     if (j < n0) {
-                        if (!(ok = mbar_wait(&sh.p_ready[0], pc[0] & 1, wc, kSiteP0))) break;
+                        if (!(ok = mbar_wait_w(&sh.p_ready[0], pc[0] & 1, wc, kSiteP0))) break;
                         ++pc[0];
                         tc_fence_after();
                         issue_pv(tmem + col_o(0), tmem + col_s(0), sRing + slot_v * kTileBytes, j > 0);
-                        if (j == n0 - 1) umma_commit(&sh.o_done[0]);
+                        if (j == n0 - 1) umma_commit_w(&sh.o_done[0]);
                     }
                     const bool more = j + 1 < n1;
                     if (more) {
                         slot_k = it % kStages;
-                        if (!(ok = mbar_wait(&sh.full[slot_k], (it / kStages) & 1, wc, kSiteRingFull))) break;
+                        if (!(ok = mbar_wait_w(&sh.full[slot_k], (it / kStages) & 1, wc, kSiteRingFull))) break;
                         ++it;
                         tc_fence_after();
                         if (j + 1 < n0) {
                             issue_qk(tmem + col_s(0), sQ, sRing + slot_k * kTileBytes);
-                            umma_commit(&sh.s_full[0]);
+                            umma_commit_w(&sh.s_full[0]);
                         }
                     }
-                    if (!(ok = mbar_wait(&sh.p_ready[1], pc[1] & 1, wc, kSiteP1))) break;
+                    if (!(ok = mbar_wait_w(&sh.p_ready[1], pc[1] & 1, wc, kSiteP1))) break;
                     ++pc[1];
                     tc_fence_after();
                     issue_pv(tmem + col_o(1), tmem + col_s(1), sRing + slot_v * kTileBytes, j > 0);
-                    umma_commit(&sh.empty[slot_v]);
-                    if (j == n1 - 1) umma_commit(&sh.o_done[1]);
+                    umma_commit_w(&sh.empty[slot_v]);
+                    if (j == n1 - 1) umma_commit_w(&sh.o_done[1]);
                     if (more) {
                         issue_qk(tmem + col_s(1), sQ + kTileBytes, sRing + slot_k * kTileBytes);
-                        umma_commit(&sh.s_full[1]);
-                        umma_commit(&sh.empty[slot_k]);
+                        umma_commit_w(&sh.s_full[1]);
+                        umma_commit_w(&sh.empty[slot_k]);
                     }
                 }
-                umma_commit(&sh.q_empty);
+                umma_commit_w(&sh.q_empty);
                 ++uc;
             }
             // Drain: all issued MMAs complete before tensor memory is freed.
-            umma_commit(&sh.drain);
+            umma_commit_w(&sh.drain);
             const uint32_t bar = smem_u32(&sh.drain);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(bar, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
