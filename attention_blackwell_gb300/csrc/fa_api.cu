@@ -82,6 +82,20 @@ int make_map(CUtensorMap* map, const void* ptr, int H, long long T) {
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_INVALID;
 }
 
+// fp32 accumulator [rows, 128] -> 2-D map {128, rows}, box {32, 128}, 128-B swizzle.
+int make_map_acc(CUtensorMap* map, const void* ptr, long long rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return FA_ERR_LAUNCH;
+    cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 4};
+    cuuint32_t box[2] = {32, (cuuint32_t)kTileM};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_INVALID;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -242,6 +256,7 @@ int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const
     if ((rc = make_map(&L.tv, v, Hkv, T)) != FA_OK) return rc;
     if ((rc = make_map(&L.tdo, dout, Hq, T)) != FA_OK) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if ((rc = make_map_acc(&L.tdq, ws + w.dq_off, (long long)Hq * T)) != FA_OK) return rc;
     BwdArgs& a = L.a;
     a.o = o;
     a.dO = dout;

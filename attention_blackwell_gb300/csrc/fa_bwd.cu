@@ -252,9 +252,16 @@ __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
+// TMA bulk tensor reduction: global[tile at (x, y)] += shared tile (fp32 add).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void named_bar(int id, int n) {
@@ -285,7 +292,8 @@ __device__ __forceinline__ void red_release_add(int* p, int v) {
 
 __global__ void __launch_bounds__(kBwdThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-           const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const BwdArgs a) {
+           const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+           const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
     extern __shared__ __align__(1024) uint8_t dsm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t base = smem_u32(dsm);
@@ -321,6 +329,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
         tma_prefetch_desc(&tdo);
+        tma_prefetch_desc(&tdq);
     }
     if (warp == 0) {
         tmem_alloc(&sh.tmem_base, 512);
@@ -429,15 +438,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, kBSiteDs))) break;
                         tc_fence_after();
                         mma_kn(tmem + kColDK, sDS, base + kOffQ + st * kT32, t > 0);
-                        if (more) {
+                        if (more) {  // Q/dO arrive by TMA: no tcgen05 fence needed
                             if (!(ok = mbar_wait_w(&sh.q_full[st2], ((jj + 1) >> 1) & 1, wc, kBSiteQFull))) break;
-                            tc_fence_after();
                             mma_kk(tmem + kColR0, sK, base + kOffQ + st2 * kT32);
                             umma_commit_w(&sh.s_full);
                         }
                         mma_nn(tmem + kColR1, sDS, sK);
                         umma_commit_w(&sh.dq_full);
-                        umma_commit_w(&sh.ds_free);
                         umma_commit_w(&sh.q_empty[st]);
                         if (more) {
                             if (!(ok = mbar_wait_w(&sh.dq_free, jj & 1, wc, kBSiteDqFree))) break;
@@ -560,11 +567,21 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 const int h = U.hk * g + t / span, i = U.i0 + t % span;
                 const int row = i * kTileM + r;
                 ok = mbar_wait(&sh.dq_full, jj & 1, wc, kBSiteDq);
-                // Deterministic mode uses named barriers below: every thread of
-                // the warpgroup must take the same path, so agree on aborts.
-                if (a.deterministic) ok = !named_bar_or(1, 128, !ok);
+                // Named barriers follow: every thread of the warpgroup must
+                // take the same path, so the warpgroup agrees on aborts.
+                ok = !named_bar_or(1, 128, !ok);
                 if (!ok) break;
                 tc_fence_after();
+                // dQ_i out of TMEM into registers; the columns are free for the
+                // next dP at once.
+                uint32_t v[128];
+                tmem_ld32(tR1 + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
+                tmem_ld32(tR1 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                tmem_ld32(tR1 + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
+                tmem_ld32(tR1 + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&sh.dq_free);
                 int* sem = a.deterministic ? a.sem + (size_t)h * a.sem_stride + U.seq + (U.tok0 + i * kTileM) / kTileN
                                            : nullptr;
                 if (sem) {
@@ -586,29 +603,47 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                                 break;
                             }
                         }
+                        fence_async_global();  // our bulk reduction follows the acquire
                     }
                     if (named_bar_or(1, 128, gave_up)) { ok = false; break; }
                 }
-                float* dst = a.dqacc + ((size_t)h * a.T + U.tok0 + row) * kHeadDim;
-                const bool valid = row < U.len;
+                // Add dQ_i into the fp32 accumulator with TMA bulk tensor
+                // reductions of whole 128-byte lines.  The staging area is the
+                // dS buffer (dQ_i complete implies dK_i and dQ_i have read dS_i):
+                // two rounds of two 32-column boxes (128 rows x 128 B, swizzled
+                // like a 128-B TMA box).  Rows past the sequence end hold exact
+                // zeros (their P, hence dS, is zero), so adding them to the
+                // neighbouring rows changes nothing.
+                const int grow = h * (int)a.T + U.tok0 + i * kTileM;
+                uint8_t* stage_row = dsm + kOffDS + r * 128;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld32(tR1 + cc * 32, v);
-                    tmem_wait_ld();
-                    if (valid) {
+                for (int half = 0; half < 2; ++half) {
 #pragma unroll
-                        for (int m = 0; m < 8; ++m)
-                            red_add_v4(dst + cc * 32 + 4 * m, __uint_as_float(v[4 * m]), __uint_as_float(v[4 * m + 1]),
-                                       __uint_as_float(v[4 * m + 2]), __uint_as_float(v[4 * m + 3]));
+                    for (int b = 0; b < 2; ++b) {
+                        const uint32_t* src = v + half * 64 + b * 32;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            *reinterpret_cast<uint4*>(stage_row + b * kBox + ((q ^ (r & 7)) << 4)) =
+                                make_uint4(src[4 * q], src[4 * q + 1], src[4 * q + 2], src[4 * q + 3]);
                     }
-                }
-                tc_fence_before();
-                mbar_arrive(&sh.dq_free);
-                if (sem) {
-                    __threadfence();
+                    fence_async_smem();
                     named_bar(1, 128);
-                    if (r == 0) red_release_add(sem, 1);
+                    if (r == 0) {
+                        tma_reduce_add_2d(&tdq, sDS, half * 64, grow);
+                        tma_reduce_add_2d(&tdq, sDS + kBox, half * 64 + 32, grow);
+                        bulk_commit();
+                        bulk_wait_read0();
+                    }
+                    named_bar(1, 128);
+                }
+                if (r == 0) {
+                    mbar_arrive(&sh.ds_free);  // the softmax may write the next dS
+                    if (sem) {
+                        bulk_wait0();          // our additions are complete
+                        fence_async_global();
+                        __threadfence();
+                        red_release_add(sem, 1);
+                    }
                 }
             }
             if (!ok) break;
@@ -641,6 +676,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             tc_fence_before();
             mbar_arrive(&sh.acc_free);
         }
+        if (r == 0) bulk_wait0();  // every bulk reduction issued here has completed
     }
 
     tc_fence_before();
@@ -674,7 +710,7 @@ cudaError_t launch_bwd(const BwdLaunch& L, int stages, cudaStream_t stream) {
                                    : (long long)a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN);
         int grid = (int)(units < L.num_sms ? units : L.num_sms);
         if (grid < 1) grid = 1;
-        bwd_kernel<<<grid, kBwdThreads, kBwdSmem, stream>>>(L.tq, L.tk, L.tv, L.tdo, a);
+        bwd_kernel<<<grid, kBwdThreads, kBwdSmem, stream>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -334,12 +334,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 Unit U;
                 if (!sched.get(u, U)) break;
                 const int n0 = kv_tiles(U, 0, a.causal), n1 = kv_tiles(U, 1, a.causal);
+                // Shared-memory operands land through TMA and are read by the
+                // tensor core (both async proxy): the mbarrier completion is
+                // the only ordering needed.  A tcgen05 fence is needed only
+                // after waits that hand over TENSOR memory (P from softmax).
                 if (!(ok = mbar_wait_w(&sh.q_full, uc & 1, wc, kSiteQFull))) break;
-                tc_fence_after();
                 uint32_t slot_k = it % kStages;
                 if (!(ok = mbar_wait_w(&sh.full[slot_k], (it / kStages) & 1, wc, kSiteRingFull))) break;
-                tc_fence_after();
                 ++it;
+                tc_fence_after();  // S of the previous unit's epilogue (O) is in order
                 issue_qk(tmem + col_s(0), sQ, sRing + slot_k * kTileBytes);
                 umma_commit_w(&sh.s_full[0]);
                 issue_qk(tmem + col_s(1), sQ + kTileBytes, sRing + slot_k * kTileBytes);
@@ -349,20 +352,19 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     const uint32_t slot_v = it % kStages;
                     if (!(ok = mbar_wait_w(&sh.full[slot_v], (it / kStages) & 1, wc, kSiteRingFull))) break;
                     ++it;
+                    const bool more = j + 1 < n1;
+                    if (more) {  // K of the next tile: waited here so PV and S issue back to back
+                        slot_k = it % kStages;
+                        if (!(ok = mbar_wait_w(&sh.full[slot_k], (it / kStages) & 1, wc, kSiteRingFull))) break;
+                        ++it;
+                    }
                     if (j < n0) {
                         if (!(ok = mbar_wait_w(&sh.p_ready[0], pc[0] & 1, wc, kSiteP0))) break;
                         ++pc[0];
                         tc_fence_after();
                         issue_pv(tmem + col_o(0), tmem + col_s(0), sRing + slot_v * kTileBytes, j > 0);
                         if (j == n0 - 1) umma_commit_w(&sh.o_done[0]);
-                    }
-                    const bool more = j + 1 < n1;
-                    if (more) {
-                        slot_k = it % kStages;
-                        if (!(ok = mbar_wait_w(&sh.full[slot_k], (it / kStages) & 1, wc, kSiteRingFull))) break;
-                        ++it;
-                        tc_fence_after();
-                        if (j + 1 < n0) {
+                        if (more && j + 1 < n0) {
                             issue_qk(tmem + col_s(0), sQ, sRing + slot_k * kTileBytes);
                             umma_commit_w(&sh.s_full[0]);
                         }

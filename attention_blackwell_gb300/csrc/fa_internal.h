@@ -95,6 +95,7 @@ struct BwdArgs {
 
 struct BwdLaunch {
     CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tdq;         // dQacc as fp32 [Hq*T, 128], box {32, 128}, 128-B swizzle
     BwdArgs a;
     int num_sms;
 };
