@@ -137,8 +137,8 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 //   warps 0-3   "softmax" warpgroup, one thread per KEY row (TMEM lane):
 //               P^T = 2^(alpha log2e S^T - LSE log2e) -> bf16 into TMEM
 //               (operand A of dV += P^T dO); dS^T = P^T (dP^T - D) -> bf16 into
-//               shared memory in the 128-B swizzled layout both the dK and the
-//               dQ UMMAs read (K-major for dK, MN-major for dQ);
+//               TMEM (operand A of dK += dS^T Q) and into shared memory in the
+//               128-B swizzled layout the dQ UMMA reads as an MN-major A;
 //   warps 4-7   dQ warpgroup, one thread per QUERY row: drains dQ_i from TMEM
 //               into the fp32 accumulator (vector reductions), then at the end
 //               of a unit stores dK (x alpha) and dV in bf16;
@@ -148,7 +148,8 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 //
 // Tensor memory (512 columns): dK acc 0-127, dV acc 128-255,
 //   R0 256-383: S^T, then P^T (bf16, first 64 columns);
-//   R1 384-511: dP^T, then dQ_i (the paper's 1-CTA sharing of dP/dS/dQ columns).
+//   R1 384-511: dP^T, then dS^T (bf16, first 64 columns; operand A of dK),
+//               then dQ_i (the paper's 1-CTA sharing of dP/dS/dQ columns).
 // Per query tile the UMMA order is dV, dK, S(next), dQ, dP(next): the next
 // tile's S^T is in flight while dQ of this tile drains (FlashAttention-4 blog,
 // "Backward pass": dK/dQ of tile j-1 overlap the elementwise work of tile j).
@@ -228,15 +229,6 @@ __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b_s
     const uint64_t bd = sdesc_sw128(b_smem, kBox, 1024);
 #pragma unroll 1
     for (uint32_t k = 0; k < 8; ++k) umma_ts_w(d, a_tmem + k * 8, bd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
-}
-
-// D (+)= A B with A K-major and B MN-major in shared memory (dK += dS^T Q).
-__device__ __forceinline__ void mma_kn(uint32_t d, uint32_t a_smem, uint32_t b_smem, uint32_t acc) {
-    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
-    const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, kBox, 1024);
-#pragma unroll 1
-    for (uint32_t k = 0; k < 8; ++k)
-        umma_ss_w(d, ad + (((k >> 2) * kBox + (k & 3) * 32) >> 4), bd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
 }
 
 // D = A B with A and B both MN-major in shared memory (dQ = dS K: dS^T is
@@ -437,7 +429,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         mma_tn(tmem + kColDV, tmem + kColR0, base + kOffDO + st * kT32, t > 0);
                         if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, kBSiteDs))) break;
                         tc_fence_after();
-                        mma_kn(tmem + kColDK, sDS, base + kOffQ + st * kT32, t > 0);
+                        mma_tn(tmem + kColDK, tmem + kColR1, base + kOffQ + st * kT32, t > 0);
                         if (more) {  // Q/dO arrive by TMA: no tcgen05 fence needed
                             if (!(ok = mbar_wait_w(&sh.q_full[st2], ((jj + 1) >> 1) & 1, wc, kBSiteQFull))) break;
                             mma_kk(tmem + kColR0, sK, base + kOffQ + st2 * kT32);
@@ -546,7 +538,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         *reinterpret_cast<uint4*>(ds_row + (q >> 3) * kBox + (((q & 7) ^ sw) << 4)) =
                             make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
                     }
+                    // dS^T also into TMEM over the dP^T columns already read
+                    // (operand A of dK += dS^T Q, like P^T for dV).
+                    tmem_st16(tR1 + cc * 16, pk);
                 }
+                tmem_wait_st();
                 fence_async_smem();
                 tc_fence_before();
                 mbar_arrive(&sh.ds_ready);
@@ -565,7 +561,6 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             const int span = U.nq - U.i0;
             for (int t = 0; t < U.n; ++t, ++jj) {
                 const int h = U.hk * g + t / span, i = U.i0 + t % span;
-                const int row = i * kTileM + r;
                 ok = mbar_wait(&sh.dq_full, jj & 1, wc, kBSiteDq);
                 // Named barriers follow: every thread of the warpgroup must
                 // take the same path, so the warpgroup agrees on aborts.

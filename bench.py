@@ -67,13 +67,23 @@ def barrier(world):
 
 
 def max_over_ranks(x, world, device=None):
+    """Largest x over all ranks (the slowest rank's time); x itself at N=1."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
+    if device is None or dist.get_backend() == "gloo":
+        device = "cpu"
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_tflops(flops_per_step, steps, world, ms_max):
+    """Whole-job throughput: every rank runs the same per-GPU workload
+    (replicas), so the job processed world * steps steps in the slowest
+    rank's time."""
+    return flops_per_step * steps * world / (ms_max / 1e3) / 1e12
 
 
 class ClockSampler:
@@ -289,7 +299,7 @@ def run_ours(args, rank, world):
         d = [evs[s][i][0].elapsed_time(evs[s][i][1]) for s in range(K)]
         per_kernel.append({"kernel": name, "avg_ms": sum(d) / K, "flops": fl, "launches_per_step": nl})
     flops_step = sum(k[2] for k in kernels)
-    value = flops_step * K * world / (ms / 1e3) / 1e12
+    value = aggregate_tflops(flops_step, K, world, ms)
 
     # End to end through the public API with host buffers: every step copies
     # the step's inputs from pinned host memory and reads its results back.
@@ -315,7 +325,7 @@ def run_ours(args, rank, world):
     for _ in range(E):
         e2e_step()
     e2e_ms = max_over_ranks((time.perf_counter() - e0) * 1e3, world, dev)
-    e2e_value = flops_step * E * world / (e2e_ms / 1e3) / 1e12
+    e2e_value = aggregate_tflops(flops_step, E, world, e2e_ms)
     return locals()
 
 
