@@ -155,16 +155,19 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 // "Backward pass": dK/dQ of tile j-1 overlap the elementwise work of tile j).
 //
 // Shared memory (dynamic, 1024-aligned, 232448 bytes):
-//   K 32K | V 32K | Q[2] 2x32K | dO[2] 2x32K | dS 32K | lse2[2][128], D[2][128] | barriers
+//   K 32K | V 32K | Q[2] 2x32K | dO 32K | dS 32K | dQ staging 32K | lse2[2][128], D[2][128] | barriers
+// dO is single-buffered: it is free once dV has read it and is next needed
+// by dP of the next tile, after dK, S, dQ and the dQ hand-off.
 constexpr int kBwdThreads = 384;
 constexpr uint32_t kT32 = 32768, kBox = 16384;
-constexpr uint32_t kOffK = 0, kOffV = kT32, kOffQ = 2 * kT32, kOffDO = 4 * kT32, kOffDS = 6 * kT32;
+constexpr uint32_t kOffK = 0, kOffV = kT32, kOffQ = 2 * kT32, kOffDO = 4 * kT32, kOffDS = 5 * kT32;
+constexpr uint32_t kOffStage = 6 * kT32;                // dQ staging for the TMA reductions
 constexpr uint32_t kOffStat = 7 * kT32;                 // lse2[2][128], D[2][128] floats
 constexpr uint32_t kOffBar = kOffStat + 4 * 128 * 4;
 constexpr uint32_t kBwdSmem = kOffBar + 1024;           // 232448
 
 struct BwdShared {
-    uint64_t kv_full, kv_empty, q_full[2], q_empty[2];
+    uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty;
     uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dq_full, dq_free, dkdv_done, acc_free, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -302,6 +305,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         mbar_init(&sh.kv_full, 1);
         mbar_init(&sh.kv_empty, 1);
         for (int s = 0; s < 2; ++s) { mbar_init(&sh.q_full[s], 1); mbar_init(&sh.q_empty[s], 1); }
+        mbar_init(&sh.do_full, 1);
+        mbar_init(&sh.do_empty, 1);
         mbar_init(&sh.s_full, 1);
         mbar_init(&sh.dp_full, 1);
         mbar_init(&sh.p_ready, 128);
@@ -380,14 +385,19 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     }
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(&sh.q_full[st], 2 * kT32);
-                        for (int c = 0; c < 2; ++c) {
+                        mbar_arrive_expect_tx(&sh.q_full[st], kT32);
+                        for (int c = 0; c < 2; ++c)
                             tma_load_3d(base + kOffQ + st * kT32 + c * kBox, &tq, &sh.q_full[st], c * 64, h,
                                         U.tok0 + i * kTileM);
-                            tma_load_3d(base + kOffDO + st * kT32 + c * kBox, &tdo, &sh.q_full[st], c * 64, h,
-                                        U.tok0 + i * kTileM);
+                        ok = mbar_wait(&sh.do_empty, (jj & 1) ^ 1, wc, kBSiteQEmpty);
+                        if (ok) {
+                            mbar_arrive_expect_tx(&sh.do_full, kT32);
+                            for (int c = 0; c < 2; ++c)
+                                tma_load_3d(base + kOffDO + c * kBox, &tdo, &sh.do_full, c * 64, h, U.tok0 + i * kTileM);
                         }
                     }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
                 }
                 ++uc;
             }
@@ -398,6 +408,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                            globaltimer_ns() - t0 < kWaitLimitNs) {}
                 if (uc > 0)
                     while (!mbar_try_wait(smem_u32(&sh.kv_full), (uc - 1) & 1) &&
+                           globaltimer_ns() - t0 < kWaitLimitNs) {}
+                if (jj > 0)
+                    while (!mbar_try_wait(smem_u32(&sh.do_full), (jj - 1) & 1) &&
                            globaltimer_ns() - t0 < kWaitLimitNs) {}
             }
             __syncwarp();
@@ -419,17 +432,20 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         if (!(ok = mbar_wait_w(&sh.dq_free, (jj - 1) & 1, wc, kBSiteDqFree))) break;
                         tc_fence_after();
                     }
-                    mma_kk(tmem + kColR1, sV, base + kOffDO + (jj & 1) * kT32);
+                    if (!(ok = mbar_wait_w(&sh.do_full, jj & 1, wc, kBSiteQFull))) break;
+                    mma_kk(tmem + kColR1, sV, base + kOffDO);
                     umma_commit_w(&sh.dp_full);
                     for (int t = 0; t < U.n; ++t, ++jj) {
                         const uint32_t st = jj & 1, st2 = (jj + 1) & 1;
                         const bool more = t + 1 < U.n;
                         if (!(ok = mbar_wait_w(&sh.p_ready, jj & 1, wc, kBSiteP))) break;
                         tc_fence_after();
-                        mma_tn(tmem + kColDV, tmem + kColR0, base + kOffDO + st * kT32, t > 0);
+                        mma_tn(tmem + kColDV, tmem + kColR0, base + kOffDO, t > 0);
+                        umma_commit_w(&sh.do_empty);     // dO read by dP and dV: the next may load
                         if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, kBSiteDs))) break;
                         tc_fence_after();
                         mma_tn(tmem + kColDK, tmem + kColR1, base + kOffQ + st * kT32, t > 0);
+                        umma_commit_w(&sh.q_empty[st]);  // Q and LSE/D of this stage are consumed
                         if (more) {  // Q/dO arrive by TMA: no tcgen05 fence needed
                             if (!(ok = mbar_wait_w(&sh.q_full[st2], ((jj + 1) >> 1) & 1, wc, kBSiteQFull))) break;
                             mma_kk(tmem + kColR0, sK, base + kOffQ + st2 * kT32);
@@ -437,11 +453,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         }
                         mma_nn(tmem + kColR1, sDS, sK);
                         umma_commit_w(&sh.dq_full);
-                        umma_commit_w(&sh.q_empty[st]);
+                        umma_commit_w(&sh.ds_free);      // dS read by dK and dQ
                         if (more) {
                             if (!(ok = mbar_wait_w(&sh.dq_free, jj & 1, wc, kBSiteDqFree))) break;
                             tc_fence_after();
-                            mma_kk(tmem + kColR1, sV, base + kOffDO + st2 * kT32);
+                            if (!(ok = mbar_wait_w(&sh.do_full, (jj + 1) & 1, wc, kBSiteQFull))) break;
+                            mma_kk(tmem + kColR1, sV, base + kOffDO);
                             umma_commit_w(&sh.dp_full);
                         }
                     }
@@ -603,14 +620,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     if (named_bar_or(1, 128, gave_up)) { ok = false; break; }
                 }
                 // Add dQ_i into the fp32 accumulator with TMA bulk tensor
-                // reductions of whole 128-byte lines.  The staging area is the
-                // dS buffer (dQ_i complete implies dK_i and dQ_i have read dS_i):
-                // two rounds of two 32-column boxes (128 rows x 128 B, swizzled
-                // like a 128-B TMA box).  Rows past the sequence end hold exact
+                // reductions of whole 128-byte lines, staged in shared memory
+                // in two rounds of two 32-column boxes (128 rows x 128 B,
+                // swizzled like a 128-B TMA box).  Rows past the sequence end hold exact
                 // zeros (their P, hence dS, is zero), so adding them to the
                 // neighbouring rows changes nothing.
                 const int grow = h * (int)a.T + U.tok0 + i * kTileM;
-                uint8_t* stage_row = dsm + kOffDS + r * 128;
+                uint8_t* stage_row = dsm + kOffStage + r * 128;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -624,15 +640,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     fence_async_smem();
                     named_bar(1, 128);
                     if (r == 0) {
-                        tma_reduce_add_2d(&tdq, sDS, half * 64, grow);
-                        tma_reduce_add_2d(&tdq, sDS + kBox, half * 64 + 32, grow);
+                        tma_reduce_add_2d(&tdq, base + kOffStage, half * 64, grow);
+                        tma_reduce_add_2d(&tdq, base + kOffStage + kBox, half * 64 + 32, grow);
                         bulk_commit();
                         bulk_wait_read0();
                     }
                     named_bar(1, 128);
                 }
                 if (r == 0) {
-                    mbar_arrive(&sh.ds_free);  // the softmax may write the next dS
                     if (sem) {
                         bulk_wait0();          // our additions are complete
                         fence_async_global();
