@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 //   K 32K | V 32K | Q[2] 2x32K | dO 32K | dS 32K | dQ staging 32K | lse2[2][128], D[2][128] | barriers
 // dO is single-buffered: it is free once dV has read it and is next needed
 // by dP of the next tile, after dK, S, dQ and the dQ hand-off.
-constexpr int kBwdThreads = 384;
+constexpr int kBwdThreads = 512;
 constexpr uint32_t kT32 = 32768, kBox = 16384;
 constexpr uint32_t kOffK = 0, kOffV = kT32, kOffQ = 2 * kT32, kOffDO = 4 * kT32, kOffDS = 5 * kT32;
 constexpr uint32_t kOffStage = 6 * kT32;                // dQ staging for the TMA reductions
@@ -309,8 +309,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         mbar_init(&sh.do_empty, 1);
         mbar_init(&sh.s_full, 1);
         mbar_init(&sh.dp_full, 1);
-        mbar_init(&sh.p_ready, 128);
-        mbar_init(&sh.ds_ready, 128);
+        mbar_init(&sh.p_ready, 256);
+        mbar_init(&sh.ds_ready, 256);
         mbar_init(&sh.ds_free, 1);
         mbar_init(&sh.dq_full, 1);
         mbar_init(&sh.dq_free, 128);
@@ -342,10 +342,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
     const int g = a.Hq / a.Hkv;
     const float scale = a.scale_log2;
 
-    // Register split (launch 384 x 168 = 64512): key-row warpgroup 232 (a
-    // 128-float P row), dQ warpgroup keeps 168, loader/UMMA warpgroup 56:
-    // 128 * (232 + 168 + 56) = 58368.
-    if (warp >= 8) {
+    // Register split (launch 512 x 128 = 65536): the two key-row warpgroups
+    // 144 each (a 64-float half row of P), the dQ warpgroup 168 (a whole dQ
+    // row), the loader/UMMA warpgroup 56: 128 * (144 + 144 + 168 + 56) = 65536.
+    if (warp >= 8 && warp < 12) {
         regs_dec<56>();
         if (warp == 8) {
             // ------------------------------------------------------------ loader
@@ -444,7 +444,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         umma_commit_w(&sh.do_empty);     // dO read by dP and dV: the next may load
                         if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, kBSiteDs))) break;
                         tc_fence_after();
-                        mma_tn(tmem + kColDK, tmem + kColR1, base + kOffQ + st * kT32, t > 0);
+                        mma_tn(tmem + kColDK, tmem + kColR0 + 64, base + kOffQ + st * kT32, t > 0);
                         umma_commit_w(&sh.q_empty[st]);  // Q and LSE/D of this stage are consumed
                         if (more) {  // Q/dO arrive by TMA: no tcgen05 fence needed
                             if (!(ok = mbar_wait_w(&sh.q_full[st2], ((jj + 1) >> 1) & 1, wc, kBSiteQFull))) break;
@@ -472,13 +472,17 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             }
             __syncwarp();
         }
-    } else if (warp < 4) {
-        regs_inc<232>();
+    } else if (warp < 4 || warp >= 12) {
+        regs_inc<144>();
         // ------------------------------------------------ P^T and dS^T (key rows)
-        const int r = tid;                                   // key row in the tile == TMEM lane
-        const uint32_t lb = (uint32_t)(warp * 32) << 16;
+        // Two warpgroups share each key row: warps 0-3 take query columns
+        // 0-63, warps 12-15 columns 64-127.
+        const int hc = warp >= 12 ? 1 : 0;                   // which column half
+        const int cb = hc * 64;
+        const int r = (warp & 3) * 32 + lane;                // key row in the tile == TMEM lane
+        const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tR0 = tmem + lb + kColR0, tR1 = tmem + lb + kColR1;
-        uint8_t* ds_row = dsm + kOffDS + r * 128;
+        uint8_t* ds_row = dsm + kOffDS + hc * kBox + r * 128;
         const int sw = r & 7;
         uint32_t jj = 0;
         bool ok = true;
@@ -492,22 +496,19 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 if (!(ok = mbar_wait(&sh.q_full[st], (jj >> 1) & 1, wc, kBSiteQFull))) break;
                 if (!(ok = mbar_wait(&sh.s_full, jj & 1, wc, kBSiteS))) break;
                 tc_fence_after();
-                float p[128];
+                float p[64];
                 {
                     uint32_t* pu = reinterpret_cast<uint32_t*>(p);
-                    tmem_ld32(tR0 + 0, *reinterpret_cast<uint32_t(*)[32]>(pu + 0));
-                    tmem_ld32(tR0 + 32, *reinterpret_cast<uint32_t(*)[32]>(pu + 32));
-                    tmem_ld32(tR0 + 64, *reinterpret_cast<uint32_t(*)[32]>(pu + 64));
-                    tmem_ld32(tR0 + 96, *reinterpret_cast<uint32_t(*)[32]>(pu + 96));
+                    tmem_ld32(tR0 + cb, *reinterpret_cast<uint32_t(*)[32]>(pu + 0));
+                    tmem_ld32(tR0 + cb + 32, *reinterpret_cast<uint32_t(*)[32]>(pu + 32));
                     tmem_wait_ld();
                 }
                 // visible columns c: query 128 i + c < len, key < len, and key <= query if causal
-                int c_lo = a.causal ? key - i * kTileM : 0;
-                int c_hi = U.len - i * kTileM;
-                if (key >= U.len) c_hi = 0;
-                const float4* l2v = reinterpret_cast<const float4*>(s_lse + st * 128);
+                const int c_lo = (a.causal ? key - i * kTileM : 0) - cb;
+                const int c_hi = (key >= U.len ? 0 : U.len - i * kTileM) - cb;
+                const float4* l2v = reinterpret_cast<const float4*>(s_lse + st * 128 + cb);
 #pragma unroll
-                for (int c4 = 0; c4 < 32; ++c4) {
+                for (int c4 = 0; c4 < 16; ++c4) {
                     const float4 l4 = l2v[c4];
                     const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
@@ -518,24 +519,27 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     }
                 }
 #pragma unroll
-                for (int stg = 0; stg < 4; ++stg) {
+                for (int stg = 0; stg < 2; ++stg) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int m = 0; m < 16; ++m) pk[m] = pack_bf16x2(p[stg * 32 + 2 * m], p[stg * 32 + 2 * m + 1]);
-                    tmem_st16(tR0 + stg * 16, pk);
+                    tmem_st16(tR0 + cb / 2 + stg * 16, pk);        // P^T: two bf16 per column
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&sh.p_ready);
 
+                // dS^T goes to R0 columns 64-127, which held S^T: wait until both
+                // halves have read S^T (p_ready complete) before writing them.
+                if (!(ok = mbar_wait(&sh.p_ready, jj & 1, wc, kBSiteP))) break;
                 if (!(ok = mbar_wait(&sh.dp_full, jj & 1, wc, kBSiteDp))) break;
                 if (!(ok = mbar_wait(&sh.ds_free, (jj & 1) ^ 1, wc, kBSiteDsFree))) break;
                 tc_fence_after();
-                const float4* dv4 = reinterpret_cast<const float4*>(s_D + st * 128);
+                const float4* dv4 = reinterpret_cast<const float4*>(s_D + st * 128 + cb);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < 2; ++cc) {
                     uint32_t dp[32];
-                    tmem_ld32(tR1 + cc * 32, dp);
+                    tmem_ld32(tR1 + cb + cc * 32, dp);
                     tmem_wait_ld();
                     uint32_t pk[16];
 #pragma unroll
@@ -547,17 +551,16 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         pk[2 * m + 1] = pack_bf16x2(p[c + 2] * (__uint_as_float(dp[4 * m + 2]) - d4.z),
                                                     p[c + 3] * (__uint_as_float(dp[4 * m + 3]) - d4.w));
                     }
-                    // 32 queries = four 16-byte chunks; chunk q of the row holds
-                    // queries 8q..8q+7: box q/8, position (q%8) ^ (row%8).
+                    // 32 queries = four 16-byte chunks; chunk q of this half's
+                    // box holds queries cb + 8q .. +7 at position q ^ (row % 8).
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
                         const int q = cc * 4 + m;
-                        *reinterpret_cast<uint4*>(ds_row + (q >> 3) * kBox + (((q & 7) ^ sw) << 4)) =
+                        *reinterpret_cast<uint4*>(ds_row + ((q ^ sw) << 4)) =
                             make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
                     }
-                    // dS^T also into TMEM over the dP^T columns already read
-                    // (operand A of dK += dS^T Q, like P^T for dV).
-                    tmem_st16(tR1 + cc * 16, pk);
+                    // dS^T also into TMEM (operand A of dK += dS^T Q, like P^T for dV).
+                    tmem_st16(tR0 + 64 + cb / 2 + cc * 16, pk);
                 }
                 tmem_wait_st();
                 fence_async_smem();
@@ -566,6 +569,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             }
         }
     } else {
+        regs_inc<168>();
         // -------------------------------------------- dQ drain, dK/dV epilogue
         const int r = tid - 128;                             // query row (dQ) / key row (dK, dV)
         const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
