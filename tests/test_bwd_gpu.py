@@ -100,6 +100,23 @@ def test_deterministic_small(fa, causal):
     check(runs[0], oracle(inp, causal))
 
 
+def test_deterministic_noncausal_many_tiles(fa):
+    """More key tiles per head than fit in one wave of CTAs: every head's
+    key tiles cannot all run at once, so the fixed-order semaphores must never
+    wait on a key tile that has not started."""
+    import attention_blackwell_gb300 as fa_mod
+    n_sm = fa_mod.num_sms()
+    N = 128 * 40                       # 40 key tiles per head
+    B, H = 1, max(4, (2 * n_sm) // 40)  # > 2 waves of units in total
+    inp = inputs(B, N, H, H, seed=31)
+    runs = gpu_grads(fa, inp, False, deterministic=True, repeats=2)
+    for a_, b_ in zip(runs[0], runs[1]):
+        assert np.array_equal(a_.view(np.uint32), b_.view(np.uint32))
+    ref_h = A.head_backward(*(inp[n][0, :, 0].float().numpy().astype(np.float64) for n in ("q", "k", "v", "do")),
+                            1 / math.sqrt(128), False)
+    check([g[0, :, 0] for g in runs[0]], ref_h)
+
+
 def test_large_q_logits(fa):
     inp = inputs(1, 384, 2, 2, seed=17, q_std=3.0)
     check(gpu_grads(fa, inp, True)[0], oracle(inp, True))
