@@ -12,7 +12,7 @@ import os
 
 import torch
 
-__all__ = ["fwd", "bwd", "bwd_workspace", "exp2_emu", "set_tuning", "device_status", "num_sms", "FAError", "library_path", "lib"]
+__all__ = ["fwd", "set_fwd_kernel", "bwd", "bwd_workspace", "exp2_emu", "set_tuning", "device_status", "num_sms", "FAError", "library_path", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libfa.so")
@@ -48,6 +48,8 @@ def lib():
         L.fa_num_sms.argtypes = []
         L.fa_set_tuning.restype = i
         L.fa_set_tuning.argtypes = [i, f]
+        L.fa_set_fwd_kernel.restype = i
+        L.fa_set_fwd_kernel.argtypes = [i]
         L.fa_fwd.restype = i
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp]
         sz = ctypes.c_size_t
@@ -105,6 +107,11 @@ def num_sms():
 def set_tuning(exp2_emu_eighths=0, tau=8.0):
     """Process-wide forward tuning (share of exp2 on the FMA pipe, rescale tau)."""
     _check(lib().fa_set_tuning(int(exp2_emu_eighths), float(tau)), "fa_set_tuning")
+
+
+def set_fwd_kernel(kernel=1):
+    """Forward kernel for later calls: 0 ping-pong 128x128 tiles, 1 256-key blocks."""
+    _check(lib().fa_set_fwd_kernel(int(kernel)), "fa_set_fwd_kernel")
 
 
 def fwd(q, k, v, causal=False, alpha=None, cu_seqlens=None, max_seqlen=None, out=None, lse=None, stream=None):

@@ -30,6 +30,7 @@ DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
 int g_emu_eighths = 0;         // share of exp2 pairs on the FMA pipe (eighths)
+int g_fwd_kernel = 1;          // 0: ping-pong of two 128-row query tiles; 1: 256-key blocks
 float g_tau = 8.0f;            // conditional-rescale threshold, log2(256)
 
 int current_device_info(DeviceInfo** out) {
@@ -67,14 +68,14 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// bf16 tensor [T, H, 128] -> 3-D map {128, H, T}, box {64, 1, 128}, 128-B swizzle.
+// bf16 tensor [T, H, 128] -> 3-D map {128, H, T}, box {64, 1, box_rows}, 128-B swizzle.
 // Rows past T read as zero.
-int make_map(CUtensorMap* map, const void* ptr, int H, long long T) {
+int make_map(CUtensorMap* map, const void* ptr, int H, long long T, int box_rows = kTileM) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return FA_ERR_LAUNCH;
     cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)H, (cuuint64_t)T};
     cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)H * kHeadDim * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)kTileM};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -161,10 +162,13 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     int rc = current_device_info(&dev);
     if (rc != FA_OK) return rc;
 
+    // The 256-key kernel serves fixed-length inputs with the MUFU-only exp2;
+    // packed varlen batches and the FMA-exp2 variants use the ping-pong kernel.
+    const bool wide = g_fwd_kernel == 1 && !varlen && g_emu_eighths == 0;
     FwdLaunch L;
     if ((rc = make_map(&L.tq, q, Hq, T)) != FA_OK) return rc;
-    if ((rc = make_map(&L.tk, k, Hkv, T)) != FA_OK) return rc;
-    if ((rc = make_map(&L.tv, v, Hkv, T)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tk, k, Hkv, T, wide ? 256 : kTileM)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tv, v, Hkv, T, wide ? 256 : kTileM)) != FA_OK) return rc;
     L.a.o = o;
     L.a.lse = lse;
     L.a.cu_seqlens = cu_seqlens;
@@ -190,8 +194,14 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     L.a.tau = g_tau;
     L.emu_eighths = g_emu_eighths;
     L.num_sms = dev->num_sms;
-    cudaError_t e = launch_fwd(L, stream);
+    cudaError_t e = wide ? launch_fwd_wide(L, stream) : launch_fwd(L, stream);
     return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_set_fwd_kernel(int kernel) {
+    if (kernel != 0 && kernel != 1) return FA_ERR_INVALID;
+    g_fwd_kernel = kernel;
+    return FA_OK;
 }
 
 static int read_and_clear(DevStatus* where) {

@@ -107,6 +107,10 @@ cudaError_t launch_bwd(const BwdLaunch& L, int stages, cudaStream_t stream);
 // Launch the forward kernel (fa_fwd.cu).  Returns a cudaError_t.
 cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream);
 
+// Launch the 256-key-block forward kernel (fa_fwd_wide.cu; fixed length
+// only).  Its K and V maps use boxes of 256 rows.
+cudaError_t launch_fwd_wide(const FwdLaunch& L, cudaStream_t stream);
+
 // Evaluate the FMA-pipe exp2 on n floats (fa_fwd.cu).
 cudaError_t launch_exp2_emu(const float* x, float* y, int64_t n, cudaStream_t stream);
 

@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--deterministic", action="store_true", help="backward in deterministic mode")
     ap.add_argument("--exp2-emu", type=int, default=0, help="forward: eighths of exp2 on the FMA pipe (0-2)")
     ap.add_argument("--tau", type=float, default=8.0, help="forward: conditional-rescale threshold (log2 units)")
+    ap.add_argument("--fwd-kernel", type=int, default=1, help="forward kernel: 0 ping-pong 128x128, 1 256-key blocks")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
     return ap.parse_args()
@@ -240,6 +241,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", local)
     w = W.WORKLOADS[args.workload]
     fa.set_tuning(args.exp2_emu, args.tau)
+    fa.set_fwd_kernel(args.fwd_kernel)
     has_bwd = hasattr(fa, "bwd") and not args.no_bwd
     inp = W.make_inputs(w, with_grad=True)
     t = {n: inp[n].to(dev) for n in ("q", "k", "v", "do")}
@@ -374,6 +376,7 @@ def main_ours(args):
         "config": {"workload": describe(w, r["inp"]),
             "step": step_name, "global_batch": w.B * world, "seq_len": w.N or max(r["inp"]["lengths"]),
             "deterministic_bwd": bool(args.deterministic), "exp2_emu_eighths": args.exp2_emu, "tau": args.tau,
+            "fwd_kernel": "256-key blocks" if args.fwd_kernel == 1 and not w.varlen else "ping-pong 2x128",
             "parallelism": "replicas" if world > 1 else "single",
             "l2": "no flush: the step's inputs (%.0f MiB) exceed the 126 MB L2" % (
                 sum(r["t"][n].numel() * 2 for n in ("q", "k", "v", "do")) / 2 ** 20)},

@@ -78,6 +78,19 @@ int fa_num_sms(void);
 int fa_set_tuning(int exp2_emu_eighths, float tau);
 
 /*
+ * Process-wide choice of the forward kernel (affects later fa_fwd calls):
+ *   0 -- two 128-row query tiles per CTA in ping-pong, 128-key tiles: the
+ *        pipeline of the FlashAttention-4 blog, "Forward pass";
+ *   1 -- (default) one 128-row query tile per CTA, 256-key blocks, so the
+ *        S = Q K^T product is a 128x256 UMMA, which runs at the tensor
+ *        core's full rate on GB300 (the 128x128 shape does not).
+ * Kernel 1 serves fixed-length inputs with exp2_emu_eighths == 0; all other
+ * calls use kernel 0.  Both compute the same attention up to rounding.
+ * Errors: FA_ERR_INVALID.
+ */
+int fa_set_fwd_kernel(int kernel);
+
+/*
  * Forward: O and LSE of exact attention (FlashAttention-4 blog, "Forward
  * pass: a new softmax pipeline with conditional rescaling").
  *
