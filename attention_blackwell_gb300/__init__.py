@@ -12,7 +12,7 @@ import os
 
 import torch
 
-__all__ = ["fwd", "set_fwd_kernel", "bwd", "bwd_workspace", "exp2_emu", "set_tuning", "device_status", "num_sms", "FAError", "library_path", "lib"]
+__all__ = ["fwd", "set_fwd_kernel", "fwd_pairs_resident", "bwd", "bwd_workspace", "exp2_emu", "set_tuning", "device_status", "num_sms", "FAError", "library_path", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libfa.so")
@@ -50,6 +50,8 @@ def lib():
         L.fa_set_tuning.argtypes = [i, f]
         L.fa_set_fwd_kernel.restype = i
         L.fa_set_fwd_kernel.argtypes = [i]
+        L.fa_fwd_pairs_resident.restype = i
+        L.fa_fwd_pairs_resident.argtypes = []
         L.fa_fwd.restype = i
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp]
         sz = ctypes.c_size_t
@@ -97,6 +99,11 @@ def _need(t, name, dtype):
         raise ValueError("%s must be contiguous" % name)
 
 
+def fwd_pairs_resident():
+    """CTA pairs forward kernel 2 keeps resident (0 before its first launch)."""
+    return int(lib().fa_fwd_pairs_resident())
+
+
 def num_sms():
     n = lib().fa_num_sms()
     if n < 0:
@@ -109,8 +116,9 @@ def set_tuning(exp2_emu_eighths=0, tau=8.0):
     _check(lib().fa_set_tuning(int(exp2_emu_eighths), float(tau)), "fa_set_tuning")
 
 
-def set_fwd_kernel(kernel=1):
-    """Forward kernel for later calls: 0 ping-pong 128x128 tiles, 1 256-key blocks."""
+def set_fwd_kernel(kernel=2):
+    """Forward kernel for later calls: 0 ping-pong 128x128 tiles, 1 256-key
+    blocks, 2 CTA pairs with 256-key blocks (the default)."""
     _check(lib().fa_set_fwd_kernel(int(kernel)), "fa_set_fwd_kernel")
 
 

@@ -30,7 +30,7 @@ DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
 int g_emu_eighths = 0;         // share of exp2 pairs on the FMA pipe (eighths)
-int g_fwd_kernel = 1;          // 0: ping-pong of two 128-row query tiles; 1: 256-key blocks
+int g_fwd_kernel = 2;          // 0: ping-pong of two 128-row query tiles; 1: 256-key blocks; 2: CTA pairs
 float g_tau = 8.0f;            // conditional-rescale threshold, log2(256)
 
 int current_device_info(DeviceInfo** out) {
@@ -162,13 +162,16 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     int rc = current_device_info(&dev);
     if (rc != FA_OK) return rc;
 
-    // The 256-key kernel serves fixed-length inputs with the MUFU-only exp2;
+    // The 256-key kernels serve fixed-length inputs with the MUFU-only exp2;
     // packed varlen batches and the FMA-exp2 variants use the ping-pong kernel.
-    const bool wide = g_fwd_kernel == 1 && !varlen && g_emu_eighths == 0;
+    const bool k256 = !varlen && g_emu_eighths == 0;
+    const bool wide = k256 && g_fwd_kernel == 1, pair = k256 && g_fwd_kernel == 2;
     FwdLaunch L;
+    // K boxes: 256 rows (one block) for kernel 1, 128 (a block's half) for the
+    // pair kernel; V boxes: 256 rows for both (the pair loads 64 columns of them).
     if ((rc = make_map(&L.tq, q, Hq, T)) != FA_OK) return rc;
     if ((rc = make_map(&L.tk, k, Hkv, T, wide ? 256 : kTileM)) != FA_OK) return rc;
-    if ((rc = make_map(&L.tv, v, Hkv, T, wide ? 256 : kTileM)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tv, v, Hkv, T, (wide || pair) ? 256 : kTileM)) != FA_OK) return rc;
     L.a.o = o;
     L.a.lse = lse;
     L.a.cu_seqlens = cu_seqlens;
@@ -194,12 +197,14 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     L.a.tau = g_tau;
     L.emu_eighths = g_emu_eighths;
     L.num_sms = dev->num_sms;
-    cudaError_t e = wide ? launch_fwd_wide(L, stream) : launch_fwd(L, stream);
+    cudaError_t e = pair ? launch_fwd_pair(L, stream) : wide ? launch_fwd_wide(L, stream) : launch_fwd(L, stream);
     return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+int fa_fwd_pairs_resident(void) { return g_pairs_resident; }
+
 int fa_set_fwd_kernel(int kernel) {
-    if (kernel != 0 && kernel != 1) return FA_ERR_INVALID;
+    if (kernel < 0 || kernel > 2) return FA_ERR_INVALID;
     g_fwd_kernel = kernel;
     return FA_OK;
 }

@@ -1,0 +1,525 @@
+// fa_fwd_pair.cu -- forward attention on CTA pairs (sm_103a, cluster of 2).
+//
+// Same result as the other forward kernels (O and LSE of exact attention,
+// online softmax with the conditional rescale; FlashAttention-4 blog,
+// "Forward pass"), with the tensor-core work of two SMs fused into one
+// M = 256 product (tcgen05 .cta_group::2).  A pair of CTAs owns 256 query rows
+// (128 per CTA) and streams keys in blocks of 256:
+//
+//   S = Q K_j^T   M = 256, N = 256 keys: each CTA holds its 128 query rows
+//                 and 128 of the block's keys; each CTA's tensor memory gets
+//                 its rows x all 256 keys.
+//   O += P V_j    M = 256, N = 128 (head dim), K = 256 keys: P from each
+//                 CTA's tensor memory, V split by head-dim columns (64 each).
+//
+// Per SM and key block this halves both the K/V bytes that TMA writes into
+// shared memory and the operand bytes the tensor core reads from it, compared
+// with one CTA running the same 128 x 256 product alone -- on GB300 the
+// single-CTA form is bounded by shared-memory bandwidth, not by the tensor
+// core.
+//
+// Tensor memory (512 columns, same layout in both CTAs): S cols 0-255 (fp32),
+// P cols 256-383 (bf16 pairs), O cols 384-511 (fp32).
+//
+// Roles (384 threads per CTA): warps 0-3 and 4-7 are two softmax warpgroups
+// splitting each row's 256 columns; warp 8 loads Q and K, warp 10 loads V
+// (both CTAs, each its own halves); in the even CTA warp 9 issues the S
+// products and warp 11 the P V products, committing to both CTAs' barriers.
+// Barriers the issuers wait on live in the even CTA: the odd CTA's TMA loads
+// and softmax arrivals count there.
+//
+// Fixed-length inputs only.
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kPThreads = 384;
+constexpr int kBlockN = 256;                        // keys per block
+constexpr uint32_t kQBytes = 32768;                 // 128 rows x 128 bf16 (this CTA's rows)
+constexpr uint32_t kQBox = 16384;                   // 128 rows x 64 bf16
+constexpr uint32_t kKHalf = 32768;                  // 128 keys x 128 bf16 (this CTA's keys)
+constexpr uint32_t kKBox = 16384;
+constexpr uint32_t kVHalf = 32768;                  // 256 keys x 64 bf16 (this CTA's head-dim half)
+constexpr int kKS = 3, kVS = 2;                     // ring slots
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kQBytes;
+constexpr uint32_t kOffV = kOffK + kKS * kKHalf;
+constexpr uint32_t kOffRed = kOffV + kVS * kVHalf;  // row max / sum exchange [2][2][128] float
+constexpr uint32_t kOffBar = kOffRed + 2 * 2 * 128 * 4;
+constexpr uint32_t kPSmem = kOffBar + 512;
+
+constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
+constexpr uint16_t kBoth = 3;                       // CTA mask: both CTAs of the pair
+
+enum : int { kPSiteQEmpty = 61, kPSiteKEmpty, kPSiteVEmpty, kPSiteQFull, kPSiteKFull, kPSiteVFull, kPSiteSFree,
+             kPSiteP, kPSiteOFree, kPSiteS, kPSitePV, kPSiteO };
+
+struct PairShared {
+    uint64_t q_full, q_empty;
+    uint64_t kfull[kKS], kempty[kKS], vfull[kVS], vempty[kVS];
+    uint64_t s_full, s_free, p_ready, pv_done, o_done, o_free, drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(PairShared) <= 512, "barrier block");
+
+struct PUnit {
+    int seq, h, m2, tok0, len;   // m2: 256-row query block
+};
+
+// Unit order over (batch, head, 256-row query block): non-causal head-major
+// with query blocks minor; causal longest-first (query blocks from the last)
+// inside L2 sections of (batch, head) pairs (FlashAttention-4 blog,
+// "Scheduling").
+__device__ __forceinline__ bool pair_unit(const FwdArgs& a, int num_m2, int u, PUnit& U) {
+    const int BH = a.B * a.Hq;
+    if (u >= BH * num_m2) return false;
+    int bh, m;
+    if (!a.causal) {
+        bh = u / num_m2;
+        m = u - bh * num_m2;
+    } else {
+        const int sec = a.l2_section, per = sec * num_m2, full = BH / sec;
+        if (u < full * per) {
+            const int s = u / per, r = u - s * per;
+            m = num_m2 - 1 - r / sec;
+            bh = s * sec + r % sec;
+        } else {
+            const int rem = BH - full * sec, r = u - full * per;
+            m = num_m2 - 1 - r / rem;
+            bh = full * sec + r % rem;
+        }
+    }
+    U.seq = bh / a.Hq;
+    U.h = bh - U.seq * a.Hq;
+    U.m2 = m;
+    U.tok0 = U.seq * a.N;
+    U.len = a.N;
+    return true;
+}
+
+// Key blocks the pair needs: causal stops at the block holding the last row.
+__device__ __forceinline__ int pair_blocks(const PUnit& U, int causal) {
+    int keys = U.len;
+    if (causal) {
+        const int last = (U.m2 + 1) * kBlockN;
+        keys = last < keys ? last : keys;
+    }
+    return (keys + kBlockN - 1) / kBlockN;
+}
+
+// S = Q K^T for the pair: M = 256, N = 256, K = d = 128; K-major, 128-B swizzle.
+__device__ __forceinline__ void pair_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+    constexpr uint32_t idesc = idesc_bf16_f32(256, 256, 0, 0);
+    const uint64_t qd = sdesc_sw128(q_smem, 16, 1024), kd = sdesc_sw128(k_smem, 16, 1024);
+#pragma unroll 1
+    for (uint32_t k = 0; k < 8; ++k) {
+        const uint32_t off = ((k >> 2) * kQBox + (k & 3) * 32) >> 4;   // Q and K halves share the layout
+        umma_ss_pair_w(d_tmem, qd + off, kd + off, idesc, k > 0);
+    }
+}
+
+// O (+)= P V for the pair: M = 256, N = 128, K = 256 keys; P from tensor
+// memory (8 columns per 16 keys), V MN-major, one 64-wide head-dim chunk per CTA.
+__device__ __forceinline__ void pair_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, uint32_t acc) {
+    constexpr uint32_t idesc = idesc_bf16_f32(256, 128, 0, 1);
+    const uint64_t vd = sdesc_sw128(v_smem, kVHalf, 1024);
+#pragma unroll 1
+    for (uint32_t k = 0; k < 16; ++k)
+        umma_ts_pair_w(d_tmem, p_tmem + k * 8, vd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
+}
+
+__device__ __forceinline__ bool pnamed_bar_or(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(n) : "memory");
+    return r != 0;
+}
+
+// Bounded wait on a phase this thread cannot report through (end-of-kernel drains).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(smem_u32(bar), parity) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
+fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t base = smem_u32(dsm);
+    // Both CTAs run the same code, so both see the same base and return together.
+    if (base & 1023u) {
+        if (tid == 0 && atomicCAS(&a.status->code, 0, -1) == 0) a.status->where = 600;
+        return;
+    }
+    // With cluster dimensions (2, 1, 1) the rank in the pair is blockIdx.x & 1.
+    const bool leader = cluster_rank() == 0;
+    PairShared& sh = *reinterpret_cast<PairShared*>(dsm + kOffBar);
+    float* red = reinterpret_cast<float*>(dsm + kOffRed);   // [2 parity][2 halves][128 rows]
+    const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
+    const int num_m2 = (a.N + kBlockN - 1) / kBlockN;
+    // Pair index and count, and this CTA's rank, are re-read from special
+    // registers where used rather than held (the softmax has no registers to spare).
+#define PAIR_ID ((int)(blockIdx.x >> 1))
+#define NUM_PAIRS ((int)(gridDim.x >> 1))
+#define RANK ((int)(blockIdx.x & 1))
+
+    if (tid == 0) {
+        mbar_init(&sh.q_full, 1);
+        mbar_init(&sh.q_empty, 1);
+        for (int i = 0; i < kKS; ++i) { mbar_init(&sh.kfull[i], 1); mbar_init(&sh.kempty[i], 1); }
+        for (int i = 0; i < kVS; ++i) { mbar_init(&sh.vfull[i], 1); mbar_init(&sh.vempty[i], 1); }
+        mbar_init(&sh.s_full, 1);
+        mbar_init(&sh.s_free, 16);     // one arrival per softmax warp of both CTAs
+        mbar_init(&sh.p_ready, 16);
+        mbar_init(&sh.pv_done, 1);
+        mbar_init(&sh.o_done, 1);
+        mbar_init(&sh.o_free, 16);
+        mbar_init(&sh.drain, 2);       // both issuers of the even CTA
+        sh.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+    }
+    if (warp == 0) {
+        tmem_alloc_pair(&sh.tmem_base, 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();   // barriers of both CTAs initialised before any remote arrival
+    tc_fence_after();
+
+    const WaitCtx wc{&sh.abort_flag, a.status};
+    const uint32_t tmem = sh.tmem_base;
+    const int group = a.Hq / a.Hkv;
+    // Cluster address of the even CTA's copy of a barrier (computed where
+    // used: the softmax threads have no registers to spare).
+    auto lead = [](uint64_t* bar) { return mapa_rank(smem_u32(bar), 0); };
+
+    // Register split: 2 * 128 * 224 + 128 * 56 == 384 * 168.
+    if (warp >= 8) {
+        regs_dec<56>();
+        if (warp == 8) {
+            // --------------------------------------------------- Q and K loader
+            if (lane == 0) {
+                uint32_t kit = 0, uc = 0;
+                bool ok = true;
+                for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
+                    PUnit U;
+                    if (!pair_unit(a, num_m2, u, U)) break;
+                    const int hk = U.h / group, nb = pair_blocks(U, a.causal);
+                    if (!(ok = mbar_wait(&sh.q_empty, (uc & 1) ^ 1, wc, kPSiteQEmpty))) break;
+                    if (leader) mbar_arrive_expect_tx(&sh.q_full, 2 * kQBytes);
+                    const int qrow = U.tok0 + U.m2 * kBlockN + RANK * kTileM;
+                    for (int c = 0; c < 2; ++c) tma_load_3d_pair(sQ + c * kQBox, &tq, lead(&sh.q_full), c * 64, U.h, qrow);
+                    for (int j = 0; j < nb; ++j) {
+                        const uint32_t slot = kit % kKS;
+                        if (!(ok = mbar_wait(&sh.kempty[slot], ((kit / kKS) & 1) ^ 1, wc, kPSiteKEmpty))) break;
+                        if (leader) mbar_arrive_expect_tx(&sh.kfull[slot], 2 * kKHalf);
+                        const uint32_t bar = lead(&sh.kfull[slot]);
+                        const int krow = U.tok0 + j * kBlockN + RANK * kTileM;
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_3d_pair(sK + slot * kKHalf + c * kKBox, &tk, bar, c * 64, hk, krow);
+                        ++kit;
+                    }
+                    ++uc;
+                }
+                // The even CTA's full barriers count both CTAs' bytes: once the
+                // last phases are complete nothing of ours is in flight.
+                if (leader) {
+                    for (uint32_t i = (kit > kKS ? kit - kKS : 0); i < kit; ++i)
+                        drain_wait(&sh.kfull[i % kKS], (i / kKS) & 1);
+                    if (uc > 0) drain_wait(&sh.q_full, (uc - 1) & 1);
+                }
+            }
+            __syncwarp();
+        } else if (warp == 10) {
+            // --------------------------------------------------------- V loader
+            if (lane == 0) {
+                uint32_t vit = 0;
+                bool ok = true;
+                for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
+                    PUnit U;
+                    if (!pair_unit(a, num_m2, u, U)) break;
+                    const int hk = U.h / group, nb = pair_blocks(U, a.causal);
+                    for (int j = 0; j < nb; ++j) {
+                        const uint32_t slot = vit % kVS;
+                        if (!(ok = mbar_wait(&sh.vempty[slot], ((vit / kVS) & 1) ^ 1, wc, kPSiteVEmpty))) break;
+                        if (leader) mbar_arrive_expect_tx(&sh.vfull[slot], 2 * kVHalf);
+                        tma_load_3d_pair(sV + slot * kVHalf, &tv, lead(&sh.vfull[slot]),
+                                         RANK * 64, hk, U.tok0 + j * kBlockN);
+                        ++vit;
+                    }
+                }
+                if (leader)
+                    for (uint32_t i = (vit > kVS ? vit - kVS : 0); i < vit; ++i)
+                        drain_wait(&sh.vfull[i % kVS], (i / kVS) & 1);
+            }
+            __syncwarp();
+        } else if (warp == 9 && leader) {
+            // ------------------------------------------------------- S issuer
+            // S(j) for every j: K block loaded and the previous S (of this or
+            // the previous unit) copied out by both CTAs.  Q is released after
+            // the unit's last S, so the next unit's Q loads while this unit's
+            // last block is still in softmax and P V.
+            uint32_t kit = 0, uc = 0, gs = 0;
+            bool ok = true;
+            for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
+                PUnit U;
+                if (!pair_unit(a, num_m2, u, U)) break;
+                const int nb = pair_blocks(U, a.causal);
+                if (!(ok = mbar_wait_w(&sh.q_full, uc & 1, wc, kPSiteQFull))) break;
+                for (int j = 0; j < nb; ++j) {
+                    const uint32_t kslot = kit % kKS;
+                    if (!(ok = mbar_wait_w(&sh.kfull[kslot], (kit / kKS) & 1, wc, kPSiteKFull))) break;
+                    ++kit;
+                    if (gs > 0 && !(ok = mbar_wait_w(&sh.s_free, (gs - 1) & 1, wc, kPSiteSFree))) break;
+                    tc_fence_after();
+                    pair_qk(tmem + kColS, sQ, sK + kslot * kKHalf);
+                    umma_commit_pair_w(&sh.s_full, kBoth);
+                    umma_commit_pair_w(&sh.kempty[kslot], kBoth);
+                    if (j + 1 == nb) umma_commit_pair_w(&sh.q_empty, kBoth);
+                    ++gs;
+                }
+                ++uc;
+            }
+            umma_commit_pair_w(&sh.drain, 1);   // this CTA only
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&sh.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+            __syncwarp();
+        } else if (warp == 11 && leader) {
+            // ----------------------------------------------------- P V issuer
+            // A warp of its own, so that neither product kind waits behind the
+            // other's issue (the tensor core's queue is short: issuing blocks
+            // until earlier products drain).
+            uint32_t vit = 0, uc = 0, gp = 0;
+            bool ok = true;
+            for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
+                PUnit U;
+                if (!pair_unit(a, num_m2, u, U)) break;
+                const int nb = pair_blocks(U, a.causal);
+                for (int j = 0; j < nb; ++j) {
+                    const uint32_t vslot = vit % kVS;
+                    if (!(ok = mbar_wait_w(&sh.vfull[vslot], (vit / kVS) & 1, wc, kPSiteVFull))) break;
+                    ++vit;
+                    if (j == 0 && !(ok = mbar_wait_w(&sh.o_free, (uc & 1) ^ 1, wc, kPSiteOFree))) break;
+                    if (!(ok = mbar_wait_w(&sh.p_ready, gp & 1, wc, kPSiteP))) break;
+                    tc_fence_after();
+                    pair_pv(tmem + kColO, tmem + kColP, sV + vslot * kVHalf, j > 0);
+                    umma_commit_pair_w(&sh.pv_done, kBoth);
+                    umma_commit_pair_w(&sh.vempty[vslot], kBoth);
+                    ++gp;
+                }
+                if (!ok) break;
+                umma_commit_pair_w(&sh.o_done, kBoth);
+                ++uc;
+            }
+            umma_commit_pair_w(&sh.drain, 1);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&sh.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+            __syncwarp();
+        }
+    } else {
+        regs_inc<224>();
+        // ------------------------------------------------------------ softmax
+        const int x = warp >> 2;                      // which half of the 256 columns
+        const int r = (warp & 3) * 32 + lane;         // row == TMEM lane
+        const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lb + kColS + x * 128;
+        const uint32_t tP = tmem + lb + kColP + x * 64;
+        const uint32_t tO = tmem + lb + kColO + x * 64;
+        const float scale = a.scale_log2;
+        uint32_t sc = 0, pc = 0, uc = 0;
+        uint32_t ep = 0;   // barrier epoch: exchange buffers alternate with it
+        bool ok = true;
+        for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
+            PUnit U;
+            if (!pair_unit(a, num_m2, u, U)) break;
+            const int nb = pair_blocks(U, a.causal);
+            const int m = U.m2 * 2 + RANK;         // this CTA's 128-row query tile
+            const int qi = m * kTileM + r;
+            float m_ref = -INFINITY, l = 0.f;           // l: this half's partial row sum
+            bool okw = true;
+            for (int j = 0; j < nb; ++j) {
+                okw = mbar_wait(&sh.s_full, sc & 1, wc, kPSiteS) && okw;
+                ++sc;
+                tc_fence_after();
+                float s[128];
+                {
+                    uint32_t* su = reinterpret_cast<uint32_t*>(s);
+                    tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(su + 0));
+                    tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
+                    tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(su + 64));
+                    tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(su + 96));
+                    tmem_wait_ld();
+                }
+                tc_fence_before();
+                mbar_arrive_remote_w(lead(&sh.s_free));   // the next S may overwrite these columns
+                const int k0 = j * kBlockN + x * 128;   // key of column 0 of this half
+                if (k0 + 128 > U.len || (a.causal && k0 + 127 > m * kTileM)) {
+                    const int lim_len = U.len - k0;
+                    const int lim_causal = a.causal ? qi - k0 + 1 : 128;
+                    const int lim = lim_len < lim_causal ? lim_len : lim_causal;
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c >= lim) s[c] = -INFINITY;
+                }
+                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int c = 4; c < 128; c += 4) {
+                    mx0 = fmaxf(mx0, s[c]);
+                    mx1 = fmaxf(mx1, s[c + 1]);
+                    mx2 = fmaxf(mx2, s[c + 2]);
+                    mx3 = fmaxf(mx3, s[c + 3]);
+                }
+                float* rb = red + (ep & 1) * 256;
+                rb[x * 128 + r] = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+                ++ep;
+                if (pnamed_bar_or(2, 256, !okw)) { ok = false; break; }
+                const float m_blk = fmaxf(rb[r], rb[128 + r]) * scale;   // whole-row max, log2 units
+                const float m_new = fmaxf(m_ref, m_blk);
+                // Conditional rescale (FlashAttention-4 blog, "Forward pass"):
+                // both halves see the same row maxima, so their warp votes agree.
+                const bool jump = (m_ref == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_ref > a.tau);
+                const bool rescale = __any_sync(0xffffffffu, jump);
+                float fac = 1.f;
+                if (rescale) {
+                    fac = (m_ref == -INFINITY) ? 0.f : ex2_mufu(m_ref - m_new);
+                    l *= fac;
+                    m_ref = m_new;
+                }
+                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                uint32_t pk[64];
+                float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const float p0 = ex2_mufu(fmaf(s[2 * i], scale, -m_use));
+                    const float p1 = ex2_mufu(fmaf(s[2 * i + 1], scale, -m_use));
+                    l0 += p0;
+                    l1 += p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                l += l0 + l1;
+                // P's columns and O are free once the previous P V is done.
+                if (j > 0) {
+                    okw = mbar_wait(&sh.pv_done, pc & 1, wc, kPSitePV) && okw;
+                    ++pc;
+                    tc_fence_after();
+                    if (rescale) {
+#pragma unroll
+                        for (int c0 = 0; c0 < 64; c0 += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + c0, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * fac);
+                            tmem_st32(tO + c0, o);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int st = 0; st < 4; ++st)
+                    tmem_st16(tP + st * 16, *reinterpret_cast<const uint32_t(*)[16]>(pk + st * 16));
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive_remote_w(lead(&sh.p_ready));
+            }
+            if (!ok) break;
+            okw = mbar_wait(&sh.o_done, uc & 1, wc, kPSiteO) && okw;
+            ++uc;
+            if (nb > 0) ++pc;   // the unit's last P V: its pv_done phase
+            tc_fence_after();
+            // Epilogue: whole-row sum from the two halves, O / l, LSE.
+            float* rl = red + (ep & 1) * 256;
+            rl[x * 128 + r] = l;
+            ++ep;
+            if (pnamed_bar_or(2, 256, !okw)) { ok = false; break; }
+            const float lt = rl[r] + rl[128 + r];
+            const bool valid = qi < U.len;
+            const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+            uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) +
+                                                   ((size_t)(U.tok0 + qi) * a.Hq + U.h) * kHeadDim + x * 64);
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld32(tO + c0, o);
+                tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float* f = reinterpret_cast<const float*>(o + 8 * q);
+                        orow[c0 / 8 + q] = make_uint4(pack_bf16x2(f[0] * inv_l, f[1] * inv_l),
+                                                      pack_bf16x2(f[2] * inv_l, f[3] * inv_l),
+                                                      pack_bf16x2(f[4] * inv_l, f[5] * inv_l),
+                                                      pack_bf16x2(f[6] * inv_l, f[7] * inv_l));
+                    }
+                }
+            }
+            if (valid && x == 0)
+                a.lse[((size_t)U.seq * a.Hq + U.h) * a.N + qi] =
+                    lt > 0.f ? (m_ref + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
+            tc_fence_before();
+            mbar_arrive_remote_w(lead(&sh.o_free));
+        }
+    }
+
+    // After an abort the odd CTA cannot observe its own last loads (they count
+    // on the even CTA's barriers): give them time to land before its shared
+    // memory is released.
+    if (sh.abort_flag) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {}
+    }
+    tc_fence_before();
+    cluster_sync_all();   // no product, load or remote arrival still targets either CTA
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc_pair(tmem, 512);
+}
+
+#undef PAIR_ID
+#undef NUM_PAIRS
+#undef RANK
+
+}  // namespace
+
+int g_pairs_resident = 0;
+
+cudaError_t launch_fwd_pair(const FwdLaunch& L, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmem);
+    if (e != cudaSuccess) return e;
+    // Persistent: as many pairs as can be resident at once (clusters must fit
+    // inside one GPC, so this can be below half the SM count).
+    int max_pairs = g_pairs_resident;
+    if (max_pairs == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (unsigned)(L.num_sms / 2), 1, 1);
+        cfg.blockDim = dim3(kPThreads, 1, 1);
+        cfg.dynamicSmemBytes = kPSmem;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, fwd_pair_kernel, &cfg) != cudaSuccess || n < 1) n = L.num_sms / 2;
+        max_pairs = g_pairs_resident = n;
+    }
+    const long long units = (long long)L.a.B * L.a.Hq * ((L.a.N + kBlockN - 1) / kBlockN);
+    int pairs = (int)(units < max_pairs ? units : max_pairs);
+    if (pairs < 1) pairs = 1;
+    fwd_pair_kernel<<<2 * pairs, kPThreads, kPSmem, stream>>>(L.tq, L.tk, L.tv, L.a);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -110,6 +110,10 @@ cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream);
 // Launch the 256-key-block forward kernel (fa_fwd_wide.cu; fixed length
 // only).  Its K and V maps use boxes of 256 rows.
 cudaError_t launch_fwd_wide(const FwdLaunch& L, cudaStream_t stream);
+// CTA-pair kernel (clusters of two), fixed length, MUFU exp2.
+cudaError_t launch_fwd_pair(const FwdLaunch& L, cudaStream_t stream);
+// CTA pairs the pair kernel keeps resident (0 until its first launch).
+extern int g_pairs_resident;
 
 // Evaluate the FMA-pipe exp2 on n floats (fa_fwd.cu).
 cudaError_t launch_exp2_emu(const float* x, float* y, int64_t n, cudaStream_t stream);

@@ -48,7 +48,8 @@ def parse():
     ap.add_argument("--deterministic", action="store_true", help="backward in deterministic mode")
     ap.add_argument("--exp2-emu", type=int, default=0, help="forward: eighths of exp2 on the FMA pipe (0-2)")
     ap.add_argument("--tau", type=float, default=8.0, help="forward: conditional-rescale threshold (log2 units)")
-    ap.add_argument("--fwd-kernel", type=int, default=1, help="forward kernel: 0 ping-pong 128x128, 1 256-key blocks")
+    ap.add_argument("--fwd-kernel", type=int, default=2,
+                    help="forward kernel: 0 ping-pong 128x128, 1 256-key blocks, 2 CTA pairs with 256-key blocks")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
     return ap.parse_args()
@@ -334,6 +335,11 @@ def run_ours(args, rank, world):
     return locals()
 
 
+def fa_pairs_resident():
+    import attention_blackwell_gb300 as fa
+    return fa.fwd_pairs_resident()
+
+
 def describe(w, inp):
     head = "%s: B=%d Hq=%d Hkv=%d d=%d %s" % (w.name, w.B, w.Hq, w.Hkv, w.d, "causal" if w.causal else "non-causal")
     if w.varlen:
@@ -376,7 +382,9 @@ def main_ours(args):
         "config": {"workload": describe(w, r["inp"]),
             "step": step_name, "global_batch": w.B * world, "seq_len": w.N or max(r["inp"]["lengths"]),
             "deterministic_bwd": bool(args.deterministic), "exp2_emu_eighths": args.exp2_emu, "tau": args.tau,
-            "fwd_kernel": "256-key blocks" if args.fwd_kernel == 1 and not w.varlen else "ping-pong 2x128",
+            "fwd_kernel": ("ping-pong 2x128" if w.varlen or args.exp2_emu else
+                           {0: "ping-pong 2x128", 1: "256-key blocks", 2: "CTA pairs, 256-key blocks"}[args.fwd_kernel]),
+            "fwd_pairs_resident": fa_pairs_resident(),
             "parallelism": "replicas" if world > 1 else "single",
             "l2": "no flush: the step's inputs (%.0f MiB) exceed the 126 MB L2" % (
                 sum(r["t"][n].numel() * 2 for n in ("q", "k", "v", "do")) / 2 ** 20)},

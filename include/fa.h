@@ -81,14 +81,25 @@ int fa_set_tuning(int exp2_emu_eighths, float tau);
  * Process-wide choice of the forward kernel (affects later fa_fwd calls):
  *   0 -- two 128-row query tiles per CTA in ping-pong, 128-key tiles: the
  *        pipeline of the FlashAttention-4 blog, "Forward pass";
- *   1 -- (default) one 128-row query tile per CTA, 256-key blocks, so the
- *        S = Q K^T product is a 128x256 UMMA, which runs at the tensor
- *        core's full rate on GB300 (the 128x128 shape does not).
- * Kernel 1 serves fixed-length inputs with exp2_emu_eighths == 0; all other
- * calls use kernel 0.  Both compute the same attention up to rounding.
+ *   1 -- one 128-row query tile per CTA, 256-key blocks, so the S = Q K^T
+ *        product is a 128x256 UMMA, which runs at the tensor core's full
+ *        rate on GB300 (the 128x128 shape does not);
+ *   2 -- (default) CTA pairs (clusters of two): 256 query rows per pair and
+ *        256-key blocks, each product one M = 256 UMMA over both SMs, so each
+ *        SM loads and reads only half of every K and V block.
+ * Kernels 1 and 2 serve fixed-length inputs with exp2_emu_eighths == 0; all
+ * other calls use kernel 0.  All compute the same attention up to rounding.
  * Errors: FA_ERR_INVALID.
  */
 int fa_set_fwd_kernel(int kernel);
+
+/*
+ * Number of CTA pairs forward kernel 2 keeps resident (its persistent grid is
+ * that many clusters of two; a cluster must fit inside one GPC, so this can be
+ * below half the SM count).  0 until the kernel has been launched once in
+ * this process.  Never fails.
+ */
+int fa_fwd_pairs_resident(void);
 
 /*
  * Forward: O and LSE of exact attention (FlashAttention-4 blog, "Forward

@@ -77,3 +77,14 @@ def test_set_tuning_validation(lib):
     assert lib.fa_set_tuning(7, 8.0) == -2
     assert lib.fa_set_tuning(0, -1.0) == -1
     assert lib.fa_set_tuning(0, 8.0) == 0
+
+
+def test_forward_kernel_selector(lib):
+    """Kernels 0-2 are accepted, others rejected; no GPU call is made and the
+    pair kernel reports no resident pairs before it has ever been launched."""
+    assert lib.fa_fwd_pairs_resident() == 0
+    for k in (0, 1, 2):
+        assert lib.fa_set_fwd_kernel(k) == 0
+    assert lib.fa_set_fwd_kernel(3) == -1
+    assert lib.fa_set_fwd_kernel(-1) == -1
+    assert lib.fa_set_fwd_kernel(2) == 0
