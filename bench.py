@@ -156,7 +156,7 @@ def measured_peaks():
 
 def kernel_traffic(name):
     """dram bytes per launch from the committed ncu summary, or None when the
-    kernel's source changed since the counters were taken."""
+    kernel's sources changed since the counters were taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
@@ -165,12 +165,22 @@ def kernel_traffic(name):
         return None
     if not rec:
         return None
-    src = os.path.join(ROOT, rec["source"])
+    h = hashlib.sha256()
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    except OSError:
+        for src in rec["sources"]:
+            h.update(open(os.path.join(ROOT, src), "rb").read())
+    except (OSError, KeyError):
         return None
-    return rec["dram_bytes_per_launch"] if sha == rec["source_sha"] else None
+    return rec["dram_bytes_per_launch"] if h.hexdigest()[:16] == rec["sources_sha"] else None
+
+
+def traffic_key(args, w, kernel):
+    """Record name in profiles/dram_traffic.json for a step kernel."""
+    if kernel != "fwd":
+        return kernel
+    if w.varlen or args.exp2_emu or args.fwd_kernel == 0:
+        return "fwd_pingpong"
+    return {1: "fwd_wide", 2: "fwd_pair"}[args.fwd_kernel]
 
 
 def _slice(inp, w, b):
@@ -398,7 +408,7 @@ def main_ours(args):
                      "peak_source": peak_src,
                      "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4)
                      if achieved and peaks and peaks.get("bf16_tflops_sustained") else None,
-                     "traffic": kernel_traffic(dom["kernel"])},
+                     "traffic": kernel_traffic(traffic_key(args, w, dom["kernel"]))},
         "e2e": {"value": round(r["e2e_value"], 2), "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "steps": r["E"]},
         "gpu_launches": K * sum(p["launches_per_step"] for p in per_kernel),
