@@ -219,19 +219,20 @@ __device__ __forceinline__ bool bwd_unit(const BwdArgs& a, int total, int u, BUn
 __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a_smem, uint32_t b_smem) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
     const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, 16, 1024);
-#pragma unroll 1
-    for (uint32_t k = 0; k < 8; ++k) {
-        const uint32_t off = ((k >> 2) * kBox + (k & 3) * 32) >> 4;
-        umma_ss_w(d, ad + off, bd + off, idesc, k > 0);
-    }
+    static_for<8>([&](auto kc) {
+        constexpr uint32_t k = kc, off = ((k >> 2) * kBox + (k & 3) * 32) >> 4;
+        umma_ss_k<off, off>(d, ad, bd, idesc, k > 0);
+    });
 }
 
 // D (+)= A[tmem] B, B MN-major in shared memory (dV += P^T dO).
 __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b_smem, uint32_t acc) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
     const uint64_t bd = sdesc_sw128(b_smem, kBox, 1024);
-#pragma unroll 1
-    for (uint32_t k = 0; k < 8; ++k) umma_ts_w(d, a_tmem + k * 8, bd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
+    static_for<8>([&](auto kc) {
+        constexpr uint32_t k = kc;
+        umma_ts_k<k * 8, ((k * 2048) >> 4)>(d, a_tmem, bd, idesc, (acc | k) != 0);
+    });
 }
 
 // D = A B with A and B both MN-major in shared memory (dQ = dS K: dS^T is
@@ -239,8 +240,10 @@ __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b_s
 __device__ __forceinline__ void mma_nn(uint32_t d, uint32_t a_smem, uint32_t b_smem) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 1, 1);
     const uint64_t ad = sdesc_sw128(a_smem, kBox, 1024), bd = sdesc_sw128(b_smem, kBox, 1024);
-#pragma unroll 1
-    for (uint32_t k = 0; k < 8; ++k) umma_ss_w(d, ad + ((k * 2048) >> 4), bd + ((k * 2048) >> 4), idesc, k > 0);
+    static_for<8>([&](auto kc) {
+        constexpr uint32_t k = kc, off = (k * 2048) >> 4;
+        umma_ss_k<off, off>(d, ad, bd, idesc, k > 0);
+    });
 }
 
 __device__ __forceinline__ void fence_async_smem() {

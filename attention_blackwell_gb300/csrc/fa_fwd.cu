@@ -150,11 +150,10 @@ struct FwdShared {
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
     const uint64_t qd = sdesc_sw128(q_smem, 16, 1024), kd = sdesc_sw128(k_smem, 16, 1024);
-#pragma unroll 1
-    for (uint32_t k = 0; k < 8; ++k) {
-        const uint32_t off = ((k >> 2) * kBoxBytes + (k & 3) * 32) >> 4;  // 16-byte units
-        umma_ss_w(d_tmem, qd + off, kd + off, idesc, k > 0);
-    }
+    static_for<8>([&](auto kc) {
+        constexpr uint32_t k = kc, off = ((k >> 2) * kBoxBytes + (k & 3) * 32) >> 4;  // 16-byte units
+        umma_ss_k<off, off>(d_tmem, qd, kd, idesc, k > 0);
+    });
 }
 
 // O (+)= P V: A = P (bf16 in TMEM, 8 columns per k-step of 16 keys),
@@ -162,9 +161,10 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, uint32_t acc) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
     const uint64_t vd = sdesc_sw128(v_smem, kBoxBytes, 1024);
-#pragma unroll 1
-    for (uint32_t k = 0; k < 8; ++k)
-        umma_ts_w(d_tmem, p_tmem + k * 8, vd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
+    static_for<8>([&](auto kc) {
+        constexpr uint32_t k = kc;
+        umma_ts_k<k * 8, ((k * 2048) >> 4)>(d_tmem, p_tmem, vd, idesc, (acc | k) != 0);
+    });
 }
 
 template <int kEmuEighths>

@@ -113,11 +113,11 @@ __device__ __forceinline__ int pair_blocks(const PUnit& U, int causal) {
 __device__ __forceinline__ void pair_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
     constexpr uint32_t idesc = idesc_bf16_f32(256, 256, 0, 0);
     const uint64_t qd = sdesc_sw128(q_smem, 16, 1024), kd = sdesc_sw128(k_smem, 16, 1024);
-#pragma unroll 1
-    for (uint32_t k = 0; k < 8; ++k) {
-        const uint32_t off = ((k >> 2) * kQBox + (k & 3) * 32) >> 4;   // Q and K halves share the layout
-        umma_ss_pair_w(d_tmem, qd + off, kd + off, idesc, k > 0);
-    }
+    static_for<8>([&](auto kc) {
+        constexpr uint32_t k = kc;
+        constexpr uint32_t off = ((k >> 2) * kQBox + (k & 3) * 32) >> 4;   // Q and K halves share the layout
+        umma_ss_k<off, off, 2>(d_tmem, qd, kd, idesc, k > 0);
+    });
 }
 
 // O (+)= P V for the pair: M = 256, N = 128, K = 256 keys; P from tensor
@@ -125,9 +125,10 @@ __device__ __forceinline__ void pair_qk(uint32_t d_tmem, uint32_t q_smem, uint32
 __device__ __forceinline__ void pair_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, uint32_t acc) {
     constexpr uint32_t idesc = idesc_bf16_f32(256, 128, 0, 1);
     const uint64_t vd = sdesc_sw128(v_smem, kVHalf, 1024);
-#pragma unroll 1
-    for (uint32_t k = 0; k < 16; ++k)
-        umma_ts_pair_w(d_tmem, p_tmem + k * 8, vd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
+    static_for<16>([&](auto kc) {
+        constexpr uint32_t k = kc;
+        umma_ts_k<k * 8, ((k * 2048) >> 4), 2>(d_tmem, p_tmem, vd, idesc, (acc | k) != 0);
+    });
 }
 
 __device__ __forceinline__ bool pnamed_bar_or(int id, int n, bool pred) {

@@ -105,12 +105,12 @@ __device__ __forceinline__ int wide_blocks(const WUnit& U, int causal) {
 __device__ __forceinline__ void wide_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 0);
     const uint64_t qd = sdesc_sw128(q_smem, 16, 1024), kd = sdesc_sw128(k_smem, 16, 1024);
-#pragma unroll 1
-    for (uint32_t k = 0; k < 8; ++k) {
-        const uint32_t qo = ((k >> 2) * kQBox + (k & 3) * 32) >> 4;
-        const uint32_t ko = ((k >> 2) * kKVBox + (k & 3) * 32) >> 4;
-        umma_ss_w(d_tmem, qd + qo, kd + ko, idesc, k > 0);
-    }
+    static_for<8>([&](auto kc) {
+        constexpr uint32_t k = kc;
+        constexpr uint32_t qo = ((k >> 2) * kQBox + (k & 3) * 32) >> 4;
+        constexpr uint32_t ko = ((k >> 2) * kKVBox + (k & 3) * 32) >> 4;
+        umma_ss_k<qo, ko>(d_tmem, qd, kd, idesc, k > 0);
+    });
 }
 
 // O (+)= P V: M = 128, N = d = 128, K = 256 keys; A = P from TMEM (8 columns
@@ -118,9 +118,10 @@ __device__ __forceinline__ void wide_qk(uint32_t d_tmem, uint32_t q_smem, uint32
 __device__ __forceinline__ void wide_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, uint32_t acc) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
     const uint64_t vd = sdesc_sw128(v_smem, kKVBox, 1024);
-#pragma unroll 1
-    for (uint32_t k = 0; k < 16; ++k)
-        umma_ts_w(d_tmem, p_tmem + k * 8, vd + ((k * 2048) >> 4), idesc, (acc | k) != 0);
+    static_for<16>([&](auto kc) {
+        constexpr uint32_t k = kc;
+        umma_ts_k<k * 8, ((k * 2048) >> 4)>(d_tmem, p_tmem, vd, idesc, (acc | k) != 0);
+    });
 }
 
 __device__ __forceinline__ bool wnamed_bar_or(int id, int n, bool pred) {

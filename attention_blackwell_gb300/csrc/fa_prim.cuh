@@ -12,6 +12,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace fa {
 
 // ----------------------------------------------------------------------------
@@ -364,6 +366,84 @@ __device__ __forceinline__ void umma_commit_pair_w(uint64_t* bar, uint16_t cta_m
         "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
         ::"r"(smem_u32(bar)), "h"(cta_mask) : "memory");
+}
+
+// ----------------------------------------------------------------------------
+// Straight-line issue.  A 128x128x16 product occupies the tensor core for 64
+// cycles; an issue loop that recomputes descriptors at run time costs the
+// issuing warp more than that per instruction, so the core starves (measured
+// on GB300: 8 K-steps from a rolled loop ~105 cycles each, from straight-line
+// code 64.1).  These forms take each step's descriptor offset as an immediate
+// and add it to the low word inside the instruction's own asm block: a shared
+// address below 256 KB keeps the 14-bit start-address field from carrying,
+// and nothing is hoisted into registers.
+// ----------------------------------------------------------------------------
+template <int... I>
+struct int_seq {};
+template <int N, int... I>
+struct make_int_seq : make_int_seq<N - 1, N - 1, I...> {};
+template <int... I>
+struct make_int_seq<0, I...> {
+    using type = int_seq<I...>;
+};
+template <typename F, int... I>
+__device__ __forceinline__ void static_for_impl(F& f, int_seq<I...>) {
+    (f(std::integral_constant<int, I>{}), ...);
+}
+// f(std::integral_constant<int, k>) for k = 0 .. N-1, unrolled at compile time.
+template <int N, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+    static_for_impl(f, typename make_int_seq<N>::type{});
+}
+
+// D[tmem] (+)= A[smem] B[smem]; AO, BO: descriptor offsets (bytes >> 4).
+template <uint32_t AO, uint32_t BO, int GROUP = 1>
+__device__ __forceinline__ void umma_ss_k(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    if constexpr (GROUP == 1)
+        asm volatile(
+            "{\n\t.reg .pred p, e;\n\t.reg .b32 al, ah, bl, bh;\n\t.reg .b64 ad, bd;\n\t"
+            "mov.b64 {al, ah}, %1;\n\tmov.b64 {bl, bh}, %2;\n\t"
+            "add.u32 al, al, %5;\n\tadd.u32 bl, bl, %6;\n\t"
+            "mov.b64 ad, {al, ah};\n\tmov.b64 bd, {bl, bh};\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n\t}"
+            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(AO), "n"(BO) : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p, e;\n\t.reg .b32 al, ah, bl, bh;\n\t.reg .b64 ad, bd;\n\t"
+            "mov.b64 {al, ah}, %1;\n\tmov.b64 {bl, bh}, %2;\n\t"
+            "add.u32 al, al, %5;\n\tadd.u32 bl, bl, %6;\n\t"
+            "mov.b64 ad, {al, ah};\n\tmov.b64 bd, {bl, bh};\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::2.kind::f16 [%0], ad, bd, %3, p;\n\t}"
+            ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(AO), "n"(BO) : "memory");
+}
+
+// D[tmem] (+)= A[tmem + AC columns] B[smem]; BO: descriptor offset (bytes >> 4).
+template <uint32_t AC, uint32_t BO, int GROUP = 1>
+__device__ __forceinline__ void umma_ts_k(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    if constexpr (GROUP == 1)
+        asm volatile(
+            "{\n\t.reg .pred p, e;\n\t.reg .b32 bl, bh, at;\n\t.reg .b64 bd;\n\t"
+            "mov.b64 {bl, bh}, %2;\n\tadd.u32 bl, bl, %6;\n\tmov.b64 bd, {bl, bh};\n\t"
+            "add.u32 at, %1, %5;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], bd, %3, p;\n\t}"
+            ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(AC), "n"(BO) : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p, e;\n\t.reg .b32 bl, bh, at;\n\t.reg .b64 bd;\n\t"
+            "mov.b64 {bl, bh}, %2;\n\tadd.u32 bl, bl, %6;\n\tmov.b64 bd, {bl, bh};\n\t"
+            "add.u32 at, %1, %5;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "elect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [at], bd, %3, p;\n\t}"
+            ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "n"(AC), "n"(BO) : "memory");
 }
 
 // Bounded wait executed by a whole warp; the result is made warp-uniform.
