@@ -144,15 +144,18 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 //               of a unit stores dK (x alpha) and dV in bf16;
 //   warp  8     loader: K, V once per unit (TMA), then Q_i, dO_i (TMA) and
 //               LSE_i, D_i (plain loads) into a two-stage ring;
-//   warp  9     UMMA issuer (one thread);  warps 10-11 idle.
+//   warp  9     issues dV, dK, dQ, dP;  warp 10 issues S;  warp 11 idle.
 //
 // Tensor memory (512 columns): dK acc 0-127, dV acc 128-255,
-//   R0 256-383: S^T, then P^T (bf16, first 64 columns);
-//   R1 384-511: dP^T, then dS^T (bf16, first 64 columns; operand A of dK),
-//               then dQ_i (the paper's 1-CTA sharing of dP/dS/dQ columns).
-// Per query tile the UMMA order is dV, dK, S(next), dQ, dP(next): the next
-// tile's S^T is in flight while dQ of this tile drains (FlashAttention-4 blog,
-// "Backward pass": dK/dQ of tile j-1 overlap the elementwise work of tile j).
+//   R0 256-383: S^T, then P^T (bf16; each key-row half packs its 64 queries
+//               into the first 32 of the 64 columns it read);
+//   R1 384-511: dP^T, then dS^T (bf16, same packing; operand A of dK), then
+//               dQ_i (the paper's 1-CTA sharing of dP/dS/dQ columns).
+// Warp 10 issues each S^T as soon as its Q tile is loaded and dV has read
+// the previous P^T out of R0, so the next tile's S^T is computed while this
+// tile's dS is (FlashAttention-4 blog, "Backward pass": the next tile's
+// products overlap the elementwise work); warp 9 issues dV, dK, dQ and the
+// next dP in that order.
 //
 // Shared memory (dynamic, 1024-aligned, 232448 bytes):
 //   K 32K | V 32K | Q[2] 2x32K | dO 32K | dS 32K | dQ staging 32K | lse2[2][128], D[2][128] | barriers
@@ -168,7 +171,7 @@ constexpr uint32_t kBwdSmem = kOffBar + 1024;           // 232448
 
 struct BwdShared {
     uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty;
-    uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dq_full, dq_free, dkdv_done, acc_free, drain;
+    uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dq_full, dq_free, dkdv_done, acc_free, drain, r0_free;
     uint32_t tmem_base;
     int abort_flag;
     int total;
@@ -225,13 +228,16 @@ __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a_smem, uint32_t b_s
     });
 }
 
-// D (+)= A[tmem] B, B MN-major in shared memory (dV += P^T dO).
+// D (+)= A[tmem] B, B MN-major in shared memory (dV += P^T dO, dK += dS^T Q).
+// A is bf16 in the region the two key-row halves wrote: queries 0-63 in
+// columns 0-31 of the region, queries 64-127 in columns 64-95 (each half
+// packs its 64 queries at the start of the 64 columns it read).
 __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b_smem, uint32_t acc) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
     const uint64_t bd = sdesc_sw128(b_smem, kBox, 1024);
     static_for<8>([&](auto kc) {
-        constexpr uint32_t k = kc;
-        umma_ts_k<k * 8, ((k * 2048) >> 4)>(d, a_tmem, bd, idesc, (acc | k) != 0);
+        constexpr uint32_t k = kc, col = k * 8 + (k >= 4 ? 32 : 0);
+        umma_ts_k<col, ((k * 2048) >> 4)>(d, a_tmem, bd, idesc, (acc | k) != 0);
     });
 }
 
@@ -256,7 +262,7 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32
                  ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y) : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -319,7 +325,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         mbar_init(&sh.dq_free, 128);
         mbar_init(&sh.dkdv_done, 1);
         mbar_init(&sh.acc_free, 128);
-        mbar_init(&sh.drain, 1);
+        mbar_init(&sh.drain, 2);   // both issuers
+        mbar_init(&sh.r0_free, 1);
         sh.abort_flag = 0;
         sh.total = a.varlen ? a.hdr->total_units : a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN);
         fence_mbar_init();
@@ -373,6 +380,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     if (lane == 0) ok = mbar_wait(&sh.q_empty[st], ((jj >> 1) & 1) ^ 1, wc, kBSiteQEmpty);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
+                    // Q first (its latency overlaps the LSE/D loads); the
+                    // phase's one arrival follows the LSE/D stores.
+                    if (lane == 0) {
+                        mbar_expect_tx(&sh.q_full[st], kT32);
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_3d(base + kOffQ + st * kT32 + c * kBox, &tq, &sh.q_full[st], c * 64, h,
+                                        U.tok0 + i * kTileM);
+                    }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int row = 4 * lane + e, q = i * kTileM + row;
@@ -388,10 +403,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     }
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(&sh.q_full[st], kT32);
-                        for (int c = 0; c < 2; ++c)
-                            tma_load_3d(base + kOffQ + st * kT32 + c * kBox, &tq, &sh.q_full[st], c * 64, h,
-                                        U.tok0 + i * kTileM);
+                        mbar_arrive(&sh.q_full[st]);
                         ok = mbar_wait(&sh.do_empty, (jj & 1) ^ 1, wc, kBSiteQEmpty);
                         if (ok) {
                             mbar_arrive_expect_tx(&sh.do_full, kT32);
@@ -417,62 +429,77 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                            globaltimer_ns() - t0 < kWaitLimitNs) {}
             }
             __syncwarp();
-        } else if (warp == 9) {
-            // ------------------------------------------------------- UMMA issuer
-            {   // the whole warp runs the issue loop (see umma_ss_w)
-                uint32_t jj = 0, uc = 0;
-                bool ok = true;
-                for (int u = blockIdx.x; ok; u += gridDim.x) {
-                    BUnit U;
-                    if (!bwd_unit(a, total, u, U)) break;
-                    if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, kBSiteKvFull))) break;
-                    if (!(ok = mbar_wait_w(&sh.acc_free, (uc & 1) ^ 1, wc, kBSiteAcc))) break;
+        } else if (warp == 10) {
+            // ------------------------------------------------------- S issuer
+            // S^T(j) = K Q_j^T into R0 as soon as Q_j is loaded and dV(j-1)
+            // has finished reading P^T(j-1) there; a warp of its own, so the
+            // wait for Q never holds back the other four products.
+            uint32_t jj = 0, uc = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok; u += gridDim.x) {
+                BUnit U;
+                if (!bwd_unit(a, total, u, U)) break;
+                if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, kBSiteKvFull))) break;
+                for (int t = 0; t < U.n; ++t, ++jj) {
                     if (!(ok = mbar_wait_w(&sh.q_full[jj & 1], (jj >> 1) & 1, wc, kBSiteQFull))) break;
+                    if (jj > 0 && !(ok = mbar_wait_w(&sh.r0_free, (jj - 1) & 1, wc, kBSiteP))) break;
                     tc_fence_after();
                     mma_kk(tmem + kColR0, sK, base + kOffQ + (jj & 1) * kT32);
                     umma_commit_w(&sh.s_full);
-                    if (jj > 0) {
-                        if (!(ok = mbar_wait_w(&sh.dq_free, (jj - 1) & 1, wc, kBSiteDqFree))) break;
-                        tc_fence_after();
-                    }
-                    if (!(ok = mbar_wait_w(&sh.do_full, jj & 1, wc, kBSiteQFull))) break;
-                    mma_kk(tmem + kColR1, sV, base + kOffDO);
-                    umma_commit_w(&sh.dp_full);
-                    for (int t = 0; t < U.n; ++t, ++jj) {
-                        const uint32_t st = jj & 1, st2 = (jj + 1) & 1;
-                        const bool more = t + 1 < U.n;
-                        if (!(ok = mbar_wait_w(&sh.p_ready, jj & 1, wc, kBSiteP))) break;
-                        tc_fence_after();
-                        mma_tn(tmem + kColDV, tmem + kColR0, base + kOffDO, t > 0);
-                        umma_commit_w(&sh.do_empty);     // dO read by dP and dV: the next may load
-                        if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, kBSiteDs))) break;
-                        tc_fence_after();
-                        mma_tn(tmem + kColDK, tmem + kColR0 + 64, base + kOffQ + st * kT32, t > 0);
-                        umma_commit_w(&sh.q_empty[st]);  // Q and LSE/D of this stage are consumed
-                        if (more) {  // Q/dO arrive by TMA: no tcgen05 fence needed
-                            if (!(ok = mbar_wait_w(&sh.q_full[st2], ((jj + 1) >> 1) & 1, wc, kBSiteQFull))) break;
-                            mma_kk(tmem + kColR0, sK, base + kOffQ + st2 * kT32);
-                            umma_commit_w(&sh.s_full);
-                        }
-                        mma_nn(tmem + kColR1, sDS, sK);
-                        umma_commit_w(&sh.dq_full);
-                        umma_commit_w(&sh.ds_free);      // dS read by dK and dQ
-                        if (more) {
-                            if (!(ok = mbar_wait_w(&sh.dq_free, jj & 1, wc, kBSiteDqFree))) break;
-                            tc_fence_after();
-                            if (!(ok = mbar_wait_w(&sh.do_full, (jj + 1) & 1, wc, kBSiteQFull))) break;
-                            mma_kk(tmem + kColR1, sV, base + kOffDO);
-                            umma_commit_w(&sh.dp_full);
-                        }
-                    }
-                    umma_commit_w(&sh.dkdv_done);
-                    umma_commit_w(&sh.kv_empty);
-                    ++uc;
                 }
-                umma_commit_w(&sh.drain);
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(smem_u32(&sh.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+                ++uc;
             }
+            umma_commit_w(&sh.drain);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&sh.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+            __syncwarp();
+        } else if (warp == 9) {
+            // ---------------------------------------- dV, dK, dQ, dP issuer
+            uint32_t jj = 0, uc = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok; u += gridDim.x) {
+                BUnit U;
+                if (!bwd_unit(a, total, u, U)) break;
+                if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, kBSiteKvFull))) break;
+                if (!(ok = mbar_wait_w(&sh.acc_free, (uc & 1) ^ 1, wc, kBSiteAcc))) break;
+                if (jj > 0) {
+                    if (!(ok = mbar_wait_w(&sh.dq_free, (jj - 1) & 1, wc, kBSiteDqFree))) break;
+                    tc_fence_after();
+                }
+                if (!(ok = mbar_wait_w(&sh.do_full, jj & 1, wc, kBSiteQFull))) break;
+                mma_kk(tmem + kColR1, sV, base + kOffDO);
+                umma_commit_w(&sh.dp_full);
+                for (int t = 0; t < U.n; ++t, ++jj) {
+                    const uint32_t st = jj & 1;
+                    const bool more = t + 1 < U.n;
+                    if (!(ok = mbar_wait_w(&sh.p_ready, jj & 1, wc, kBSiteP))) break;
+                    tc_fence_after();
+                    mma_tn(tmem + kColDV, tmem + kColR0, base + kOffDO, t > 0);
+                    umma_commit_w(&sh.do_empty);     // dO read by dP and dV: the next may load
+                    umma_commit_w(&sh.r0_free);      // P^T read: the next S^T may overwrite R0
+                    if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, kBSiteDs))) break;
+                    tc_fence_after();
+                    mma_tn(tmem + kColDK, tmem + kColR1, base + kOffQ + st * kT32, t > 0);
+                    umma_commit_w(&sh.q_empty[st]);  // Q and LSE/D of this stage are consumed
+                    mma_nn(tmem + kColR1, sDS, sK);  // dQ overwrites dS^T after dK has read it
+                    umma_commit_w(&sh.dq_full);
+                    umma_commit_w(&sh.ds_free);      // dS read by dK and dQ
+                    if (more) {
+                        if (!(ok = mbar_wait_w(&sh.dq_free, jj & 1, wc, kBSiteDqFree))) break;
+                        tc_fence_after();
+                        if (!(ok = mbar_wait_w(&sh.do_full, (jj + 1) & 1, wc, kBSiteQFull))) break;
+                        mma_kk(tmem + kColR1, sV, base + kOffDO);
+                        umma_commit_w(&sh.dp_full);
+                    }
+                }
+                if (!ok) break;
+                umma_commit_w(&sh.dkdv_done);
+                umma_commit_w(&sh.kv_empty);
+                ++uc;
+            }
+            umma_commit_w(&sh.drain);
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(&sh.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
             __syncwarp();
         }
     } else if (warp < 4 || warp >= 12) {
@@ -526,15 +553,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     uint32_t pk[16];
 #pragma unroll
                     for (int m = 0; m < 16; ++m) pk[m] = pack_bf16x2(p[stg * 32 + 2 * m], p[stg * 32 + 2 * m + 1]);
-                    tmem_st16(tR0 + cb / 2 + stg * 16, pk);        // P^T: two bf16 per column
+                    tmem_st16(tR0 + cb + stg * 16, pk);   // P^T: two bf16 per column, in this half's own columns
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&sh.p_ready);
 
-                // dS^T goes to R0 columns 64-127, which held S^T: wait until both
-                // halves have read S^T (p_ready complete) before writing them.
-                if (!(ok = mbar_wait(&sh.p_ready, jj & 1, wc, kBSiteP))) break;
+                // dS^T replaces dP^T in this half's own R1 columns.
                 if (!(ok = mbar_wait(&sh.dp_full, jj & 1, wc, kBSiteDp))) break;
                 if (!(ok = mbar_wait(&sh.ds_free, (jj & 1) ^ 1, wc, kBSiteDsFree))) break;
                 tc_fence_after();
@@ -562,8 +587,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         *reinterpret_cast<uint4*>(ds_row + ((q ^ sw) << 4)) =
                             make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
                     }
-                    // dS^T also into TMEM (operand A of dK += dS^T Q, like P^T for dV).
-                    tmem_st16(tR0 + 64 + cb / 2 + cc * 16, pk);
+                    // dS^T also into TMEM (operand A of dK += dS^T Q, like P^T for
+                    // dV), over the dP^T columns this thread has just read.
+                    tmem_st16(tR1 + cb + cc * 16, pk);
                 }
                 tmem_wait_st();
                 fence_async_smem();
@@ -628,31 +654,32 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 }
                 // Add dQ_i into the fp32 accumulator with TMA bulk tensor
                 // reductions of whole 128-byte lines, staged in shared memory
-                // in two rounds of two 32-column boxes (128 rows x 128 B,
-                // swizzled like a 128-B TMA box).  Rows past the sequence end hold exact
-                // zeros (their P, hence dS, is zero), so adding them to the
-                // neighbouring rows changes nothing.
+                // in four rounds of one 32-column box (128 rows x 128 B,
+                // swizzled like a 128-B TMA box) alternating between two
+                // buffers, so each round's reduction reads one buffer while
+                // the threads fill the other.  Rows past the sequence end hold
+                // exact zeros (their P, hence dS, is zero), so adding them to
+                // the neighbouring rows changes nothing.
                 const int grow = h * (int)a.T + U.tok0 + i * kTileM;
                 uint8_t* stage_row = dsm + kOffStage + r * 128;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int rnd = 0; rnd < 4; ++rnd) {
+                    const int b = rnd & 1;
+                    // At most the latest group may still be reading: the one
+                    // before it used this buffer.
+                    if (r == 0) bulk_wait_read1();
+                    named_bar(1, 128);
+                    const uint32_t* src = v + rnd * 32;
 #pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        const uint32_t* src = v + half * 64 + b * 32;
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            *reinterpret_cast<uint4*>(stage_row + b * kBox + ((q ^ (r & 7)) << 4)) =
-                                make_uint4(src[4 * q], src[4 * q + 1], src[4 * q + 2], src[4 * q + 3]);
-                    }
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<uint4*>(stage_row + b * kBox + ((q ^ (r & 7)) << 4)) =
+                            make_uint4(src[4 * q], src[4 * q + 1], src[4 * q + 2], src[4 * q + 3]);
                     fence_async_smem();
                     named_bar(1, 128);
                     if (r == 0) {
-                        tma_reduce_add_2d(&tdq, base + kOffStage, half * 64, grow);
-                        tma_reduce_add_2d(&tdq, base + kOffStage + kBox, half * 64 + 32, grow);
+                        tma_reduce_add_2d(&tdq, base + kOffStage + b * kBox, rnd * 32, grow);
                         bulk_commit();
-                        bulk_wait_read0();
                     }
-                    named_bar(1, 128);
                 }
                 if (r == 0) {
                     if (sem) {
