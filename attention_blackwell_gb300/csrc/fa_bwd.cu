@@ -537,15 +537,26 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 const int c_lo = (a.causal ? key - i * kTileM : 0) - cb;
                 const int c_hi = (key >= U.len ? 0 : U.len - i * kTileM) - cb;
                 const float4* l2v = reinterpret_cast<const float4*>(s_lse + st * 128 + cb);
+                if (c_lo <= 0 && c_hi >= 64) {   // every column visible: no mask
 #pragma unroll
-                for (int c4 = 0; c4 < 16; ++c4) {
-                    const float4 l4 = l2v[c4];
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                    for (int c4 = 0; c4 < 16; ++c4) {
+                        const float4 l4 = l2v[c4];
+                        p[4 * c4] = ex2_mufu(fmaf(p[4 * c4], scale, -l4.x));
+                        p[4 * c4 + 1] = ex2_mufu(fmaf(p[4 * c4 + 1], scale, -l4.y));
+                        p[4 * c4 + 2] = ex2_mufu(fmaf(p[4 * c4 + 2], scale, -l4.z));
+                        p[4 * c4 + 3] = ex2_mufu(fmaf(p[4 * c4 + 3], scale, -l4.w));
+                    }
+                } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = 4 * c4 + e;
-                        const float pe = ex2_mufu(fmaf(p[c], scale, -lv[e]));
-                        p[c] = (c >= c_lo && c < c_hi) ? pe : 0.f;
+                    for (int c4 = 0; c4 < 16; ++c4) {
+                        const float4 l4 = l2v[c4];
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = 4 * c4 + e;
+                            const float pe = ex2_mufu(fmaf(p[c], scale, -lv[e]));
+                            p[c] = (c >= c_lo && c < c_hi) ? pe : 0.f;
+                        }
                     }
                 }
 #pragma unroll
