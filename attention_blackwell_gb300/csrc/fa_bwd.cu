@@ -187,15 +187,28 @@ struct BUnit {
     int seq, hk, k, tok0, len, n, nq, i0;
 };
 
-// Decode unit u: fixed length -> key tile k = u / (B*Hkv) (all first key
-// tiles before any second one: the order the deterministic semaphores and the
-// causal longest-first rule both want); varlen -> the planned work list.
+// Decode unit u.  Fixed length, non-causal, atomic mode: (sequence,
+// key/value head) major, key tiles ascending within it, so the CTAs at work
+// at any time share a few heads and those heads' Q, dO and fp32 dQ
+// accumulator stay in L2 (FlashAttention-4 blog, "Scheduling": L2-sized
+// batch-head sections).  Fixed length otherwise: key tile k = u / (B*Hkv),
+// all first key tiles before any second one -- longest first under a causal
+// mask, and in deterministic mode a key tile waits at its semaphores only on
+// tiles that started a wave earlier.  Both orders put every unit after the
+// ones it waits on.  Varlen: the planned work list.
 __device__ __forceinline__ bool bwd_unit(const BwdArgs& a, int total, int u, BUnit& U) {
     if (u >= total) return false;
     if (!a.varlen) {
         const int bh = a.B * a.Hkv;
-        U.k = u / bh;
-        const int r = u - U.k * bh;
+        int r;
+        if (a.deterministic || a.causal) {
+            U.k = u / bh;
+            r = u - U.k * bh;
+        } else {
+            const int nk = (a.N + kTileN - 1) / kTileN;
+            r = u / nk;
+            U.k = u - r * nk;
+        }
         U.seq = r / a.Hkv;
         U.hk = r - U.seq * a.Hkv;
         U.tok0 = U.seq * a.N;
