@@ -12,7 +12,7 @@ import os
 
 import torch
 
-__all__ = ["fwd", "set_fwd_kernel", "fwd_pairs_resident", "bwd", "bwd_workspace", "exp2_emu", "set_tuning", "device_status", "num_sms", "FAError", "library_path", "lib"]
+__all__ = ["fwd", "set_fwd_kernel", "fwd_pairs_resident", "set_bwd_kernel", "bwd_pairs_resident", "bwd", "bwd_workspace", "exp2_emu", "set_tuning", "device_status", "num_sms", "FAError", "library_path", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libfa.so")
@@ -52,6 +52,10 @@ def lib():
         L.fa_set_fwd_kernel.argtypes = [i]
         L.fa_fwd_pairs_resident.restype = i
         L.fa_fwd_pairs_resident.argtypes = []
+        L.fa_set_bwd_kernel.restype = i
+        L.fa_set_bwd_kernel.argtypes = [i]
+        L.fa_bwd_pairs_resident.restype = i
+        L.fa_bwd_pairs_resident.argtypes = []
         L.fa_fwd.restype = i
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp]
         sz = ctypes.c_size_t
@@ -97,6 +101,17 @@ def _need(t, name, dtype):
         raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
+
+
+def set_bwd_kernel(kernel=0):
+    """Backward main kernel for later calls: 0 one CTA per 128-key tile (the
+    default), 1 CTA pairs per 256-key block (fixed length, atomic mode)."""
+    _check(lib().fa_set_bwd_kernel(int(kernel)), "fa_set_bwd_kernel")
+
+
+def bwd_pairs_resident():
+    """CTA pairs backward kernel 1 keeps resident (0 before its first launch)."""
+    return int(lib().fa_bwd_pairs_resident())
 
 
 def fwd_pairs_resident():

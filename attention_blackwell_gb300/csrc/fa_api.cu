@@ -30,6 +30,7 @@ DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
 int g_emu_eighths = 0;         // share of exp2 pairs on the FMA pipe (eighths)
+int g_bwd_kernel = 0;          // 0: one CTA per 128-key tile; 1: CTA pairs per 256-key block
 int g_fwd_kernel = 2;          // 0: ping-pong of two 128-row query tiles; 1: 256-key blocks; 2: CTA pairs
 float g_tau = 8.0f;            // conditional-rescale threshold, log2(256)
 
@@ -84,12 +85,12 @@ int make_map(CUtensorMap* map, const void* ptr, int H, long long T, int box_rows
 }
 
 // fp32 accumulator [rows, 128] -> 2-D map {128, rows}, box {32, 128}, 128-B swizzle.
-int make_map_acc(CUtensorMap* map, const void* ptr, long long rows) {
+int make_map_acc(CUtensorMap* map, const void* ptr, long long rows, int box_rows = kTileM) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return FA_ERR_LAUNCH;
     cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 4};
-    cuuint32_t box[2] = {32, (cuuint32_t)kTileM};
+    cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -203,6 +204,14 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 int fa_fwd_pairs_resident(void) { return g_pairs_resident; }
 
+int fa_set_bwd_kernel(int kernel) {
+    if (kernel < 0 || kernel > 1) return FA_ERR_INVALID;
+    g_bwd_kernel = kernel;
+    return FA_OK;
+}
+
+int fa_bwd_pairs_resident(void) { return g_bwd_pairs_resident; }
+
 int fa_set_fwd_kernel(int kernel) {
     if (kernel < 0 || kernel > 2) return FA_ERR_INVALID;
     g_fwd_kernel = kernel;
@@ -298,6 +307,12 @@ int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const
     a.alpha = alpha;
     a.scale_log2 = alpha * 1.4426950408889634f;
     L.num_sms = dev->num_sms;
+    L.pair = g_bwd_kernel == 1 && bwd_pair_supported(a) ? 1 : 0;
+    if (L.pair) {
+        if ((rc = make_map(&L.tq64, q, Hq, T, 64)) != FA_OK) return rc;
+        if ((rc = make_map(&L.tdo64, dout, Hq, T, 64)) != FA_OK) return rc;
+        if ((rc = make_map_acc(&L.tdq64, ws + w.dq_off, (long long)Hq * T, 64)) != FA_OK) return rc;
+    }
     cudaError_t e = launch_bwd(L, stages, stream);
     return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }

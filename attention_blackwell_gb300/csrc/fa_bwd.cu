@@ -771,7 +771,10 @@ cudaError_t launch_bwd(const BwdLaunch& L, int stages, cudaStream_t stream) {
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if (stages & 2) {
+    if ((stages & 2) && L.pair) {
+        cudaError_t e = launch_bwd_pair_main(L, stream);
+        if (e != cudaSuccess) return e;
+    } else if (stages & 2) {
         cudaError_t e0 = cudaFuncSetAttribute(bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdSmem);
         if (e0 != cudaSuccess) return e0;
         long long units = a.varlen ? (long long)a.Hkv * ((a.T + kTileN - 1) / kTileN + a.B)

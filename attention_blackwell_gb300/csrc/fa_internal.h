@@ -96,9 +96,17 @@ struct BwdArgs {
 struct BwdLaunch {
     CUtensorMap tq, tk, tv, tdo;
     CUtensorMap tdq;         // dQacc as fp32 [Hq*T, 128], box {32, 128}, 128-B swizzle
+    // CTA-pair main kernel only: Q and dO with 64-row boxes, dQacc with 64-row boxes.
+    CUtensorMap tq64, tdo64, tdq64;
     BwdArgs a;
     int num_sms;
+    int pair;                // stage 2 runs the CTA-pair kernel (fa_bwd_pair.cu)
 };
+
+// CTA-pair backward main kernel (fa_bwd_pair.cu): fixed length, atomic mode.
+bool bwd_pair_supported(const BwdArgs& a);
+cudaError_t launch_bwd_pair_main(const BwdLaunch& L, cudaStream_t stream);
+extern int g_bwd_pairs_resident;
 
 // Backward stages (fa_bwd.cu): 1 = preprocess (D, zero dQacc/semaphores,
 // varlen plan), 2 = main kernel (dK, dV, dQacc), 4 = dQ postprocess.

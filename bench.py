@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--deterministic", action="store_true", help="backward in deterministic mode")
     ap.add_argument("--exp2-emu", type=int, default=0, help="forward: eighths of exp2 on the FMA pipe (0-2)")
     ap.add_argument("--tau", type=float, default=8.0, help="forward: conditional-rescale threshold (log2 units)")
+    ap.add_argument("--bwd-kernel", type=int, default=0,
+                    help="backward main kernel: 0 one CTA per 128-key tile, 1 CTA pairs per 256-key block")
     ap.add_argument("--fwd-kernel", type=int, default=2,
                     help="forward kernel: 0 ping-pong 128x128, 1 256-key blocks, 2 CTA pairs with 256-key blocks")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -176,6 +178,8 @@ def kernel_traffic(name):
 
 def traffic_key(args, w, kernel):
     """Record name in profiles/dram_traffic.json for a step kernel."""
+    if kernel == "bwd":
+        return "bwd" if (w.varlen or args.deterministic or args.bwd_kernel == 0) else "bwd_pair"
     if kernel != "fwd":
         return kernel
     if w.varlen or args.exp2_emu or args.fwd_kernel == 0:
@@ -253,6 +257,7 @@ def run_ours(args, rank, world):
     w = W.WORKLOADS[args.workload]
     fa.set_tuning(args.exp2_emu, args.tau)
     fa.set_fwd_kernel(args.fwd_kernel)
+    fa.set_bwd_kernel(args.bwd_kernel)
     has_bwd = hasattr(fa, "bwd") and not args.no_bwd
     inp = W.make_inputs(w, with_grad=True)
     t = {n: inp[n].to(dev) for n in ("q", "k", "v", "do")}
@@ -345,6 +350,11 @@ def run_ours(args, rank, world):
     return locals()
 
 
+def bwd_pairs_resident():
+    import attention_blackwell_gb300 as fa
+    return fa.bwd_pairs_resident()
+
+
 def fa_pairs_resident():
     import attention_blackwell_gb300 as fa
     return fa.fwd_pairs_resident()
@@ -395,6 +405,9 @@ def main_ours(args):
             "fwd_kernel": ("ping-pong 2x128" if w.varlen or args.exp2_emu else
                            {0: "ping-pong 2x128", 1: "256-key blocks", 2: "CTA pairs, 256-key blocks"}[args.fwd_kernel]),
             "fwd_pairs_resident": fa_pairs_resident(),
+            "bwd_kernel": ("one CTA per 128-key tile" if w.varlen or args.deterministic or args.bwd_kernel == 0
+                           else "CTA pairs per 256-key block"),
+            "bwd_pairs_resident": bwd_pairs_resident(),
             "parallelism": "replicas" if world > 1 else "single",
             "l2": "no flush: the step's inputs (%.0f MiB) exceed the 126 MB L2" % (
                 sum(r["t"][n].numel() * 2 for n in ("q", "k", "v", "do")) / 2 ** 20)},

@@ -102,6 +102,26 @@ int fa_set_fwd_kernel(int kernel);
 int fa_fwd_pairs_resident(void);
 
 /*
+ * Process-wide choice of the backward main kernel (affects later fa_bwd
+ * calls; FlashAttention-4 blog, "2-CTA backward"):
+ *   0 -- (default) one CTA per 128-key tile;
+ *   1 -- CTA pairs per 256-key block: S^T, dP^T, dV and dK are
+ *        M = 256 products over both SMs (each stages half of every B
+ *        operand), dQ an M = 128 pair product after an exchange of half of
+ *        dS through distributed shared memory.
+ * Kernel 1 serves fixed-length inputs in atomic mode; packed varlen batches
+ * and deterministic mode use kernel 0.  Both compute the same gradients up to
+ * the order of the fp32 dQ additions.  Errors: FA_ERR_INVALID.
+ */
+int fa_set_bwd_kernel(int kernel);
+
+/*
+ * Number of CTA pairs backward kernel 1 keeps resident; 0 until it has been
+ * launched once in this process.  Never fails.
+ */
+int fa_bwd_pairs_resident(void);
+
+/*
  * Forward: O and LSE of exact attention (FlashAttention-4 blog, "Forward
  * pass: a new softmax pipeline with conditional rescaling").
  *

@@ -88,3 +88,13 @@ def test_forward_kernel_selector(lib):
     assert lib.fa_set_fwd_kernel(3) == -1
     assert lib.fa_set_fwd_kernel(-1) == -1
     assert lib.fa_set_fwd_kernel(2) == 0
+
+
+def test_backward_kernel_selector(lib):
+    """Kernels 0-1 are accepted, others rejected; no GPU call is made."""
+    assert lib.fa_bwd_pairs_resident() == 0
+    for k in (0, 1):
+        assert lib.fa_set_bwd_kernel(k) == 0
+    assert lib.fa_set_bwd_kernel(2) == -1
+    assert lib.fa_set_bwd_kernel(-1) == -1
+    assert lib.fa_set_bwd_kernel(0) == 0
