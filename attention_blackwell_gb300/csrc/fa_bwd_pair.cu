@@ -28,10 +28,17 @@
 // Roles (512 threads per CTA, both CTAs): warps 0-3 and 12-15 key-row
 // warpgroups (P^T, dS^T; one thread per key row, each group half of the 128
 // query columns); warps 4-7 dQ drain (one thread per TMEM lane: 64 columns of
-// one dQ row) and the dK/dV epilogue; warp 8 loader.  In the even CTA warp 9
-// issues dP, dV, dK, dQ and warp 10 issues S; warp 11 idles.  Barriers an
-// issuer waits on live in the even CTA: the odd CTA's TMA bytes and warp
-// arrivals count there; commits go to both CTAs.
+// one dQ row) and the dK/dV epilogue; warp 8 loader; warp 11 relays "this
+// CTA's dS buffer is complete" to the even CTA.  In the even CTA warp 9
+// issues dP, dV, dK, dQ and warp 10 issues S.  Barriers an issuer waits on
+// live in the even CTA: the odd CTA's TMA bytes and warp arrivals count
+// there; commits go to both CTAs.
+//
+// The dS exchange: the key-row half whose queries belong to this CTA writes
+// its rows into this CTA's dS buffer; the other half writes them into an
+// outbox, and one bulk copy (shared memory to the peer's shared memory,
+// completing on the peer's barrier) moves them -- async-proxy traffic end to
+// end, so no thread waits for remote stores to drain.
 //
 // Tensor memory (512 columns, both CTAs): dK 0-127, dV 128-255,
 //   R0 256-383: S^T, then P^T (bf16; each half packs its 64 queries into the
@@ -53,8 +60,9 @@ constexpr uint32_t kT16 = 16384, kT32 = 32768;
 constexpr uint32_t kOffK = 0;                       // own 128 keys x 128 d, K-major (2 boxes)
 constexpr uint32_t kOffV = kOffK + kT32;            // own V
 constexpr uint32_t kOffKdq = kOffV + kT32;          // 256 keys x this CTA's 64 d (2 boxes), MN-major B of dQ
-constexpr uint32_t kOffQs = kOffKdq + kT32;         // [2] 64 queries x 128 d (2 boxes of 8 KB)
-constexpr uint32_t kOffQd = kOffQs + 2 * kT16;      // 128 queries x this CTA's 64 d
+constexpr uint32_t kOffQs = kOffKdq + kT32;         // 64 queries x 128 d (2 boxes of 8 KB), read by S^T only
+constexpr uint32_t kOffOut = kOffQs + kT16;         // dS rows of this CTA's keys for the peer's query half
+constexpr uint32_t kOffQd = kOffOut + kT16;         // 128 queries x this CTA's 64 d
 constexpr uint32_t kOffDOs = kOffQd + kT16;         // dO: 64 queries x 128 d
 constexpr uint32_t kOffDOd = kOffDOs + kT16;        // dO: 128 queries x 64 d
 constexpr uint32_t kOffDS = kOffDOd + kT16;         // dS for this CTA's 64 queries x 256 keys, MN-major A of dQ
@@ -71,8 +79,9 @@ enum : int { kPBSiteKv = 81, kPBSiteQ, kPBSiteDo, kPBSiteS, kPBSiteP, kPBSiteDp,
              kPBSiteDq, kPBSiteDqFree, kPBSiteDkdv, kPBSiteAcc, kPBSiteR0, kPBSiteSt };
 
 struct PBShared {
-    uint64_t kv_full, kv_empty, qs_full[2], q_empty[2], qd_full, do_full, do_empty, st_full[2];
+    uint64_t kv_full, kv_empty, qs_full, qs_empty, q_empty[2], qd_full, do_full, do_empty, st_full[2];
     uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dq_full, dq_free, dkdv_done, acc_free, r0_free, drain;
+    uint64_t dsx, dsx_ready;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -143,14 +152,7 @@ __device__ __forceinline__ void pb_mma_dq(uint32_t d, uint32_t a_smem, uint32_t 
     });
 }
 
-__device__ __forceinline__ void pb_fence_async_cluster() {
-    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-}
 __device__ __forceinline__ void pb_fence_async_cta() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void pb_st_cluster_v4(uint32_t addr, uint4 v) {
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w) : "memory");
-}
 // Per-warp arrival (elected lane) with cluster-scope release: the even CTA's
 // tensor core reads shared memory this warp wrote (dS exchange).
 __device__ __forceinline__ void pb_arrive_release_cluster_w(uint32_t cluster_addr) {
@@ -230,11 +232,14 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     if (tid == 0) {
         mbar_init(&sh.kv_full, 1);
         mbar_init(&sh.kv_empty, 1);
+        mbar_init(&sh.qs_full, 1);
+        mbar_init(&sh.qs_empty, 1);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(&sh.qs_full[s], 1);
             mbar_init(&sh.q_empty[s], 1);
             mbar_init(&sh.st_full[s], 1);
         }
+        mbar_init(&sh.dsx, 4);         // the local half's warps (one carries the peer's bytes)
+        mbar_init(&sh.dsx_ready, 2);   // one relay arrival from each CTA
         mbar_init(&sh.qd_full, 1);
         mbar_init(&sh.do_full, 1);
         mbar_init(&sh.do_empty, 1);
@@ -305,14 +310,16 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 for (int t = 0; t < U.n; ++t, ++jj) {
                     const int st = jj & 1, h = U.hk * g + t / span, i = U.i0 + t % span;
                     const int q0 = U.tok0 + i * kTileM;
-                    // Q rows of this CTA's query half (S^T) once dK two tiles back is done.
+                    // Q rows of this CTA's query half (read by S^T only) once the
+                    // previous S^T is done; LSE/D slot once dK two tiles back is.
                     if (lane == 0) {
-                        ok = mbar_wait(&sh.q_empty[st], ((jj >> 1) & 1) ^ 1, wc, kPBSiteQ);
+                        ok = mbar_wait(&sh.qs_empty, (jj & 1) ^ 1, wc, kPBSiteQ);
                         if (ok) {
-                            if (leader) mbar_arrive_expect_tx(&sh.qs_full[st], 2 * kT16);
+                            if (leader) mbar_arrive_expect_tx(&sh.qs_full, 2 * kT16);
                             for (int c = 0; c < 2; ++c)
-                                tma_load_3d_pair(base + kOffQs + st * kT16 + c * 8192, &tq64, lead(&sh.qs_full[st]),
-                                                 c * 64, h, q0 + PB_RANK * 64);
+                                tma_load_3d_pair(base + kOffQs + c * 8192, &tq64, lead(&sh.qs_full), c * 64, h,
+                                                 q0 + PB_RANK * 64);
+                            ok = mbar_wait(&sh.q_empty[st], ((jj >> 1) & 1) ^ 1, wc, kPBSiteQ);
                         }
                     }
                     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -356,8 +363,8 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             // The even CTA's full barriers count both CTAs' bytes: once their
             // last phases are complete nothing is in flight.
             if (lane == 0 && leader) {
-                for (uint32_t d = (jj > 2 ? jj - 2 : 0); d < jj; ++d) pb_drain_wait(&sh.qs_full[d & 1], (d >> 1) & 1);
                 if (jj > 0) {
+                    pb_drain_wait(&sh.qs_full, (jj - 1) & 1);
                     pb_drain_wait(&sh.qd_full, (jj - 1) & 1);
                     pb_drain_wait(&sh.do_full, (jj - 1) & 1);
                 }
@@ -373,17 +380,34 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 if (!pb_unit(a, u, U)) break;
                 if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, kPBSiteKv))) break;
                 for (int t = 0; t < U.n; ++t, ++jj) {
-                    if (!(ok = mbar_wait_w(&sh.qs_full[jj & 1], (jj >> 1) & 1, wc, kPBSiteQ))) break;
+                    if (!(ok = mbar_wait_w(&sh.qs_full, jj & 1, wc, kPBSiteQ))) break;
                     if (jj > 0 && !(ok = mbar_wait_w(&sh.r0_free, (jj - 1) & 1, wc, kPBSiteR0))) break;
                     tc_fence_after();
-                    pb_mma_kq(tmem + kColR0, sK, base + kOffQs + (jj & 1) * kT16);
+                    pb_mma_kq(tmem + kColR0, sK, base + kOffQs);
                     umma_commit_pair_w(&sh.s_full, kBoth);
+                    umma_commit_pair_w(&sh.qs_empty, kBoth);   // the Q rows may reload
                 }
                 ++uc;
             }
             umma_commit_pair_w(&sh.drain, kLead);
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(smem_u32(&sh.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+            __syncwarp();
+        } else if (warp == 11) {
+            // --------------------------------------------------- dS relay
+            // This CTA's dS buffer is complete once its own half has written
+            // its rows and the peer's rows have arrived (bulk copy, counted on
+            // dsx): tell the even CTA's issuer, whose dQ product reads it.
+            uint32_t jj = 0;
+            bool ok = true;
+            for (int u = PB_PAIR; ok; u += PB_NPAIRS) {
+                PBUnit U;
+                if (!pb_unit(a, u, U)) break;
+                for (int t = 0; t < U.n; ++t, ++jj) {
+                    if (!(ok = mbar_wait_w(&sh.dsx, jj & 1, wc, kPBSiteDs))) break;
+                    pb_arrive_release_cluster_w(lead(&sh.dsx_ready));
+                }
+            }
             __syncwarp();
         } else if (warp == 9 && leader) {
             // -------------------------------------------- dP, dV, dK, dQ issuer
@@ -417,11 +441,14 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     pb_mma_tn<32>(tmem + kColDV, tmem + kColR0, base + kOffDOd, t > 0);
                     umma_commit_pair_w(&sh.do_empty, kBoth);   // dO read by dP and dV
                     umma_commit_pair_w(&sh.r0_free, kLead);    // P^T read: the next S^T may overwrite R0
-                    if (!(ok = pb_wait_cluster_w(&sh.ds_ready, jj & 1, wc, kPBSiteDs))) break;
+                    if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, kPBSiteDs))) break;
                     if (!(ok = mbar_wait_w(&sh.qd_full, jj & 1, wc, kPBSiteQ))) break;
                     tc_fence_after();
                     pb_mma_tn<64>(tmem + kColDK, tmem + kColR1, base + kOffQd, t > 0);
-                    umma_commit_pair_w(&sh.q_empty[st], kBoth);  // Q halves and LSE/D of this tile consumed
+                    umma_commit_pair_w(&sh.q_empty[st], kBoth);  // Q columns and LSE/D of this tile consumed
+                    // dQ once both CTAs' dS buffers are complete (relayed below).
+                    if (!(ok = pb_wait_cluster_w(&sh.dsx_ready, jj & 1, wc, kPBSiteDs))) break;
+                    tc_fence_after();
                     pb_mma_dq(tmem + kColR1 + 32, sDS, sKdq);
                     umma_commit_pair_w(&sh.dq_full, kBoth);
                     umma_commit_pair_w(&sh.ds_free, kBoth);      // both CTAs' dS buffers read
@@ -452,10 +479,13 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tR0 = tmem + lb + kColR0, tR1 = tmem + lb + kColR1;
         // dS row of this key in the dQ A operand of CTA hc (queries 64 hc .. +63):
-        // key row R = 128 rank + r of that CTA's 256-row buffer.
-        const int R = PB_RANK * 128 + r;
-        const uint32_t ds_row = mapa_rank(sDS + R * 128, hc);
-        const int sw = R & 7;
+        // key row R = 128 rank + r of that CTA's 256-row buffer.  The half for
+        // this CTA writes it in place; the other half writes it to the outbox
+        // (same row layout: R % 8 == r % 8), which one bulk copy moves to the
+        // peer.
+        const bool local_half = hc == PB_RANK;
+        uint8_t* ds_row = local_half ? dsm + kOffDS + (PB_RANK * 128 + r) * 128 : dsm + kOffOut + r * 128;
+        const int sw = r & 7;
         uint32_t jj = 0;
         bool ok = true;
         for (int u = PB_PAIR; ok; u += PB_NPAIRS) {
@@ -540,8 +570,8 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
                             const int q = cc * 4 + m;
-                            pb_st_cluster_v4(ds_row + ((q ^ sw) << 4),
-                                             make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]));
+                            *reinterpret_cast<uint4*>(ds_row + ((q ^ sw) << 4)) =
+                                make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
                         }
                         tmem_st16(tR1 + hc * 96 + cc * 16, pk);
                     };
@@ -555,9 +585,27 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 }
                 if (!okw) { ok = false; break; }
                 tmem_wait_st();
-                pb_fence_async_cluster();   // the dS rows (local and remote) before the pair product
                 tc_fence_before();
-                pb_arrive_release_cluster_w(lead(&sh.ds_ready));
+                mbar_arrive_remote_w(lead(&sh.ds_ready));   // dS^T in TMEM: dK may start
+                pb_fence_async_cta();                        // this thread's dS rows before the copy / product
+                __syncwarp();
+                if (lane == 0) {
+                    if (local_half) {
+                        if ((warp & 3) == 0) mbar_arrive_expect_tx(&sh.dsx, kT16);   // the peer's rows, by bulk copy
+                        else mbar_arrive(&sh.dsx);
+                    } else {
+                        // This warp's 32 rows (keys of this CTA, the peer's
+                        // queries) into the peer's buffer at rows 128 rank +
+                        // 32 w .. +31, counted on the peer's dsx: four copies in
+                        // flight per CTA.
+                        const uint32_t rows = (uint32_t)(warp & 3) * 32 * 128;
+                        const uint32_t dst = mapa_rank(sDS + PB_RANK * 128 * 128 + rows, hc);
+                        const uint32_t bar = mapa_rank(smem_u32(&sh.dsx), hc);
+                        asm volatile(
+                            "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                            ::"r"(dst), "r"(base + kOffOut + rows), "r"(32 * 128), "r"(bar) : "memory");
+                    }
+                }
             }
         }
     } else {
