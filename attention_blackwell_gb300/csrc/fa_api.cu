@@ -163,10 +163,10 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     int rc = current_device_info(&dev);
     if (rc != FA_OK) return rc;
 
-    // The 256-key kernels serve fixed-length inputs with the MUFU-only exp2;
-    // packed varlen batches and the FMA-exp2 variants use the ping-pong kernel.
-    const bool k256 = !varlen && g_emu_eighths == 0;
-    const bool wide = k256 && g_fwd_kernel == 1, pair = k256 && g_fwd_kernel == 2;
+    // The 256-key kernels use the MUFU-only exp2 (the FMA-exp2 variants run on
+    // the ping-pong kernel); the single-CTA one serves fixed-length inputs only.
+    const bool wide = !varlen && g_emu_eighths == 0 && g_fwd_kernel == 1;
+    const bool pair = g_emu_eighths == 0 && g_fwd_kernel == 2;
     FwdLaunch L;
     // K boxes: 256 rows (one block) for kernel 1, 128 (a block's half) for the
     // pair kernel; V boxes: 256 rows for both (the pair loads 64 columns of them).

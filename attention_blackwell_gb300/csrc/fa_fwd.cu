@@ -30,6 +30,7 @@
 // writes P as bf16 into TMEM in four 32-column stages and signals the UMMA
 // warp.  After the last tile it normalises O by 1/l and stores O and LSE.
 #include "fa_internal.h"
+#include "fa_sched.cuh"
 #include "fa_exp2.cuh"
 
 namespace fa {
@@ -40,7 +41,6 @@ constexpr int kThreads = 384;
 constexpr uint32_t kTileBytes = 32768;         // 128 x 128 bf16
 constexpr uint32_t kBoxBytes = 16384;          // 128 rows x 64 bf16 (one TMA box)
 constexpr uint32_t kSmemTiles = 2 * kTileBytes + kStages * kTileBytes;
-constexpr uint32_t kTableInts = (kMaxVarlenSeqs + 1) + kMaxVarlenSeqs + (kMaxVarlenSeqs + 1);
 constexpr uint32_t kSmemBytes = 1024 + kSmemTiles + kTableInts * 4;
 
 // TMEM column bases of O and S/P for tile x.
@@ -50,81 +50,6 @@ __device__ __forceinline__ uint32_t col_s(int x) { return 256u + (uint32_t)x * 1
 // Wait-site identifiers reported through the status word.
 enum : int { kSiteQEmpty = 1, kSiteRingEmpty, kSiteQFull, kSiteRingFull, kSiteP0, kSiteP1, kSiteS, kSiteO,
              kSiteDrain };
-
-struct Unit {
-    int seq, m, h, tok0, len;
-};
-
-// Work-unit order.
-//  fixed length, non-causal: (batch, head)-major, query block minor, so the
-//    CTAs running at one time share the K/V of few heads in L2;
-//  fixed length, causal: longest-processing-time first inside L2-sized
-//    sections of (batch, head) pairs -- sections in order, query blocks in
-//    reverse (longest first), then the pairs of the section (FlashAttention-4
-//    blog, "Scheduling");
-//  varlen: sequences sorted by block count (descending); causal walks query
-//    block levels from the top down over the sorted sequences (longest
-//    first), non-causal walks the sorted sequences head-major.
-struct Sched {
-    int B, Hq, N, causal, varlen, num_m, sec, total, maxm;
-    const int* s_cu;
-    const int* s_order;
-    const int* s_pref;
-
-    __device__ __forceinline__ int nblk(int s) const {
-        return (s_cu[s + 1] - s_cu[s] + kUnitRows - 1) / kUnitRows;
-    }
-
-    __device__ __forceinline__ bool get(int u, Unit& U) const {
-        if (u >= total) return false;
-        if (!varlen) {
-            const int BH = B * Hq;
-            int bh, m;
-            if (!causal) {
-                bh = u / num_m;
-                m = u - bh * num_m;
-            } else {
-                const int per_sec = sec * num_m;
-                const int full = BH / sec;
-                if (u < full * per_sec) {
-                    const int s = u / per_sec, r = u - s * per_sec;
-                    m = num_m - 1 - r / sec;
-                    bh = s * sec + r % sec;
-                } else {
-                    const int rem = BH - full * sec, r = u - full * per_sec;
-                    m = num_m - 1 - r / rem;
-                    bh = full * sec + r % rem;
-                }
-            }
-            U.seq = bh / Hq;
-            U.h = bh - U.seq * Hq;
-            U.m = m;
-            U.tok0 = U.seq * N;
-            U.len = N;
-            return true;
-        }
-        const int n = causal ? maxm : B;
-        int lo = 0, hi = n;  // first index with pref > u, minus one
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (s_pref[mid + 1] > u) hi = mid; else lo = mid + 1;
-        }
-        const int r = u - s_pref[lo];
-        if (causal) {
-            U.seq = s_order[r / Hq];
-            U.h = r % Hq;
-            U.m = maxm - 1 - lo;
-        } else {
-            U.seq = s_order[lo];
-            const int nb = nblk(U.seq);
-            U.h = r / nb;
-            U.m = r - U.h * nb;
-        }
-        U.tok0 = s_cu[U.seq];
-        U.len = s_cu[U.seq + 1] - U.tok0;
-        return true;
-    }
-};
 
 // Key tiles tile x (0/1) of a unit needs.
 __device__ __forceinline__ int kv_tiles(const Unit& U, int x, int causal) {
@@ -206,57 +131,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         tmem_relinquish();
     }
 
-    // Work-unit tables (varlen): sanitised offsets, sequences sorted by
-    // block count, and the unit prefix used by Sched::get.
-    if (a.varlen) {
-        for (int i = tid; i <= a.B; i += kThreads) {
-            int c = a.cu_seqlens[i];
-            s_cu[i] = c < 0 ? 0 : (c > a.N ? a.N : c);
-        }
-        __syncthreads();
-        if (tid == 0)
-            for (int i = 1; i <= a.B; ++i) s_cu[i] = s_cu[i] > s_cu[i - 1] ? s_cu[i] : s_cu[i - 1];
-        __syncthreads();
-        for (int i = tid; i < a.B; i += kThreads) {
-            const int ni = (s_cu[i + 1] - s_cu[i] + kUnitRows - 1) / kUnitRows;
-            int rank = 0;
-            for (int j = 0; j < a.B; ++j) {
-                const int nj = (s_cu[j + 1] - s_cu[j] + kUnitRows - 1) / kUnitRows;
-                rank += (nj > ni) || (nj == ni && j < i);
-            }
-            s_order[rank] = i;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            auto nb = [&](int s) { return (s_cu[s + 1] - s_cu[s] + kUnitRows - 1) / kUnitRows; };
-            const int maxm = a.B > 0 ? nb(s_order[0]) : 0;
-            int acc = 0;
-            if (maxm > kMaxUnitLevels) {
-                if (atomicCAS(&a.status->code, 0, -1) == 0) { a.status->where = 100; a.status->block = blockIdx.x; }
-                sh.maxm = 0;
-                sh.total = 0;
-            } else if (a.causal) {
-                int p = 0;
-                for (int l = 0; l < maxm; ++l) {
-                    const int m = maxm - 1 - l;
-                    while (p < a.B && nb(s_order[p]) > m) ++p;
-                    s_pref[l] = acc;
-                    acc += a.Hq * p;
-                }
-                s_pref[maxm] = acc;
-                sh.maxm = maxm;
-                sh.total = acc;
-            } else {
-                for (int i = 0; i < a.B; ++i) { s_pref[i] = acc; acc += a.Hq * nb(s_order[i]); }
-                s_pref[a.B] = acc;
-                sh.maxm = maxm;
-                sh.total = acc;
-            }
-        }
-    } else if (tid == 0) {
-        sh.maxm = (a.N + kUnitRows - 1) / kUnitRows;
-        sh.total = a.B * a.Hq * sh.maxm;
-    }
+    build_sched_tables(a, s_cu, s_order, s_pref, &sh.maxm, &sh.total, tid, kThreads);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

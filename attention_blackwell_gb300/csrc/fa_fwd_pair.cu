@@ -28,8 +28,9 @@
 // Barriers the issuers wait on live in the even CTA: the odd CTA's TMA loads
 // and softmax arrivals count there.
 //
-// Fixed-length inputs only.
+// Fixed-length and packed varlen inputs.
 #include "fa_internal.h"
+#include "fa_sched.cuh"
 
 namespace fa {
 namespace {
@@ -46,7 +47,8 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
 constexpr uint32_t kOffV = kOffK + kKS * kKHalf;
 constexpr uint32_t kOffRed = kOffV + kVS * kVHalf;  // row max / sum exchange [2][2][128] float
-constexpr uint32_t kOffBar = kOffRed + 2 * 2 * 128 * 4;
+constexpr uint32_t kOffTab = kOffRed + 2 * 2 * 128 * 4;   // varlen unit tables (fa_sched.cuh)
+constexpr uint32_t kOffBar = kOffTab + ((kTableInts * 4 + 15) & ~15u);
 constexpr uint32_t kPSmem = kOffBar + 512;
 
 constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
@@ -61,49 +63,21 @@ struct PairShared {
     uint64_t s_full, s_free, p_ready, pv_done, o_done, o_free, drain;
     uint32_t tmem_base;
     int abort_flag;
+    int total, maxm;
+    Sched sched;
 };
 static_assert(sizeof(PairShared) <= 512, "barrier block");
 
-struct PUnit {
-    int seq, h, m2, tok0, len;   // m2: 256-row query block
-};
-
-// Unit order over (batch, head, 256-row query block): non-causal head-major
-// with query blocks minor; causal longest-first (query blocks from the last)
-// inside L2 sections of (batch, head) pairs (FlashAttention-4 blog,
-// "Scheduling").
-__device__ __forceinline__ bool pair_unit(const FwdArgs& a, int num_m2, int u, PUnit& U) {
-    const int BH = a.B * a.Hq;
-    if (u >= BH * num_m2) return false;
-    int bh, m;
-    if (!a.causal) {
-        bh = u / num_m2;
-        m = u - bh * num_m2;
-    } else {
-        const int sec = a.l2_section, per = sec * num_m2, full = BH / sec;
-        if (u < full * per) {
-            const int s = u / per, r = u - s * per;
-            m = num_m2 - 1 - r / sec;
-            bh = s * sec + r % sec;
-        } else {
-            const int rem = BH - full * sec, r = u - full * per;
-            m = num_m2 - 1 - r / rem;
-            bh = full * sec + r % rem;
-        }
-    }
-    U.seq = bh / a.Hq;
-    U.h = bh - U.seq * a.Hq;
-    U.m2 = m;
-    U.tok0 = U.seq * a.N;
-    U.len = a.N;
-    return true;
-}
+// Unit order (fa_sched.cuh): fixed length non-causal head-major with query
+// blocks minor; causal longest-first (query blocks from the last) inside L2
+// sections of (batch, head) pairs; varlen sequences sorted by block count,
+// longest first (FlashAttention-4 blog, "Scheduling").
 
 // Key blocks the pair needs: causal stops at the block holding the last row.
-__device__ __forceinline__ int pair_blocks(const PUnit& U, int causal) {
+__device__ __forceinline__ int pair_blocks(const Unit& U, int causal) {
     int keys = U.len;
     if (causal) {
-        const int last = (U.m2 + 1) * kBlockN;
+        const int last = (U.m + 1) * kBlockN;
         keys = last < keys ? last : keys;
     }
     return (keys + kBlockN - 1) / kBlockN;
@@ -164,7 +138,6 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
     PairShared& sh = *reinterpret_cast<PairShared*>(dsm + kOffBar);
     float* red = reinterpret_cast<float*>(dsm + kOffRed);   // [2 parity][2 halves][128 rows]
     const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
-    const int num_m2 = (a.N + kBlockN - 1) / kBlockN;
     // Pair index and count, and this CTA's rank, are re-read from special
     // registers where used rather than held (the softmax has no registers to spare).
 #define PAIR_ID ((int)(blockIdx.x >> 1))
@@ -195,9 +168,25 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         tmem_alloc_pair(&sh.tmem_base, 512);
         tmem_relinquish_pair();
     }
+    {   // unit tables: both CTAs build the same ones
+        int* s_cu = reinterpret_cast<int*>(dsm + kOffTab);
+        int* s_order = s_cu + (kMaxVarlenSeqs + 1);
+        int* s_pref = s_order + kMaxVarlenSeqs;
+        build_sched_tables(a, s_cu, s_order, s_pref, &sh.maxm, &sh.total, tid, kPThreads);
+        __syncthreads();
+        if (tid == 0) {
+            sh.sched.B = a.B; sh.sched.Hq = a.Hq; sh.sched.N = a.N; sh.sched.causal = a.causal;
+            sh.sched.varlen = a.varlen; sh.sched.num_m = sh.maxm; sh.sched.maxm = sh.maxm;
+            sh.sched.sec = a.l2_section; sh.sched.total = sh.total;
+            sh.sched.s_cu = s_cu; sh.sched.s_order = s_order; sh.sched.s_pref = s_pref;
+        }
+    }
     tc_fence_before();
     cluster_sync_all();   // barriers of both CTAs initialised before any remote arrival
     tc_fence_after();
+    // Read through shared memory on every call (keeps the decode state out of
+    // the registers of the lean warps).
+    const Sched& sched = sh.sched;
 
     const WaitCtx wc{&sh.abort_flag, a.status};
     const uint32_t tmem = sh.tmem_base;
@@ -215,12 +204,12 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 uint32_t kit = 0, uc = 0;
                 bool ok = true;
                 for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
-                    PUnit U;
-                    if (!pair_unit(a, num_m2, u, U)) break;
+                    Unit U;
+                    if (!sched.get(u, U)) break;
                     const int hk = U.h / group, nb = pair_blocks(U, a.causal);
                     if (!(ok = mbar_wait(&sh.q_empty, (uc & 1) ^ 1, wc, kPSiteQEmpty))) break;
                     if (leader) mbar_arrive_expect_tx(&sh.q_full, 2 * kQBytes);
-                    const int qrow = U.tok0 + U.m2 * kBlockN + RANK * kTileM;
+                    const int qrow = U.tok0 + U.m * kBlockN + RANK * kTileM;
                     for (int c = 0; c < 2; ++c) tma_load_3d_pair(sQ + c * kQBox, &tq, lead(&sh.q_full), c * 64, U.h, qrow);
                     for (int j = 0; j < nb; ++j) {
                         const uint32_t slot = kit % kKS;
@@ -249,8 +238,8 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 uint32_t vit = 0;
                 bool ok = true;
                 for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
-                    PUnit U;
-                    if (!pair_unit(a, num_m2, u, U)) break;
+                    Unit U;
+                    if (!sched.get(u, U)) break;
                     const int hk = U.h / group, nb = pair_blocks(U, a.causal);
                     for (int j = 0; j < nb; ++j) {
                         const uint32_t slot = vit % kVS;
@@ -275,8 +264,8 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             uint32_t kit = 0, uc = 0, gs = 0;
             bool ok = true;
             for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
-                PUnit U;
-                if (!pair_unit(a, num_m2, u, U)) break;
+                Unit U;
+                if (!sched.get(u, U)) break;
                 const int nb = pair_blocks(U, a.causal);
                 if (!(ok = mbar_wait_w(&sh.q_full, uc & 1, wc, kPSiteQFull))) break;
                 for (int j = 0; j < nb; ++j) {
@@ -305,8 +294,8 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             uint32_t vit = 0, uc = 0, gp = 0;
             bool ok = true;
             for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
-                PUnit U;
-                if (!pair_unit(a, num_m2, u, U)) break;
+                Unit U;
+                if (!sched.get(u, U)) break;
                 const int nb = pair_blocks(U, a.causal);
                 for (int j = 0; j < nb; ++j) {
                     const uint32_t vslot = vit % kVS;
@@ -343,10 +332,10 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         uint32_t ep = 0;   // barrier epoch: exchange buffers alternate with it
         bool ok = true;
         for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
-            PUnit U;
-            if (!pair_unit(a, num_m2, u, U)) break;
+            Unit U;
+            if (!sched.get(u, U)) break;
             const int nb = pair_blocks(U, a.causal);
-            const int m = U.m2 * 2 + RANK;         // this CTA's 128-row query tile
+            const int m = U.m * 2 + RANK;         // this CTA's 128-row query tile
             const int qi = m * kTileM + r;
             float m_ref = -INFINITY, l = 0.f;           // l: this half's partial row sum
             bool okw = true;
@@ -465,9 +454,10 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     }
                 }
             }
-            if (valid && x == 0)
-                a.lse[((size_t)U.seq * a.Hq + U.h) * a.N + qi] =
-                    lt > 0.f ? (m_ref + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
+            if (valid && x == 0) {
+                const size_t li = a.varlen ? (size_t)U.h * a.N + U.tok0 + qi : ((size_t)U.seq * a.Hq + U.h) * a.N + qi;
+                a.lse[li] = lt > 0.f ? (m_ref + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
+            }
             tc_fence_before();
             mbar_arrive_remote_w(lead(&sh.o_free));
         }
@@ -516,7 +506,9 @@ cudaError_t launch_fwd_pair(const FwdLaunch& L, cudaStream_t stream) {
         if (cudaOccupancyMaxActiveClusters(&n, fwd_pair_kernel, &cfg) != cudaSuccess || n < 1) n = L.num_sms / 2;
         max_pairs = g_pairs_resident = n;
     }
-    const long long units = (long long)L.a.B * L.a.Hq * ((L.a.N + kBlockN - 1) / kBlockN);
+    // Upper bound on the unit count (varlen: the kernel computes the exact one).
+    const long long units = L.a.varlen ? ((long long)L.a.N / kBlockN + L.a.B) * L.a.Hq
+                                       : (long long)L.a.B * L.a.Hq * ((L.a.N + kBlockN - 1) / kBlockN);
     int pairs = (int)(units < max_pairs ? units : max_pairs);
     if (pairs < 1) pairs = 1;
     fwd_pair_kernel<<<2 * pairs, kPThreads, kPSmem, stream>>>(L.tq, L.tk, L.tv, L.a);

@@ -182,7 +182,7 @@ def traffic_key(args, w, kernel):
         return "bwd" if (w.varlen or args.deterministic or args.bwd_kernel == 0) else "bwd_pair"
     if kernel != "fwd":
         return kernel
-    if w.varlen or args.exp2_emu or args.fwd_kernel == 0:
+    if args.exp2_emu or args.fwd_kernel == 0 or (w.varlen and args.fwd_kernel == 1):
         return "fwd_pingpong"
     return {1: "fwd_wide", 2: "fwd_pair"}[args.fwd_kernel]
 
@@ -402,7 +402,7 @@ def main_ours(args):
         "config": {"workload": describe(w, r["inp"]),
             "step": step_name, "global_batch": w.B * world, "seq_len": w.N or max(r["inp"]["lengths"]),
             "deterministic_bwd": bool(args.deterministic), "exp2_emu_eighths": args.exp2_emu, "tau": args.tau,
-            "fwd_kernel": ("ping-pong 2x128" if w.varlen or args.exp2_emu else
+            "fwd_kernel": ("ping-pong 2x128" if args.exp2_emu or (w.varlen and args.fwd_kernel == 1) else
                            {0: "ping-pong 2x128", 1: "256-key blocks", 2: "CTA pairs, 256-key blocks"}[args.fwd_kernel]),
             "fwd_pairs_resident": fa_pairs_resident(),
             "bwd_kernel": ("one CTA per 128-key tile" if w.varlen or args.deterministic or args.bwd_kernel == 0

@@ -87,8 +87,9 @@ int fa_set_tuning(int exp2_emu_eighths, float tau);
  *   2 -- (default) CTA pairs (clusters of two): 256 query rows per pair and
  *        256-key blocks, each product one M = 256 UMMA over both SMs, so each
  *        SM loads and reads only half of every K and V block.
- * Kernels 1 and 2 serve fixed-length inputs with exp2_emu_eighths == 0; all
- * other calls use kernel 0.  All compute the same attention up to rounding.
+ * Kernel 2 serves fixed-length and packed varlen inputs, kernel 1 fixed-length
+ * inputs, both with exp2_emu_eighths == 0; all other calls use kernel 0.  All
+ * compute the same attention up to rounding.
  * Errors: FA_ERR_INVALID.
  */
 int fa_set_fwd_kernel(int kernel);

@@ -23,9 +23,9 @@ O_MAX, O_MEAN, LSE_ABS = 2e-2, 1e-3, 1e-3
 @pytest.fixture(scope="module", params=[0, 1, 2], ids=["pingpong", "wide", "pair"])
 def fa(request):
     """Every forward test runs on all forward kernels: 0 = two 128-row query
-    tiles in ping-pong with 128-key tiles, 1 = 256-key blocks, 2 = CTA pairs
-    with 256-key blocks (1 and 2: fixed-length inputs; varlen and the
-    FMA-exp2 variants always use kernel 0)."""
+    tiles in ping-pong with 128-key tiles, 1 = 256-key blocks (fixed length),
+    2 = CTA pairs with 256-key blocks (fixed length and varlen); the FMA-exp2
+    variants always use kernel 0."""
     import attention_blackwell_gb300 as fa
     fa.lib()
     fa.set_tuning(0, 8.0)
