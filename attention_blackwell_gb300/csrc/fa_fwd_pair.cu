@@ -363,13 +363,15 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     for (int c = 0; c < 128; ++c)
                         if (c >= lim) s[c] = -INFINITY;
                 }
-                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+                // Row max of this half: three-input max, four chains.
+                float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]),
+                      mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-                for (int c = 4; c < 128; c += 4) {
-                    mx0 = fmaxf(mx0, s[c]);
-                    mx1 = fmaxf(mx1, s[c + 1]);
-                    mx2 = fmaxf(mx2, s[c + 2]);
-                    mx3 = fmaxf(mx3, s[c + 3]);
+                for (int c = 8; c < 128; c += 8) {
+                    mx0 = fmax3(mx0, s[c], s[c + 1]);
+                    mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+                    mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+                    mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
                 }
                 float* rb = red + (ep & 1) * 256;
                 rb[x * 128 + r] = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
@@ -388,17 +390,26 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     m_ref = m_new;
                 }
                 const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                // Exponents two at a time (packed fp32 FMA), exp2 on MUFU,
+                // row sum in two packed accumulators.
                 uint32_t pk[64];
-                float l0 = 0.f, l1 = 0.f;
+                const uint64_t sc2 = f2_pack(scale, scale), nm2 = f2_pack(-m_use, -m_use);
+                uint64_t la = f2_pack(0.f, 0.f), lb = la;
 #pragma unroll
                 for (int i = 0; i < 64; ++i) {
-                    const float p0 = ex2_mufu(fmaf(s[2 * i], scale, -m_use));
-                    const float p1 = ex2_mufu(fmaf(s[2 * i + 1], scale, -m_use));
-                    l0 += p0;
-                    l1 += p1;
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sc2, nm2), x0, x1);
+                    const float p0 = ex2_mufu(x0), p1 = ex2_mufu(x1);
+                    if (i & 1) lb = f2_add(lb, f2_pack(p0, p1));
+                    else la = f2_add(la, f2_pack(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
                 }
-                l += l0 + l1;
+                {
+                    float a0, a1, b0, b1;
+                    f2_unpack(la, a0, a1);
+                    f2_unpack(lb, b0, b1);
+                    l += (a0 + a1) + (b0 + b1);
+                }
                 // P's columns and O are free once the previous P V is done.
                 if (j > 0) {
                     okw = mbar_wait(&sh.pv_done, pc & 1, wc, kPSitePV) && okw;
@@ -410,8 +421,14 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                             uint32_t o[32];
                             tmem_ld32(tO + c0, o);
                             tmem_wait_ld();
+                            const uint64_t f2 = f2_pack(fac, fac);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * fac);
+                            for (int i = 0; i < 32; i += 2) {
+                                float y0, y1;
+                                f2_unpack(f2_mul(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), f2), y0, y1);
+                                o[i] = __float_as_uint(y0);
+                                o[i + 1] = __float_as_uint(y1);
+                            }
                             tmem_st32(tO + c0, o);
                         }
                     }
