@@ -173,6 +173,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     if ((rc = make_map(&L.tq, q, Hq, T)) != FA_OK) return rc;
     if ((rc = make_map(&L.tk, k, Hkv, T, wide ? 256 : kTileM)) != FA_OK) return rc;
     if ((rc = make_map(&L.tv, v, Hkv, T, (wide || pair) ? 256 : kTileM)) != FA_OK) return rc;
+    if (pair && (rc = make_map(&L.to, o, Hq, T)) != FA_OK) return rc;
     L.a.o = o;
     L.a.lse = lse;
     L.a.cu_seqlens = cu_seqlens;

@@ -49,7 +49,9 @@ constexpr uint32_t kOffV = kOffK + kKS * kKHalf;
 constexpr uint32_t kOffRed = kOffV + kVS * kVHalf;  // row max / sum exchange [2][2][128] float
 constexpr uint32_t kOffTab = kOffRed + 2 * 2 * 128 * 4;   // varlen unit tables (fa_sched.cuh)
 constexpr uint32_t kOffBar = kOffTab + ((kTableInts * 4 + 15) & ~15u);
-constexpr uint32_t kPSmem = kOffBar + 512;
+constexpr uint32_t kOffStg = (kOffBar + 512 + 1023) & ~1023u;   // O staging: 128 rows x 64 bf16 (one TMA box)
+constexpr uint32_t kPSmem = kOffStg + 16384;
+static_assert(kPSmem <= 232448, "shared memory plan");
 
 constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
 constexpr uint16_t kBoth = 3;                       // CTA mask: both CTAs of the pair
@@ -124,7 +126,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
 fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
+                const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, const FwdArgs a) {
     extern __shared__ __align__(1024) uint8_t dsm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t base = smem_u32(dsm);
@@ -453,23 +455,49 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             const float lt = rl[r] + rl[128 + r];
             const bool valid = qi < U.len;
             const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
-            uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) +
-                                                   ((size_t)(U.tok0 + qi) * a.Hq + U.h) * kHeadDim + x * 64);
+            uint4 ov[8];   // this thread's 64 output columns, bf16
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t o[32];
                 tmem_ld32(tO + c0, o);
                 tmem_wait_ld();
-                if (valid) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float* f = reinterpret_cast<const float*>(o + 8 * q);
-                        orow[c0 / 8 + q] = make_uint4(pack_bf16x2(f[0] * inv_l, f[1] * inv_l),
-                                                      pack_bf16x2(f[2] * inv_l, f[3] * inv_l),
-                                                      pack_bf16x2(f[4] * inv_l, f[5] * inv_l),
-                                                      pack_bf16x2(f[6] * inv_l, f[7] * inv_l));
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    const float* f = reinterpret_cast<const float*>(o + 8 * q);
+                    ov[c0 / 8 + q] = make_uint4(pack_bf16x2(f[0] * inv_l, f[1] * inv_l),
+                                                pack_bf16x2(f[2] * inv_l, f[3] * inv_l),
+                                                pack_bf16x2(f[4] * inv_l, f[5] * inv_l),
+                                                pack_bf16x2(f[6] * inv_l, f[7] * inv_l));
                 }
+            }
+            if ((m + 1) * kTileM <= U.len) {
+                // A full tile: each half in turn through the 128-B-swizzled
+                // staging box and one TMA store (scattered 16-byte row stores
+                // from every thread serialise in the load/store unit).
+                uint8_t* srow = dsm + kOffStg + r * 128;
+#pragma unroll
+                for (int xr = 0; xr < 2; ++xr) {
+                    if (x == xr) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(srow + ((q ^ (r & 7)) << 4)) = ov[q];
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    }
+                    asm volatile("bar.sync 2, 256;" ::: "memory");
+                    if (x == 0 && r == 0) {
+                        asm volatile(
+                            "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];\n\t"
+                            "cp.async.bulk.commit_group;\n\t"
+                            "cp.async.bulk.wait_group.read 0;"
+                            ::"l"(reinterpret_cast<uint64_t>(&to)), "r"(xr * 64), "r"(U.h), "r"(U.tok0 + m * kTileM),
+                              "r"(base + kOffStg) : "memory");
+                    }
+                    asm volatile("bar.sync 2, 256;" ::: "memory");
+                }
+            } else if (valid) {
+                uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) +
+                                                       ((size_t)(U.tok0 + qi) * a.Hq + U.h) * kHeadDim + x * 64);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) orow[q] = ov[q];
             }
             if (valid && x == 0) {
                 const size_t li = a.varlen ? (size_t)U.h * a.N + U.tok0 + qi : ((size_t)U.seq * a.Hq + U.h) * a.N + qi;
@@ -479,6 +507,8 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             mbar_arrive_remote_w(lead(&sh.o_free));
         }
     }
+
+    if (warp == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // O stores complete
 
     // After an abort the odd CTA cannot observe its own last loads (they count
     // on the even CTA's barriers): give them time to land before its shared
@@ -528,7 +558,7 @@ cudaError_t launch_fwd_pair(const FwdLaunch& L, cudaStream_t stream) {
                                        : (long long)L.a.B * L.a.Hq * ((L.a.N + kBlockN - 1) / kBlockN);
     int pairs = (int)(units < max_pairs ? units : max_pairs);
     if (pairs < 1) pairs = 1;
-    fwd_pair_kernel<<<2 * pairs, kPThreads, kPSmem, stream>>>(L.tq, L.tk, L.tv, L.a);
+    fwd_pair_kernel<<<2 * pairs, kPThreads, kPSmem, stream>>>(L.tq, L.tk, L.tv, L.to, L.a);
     return cudaGetLastError();
 }
 

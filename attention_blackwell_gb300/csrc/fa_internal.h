@@ -33,6 +33,7 @@ struct FwdArgs {
 
 struct FwdLaunch {
     CUtensorMap tq, tk, tv;  // 3-D maps {128, H, T}, box {64, 1, 128}, 128-B swizzle
+    CUtensorMap to;          // O, same shape as tq (pair kernel: TMA stores of full tiles)
     FwdArgs a;
     int emu_eighths;         // 0..4: share of exp2 pairs on the FMA pipe, in eighths
     int num_sms;
