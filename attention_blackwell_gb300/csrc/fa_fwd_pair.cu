@@ -330,9 +330,84 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         const uint32_t tP = tmem + lb + kColP + x * 64;
         const uint32_t tO = tmem + lb + kColO + x * 64;
         const float scale = a.scale_log2;
-        uint32_t sc = 0, pc = 0, uc = 0;
+        uint32_t sc = 0, pc = 0, ucd = 0;   // S phases, P V phases, epilogues done
         uint32_t ep = 0;   // barrier epoch: exchange buffers alternate with it
         bool ok = true;
+        bool first = true;                   // no P V precedes this CTA's first block
+        int u_pend = -1;                     // unit whose output is still in TMEM
+        float l_pend = 0.f, m_pend = 0.f;
+        // Epilogue of unit up (run after the next unit's first P is out, so
+        // the wait for the unit's last P V overlaps that block): whole-row sum
+        // from the two halves, O / l, LSE; then O's columns are free for the
+        // next unit's first P V.
+        auto epilogue = [&](int up, float lp, float mp, bool okw) -> bool {
+            Unit U;
+            sched.get(up, U);
+            const int m = U.m * 2 + RANK;
+            const int qi = m * kTileM + r;
+            okw = mbar_wait(&sh.o_done, ucd & 1, wc, kPSiteO) && okw;
+            ++ucd;
+            tc_fence_after();
+            // Epilogue: whole-row sum from the two halves, O / l, LSE.
+            float* rl = red + (ep & 1) * 256;
+            rl[x * 128 + r] = lp;
+            ++ep;
+            if (pnamed_bar_or(2, 256, !okw)) return false;
+            const float lt = rl[r] + rl[128 + r];
+            const bool valid = qi < U.len;
+            const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
+            uint4 ov[8];   // this thread's 64 output columns, bf16
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld32(tO + c0, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float* f = reinterpret_cast<const float*>(o + 8 * q);
+                    ov[c0 / 8 + q] = make_uint4(pack_bf16x2(f[0] * inv_l, f[1] * inv_l),
+                                                pack_bf16x2(f[2] * inv_l, f[3] * inv_l),
+                                                pack_bf16x2(f[4] * inv_l, f[5] * inv_l),
+                                                pack_bf16x2(f[6] * inv_l, f[7] * inv_l));
+                }
+            }
+            if ((m + 1) * kTileM <= U.len) {
+                // A full tile: each half in turn through the 128-B-swizzled
+                // staging box and one TMA store (scattered 16-byte row stores
+                // from every thread serialise in the load/store unit).
+                uint8_t* srow = dsm + kOffStg + r * 128;
+#pragma unroll
+                for (int xr = 0; xr < 2; ++xr) {
+                    if (x == xr) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(srow + ((q ^ (r & 7)) << 4)) = ov[q];
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    }
+                    asm volatile("bar.sync 2, 256;" ::: "memory");
+                    if (x == 0 && r == 0) {
+                        asm volatile(
+                            "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];\n\t"
+                            "cp.async.bulk.commit_group;\n\t"
+                            "cp.async.bulk.wait_group.read 0;"
+                            ::"l"(reinterpret_cast<uint64_t>(&to)), "r"(xr * 64), "r"(U.h), "r"(U.tok0 + m * kTileM),
+                              "r"(base + kOffStg) : "memory");
+                    }
+                    asm volatile("bar.sync 2, 256;" ::: "memory");
+                }
+            } else if (valid) {
+                uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) +
+                                                       ((size_t)(U.tok0 + qi) * a.Hq + U.h) * kHeadDim + x * 64);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) orow[q] = ov[q];
+            }
+            if (valid && x == 0) {
+                const size_t li = a.varlen ? (size_t)U.h * a.N + U.tok0 + qi : ((size_t)U.seq * a.Hq + U.h) * a.N + qi;
+                a.lse[li] = lt > 0.f ? (mp + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
+            }
+            tc_fence_before();
+            mbar_arrive_remote_w(lead(&sh.o_free));
+            return true;
+        };
         for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
             Unit U;
             if (!sched.get(u, U)) break;
@@ -412,12 +487,14 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     f2_unpack(lb, b0, b1);
                     l += (a0 + a1) + (b0 + b1);
                 }
-                // P's columns and O are free once the previous P V is done.
-                if (j > 0) {
+                // P's columns (and, inside a unit, O) are free once the previous
+                // P V is done -- also across units: the previous unit's last
+                // P V still reads P.
+                if (!first) {
                     okw = mbar_wait(&sh.pv_done, pc & 1, wc, kPSitePV) && okw;
                     ++pc;
                     tc_fence_after();
-                    if (rescale) {
+                    if (j > 0 && rescale) {
 #pragma unroll
                         for (int c0 = 0; c0 < 64; c0 += 32) {
                             uint32_t o[32];
@@ -441,71 +518,18 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive_remote_w(lead(&sh.p_ready));
+                first = false;
+                if (j == 0 && u_pend >= 0) {   // the previous unit's output
+                    if (!epilogue(u_pend, l_pend, m_pend, okw)) { ok = false; break; }
+                    u_pend = -1;
+                }
             }
             if (!ok) break;
-            okw = mbar_wait(&sh.o_done, uc & 1, wc, kPSiteO) && okw;
-            ++uc;
-            if (nb > 0) ++pc;   // the unit's last P V: its pv_done phase
-            tc_fence_after();
-            // Epilogue: whole-row sum from the two halves, O / l, LSE.
-            float* rl = red + (ep & 1) * 256;
-            rl[x * 128 + r] = l;
-            ++ep;
-            if (pnamed_bar_or(2, 256, !okw)) { ok = false; break; }
-            const float lt = rl[r] + rl[128 + r];
-            const bool valid = qi < U.len;
-            const float inv_l = lt > 0.f ? 1.f / lt : 0.f;
-            uint4 ov[8];   // this thread's 64 output columns, bf16
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-                uint32_t o[32];
-                tmem_ld32(tO + c0, o);
-                tmem_wait_ld();
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float* f = reinterpret_cast<const float*>(o + 8 * q);
-                    ov[c0 / 8 + q] = make_uint4(pack_bf16x2(f[0] * inv_l, f[1] * inv_l),
-                                                pack_bf16x2(f[2] * inv_l, f[3] * inv_l),
-                                                pack_bf16x2(f[4] * inv_l, f[5] * inv_l),
-                                                pack_bf16x2(f[6] * inv_l, f[7] * inv_l));
-                }
-            }
-            if ((m + 1) * kTileM <= U.len) {
-                // A full tile: each half in turn through the 128-B-swizzled
-                // staging box and one TMA store (scattered 16-byte row stores
-                // from every thread serialise in the load/store unit).
-                uint8_t* srow = dsm + kOffStg + r * 128;
-#pragma unroll
-                for (int xr = 0; xr < 2; ++xr) {
-                    if (x == xr) {
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(srow + ((q ^ (r & 7)) << 4)) = ov[q];
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    }
-                    asm volatile("bar.sync 2, 256;" ::: "memory");
-                    if (x == 0 && r == 0) {
-                        asm volatile(
-                            "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];\n\t"
-                            "cp.async.bulk.commit_group;\n\t"
-                            "cp.async.bulk.wait_group.read 0;"
-                            ::"l"(reinterpret_cast<uint64_t>(&to)), "r"(xr * 64), "r"(U.h), "r"(U.tok0 + m * kTileM),
-                              "r"(base + kOffStg) : "memory");
-                    }
-                    asm volatile("bar.sync 2, 256;" ::: "memory");
-                }
-            } else if (valid) {
-                uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) +
-                                                       ((size_t)(U.tok0 + qi) * a.Hq + U.h) * kHeadDim + x * 64);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) orow[q] = ov[q];
-            }
-            if (valid && x == 0) {
-                const size_t li = a.varlen ? (size_t)U.h * a.N + U.tok0 + qi : ((size_t)U.seq * a.Hq + U.h) * a.N + qi;
-                a.lse[li] = lt > 0.f ? (m_ref + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
-            }
-            tc_fence_before();
-            mbar_arrive_remote_w(lead(&sh.o_free));
+            u_pend = u;
+            l_pend = l;
+            m_pend = m_ref;
         }
+        if (ok && u_pend >= 0) ok = epilogue(u_pend, l_pend, m_pend, true);
     }
 
     if (warp == 0 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // O stores complete
