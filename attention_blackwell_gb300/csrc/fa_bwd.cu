@@ -629,6 +629,20 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         const uint32_t tR1 = tmem + lb + kColR1;
         uint32_t jj = 0, uc = 0;
         bool ok = true;
+        // Deterministic mode: the semaphore of the previous query tile, to be
+        // released once that tile's reductions are complete -- checked at the
+        // start of the next tile instead of waited for at the end of this one,
+        // so the drain does not stall on the round trip to L2 every tile.
+        int* sem_pend = nullptr;
+        auto release_pending = [&]() {
+            if (r == 0 && sem_pend) {
+                bulk_wait0();          // the tile's additions are complete
+                fence_async_global();
+                __threadfence();
+                red_release_add(sem_pend, 1);
+            }
+            sem_pend = nullptr;
+        };
         for (int u = blockIdx.x; ok; u += gridDim.x) {
             BUnit U;
             if (!bwd_unit(a, total, u, U)) break;
@@ -654,6 +668,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 int* sem = a.deterministic ? a.sem + (size_t)h * a.sem_stride + U.seq + (U.tok0 + i * kTileM) / kTileN
                                            : nullptr;
                 if (sem) {
+                    release_pending();
                     // Key tiles add into this query tile in ascending order;
                     // wait (bounded) until the previous one has released it.
                     bool gave_up = false;
@@ -705,16 +720,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         bulk_commit();
                     }
                 }
-                if (r == 0) {
-                    if (sem) {
-                        bulk_wait0();          // our additions are complete
-                        fence_async_global();
-                        __threadfence();
-                        red_release_add(sem, 1);
-                    }
-                }
+                sem_pend = sem;
             }
             if (!ok) break;
+            release_pending();   // before the dK/dV epilogue: the next key tile is waiting
             if (!(ok = mbar_wait(&sh.dkdv_done, uc & 1, wc, kBSiteDkdv))) break;
             ++uc;
             tc_fence_after();
