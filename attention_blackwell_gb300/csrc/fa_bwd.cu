@@ -9,7 +9,8 @@
 // Three stages on the caller's stream:
 //   1. preprocess: D (one warp per query row and head), dQacc := 0,
 //      semaphores := 0, and for varlen a work list in longest-first order;
-//   2. main kernel: one persistent CTA per SM; a work unit is one 128-key
+//   2. main kernel: one persistent CTA per SM, claiming work units in list
+//      order from a global counter as it frees up; a work unit is one 128-key
 //      tile of one (sequence, key/value head); the CTA keeps K, V and the dK,
 //      dV accumulators resident and streams the query tiles of every query
 //      head of the group.  It recomputes S and P transposed (keys on the
@@ -58,13 +59,23 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
     }
 }
 
-// Varlen work list: units (sequence, key/value head, key tile k) ordered by
-// k ascending (longest remaining query range first under a causal mask, and
-// the order the deterministic semaphores need), sequences within a level by
-// key-tile count, descending.  One CTA of 1024 threads.
+// Varlen work list: units (sequence, key/value head, key tile k), the most
+// expensive first, so that CTAs claiming them in list order finish close
+// together (longest-processing-time-first).  A unit streams every query tile
+// its key tile sees, times the group's query heads, so its cost is set by
+// the number of those query tiles: nk - k under a causal mask, nk without
+// (nk = the sequence's tile count).
+//   causal: level L holds the units that see c = maxk - L query tiles: one
+//     per sequence with at least c tiles and key/value head, the shortest
+//     sequence first -- which lists each sequence's key tiles in ascending
+//     order, the order the deterministic semaphores need;
+//   non-causal: level L is sequence order[L] (longest first), key/value
+//     head major, key tiles ascending (the heads' Q and dO stay in L2 while
+//     their key tiles run).
+// One CTA of 1024 threads.
 __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a) {
-    __shared__ int s_cu[kMaxVarlenSeqs + 1], s_order[kMaxVarlenSeqs], s_pref[kLevelsMax + 1];
-    __shared__ int s_maxk;
+    __shared__ int s_cu[kMaxVarlenSeqs + 1], s_order[kMaxVarlenSeqs], s_pref[kLevelsMax + 1], s_cnt[kLevelsMax];
+    __shared__ int s_maxk, s_levels;
     const int tid = threadIdx.x, B = a.B;
     for (int i = tid; i <= B; i += blockDim.x) {
         const int c = a.cu_seqlens[i];
@@ -82,7 +93,7 @@ __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a) {
             const int nj = nkv(j);
             rank += (nj > ni) || (nj == ni && j < i);
         }
-        s_order[rank] = i;
+        s_order[rank] = i;   // tile count descending, index ascending among equals
     }
     __syncthreads();
     if (tid == 0) {
@@ -91,26 +102,49 @@ __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a) {
             if (atomicCAS(&a.hdr->status.code, 0, -1) == 0) a.hdr->status.where = 200;
             maxk = 0;
         }
-        int acc = 0, p = B;
-        for (int k = 0; k < maxk; ++k) {
-            while (p > 0 && nkv(s_order[p - 1]) <= k) --p;   // sequences with more than k key tiles
-            s_pref[k] = acc;
-            acc += p * a.Hkv;
+        int acc = 0, levels;
+        if (a.causal) {
+            int p = 0;
+            for (int L = 0; L < maxk; ++L) {
+                while (p < B && nkv(s_order[p]) >= maxk - L) ++p;   // sequences with >= c tiles
+                s_cnt[L] = p;
+                s_pref[L] = acc;
+                acc += p * a.Hkv;
+            }
+            levels = maxk;
+        } else {
+            levels = maxk > 0 ? B : 0;
+            for (int L = 0; L < levels; ++L) {
+                s_pref[L] = acc;
+                acc += nkv(s_order[L]) * a.Hkv;
+            }
         }
-        s_pref[maxk] = acc;
+        s_pref[levels] = acc;
         s_maxk = maxk;
+        s_levels = levels;
         a.hdr->total_units = acc;
     }
     __syncthreads();
-    const int maxk = s_maxk, total = s_pref[maxk];
+    const int maxk = s_maxk, levels = s_levels, total = s_pref[levels];
     for (int u = tid; u < total; u += blockDim.x) {
-        int lo = 0, hi = maxk;
+        int lo = 0, hi = levels;
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
             if (s_pref[mid + 1] > u) hi = mid; else lo = mid + 1;
         }
         const int r = u - s_pref[lo];
-        a.units[u] = make_int4(s_order[r / a.Hkv], r % a.Hkv, lo, 0);
+        int seq, hk, k;
+        if (a.causal) {
+            seq = s_order[s_cnt[lo] - 1 - r / a.Hkv];
+            hk = r % a.Hkv;
+            k = nkv(seq) - (maxk - lo);
+        } else {
+            seq = s_order[lo];
+            const int nk = nkv(seq);
+            hk = r / nk;
+            k = r - hk * nk;
+        }
+        a.units[u] = make_int4(seq, hk, k, 0);
     }
 }
 
@@ -172,6 +206,8 @@ constexpr uint32_t kBwdSmem = kOffBar + 1024;           // 232448
 struct BwdShared {
     uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty;
     uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dq_full, dq_free, dkdv_done, acc_free, drain, r0_free;
+    uint64_t unit_full[4], unit_empty[4];   // ring of claimed unit indices
+    int unit_id[4];
     uint32_t tmem_base;
     int abort_flag;
     int total;
@@ -181,7 +217,11 @@ static_assert(sizeof(BwdShared) <= 1024, "barrier block");
 constexpr uint32_t kColDK = 0, kColDV = 128, kColR0 = 256, kColR1 = 384;
 
 enum : int { kBSiteKvEmpty = 11, kBSiteQEmpty, kBSiteKvFull, kBSiteAcc, kBSiteQFull, kBSiteP, kBSiteDs,
-             kBSiteDqFree, kBSiteS, kBSiteDp, kBSiteDsFree, kBSiteDq, kBSiteDkdv, kBSiteSem };
+             kBSiteDqFree, kBSiteS, kBSiteDp, kBSiteDsFree, kBSiteDq, kBSiteDkdv, kBSiteSem, kBSiteUnit };
+
+// Readers of each claimed unit index: the two issuer warps (one arrival
+// each), the 256 key-row threads and the 128 dQ threads.
+constexpr uint32_t kUnitReaders = 2 + 256 + 128;
 
 struct BUnit {
     int seq, hk, k, tok0, len, n, nq, i0;
@@ -194,10 +234,12 @@ struct BUnit {
 // batch-head sections).  Fixed length otherwise: key tile k = u / (B*Hkv),
 // all first key tiles before any second one -- longest first under a causal
 // mask, and in deterministic mode a key tile waits at its semaphores only on
-// tiles that started a wave earlier.  Both orders put every unit after the
-// ones it waits on.  Varlen: the planned work list.
+// tiles that are already claimed.  Both orders put every unit after the
+// ones it waits on, and CTAs claim units in list order, so the earliest
+// unfinished unit always runs.  Varlen: the planned work list.  u < 0 is the
+// end of the list.
 __device__ __forceinline__ bool bwd_unit(const BwdArgs& a, int total, int u, BUnit& U) {
-    if (u >= total) return false;
+    if (u < 0 || u >= total) return false;
     if (!a.varlen) {
         const int bh = a.B * a.Hkv;
         int r;
@@ -340,6 +382,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         mbar_init(&sh.acc_free, 128);
         mbar_init(&sh.drain, 2);   // both issuers
         mbar_init(&sh.r0_free, 1);
+        for (int s = 0; s < 4; ++s) { mbar_init(&sh.unit_full[s], 1); mbar_init(&sh.unit_empty[s], kUnitReaders); }
         sh.abort_flag = 0;
         sh.total = a.varlen ? a.hdr->total_units : a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN);
         fence_mbar_init();
@@ -374,7 +417,31 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             // ------------------------------------------------------------ loader
             uint32_t jj = 0, uc = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok; u += gridDim.x) {
+            for (uint32_t n = 0; ok; ++n) {
+                // Claim the next unit: the first by block index, then in
+                // list order from the global counter, so that a CTA that
+                // finishes early takes more.  Exhausting the list counts the
+                // CTA out; the last one out rewinds the counter for the next
+                // launch.
+                int u = -1;
+                if (lane == 0) {
+                    ok = mbar_wait(&sh.unit_empty[n & 3], ((n >> 2) & 1) ^ 1, wc, kBSiteUnit);
+                    if (ok) {
+                        u = n == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&a.hdr->next_unit, 1);
+                        if (u >= total) {
+                            u = -1;
+                            if (atomicAdd(&a.hdr->done_ctas, 1) == (int)gridDim.x - 1) {
+                                atomicExch(&a.hdr->next_unit, 0);
+                                atomicExch(&a.hdr->done_ctas, 0);
+                            }
+                        }
+                        sh.unit_id[n & 3] = u;
+                        mbar_arrive(&sh.unit_full[n & 3]);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                u = __shfl_sync(0xffffffffu, u, 0);
+                if (!ok) break;
                 BUnit U;
                 if (!bwd_unit(a, total, u, U)) break;
                 if (lane == 0) ok = mbar_wait(&sh.kv_empty, (uc & 1) ^ 1, wc, kBSiteKvEmpty);
@@ -449,7 +516,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             // wait for Q never holds back the other four products.
             uint32_t jj = 0, uc = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok; u += gridDim.x) {
+            for (uint32_t n = 0; ok; ++n) {
+                if (!(ok = mbar_wait_w(&sh.unit_full[n & 3], (n >> 2) & 1, wc, kBSiteUnit))) break;
+                const int u = *(volatile int*)&sh.unit_id[n & 3];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.unit_empty[n & 3]);
                 BUnit U;
                 if (!bwd_unit(a, total, u, U)) break;
                 if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, kBSiteKvFull))) break;
@@ -470,7 +541,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             // ---------------------------------------- dV, dK, dQ, dP issuer
             uint32_t jj = 0, uc = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok; u += gridDim.x) {
+            for (uint32_t n = 0; ok; ++n) {
+                if (!(ok = mbar_wait_w(&sh.unit_full[n & 3], (n >> 2) & 1, wc, kBSiteUnit))) break;
+                const int u = *(volatile int*)&sh.unit_id[n & 3];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.unit_empty[n & 3]);
                 BUnit U;
                 if (!bwd_unit(a, total, u, U)) break;
                 if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, kBSiteKvFull))) break;
@@ -529,7 +604,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         const int sw = r & 7;
         uint32_t jj = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok; u += gridDim.x) {
+        for (uint32_t n = 0; ok; ++n) {
+            if (!(ok = mbar_wait(&sh.unit_full[n & 3], (n >> 2) & 1, wc, kBSiteUnit))) break;
+            const int u = *(volatile int*)&sh.unit_id[n & 3];
+            mbar_arrive(&sh.unit_empty[n & 3]);
             BUnit U;
             if (!bwd_unit(a, total, u, U)) break;
             const int key = U.k * kTileN + r;
@@ -643,7 +721,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             }
             sem_pend = nullptr;
         };
-        for (int u = blockIdx.x; ok; u += gridDim.x) {
+        for (uint32_t n = 0; ok; ++n) {
+            ok = mbar_wait(&sh.unit_full[n & 3], (n >> 2) & 1, wc, kBSiteUnit);
+            // The warpgroup meets at named barriers below: it leaves together.
+            if (named_bar_or(1, 128, !ok)) { ok = false; break; }
+            const int u = *(volatile int*)&sh.unit_id[n & 3];
+            mbar_arrive(&sh.unit_empty[n & 3]);
             BUnit U;
             if (!bwd_unit(a, total, u, U)) break;
             const int span = U.nq - U.i0;
@@ -724,7 +807,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             }
             if (!ok) break;
             release_pending();   // before the dK/dV epilogue: the next key tile is waiting
-            if (!(ok = mbar_wait(&sh.dkdv_done, uc & 1, wc, kBSiteDkdv))) break;
+            ok = mbar_wait(&sh.dkdv_done, uc & 1, wc, kBSiteDkdv);
+            if (named_bar_or(1, 128, !ok)) { ok = false; break; }
             ++uc;
             tc_fence_after();
             const int key = U.k * kTileN + r;
@@ -766,6 +850,8 @@ __global__ void bwd_reset_status_kernel(BwdHeader* hdr) {
     hdr->status.code = 0;
     hdr->status.where = 0;
     hdr->status.block = 0;
+    hdr->next_unit = 0;
+    hdr->done_ctas = 0;
 }
 
 }  // namespace

@@ -51,8 +51,11 @@ struct FwdLaunch {
 struct BwdHeader {
     DevStatus status;
     int total_units;   // varlen: written by the plan kernel
-    int pad[59];
+    int next_unit;     // main kernel: units claimed past the first wave
+    int done_ctas;     // main kernel: CTAs that found the list exhausted
+    int pad[57];
 };
+static_assert(sizeof(BwdHeader) == 256, "backward workspace header");
 
 struct WsLayout {
     size_t d_off, dq_off, sem_off, unit_off, total;

@@ -158,3 +158,59 @@ def test_full_size_deterministic_bit_identical(full):
             assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
     for a, b in zip(det[0], atomic):  # the two modes agree up to summation order
         assert np.abs(a - b).max() <= 1e-2 * max(np.abs(b).max(), 1e-6)
+
+
+# ------------------------------------------- work-list order and claiming
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_deterministic_many_units(fa, causal):
+    """Varlen work list, most expensive unit first, claimed dynamically: with
+    more than two waves of units the fixed-order semaphores must still see
+    every sequence's key tiles in ascending order (no wait on an unclaimed
+    unit), and the result must repeat bit for bit."""
+    lengths = [2500, 2000, 1500, 1000, 700, 300, 129, 0, 1]
+    inp = inputs(0, 0, 8, 8, seed=41, lengths=lengths)
+    runs = gpu_grads(fa, inp, causal, deterministic=True, repeats=3)
+    for r in runs[1:]:
+        for a_, b_ in zip(runs[0], r):
+            assert np.array_equal(a_.view(np.uint32), b_.view(np.uint32))
+    check(runs[0], oracle(inp, causal))
+
+
+def test_varlen_full_size_mqa_sampled(fa):
+    """The packed causal workload at full size (16 sequences of 512-8192
+    tokens, 32 query heads on one key/value head): the two shortest
+    sequences checked whole, all 32 heads, against the oracle."""
+    w = W.WORKLOADS["varlen"]
+    inp = W.make_inputs(w, with_grad=True)
+    dq, dk, dv = gpu_grads(fa, inp, True)[0]
+    cu = inp["cu_seqlens"]
+    for s in np.argsort(inp["lengths"])[:2]:
+        c0, c1 = int(cu[s]), int(cu[s + 1])
+        sl = {n: inp[n][c0:c1].unsqueeze(0) for n in ("q", "k", "v", "do")}
+        ref = A.backward(sl["q"], sl["k"], sl["v"], sl["do"], w.alpha, True)
+        check([g[c0:c1] for g in (dq, dk, dv)], [r[0] for r in ref])
+
+
+def test_claim_counter_rewinds(fa):
+    """The main stage claims units from a counter in the workspace header;
+    the last CTA to find the list exhausted rewinds it, so the main stage
+    can run again on the same workspace without the preprocess."""
+    inp = inputs(2, 1000, 4, 2, seed=43)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.fwd(q, k, v, causal=True)
+    ws = fa.bwd_workspace(2, 4, 1000)
+    dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
+    fa.bwd(q, k, v, o, lse, do, causal=True, workspace=ws, dq=dq, dk=dk, dv=dv, stages=1)
+    fa.bwd(q, k, v, o, lse, do, causal=True, workspace=ws, dq=dq, dk=dk, dv=dv, stages=2)
+    torch.cuda.synchronize()
+    hdr = ws[:32].view(torch.int32).cpu().numpy()
+    assert fa.device_status(ws) == 0
+    assert hdr[5] == 0 and hdr[6] == 0, hdr     # next unit, CTAs counted out
+    first = (dk.clone(), dv.clone())
+    dk.zero_()
+    dv.zero_()
+    fa.bwd(q, k, v, o, lse, do, causal=True, workspace=ws, dq=dq, dk=dk, dv=dv, stages=2)
+    torch.cuda.synchronize()
+    assert fa.device_status(ws) == 0
+    assert torch.equal(dk, first[0]) and torch.equal(dv, first[1])
