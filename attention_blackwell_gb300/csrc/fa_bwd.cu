@@ -170,31 +170,34 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 // Warp roles (384 threads):
 //   warps 0-3   "softmax" warpgroup, one thread per KEY row (TMEM lane):
 //               P^T = 2^(alpha log2e S^T - LSE log2e) -> bf16 into TMEM
-//               (operand A of dV += P^T dO); dS^T = P^T (dP^T - D) -> bf16 into
-//               TMEM (operand A of dK += dS^T Q) and into shared memory in the
-//               128-B swizzled layout the dQ UMMA reads as an MN-major A;
+//               (operand A of dV += P^T dO); dS^T = P^T (dP^T - D) -> bf16
+//               into shared memory in the 128-B swizzled key-major layout,
+//               which the dQ UMMA reads as an MN-major A and the dK UMMA as
+//               a K-major A;
 //   warps 4-7   dQ warpgroup, one thread per QUERY row: drains dQ_i from TMEM
 //               into the fp32 accumulator (vector reductions), then at the end
 //               of a unit stores dK (x alpha) and dV in bf16;
 //   warp  8     loader: K, V once per unit (TMA), then Q_i, dO_i (TMA) and
 //               LSE_i, D_i (plain loads) into a two-stage ring;
-//   warp  9     issues dV, dK, dQ, dP;  warp 10 issues S;  warp 11 idle.
+//   warp  9     issues dV, dQ, dK, dP;  warp 10 issues S;  warp 11 idle.
 //
 // Tensor memory (512 columns): dK acc 0-127, dV acc 128-255,
 //   R0 256-383: S^T, then P^T (bf16; each key-row half packs its 64 queries
 //               into the first 32 of the 64 columns it read);
-//   R1 384-511: dP^T, then dS^T (bf16, same packing; operand A of dK), then
-//               dQ_i (the paper's 1-CTA sharing of dP/dS/dQ columns).
+//   R1 384-511: dP^T, then dQ_i once the dS step has read dP^T (the
+//               paper's 1-CTA sharing of dP/dS/dQ columns; dS itself stays in
+//               shared memory).
 // Warp 10 issues each S^T as soon as its Q tile is loaded and dV has read
 // the previous P^T out of R0, so the next tile's S^T is computed while this
 // tile's dS is (FlashAttention-4 blog, "Backward pass": the next tile's
-// products overlap the elementwise work); warp 9 issues dV, dK, dQ and the
-// next dP in that order.
+// products overlap the elementwise work); warp 9 issues dV, dQ, dK and the
+// next dP in that order: dQ before dK, so that the hand-off of dQ out of R1
+// (which the next dP waits for) overlaps the dK product.
 //
 // Shared memory (dynamic, 1024-aligned, 232448 bytes):
 //   K 32K | V 32K | Q[2] 2x32K | dO 32K | dS 32K | dQ staging 32K | lse2[2][128], D[2][128] | barriers
 // dO is single-buffered: it is free once dV has read it and is next needed
-// by dP of the next tile, after dK, S, dQ and the dQ hand-off.
+// by dP of the next tile, after S, dQ, dK and the dQ hand-off.
 constexpr int kBwdThreads = 512;
 constexpr uint32_t kT32 = 32768, kBox = 16384;
 constexpr uint32_t kOffK = 0, kOffV = kT32, kOffQ = 2 * kT32, kOffDO = 4 * kT32, kOffDS = 5 * kT32;
@@ -283,7 +286,7 @@ __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a_smem, uint32_t b_s
     });
 }
 
-// D (+)= A[tmem] B, B MN-major in shared memory (dV += P^T dO, dK += dS^T Q).
+// D (+)= A[tmem] B, B MN-major in shared memory (dV += P^T dO).
 // A is bf16 in the region the two key-row halves wrote: queries 0-63 in
 // columns 0-31 of the region, queries 64-127 in columns 64-95 (each half
 // packs its 64 queries at the start of the 64 columns it read).
@@ -293,6 +296,18 @@ __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b_s
     static_for<8>([&](auto kc) {
         constexpr uint32_t k = kc, col = k * 8 + (k >= 4 ? 32 : 0);
         umma_ts_k<col, ((k * 2048) >> 4)>(d, a_tmem, bd, idesc, (acc | k) != 0);
+    });
+}
+
+// D (+)= A B with A K-major and B MN-major in shared memory (dK += dS^T Q:
+// dS^T is stored key-major with the queries contiguous, as the K-major A of
+// this product; Q as loaded, d contiguous, is its MN-major B).
+__device__ __forceinline__ void mma_ks(uint32_t d, uint32_t a_smem, uint32_t b_smem, uint32_t acc) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+    const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, kBox, 1024);
+    static_for<8>([&](auto kc) {
+        constexpr uint32_t k = kc, ao = ((k >> 2) * kBox + (k & 3) * 32) >> 4, bo = (k * 2048) >> 4;
+        umma_ss_k<ao, bo>(d, ad, bd, idesc, (acc | k) != 0);
     });
 }
 
@@ -455,13 +470,32 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     }
                 }
                 const int span = U.nq - U.i0;
+                // LSE and D of a query tile are loaded one tile ahead, into
+                // registers, so that their latency overlaps the waits for the
+                // ring instead of delaying the tile's q_full.
+                float nl[4], nd[4];
+                auto load_stats = [&](int t) {
+                    const int h = U.hk * g + t / span, i = U.i0 + t % span;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int q = i * kTileM + 4 * lane + e;
+                        nl[e] = 0.f;
+                        nd[e] = 0.f;
+                        if (q < U.len) {
+                            const size_t li = a.varlen ? (size_t)h * a.T + U.tok0 + q
+                                                       : ((size_t)U.seq * a.Hq + h) * a.N + q;
+                            nl[e] = a.lse[li] * 1.4426950408889634f;
+                            nd[e] = a.D[(size_t)h * a.T + U.tok0 + q];
+                        }
+                    }
+                };
+                load_stats(0);
                 for (int t = 0; t < U.n; ++t, ++jj) {
                     const int st = jj & 1, h = U.hk * g + t / span, i = U.i0 + t % span;
                     if (lane == 0) ok = mbar_wait(&sh.q_empty[st], ((jj >> 1) & 1) ^ 1, wc, kBSiteQEmpty);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
-                    // Q first (its latency overlaps the LSE/D loads); the
-                    // phase's one arrival follows the LSE/D stores.
+                    // Q first; the phase's one arrival follows the LSE/D stores.
                     if (lane == 0) {
                         mbar_expect_tx(&sh.q_full[st], kT32);
                         for (int c = 0; c < 2; ++c)
@@ -470,16 +504,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     }
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int row = 4 * lane + e, q = i * kTileM + row;
-                        float l2 = 0.f, dd = 0.f;
-                        if (q < U.len) {
-                            const size_t li = a.varlen ? (size_t)h * a.T + U.tok0 + q
-                                                       : ((size_t)U.seq * a.Hq + h) * a.N + q;
-                            l2 = a.lse[li] * 1.4426950408889634f;
-                            dd = a.D[(size_t)h * a.T + U.tok0 + q];
-                        }
-                        s_lse[st * 128 + row] = l2;
-                        s_D[st * 128 + row] = dd;
+                        s_lse[st * 128 + 4 * lane + e] = nl[e];
+                        s_D[st * 128 + 4 * lane + e] = nd[e];
                     }
                     __syncwarp();
                     if (lane == 0) {
@@ -491,6 +517,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                                 tma_load_3d(base + kOffDO + c * kBox, &tdo, &sh.do_full, c * 64, h, U.tok0 + i * kTileM);
                         }
                     }
+                    if (t + 1 < U.n) load_stats(t + 1);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
                 }
@@ -567,11 +594,13 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     umma_commit_w(&sh.r0_free);      // P^T read: the next S^T may overwrite R0
                     if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, kBSiteDs))) break;
                     tc_fence_after();
-                    mma_tn(tmem + kColDK, tmem + kColR1, base + kOffQ + st * kT32, t > 0);
-                    umma_commit_w(&sh.q_empty[st]);  // Q and LSE/D of this stage are consumed
-                    mma_nn(tmem + kColR1, sDS, sK);  // dQ overwrites dS^T after dK has read it
+                    // dQ first (over dP^T, which the dS step has read), so its
+                    // drain overlaps dK; both read dS from shared memory.
+                    mma_nn(tmem + kColR1, sDS, sK);
                     umma_commit_w(&sh.dq_full);
-                    umma_commit_w(&sh.ds_free);      // dS read by dK and dQ
+                    mma_ks(tmem + kColDK, sDS, base + kOffQ + st * kT32, t > 0);
+                    umma_commit_w(&sh.q_empty[st]);  // Q and LSE/D of this stage are consumed
+                    umma_commit_w(&sh.ds_free);      // dS read by dQ and dK
                     if (more) {
                         if (!(ok = mbar_wait_w(&sh.dq_free, jj & 1, wc, kBSiteDqFree))) break;
                         tc_fence_after();
@@ -661,7 +690,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 tc_fence_before();
                 mbar_arrive(&sh.p_ready);
 
-                // dS^T replaces dP^T in this half's own R1 columns.
+                // dS^T from this half's dP^T columns, into shared memory.
                 if (!(ok = mbar_wait(&sh.dp_full, jj & 1, wc, kBSiteDp))) break;
                 if (!(ok = mbar_wait(&sh.ds_free, (jj & 1) ^ 1, wc, kBSiteDsFree))) break;
                 tc_fence_after();
@@ -689,13 +718,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         *reinterpret_cast<uint4*>(ds_row + ((q ^ sw) << 4)) =
                             make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
                     }
-                    // dS^T also into TMEM (operand A of dK += dS^T Q, like P^T for
-                    // dV), over the dP^T columns this thread has just read.
-                    tmem_st16(tR1 + cb + cc * 16, pk);
                 }
-                tmem_wait_st();
-                fence_async_smem();
-                tc_fence_before();
+                fence_async_smem();   // dS is read by the dQ and dK products
+                tc_fence_before();    // dP^T read: dQ may overwrite it
                 mbar_arrive(&sh.ds_ready);
             }
         }
