@@ -140,6 +140,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         sh.sched.B = a.B; sh.sched.Hq = a.Hq; sh.sched.N = a.N; sh.sched.causal = a.causal;
         sh.sched.varlen = a.varlen; sh.sched.num_m = sh.maxm; sh.sched.maxm = sh.maxm;
         sh.sched.sec = a.l2_section; sh.sched.total = sh.total;
+            sh.sched.zz = a.causal && !a.varlen && sh.maxm % 2 == 0;
         sh.sched.s_cu = s_cu; sh.sched.s_order = s_order; sh.sched.s_pref = s_pref;
     }
     __syncthreads();
@@ -161,7 +162,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         if (lane == 0) {
             uint32_t it = 0, uc = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok; u += gridDim.x) {
+            for (int un = 0; ok; ++un) {
+                const int u = sched.nth((int)blockIdx.x, (int)gridDim.x, un);
                 Unit U;
                 if (!sched.get(u, U)) break;
                 const int hk = U.h / group;
@@ -205,7 +207,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         {   // the whole warp runs the issue loop (see umma_ss_w)
             uint32_t it = 0, uc = 0, pc[2] = {0, 0};
             bool ok = true;
-            for (int u = blockIdx.x; ok; u += gridDim.x) {
+            for (int un = 0; ok; ++un) {
+                const int u = sched.nth((int)blockIdx.x, (int)gridDim.x, un);
                 Unit U;
                 if (!sched.get(u, U)) break;
                 const int n0 = kv_tiles(U, 0, a.causal), n1 = kv_tiles(U, 1, a.causal);
@@ -278,7 +281,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         const float scale = a.scale_log2;
         uint32_t sc = 0, uc = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok; u += gridDim.x) {
+        for (int un = 0; ok; ++un) {
+            const int u = sched.nth((int)blockIdx.x, (int)gridDim.x, un);
             Unit U;
             if (!sched.get(u, U)) break;
             const int n = kv_tiles(U, x, a.causal);

@@ -180,6 +180,7 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             sh.sched.B = a.B; sh.sched.Hq = a.Hq; sh.sched.N = a.N; sh.sched.causal = a.causal;
             sh.sched.varlen = a.varlen; sh.sched.num_m = sh.maxm; sh.sched.maxm = sh.maxm;
             sh.sched.sec = a.l2_section; sh.sched.total = sh.total;
+            sh.sched.zz = a.causal && !a.varlen && sh.maxm % 2 == 0;
             sh.sched.s_cu = s_cu; sh.sched.s_order = s_order; sh.sched.s_pref = s_pref;
         }
     }
@@ -205,7 +206,8 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             if (lane == 0) {
                 uint32_t kit = 0, uc = 0;
                 bool ok = true;
-                for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
+                for (int n = 0; ok; ++n) {
+                    const int u = sched.nth(PAIR_ID, NUM_PAIRS, n);
                     Unit U;
                     if (!sched.get(u, U)) break;
                     const int hk = U.h / group, nb = pair_blocks(U, a.causal);
@@ -239,7 +241,8 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             if (lane == 0) {
                 uint32_t vit = 0;
                 bool ok = true;
-                for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
+                for (int n = 0; ok; ++n) {
+                    const int u = sched.nth(PAIR_ID, NUM_PAIRS, n);
                     Unit U;
                     if (!sched.get(u, U)) break;
                     const int hk = U.h / group, nb = pair_blocks(U, a.causal);
@@ -265,7 +268,8 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             // last block is still in softmax and P V.
             uint32_t kit = 0, uc = 0, gs = 0;
             bool ok = true;
-            for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
+            for (int n = 0; ok; ++n) {
+                const int u = sched.nth(PAIR_ID, NUM_PAIRS, n);
                 Unit U;
                 if (!sched.get(u, U)) break;
                 const int nb = pair_blocks(U, a.causal);
@@ -295,7 +299,8 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             // until earlier products drain).
             uint32_t vit = 0, uc = 0, gp = 0;
             bool ok = true;
-            for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
+            for (int n = 0; ok; ++n) {
+                const int u = sched.nth(PAIR_ID, NUM_PAIRS, n);
                 Unit U;
                 if (!sched.get(u, U)) break;
                 const int nb = pair_blocks(U, a.causal);
@@ -408,7 +413,8 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             mbar_arrive_remote_w(lead(&sh.o_free));
             return true;
         };
-        for (int u = PAIR_ID; ok; u += NUM_PAIRS) {
+        for (int n = 0; ok; ++n) {
+            const int u = sched.nth(PAIR_ID, NUM_PAIRS, n);
             Unit U;
             if (!sched.get(u, U)) break;
             const int nb = pair_blocks(U, a.causal);

@@ -21,12 +21,17 @@ struct Unit {
 //  fixed length, causal: longest-processing-time first inside L2-sized
 //    sections of (batch, head) pairs -- sections in order, query blocks in
 //    reverse (longest first), then the pairs of the section (FlashAttention-4
-//    blog, "Scheduling");
+//    blog, "Scheduling").  With an even block count the blocks go out in
+//    zig-zag couples instead: block m and block num_m - 1 - m of one (batch,
+//    head), one after the other to the same worker, so every couple costs
+//    num_m + 1 key blocks and a static stride over the couples leaves no
+//    worker with more than one couple of extra work;
 //  varlen: sequences sorted by block count (descending); causal walks query
 //    block levels from the top down over the sorted sequences (longest
 //    first), non-causal walks the sorted sequences head-major.
 struct Sched {
     int B, Hq, N, causal, varlen, num_m, sec, total, maxm;
+    int zz;   // fixed length, causal, even num_m: zig-zag couples
     const int* s_cu;
     const int* s_order;
     const int* s_pref;
@@ -35,14 +40,36 @@ struct Sched {
         return (s_cu[s + 1] - s_cu[s] + kUnitRows - 1) / kUnitRows;
     }
 
+    // Index of worker p's n-th unit (of P workers); at least total past the end.
+    __device__ __forceinline__ int nth(int p, int P, int n) const {
+        if (zz) return 2 * (p + (n >> 1) * P) + (n & 1);
+        return p + n * P;
+    }
+
     __device__ __forceinline__ bool get(int u, Unit& U) const {
-        if (u >= total) return false;
+        if (u < 0 || u >= total) return false;
         if (!varlen) {
             const int BH = B * Hq;
             int bh, m;
             if (!causal) {
                 bh = u / num_m;
                 m = u - bh * num_m;
+            } else if (zz) {
+                // couple c = u / 2 of the section order; its first unit is the
+                // longer block
+                const int c = u >> 1, hm = num_m >> 1, per_sec = sec * hm;
+                const int full = BH / sec;
+                int mm;
+                if (c < full * per_sec) {
+                    const int s = c / per_sec, r = c - s * per_sec;
+                    mm = r / sec;
+                    bh = s * sec + r % sec;
+                } else {
+                    const int rem = BH - full * sec, r = c - full * per_sec;
+                    mm = r / rem;
+                    bh = full * sec + r % rem;
+                }
+                m = (u & 1) ? mm : num_m - 1 - mm;
             } else {
                 const int per_sec = sec * num_m;
                 const int full = BH / sec;
