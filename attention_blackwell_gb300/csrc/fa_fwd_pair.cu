@@ -47,8 +47,11 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
 constexpr uint32_t kOffV = kOffK + kKS * kKHalf;
 constexpr uint32_t kOffRed = kOffV + kVS * kVHalf;  // row max / sum exchange [2][2][128] float
-constexpr uint32_t kOffTab = kOffRed + 2 * 2 * 128 * 4;   // varlen unit tables (fa_sched.cuh)
-constexpr uint32_t kOffBar = kOffTab + ((kTableInts * 4 + 15) & ~15u);
+// Varlen unit tables (fa_sched.cuh); a fixed-length call has none and uses
+// the region as the second O staging box.
+constexpr uint32_t kOffTab = kOffRed + 2 * 2 * 128 * 4;
+static_assert(kOffTab % 1024 == 0 && kTableInts * 4 <= 16384, "tables / second staging box");
+constexpr uint32_t kOffBar = kOffTab + 16384;
 constexpr uint32_t kOffStg = (kOffBar + 512 + 1023) & ~1023u;   // O staging: 128 rows x 64 bf16 (one TMA box)
 constexpr uint32_t kPSmem = kOffStg + 16384;
 static_assert(kPSmem <= 232448, "shared memory plan");
@@ -357,6 +360,9 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             float* rl = red + (ep & 1) * 256;
             rl[x * 128 + r] = lp;
             ++ep;
+            // The previous unit's O stores have read the staging boxes before
+            // anyone passes the barrier below and refills them.
+            if (x == 0 && r == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             if (pnamed_bar_or(2, 256, !okw)) return false;
             const float lt = rl[r] + rl[128 + r];
             const bool valid = qi < U.len;
@@ -376,10 +382,29 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                                                 pack_bf16x2(f[6] * inv_l, f[7] * inv_l));
                 }
             }
-            if ((m + 1) * kTileM <= U.len) {
-                // A full tile: each half in turn through the 128-B-swizzled
-                // staging box and one TMA store (scattered 16-byte row stores
-                // from every thread serialise in the load/store unit).
+            if ((m + 1) * kTileM <= U.len && !a.varlen) {
+                // A full tile, fixed length: the two halves into two 128-B-
+                // swizzled staging boxes at once (the second in the unused
+                // table region), then one thread sends both with TMA stores;
+                // their reads of the boxes are waited for by the next epilogue
+                // (scattered 16-byte row stores from every thread serialise in
+                // the load/store unit).
+                uint8_t* srow = dsm + (x ? kOffTab : kOffStg) + r * 128;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(srow + ((q ^ (r & 7)) << 4)) = ov[q];
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                asm volatile("bar.sync 2, 256;" ::: "memory");
+                if (x == 0 && r == 0) {
+                    asm volatile(
+                        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];\n\t"
+                        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%5, %2, %3}], [%6];\n\t"
+                        "cp.async.bulk.commit_group;"
+                        ::"l"(reinterpret_cast<uint64_t>(&to)), "r"(0), "r"(U.h), "r"(U.tok0 + m * kTileM),
+                          "r"(base + kOffStg), "r"(64), "r"(base + kOffTab) : "memory");
+                }
+            } else if ((m + 1) * kTileM <= U.len) {
+                // A full tile, varlen (the tables hold the second box's
+                // space): each half in turn through the one staging box.
                 uint8_t* srow = dsm + kOffStg + r * 128;
 #pragma unroll
                 for (int xr = 0; xr < 2; ++xr) {
