@@ -34,22 +34,36 @@ __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u &
 // ---------------------------------------------------------------- stage 1
 
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
+    // One warp per (token, head) row, four consecutive rows (1 KB of O and of
+    // dO) per step with all eight loads issued before any is used.
     const int lane = threadIdx.x & 31;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
     const long long rows = a.T * a.Hq;
-    for (long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < rows; w += nwarps) {
-        const long long tok = w / a.Hq;
-        const int h = (int)(w - tok * a.Hq);
-        const size_t off = ((size_t)tok * a.Hq + h) * kHeadDim;
-        const uint2 ov = reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.o) + off)[lane];
-        const uint2 dv = reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(a.dO) + off)[lane];
-        float s = bf16lo(ov.x) * bf16lo(dv.x) + bf16hi(ov.x) * bf16hi(dv.x) + bf16lo(ov.y) * bf16lo(dv.y) +
-                  bf16hi(ov.y) * bf16hi(dv.y);
+    const uint2* o2 = reinterpret_cast<const uint2*>(a.o);
+    const uint2* d2 = reinterpret_cast<const uint2*>(a.dO);
+    for (long long w0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 4; w0 < rows; w0 += nwarps * 4) {
+        uint2 ov[4], dv[4];
 #pragma unroll
-        for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
-        const size_t r = (size_t)h * a.T + tok;
-        if (lane == 0) a.D[r] = s;
-        reinterpret_cast<float4*>(a.dqacc + r * kHeadDim)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e = 0; e < 4; ++e) {
+            const long long w = w0 + e < rows ? w0 + e : rows - 1;
+            ov[e] = o2[w * (kHeadDim / 4) + lane];
+            dv[e] = d2[w * (kHeadDim / 4) + lane];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const long long w = w0 + e;
+            float s = bf16lo(ov[e].x) * bf16lo(dv[e].x) + bf16hi(ov[e].x) * bf16hi(dv[e].x) +
+                      bf16lo(ov[e].y) * bf16lo(dv[e].y) + bf16hi(ov[e].y) * bf16hi(dv[e].y);
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+            if (w < rows) {
+                const long long tok = w / a.Hq;
+                const int h = (int)(w - tok * a.Hq);
+                const size_t r = (size_t)h * a.T + tok;
+                if (lane == 0) a.D[r] = s;
+                reinterpret_cast<float4*>(a.dqacc + r * kHeadDim)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
     }
     if (a.deterministic) {
         const long long n = (long long)a.Hq * a.sem_stride;
@@ -154,14 +168,25 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
     const int lane = threadIdx.x & 31;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
     const long long rows = a.T * a.Hq;
-    for (long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < rows; w += nwarps) {
-        const long long tok = w / a.Hq;
-        const int h = (int)(w - tok * a.Hq);
-        const float4 g = reinterpret_cast<const float4*>(a.dqacc + ((size_t)h * a.T + tok) * kHeadDim)[lane];
-        uint2 o;
-        o.x = pack_bf16x2(g.x * a.alpha, g.y * a.alpha);
-        o.y = pack_bf16x2(g.z * a.alpha, g.w * a.alpha);
-        reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.dq) + ((size_t)tok * a.Hq + h) * kHeadDim)[lane] = o;
+    // Four rows per warp and step, all loads issued first.
+    for (long long w0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 4; w0 < rows; w0 += nwarps * 4) {
+        float4 g[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {   // rows of dQacc in its own (head, token) order
+            const long long w = w0 + e < rows ? w0 + e : rows - 1;
+            g[e] = reinterpret_cast<const float4*>(a.dqacc + (size_t)w * kHeadDim)[lane];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const long long w = w0 + e;
+            if (w < rows) {
+                const long long h = w / a.T, tok = w - h * a.T;
+                uint2 o;
+                o.x = pack_bf16x2(g[e].x * a.alpha, g[e].y * a.alpha);
+                o.y = pack_bf16x2(g[e].z * a.alpha, g[e].w * a.alpha);
+                reinterpret_cast<uint2*>(a.dq)[(tok * a.Hq + h) * (kHeadDim / 4) + lane] = o;
+            }
+        }
     }
 }
 
