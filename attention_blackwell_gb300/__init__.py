@@ -140,10 +140,10 @@ def set_fwd_kernel(kernel=2):
 def fwd(q, k, v, causal=False, alpha=None, cu_seqlens=None, max_seqlen=None, out=None, lse=None, stream=None):
     """Forward attention.  Returns (o, lse).
 
-    Fixed length: q [B,N,Hq,128], k/v [B,N,Hkv,128] bf16 -> o like q,
-    lse float32 [B,Hq,N].  Varlen: q [T,Hq,128], k/v [T,Hkv,128],
-    cu_seqlens int32 [B+1] on the device, max_seqlen -> o [T,Hq,128],
-    lse [Hq,T].
+    Fixed length: q [B,N,Hq,d], k/v [B,N,Hkv,d] bf16 -> o like q,
+    lse float32 [B,Hq,N].  Varlen: q [T,Hq,d], k/v [T,Hkv,d],
+    cu_seqlens int32 [B+1] on the device, max_seqlen -> o [T,Hq,d],
+    lse [Hq,T].  d = 128 or 64.
     """
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16)
@@ -189,9 +189,9 @@ def _shapes(q, k, cu_seqlens, max_seqlen):
     return B, N, Hq, k.shape[2], d, N
 
 
-def bwd_workspace(B, Hq, N, deterministic=False, varlen=False, device=None):
+def bwd_workspace(B, Hq, N, deterministic=False, varlen=False, device=None, d=HEAD_DIM):
     """A uint8 CUDA tensor large enough for fa_bwd (N = total tokens if varlen)."""
-    n = lib().fa_bwd_workspace_size(int(B), int(Hq), int(N), HEAD_DIM, int(bool(deterministic)), int(bool(varlen)))
+    n = lib().fa_bwd_workspace_size(int(B), int(Hq), int(N), int(d), int(bool(deterministic)), int(bool(varlen)))
     if n == 0:
         raise ValueError("invalid sizes for the backward workspace")
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
@@ -216,7 +216,7 @@ def bwd(q, k, v, o, lse, do, causal=False, alpha=None, cu_seqlens=None, max_seql
     if alpha is None:
         alpha = 1.0 / (d ** 0.5)
     if workspace is None:
-        workspace = bwd_workspace(B, Hq, N, deterministic, varlen, device=q.device)
+        workspace = bwd_workspace(B, Hq, N, deterministic, varlen, device=q.device, d=d)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv

@@ -69,13 +69,13 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// bf16 tensor [T, H, 128] -> 3-D map {128, H, T}, box {64, 1, box_rows}, 128-B swizzle.
+// bf16 tensor [T, H, d] -> 3-D map {d, H, T}, box {64, 1, box_rows}, 128-B swizzle.
 // Rows past T read as zero.
-int make_map(CUtensorMap* map, const void* ptr, int H, long long T, int box_rows = kTileM) {
+int make_map(CUtensorMap* map, const void* ptr, int H, long long T, int box_rows = kTileM, int d = kHeadDim) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return FA_ERR_LAUNCH;
-    cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)H, (cuuint64_t)T};
-    cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)H * kHeadDim * 2};
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
     cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -84,12 +84,12 @@ int make_map(CUtensorMap* map, const void* ptr, int H, long long T, int box_rows
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_INVALID;
 }
 
-// fp32 accumulator [rows, 128] -> 2-D map {128, rows}, box {32, 128}, 128-B swizzle.
-int make_map_acc(CUtensorMap* map, const void* ptr, long long rows, int box_rows = kTileM) {
+// fp32 accumulator [rows, d] -> 2-D map {d, rows}, box {32, 128}, 128-B swizzle.
+int make_map_acc(CUtensorMap* map, const void* ptr, long long rows, int box_rows = kTileM, int d = kHeadDim) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return FA_ERR_LAUNCH;
-    cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 4};
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d * 4};
     cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -146,7 +146,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     if (B < 1 || N < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return FA_ERR_INVALID;
     if (!(alpha > 0.0f) || !isfinite(alpha)) return FA_ERR_INVALID;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID;
-    if (d != kHeadDim) return FA_ERR_UNSUPPORTED;
+    if (d != 128 && d != 64) return FA_ERR_UNSUPPORTED;
     const bool varlen = cu_seqlens != nullptr;
     if (varlen) {
         if (max_seqlen < 1) return FA_ERR_INVALID;
@@ -164,15 +164,17 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     if (rc != FA_OK) return rc;
 
     // The 256-key kernels use the MUFU-only exp2 (the FMA-exp2 variants run on
-    // the ping-pong kernel); the single-CTA one serves fixed-length inputs only.
-    const bool wide = !varlen && g_emu_eighths == 0 && g_fwd_kernel == 1;
-    const bool pair = g_emu_eighths == 0 && g_fwd_kernel == 2;
+    // the ping-pong kernel); the single-CTA one serves fixed-length inputs
+    // only; d = 64 runs on the ping-pong kernel.
+    const bool wide = d == 128 && !varlen && g_emu_eighths == 0 && g_fwd_kernel == 1;
+    const bool pair = d == 128 && g_emu_eighths == 0 && g_fwd_kernel == 2;
     FwdLaunch L;
+    L.d = d;
     // K boxes: 256 rows (one block) for kernel 1, 128 (a block's half) for the
     // pair kernel; V boxes: 256 rows for both (the pair loads 64 columns of them).
-    if ((rc = make_map(&L.tq, q, Hq, T)) != FA_OK) return rc;
-    if ((rc = make_map(&L.tk, k, Hkv, T, wide ? 256 : kTileM)) != FA_OK) return rc;
-    if ((rc = make_map(&L.tv, v, Hkv, T, (wide || pair) ? 256 : kTileM)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tq, q, Hq, T, kTileM, d)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tk, k, Hkv, T, wide ? 256 : kTileM, d)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tv, v, Hkv, T, (wide || pair) ? 256 : kTileM, d)) != FA_OK) return rc;
     if (pair && (rc = make_map(&L.to, o, Hq, T)) != FA_OK) return rc;
     L.a.o = o;
     L.a.lse = lse;
@@ -186,10 +188,10 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     L.a.varlen = varlen ? 1 : 0;
     L.a.max_seqlen = varlen ? max_seqlen : N;
     // Causal fixed length: (batch, head) pairs per L2 section so that the K/V
-    // of one section (2 * N * 128 * 2 bytes per key/value head) fill about
+    // of one section (2 * N * d * 2 bytes per key/value head) fill about
     // half of L2; pairs of one group share their K/V head.
     {
-        const long long kv_bytes = 512LL * (N > 0 ? N : 1);
+        const long long kv_bytes = 4LL * d * (N > 0 ? N : 1);
         long long sec = (long long)(Hq / Hkv) * ((long long)dev->l2_bytes / 2) / kv_bytes;
         if (sec < 1) sec = 1;
         if (sec > (long long)B * Hq) sec = (long long)B * Hq;
@@ -241,9 +243,9 @@ int fa_get_device_status(const void* workspace, cudaStream_t stream) {
 }
 
 size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, int deterministic, int varlen) {
-    if (B < 1 || Hq < 1 || N < 0 || d != kHeadDim) return 0;
+    if (B < 1 || Hq < 1 || N < 0 || (d != 128 && d != 64)) return 0;
     const long long T = varlen ? (long long)N : (long long)B * N;
-    return ws_layout(T, B, Hq, deterministic ? 1 : 0, varlen ? 1 : 0).total;
+    return ws_layout(T, B, Hq, deterministic ? 1 : 0, varlen ? 1 : 0, d).total;
 }
 
 int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -255,7 +257,7 @@ int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const
     if (B < 1 || N < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return FA_ERR_INVALID;
     if (!(alpha > 0.0f) || !isfinite(alpha)) return FA_ERR_INVALID;
     if ((causal != 0 && causal != 1) || (deterministic != 0 && deterministic != 1)) return FA_ERR_INVALID;
-    if (d != kHeadDim) return FA_ERR_UNSUPPORTED;
+    if (d != 128 && d != 64) return FA_ERR_UNSUPPORTED;
     const bool varlen = cu_seqlens != nullptr;
     if (varlen) {
         if (max_seqlen < 1) return FA_ERR_INVALID;
@@ -268,7 +270,7 @@ int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const
     const long long T = varlen ? (long long)N : (long long)B * N;
     if (T == 0) return FA_OK;
     if (T > 0x7fffffffLL || (long long)Hq * T > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-    const WsLayout w = ws_layout(T, B, Hq, deterministic, varlen ? 1 : 0);
+    const WsLayout w = ws_layout(T, B, Hq, deterministic, varlen ? 1 : 0, d);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
         return FA_ERR_WORKSPACE;
 
@@ -276,12 +278,13 @@ int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const
     int rc = current_device_info(&dev);
     if (rc != FA_OK) return rc;
     BwdLaunch L;
-    if ((rc = make_map(&L.tq, q, Hq, T)) != FA_OK) return rc;
-    if ((rc = make_map(&L.tk, k, Hkv, T)) != FA_OK) return rc;
-    if ((rc = make_map(&L.tv, v, Hkv, T)) != FA_OK) return rc;
-    if ((rc = make_map(&L.tdo, dout, Hq, T)) != FA_OK) return rc;
+    L.d = d;
+    if ((rc = make_map(&L.tq, q, Hq, T, kTileM, d)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tk, k, Hkv, T, kTileM, d)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tv, v, Hkv, T, kTileM, d)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tdo, dout, Hq, T, kTileM, d)) != FA_OK) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    if ((rc = make_map_acc(&L.tdq, ws + w.dq_off, (long long)Hq * T)) != FA_OK) return rc;
+    if ((rc = make_map_acc(&L.tdq, ws + w.dq_off, (long long)Hq * T, kTileM, d)) != FA_OK) return rc;
     BwdArgs& a = L.a;
     a.o = o;
     a.dO = dout;
@@ -308,7 +311,7 @@ int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const
     a.alpha = alpha;
     a.scale_log2 = alpha * 1.4426950408889634f;
     L.num_sms = dev->num_sms;
-    L.pair = g_bwd_kernel == 1 && bwd_pair_supported(a) ? 1 : 0;
+    L.pair = d == 128 && g_bwd_kernel == 1 && bwd_pair_supported(a) ? 1 : 0;
     if (L.pair) {
         if ((rc = make_map(&L.tq64, q, Hq, T, 64)) != FA_OK) return rc;
         if ((rc = make_map(&L.tdo64, dout, Hq, T, 64)) != FA_OK) return rc;

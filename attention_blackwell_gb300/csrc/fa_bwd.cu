@@ -1,6 +1,6 @@
 // fa_bwd.cu -- backward attention for sm_103a (tcgen05 / TMEM / TMA).
 //
-// Gradients of O = softmax(alpha Q K^T [+ causal]) V for d = 128
+// Gradients of O = softmax(alpha Q K^T [+ causal]) V for d = 128 or 64
 // (FlashAttention-4 blog, "Backward pass" section): with upstream dO,
 //   D_i = sum_d dO_id O_id,  P = exp(alpha Q K^T - LSE),
 //   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),
@@ -33,27 +33,47 @@ __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u &
 
 // ---------------------------------------------------------------- stage 1
 
+// Per lane of a warp on one row of D elements: D / 32 consecutive elements.
+template <int D> struct LaneVec;
+template <> struct LaneVec<128> { using bf = uint2; using f = float4; };
+template <> struct LaneVec<64> { using bf = uint32_t; using f = float2; };
+
+__device__ __forceinline__ float dot_bf16(uint2 a, uint2 b) {
+    return bf16lo(a.x) * bf16lo(b.x) + bf16hi(a.x) * bf16hi(b.x) + bf16lo(a.y) * bf16lo(b.y) + bf16hi(a.y) * bf16hi(b.y);
+}
+__device__ __forceinline__ float dot_bf16(uint32_t a, uint32_t b) {
+    return bf16lo(a) * bf16lo(b) + bf16hi(a) * bf16hi(b);
+}
+__device__ __forceinline__ void zero_vec(float4& v) { v = make_float4(0.f, 0.f, 0.f, 0.f); }
+__device__ __forceinline__ void zero_vec(float2& v) { v = make_float2(0.f, 0.f); }
+__device__ __forceinline__ uint2 pack_scaled(float4 g, float s) {
+    return make_uint2(pack_bf16x2(g.x * s, g.y * s), pack_bf16x2(g.z * s, g.w * s));
+}
+__device__ __forceinline__ uint32_t pack_scaled(float2 g, float s) { return pack_bf16x2(g.x * s, g.y * s); }
+
+template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
-    // One warp per (token, head) row, four consecutive rows (1 KB of O and of
-    // dO) per step with all eight loads issued before any is used.
+    // One warp per (token, head) row, four consecutive rows (4 D bf16 of O and
+    // of dO) per step with all eight loads issued before any is used.
+    using BV = typename LaneVec<D>::bf;
+    using FV = typename LaneVec<D>::f;
     const int lane = threadIdx.x & 31;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
     const long long rows = a.T * a.Hq;
-    const uint2* o2 = reinterpret_cast<const uint2*>(a.o);
-    const uint2* d2 = reinterpret_cast<const uint2*>(a.dO);
+    const BV* o2 = reinterpret_cast<const BV*>(a.o);
+    const BV* d2 = reinterpret_cast<const BV*>(a.dO);
     for (long long w0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 4; w0 < rows; w0 += nwarps * 4) {
-        uint2 ov[4], dv[4];
+        BV ov[4], dv[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const long long w = w0 + e < rows ? w0 + e : rows - 1;
-            ov[e] = o2[w * (kHeadDim / 4) + lane];
-            dv[e] = d2[w * (kHeadDim / 4) + lane];
+            ov[e] = o2[w * 32 + lane];
+            dv[e] = d2[w * 32 + lane];
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const long long w = w0 + e;
-            float s = bf16lo(ov[e].x) * bf16lo(dv[e].x) + bf16hi(ov[e].x) * bf16hi(dv[e].x) +
-                      bf16lo(ov[e].y) * bf16lo(dv[e].y) + bf16hi(ov[e].y) * bf16hi(dv[e].y);
+            float s = dot_bf16(ov[e], dv[e]);
 #pragma unroll
             for (int m = 16; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
             if (w < rows) {
@@ -61,7 +81,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
                 const int h = (int)(w - tok * a.Hq);
                 const size_t r = (size_t)h * a.T + tok;
                 if (lane == 0) a.D[r] = s;
-                reinterpret_cast<float4*>(a.dqacc + r * kHeadDim)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+                FV z;
+                zero_vec(z);
+                reinterpret_cast<FV*>(a.dqacc + r * D)[lane] = z;
             }
         }
     }
@@ -164,27 +186,27 @@ __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a) {
 
 // ---------------------------------------------------------------- stage 3
 
+template <int D>
 __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
+    using BV = typename LaneVec<D>::bf;
+    using FV = typename LaneVec<D>::f;
     const int lane = threadIdx.x & 31;
     const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
     const long long rows = a.T * a.Hq;
     // Four rows per warp and step, all loads issued first.
     for (long long w0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 4; w0 < rows; w0 += nwarps * 4) {
-        float4 g[4];
+        FV g[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {   // rows of dQacc in its own (head, token) order
             const long long w = w0 + e < rows ? w0 + e : rows - 1;
-            g[e] = reinterpret_cast<const float4*>(a.dqacc + (size_t)w * kHeadDim)[lane];
+            g[e] = reinterpret_cast<const FV*>(a.dqacc + (size_t)w * D)[lane];
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const long long w = w0 + e;
             if (w < rows) {
                 const long long h = w / a.T, tok = w - h * a.T;
-                uint2 o;
-                o.x = pack_bf16x2(g[e].x * a.alpha, g[e].y * a.alpha);
-                o.y = pack_bf16x2(g[e].z * a.alpha, g[e].w * a.alpha);
-                reinterpret_cast<uint2*>(a.dq)[(tok * a.Hq + h) * (kHeadDim / 4) + lane] = o;
+                reinterpret_cast<BV*>(a.dq)[(tok * a.Hq + h) * 32 + lane] = pack_scaled(g[e], a.alpha);
             }
         }
     }
@@ -206,10 +228,10 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 //               LSE_i, D_i (plain loads) into a two-stage ring;
 //   warp  9     issues dV, dQ, dK, dP;  warp 10 issues S;  warp 11 idle.
 //
-// Tensor memory (512 columns): dK acc 0-127, dV acc 128-255,
+// Tensor memory (512 columns): dK acc 0-127, dV acc 128-255 (d columns used),
 //   R0 256-383: S^T, then P^T (bf16; each key-row half packs its 64 queries
 //               into the first 32 of the 64 columns it read);
-//   R1 384-511: dP^T, then dQ_i once the dS step has read dP^T (the
+//   R1 384-511: dP^T, then dQ_i (d columns) once the dS step has read dP^T (the
 //               paper's 1-CTA sharing of dP/dS/dQ columns; dS itself stays in
 //               shared memory).
 // Warp 10 issues each S^T as soon as its Q tile is loaded and dV has read
@@ -219,17 +241,24 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 // next dP in that order: dQ before dK, so that the hand-off of dQ out of R1
 // (which the next dP waits for) overlaps the dK product.
 //
-// Shared memory (dynamic, 1024-aligned, 232448 bytes):
-//   K 32K | V 32K | Q[2] 2x32K | dO 32K | dS 32K | dQ staging 32K | lse2[2][128], D[2][128] | barriers
+// Shared memory (dynamic, 1024-aligned; 232448 bytes at d = 128), a tile
+// being 128 rows x d bf16 (32K at d = 128, 16K at d = 64):
+//   K | V | Q[2] | dO | dS 32K | dQ staging 32K | lse2[2][128], D[2][128] | barriers
 // dO is single-buffered: it is free once dV has read it and is next needed
 // by dP of the next tile, after S, dQ, dK and the dQ hand-off.
 constexpr int kBwdThreads = 512;
-constexpr uint32_t kT32 = 32768, kBox = 16384;
-constexpr uint32_t kOffK = 0, kOffV = kT32, kOffQ = 2 * kT32, kOffDO = 4 * kT32, kOffDS = 5 * kT32;
-constexpr uint32_t kOffStage = 6 * kT32;                // dQ staging for the TMA reductions
-constexpr uint32_t kOffStat = 7 * kT32;                 // lse2[2][128], D[2][128] floats
-constexpr uint32_t kOffBar = kOffStat + 4 * 128 * 4;
-constexpr uint32_t kBwdSmem = kOffBar + 1024;           // 232448
+constexpr uint32_t kBox = 16384;                        // one TMA box: 128 rows x 128 bytes
+template <int D> struct BGeo {
+    static_assert(D == 64 || D == 128, "head dim");
+    static constexpr int kBoxes = D / 64;               // boxes per Q, K, V or dO tile
+    static constexpr uint32_t kTile = 256u * D;         // 128 rows x D bf16
+    static constexpr uint32_t kOffK = 0, kOffV = kTile, kOffQ = 2 * kTile, kOffDO = 4 * kTile, kOffDS = 5 * kTile;
+    static constexpr uint32_t kOffStage = kOffDS + 32768;   // dQ staging for the TMA reductions
+    static constexpr uint32_t kOffStat = kOffStage + 32768; // lse2[2][128], D[2][128] floats
+    static constexpr uint32_t kOffBar = kOffStat + 4 * 128 * 4;
+    static constexpr uint32_t kSmem = kOffBar + 1024;
+};
+static_assert(BGeo<128>::kSmem == 232448, "shared memory plan");
 
 struct BwdShared {
     uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full, do_empty;
@@ -300,12 +329,13 @@ __device__ __forceinline__ bool bwd_unit(const BwdArgs& a, int total, int u, BUn
     return true;
 }
 
-// A 128x128x128 product with both operands K-major in shared memory
-// (S^T = K Q^T and dP^T = V dO^T).
+// A 128x128 product over the head dim (D / 16 steps) with both operands
+// K-major in shared memory (S^T = K Q^T and dP^T = V dO^T).
+template <int D>
 __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a_smem, uint32_t b_smem) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
     const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, 16, 1024);
-    static_for<8>([&](auto kc) {
+    static_for<D / 16>([&](auto kc) {
         constexpr uint32_t k = kc, off = ((k >> 2) * kBox + (k & 3) * 32) >> 4;
         umma_ss_k<off, off>(d, ad, bd, idesc, k > 0);
     });
@@ -314,9 +344,10 @@ __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a_smem, uint32_t b_s
 // D (+)= A[tmem] B, B MN-major in shared memory (dV += P^T dO).
 // A is bf16 in the region the two key-row halves wrote: queries 0-63 in
 // columns 0-31 of the region, queries 64-127 in columns 64-95 (each half
-// packs its 64 queries at the start of the 64 columns it read).
+// packs its 64 queries at the start of the 64 columns it read).  N = D.
+template <int D>
 __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b_smem, uint32_t acc) {
-    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+    constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
     const uint64_t bd = sdesc_sw128(b_smem, kBox, 1024);
     static_for<8>([&](auto kc) {
         constexpr uint32_t k = kc, col = k * 8 + (k >= 4 ? 32 : 0);
@@ -326,9 +357,10 @@ __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b_s
 
 // D (+)= A B with A K-major and B MN-major in shared memory (dK += dS^T Q:
 // dS^T is stored key-major with the queries contiguous, as the K-major A of
-// this product; Q as loaded, d contiguous, is its MN-major B).
+// this product; Q as loaded, d contiguous, is its MN-major B).  N = D.
+template <int D>
 __device__ __forceinline__ void mma_ks(uint32_t d, uint32_t a_smem, uint32_t b_smem, uint32_t acc) {
-    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+    constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
     const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, kBox, 1024);
     static_for<8>([&](auto kc) {
         constexpr uint32_t k = kc, ao = ((k >> 2) * kBox + (k & 3) * 32) >> 4, bo = (k * 2048) >> 4;
@@ -337,9 +369,10 @@ __device__ __forceinline__ void mma_ks(uint32_t d, uint32_t a_smem, uint32_t b_s
 }
 
 // D = A B with A and B both MN-major in shared memory (dQ = dS K: dS^T is
-// stored key-major, i.e. queries contiguous = M contiguous).
+// stored key-major, i.e. queries contiguous = M contiguous).  N = D.
+template <int D>
 __device__ __forceinline__ void mma_nn(uint32_t d, uint32_t a_smem, uint32_t b_smem) {
-    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 1, 1);
+    constexpr uint32_t idesc = idesc_bf16_f32(128, D, 1, 1);
     const uint64_t ad = sdesc_sw128(a_smem, kBox, 1024), bd = sdesc_sw128(b_smem, kBox, 1024);
     static_for<8>([&](auto kc) {
         constexpr uint32_t k = kc, off = (k * 2048) >> 4;
@@ -389,11 +422,15 @@ __device__ __forceinline__ void red_release_add(int* p, int v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
            const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
            const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
     extern __shared__ __align__(1024) uint8_t dsm[];
+    using G = BGeo<D>;
+    constexpr uint32_t kOffK = G::kOffK, kOffV = G::kOffV, kOffQ = G::kOffQ, kOffDO = G::kOffDO, kOffDS = G::kOffDS,
+                       kOffStage = G::kOffStage, kOffStat = G::kOffStat, kOffBar = G::kOffBar, kT32 = G::kTile;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t base = smem_u32(dsm);
     if (base & 1023u) {  // the swizzled tiles need a 1024-byte aligned window
@@ -489,7 +526,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 if (!ok) break;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&sh.kv_full, 2 * kT32);
-                    for (int c = 0; c < 2; ++c) {
+                    for (int c = 0; c < G::kBoxes; ++c) {
                         tma_load_3d(sK + c * kBox, &tk, &sh.kv_full, c * 64, U.hk, U.tok0 + U.k * kTileN);
                         tma_load_3d(sV + c * kBox, &tv, &sh.kv_full, c * 64, U.hk, U.tok0 + U.k * kTileN);
                     }
@@ -523,7 +560,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     // Q first; the phase's one arrival follows the LSE/D stores.
                     if (lane == 0) {
                         mbar_expect_tx(&sh.q_full[st], kT32);
-                        for (int c = 0; c < 2; ++c)
+                        for (int c = 0; c < G::kBoxes; ++c)
                             tma_load_3d(base + kOffQ + st * kT32 + c * kBox, &tq, &sh.q_full[st], c * 64, h,
                                         U.tok0 + i * kTileM);
                     }
@@ -538,7 +575,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         ok = mbar_wait(&sh.do_empty, (jj & 1) ^ 1, wc, kBSiteQEmpty);
                         if (ok) {
                             mbar_arrive_expect_tx(&sh.do_full, kT32);
-                            for (int c = 0; c < 2; ++c)
+                            for (int c = 0; c < G::kBoxes; ++c)
                                 tma_load_3d(base + kOffDO + c * kBox, &tdo, &sh.do_full, c * 64, h, U.tok0 + i * kTileM);
                         }
                     }
@@ -580,7 +617,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     if (!(ok = mbar_wait_w(&sh.q_full[jj & 1], (jj >> 1) & 1, wc, kBSiteQFull))) break;
                     if (jj > 0 && !(ok = mbar_wait_w(&sh.r0_free, (jj - 1) & 1, wc, kBSiteP))) break;
                     tc_fence_after();
-                    mma_kk(tmem + kColR0, sK, base + kOffQ + (jj & 1) * kT32);
+                    mma_kk<D>(tmem + kColR0, sK, base + kOffQ + (jj & 1) * kT32);
                     umma_commit_w(&sh.s_full);
                 }
                 ++uc;
@@ -607,30 +644,30 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     tc_fence_after();
                 }
                 if (!(ok = mbar_wait_w(&sh.do_full, jj & 1, wc, kBSiteQFull))) break;
-                mma_kk(tmem + kColR1, sV, base + kOffDO);
+                mma_kk<D>(tmem + kColR1, sV, base + kOffDO);
                 umma_commit_w(&sh.dp_full);
                 for (int t = 0; t < U.n; ++t, ++jj) {
                     const uint32_t st = jj & 1;
                     const bool more = t + 1 < U.n;
                     if (!(ok = mbar_wait_w(&sh.p_ready, jj & 1, wc, kBSiteP))) break;
                     tc_fence_after();
-                    mma_tn(tmem + kColDV, tmem + kColR0, base + kOffDO, t > 0);
+                    mma_tn<D>(tmem + kColDV, tmem + kColR0, base + kOffDO, t > 0);
                     umma_commit_w(&sh.do_empty);     // dO read by dP and dV: the next may load
                     umma_commit_w(&sh.r0_free);      // P^T read: the next S^T may overwrite R0
                     if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, kBSiteDs))) break;
                     tc_fence_after();
                     // dQ first (over dP^T, which the dS step has read), so its
                     // drain overlaps dK; both read dS from shared memory.
-                    mma_nn(tmem + kColR1, sDS, sK);
+                    mma_nn<D>(tmem + kColR1, sDS, sK);
                     umma_commit_w(&sh.dq_full);
-                    mma_ks(tmem + kColDK, sDS, base + kOffQ + st * kT32, t > 0);
+                    mma_ks<D>(tmem + kColDK, sDS, base + kOffQ + st * kT32, t > 0);
                     umma_commit_w(&sh.q_empty[st]);  // Q and LSE/D of this stage are consumed
                     umma_commit_w(&sh.ds_free);      // dS read by dQ and dK
                     if (more) {
                         if (!(ok = mbar_wait_w(&sh.dq_free, jj & 1, wc, kBSiteDqFree))) break;
                         tc_fence_after();
                         if (!(ok = mbar_wait_w(&sh.do_full, (jj + 1) & 1, wc, kBSiteQFull))) break;
-                        mma_kk(tmem + kColR1, sV, base + kOffDO);
+                        mma_kk<D>(tmem + kColR1, sV, base + kOffDO);
                         umma_commit_w(&sh.dp_full);
                     }
                 }
@@ -790,11 +827,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 tc_fence_after();
                 // dQ_i out of TMEM into registers; the columns are free for the
                 // next dP at once.
-                uint32_t v[128];
-                tmem_ld32(tR1 + 0, *reinterpret_cast<uint32_t(*)[32]>(v + 0));
-                tmem_ld32(tR1 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-                tmem_ld32(tR1 + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
-                tmem_ld32(tR1 + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+                uint32_t v[D];
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32)
+                    tmem_ld32(tR1 + c0, *reinterpret_cast<uint32_t(*)[32]>(v + c0));
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(&sh.dq_free);
@@ -826,7 +862,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 }
                 // Add dQ_i into the fp32 accumulator with TMA bulk tensor
                 // reductions of whole 128-byte lines, staged in shared memory
-                // in four rounds of one 32-column box (128 rows x 128 B,
+                // in D / 32 rounds of one 32-column box (128 rows x 128 B,
                 // swizzled like a 128-B TMA box) alternating between two
                 // buffers, so each round's reduction reads one buffer while
                 // the threads fill the other.  Rows past the sequence end hold
@@ -835,7 +871,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 const int grow = h * (int)a.T + U.tok0 + i * kTileM;
                 uint8_t* stage_row = dsm + kOffStage + r * 128;
 #pragma unroll
-                for (int rnd = 0; rnd < 4; ++rnd) {
+                for (int rnd = 0; rnd < D / 32; ++rnd) {
                     const int b = rnd & 1;
                     // At most the latest group may still be reading: the one
                     // before it used this buffer.
@@ -863,14 +899,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             tc_fence_after();
             const int key = U.k * kTileN + r;
             const bool kvalid = key < U.len;
-            const size_t orow = ((size_t)(U.tok0 + key) * a.Hkv + U.hk) * kHeadDim;
+            const size_t orow = ((size_t)(U.tok0 + key) * a.Hkv + U.hk) * D;
 #pragma unroll
             for (int which = 0; which < 2; ++which) {
                 const uint32_t tacc = tmem + lb + (which ? kColDV : kColDK);
                 const float mul = which ? 1.f : a.alpha;
                 uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which ? a.dv : a.dk) + orow);
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t v[32];
                     tmem_ld32(tacc + cc * 32, v);
                     tmem_wait_ld();
@@ -906,12 +942,13 @@ __global__ void bwd_reset_status_kernel(BwdHeader* hdr) {
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdLaunch& L, int stages, cudaStream_t stream) {
+template <int D>
+cudaError_t launch_bwd_d(const BwdLaunch& L, int stages, cudaStream_t stream) {
     const BwdArgs& a = L.a;
     const int ew_grid = L.num_sms * 8;
     if (stages & 1) {
         bwd_reset_status_kernel<<<1, 1, 0, stream>>>(a.hdr);
-        bwd_pre_kernel<<<ew_grid, 256, 0, stream>>>(a);
+        bwd_pre_kernel<D><<<ew_grid, 256, 0, stream>>>(a);
         if (a.varlen) bwd_plan_kernel<<<1, 1024, 0, stream>>>(a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -920,22 +957,29 @@ cudaError_t launch_bwd(const BwdLaunch& L, int stages, cudaStream_t stream) {
         cudaError_t e = launch_bwd_pair_main(L, stream);
         if (e != cudaSuccess) return e;
     } else if (stages & 2) {
-        cudaError_t e0 = cudaFuncSetAttribute(bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBwdSmem);
+        constexpr uint32_t smem = BGeo<D>::kSmem;
+        cudaError_t e0 = cudaFuncSetAttribute(bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e0 != cudaSuccess) return e0;
         long long units = a.varlen ? (long long)a.Hkv * ((a.T + kTileN - 1) / kTileN + a.B)
                                    : (long long)a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN);
         int grid = (int)(units < L.num_sms ? units : L.num_sms);
         if (grid < 1) grid = 1;
-        bwd_kernel<<<grid, kBwdThreads, kBwdSmem, stream>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, a);
+        bwd_kernel<D><<<grid, kBwdThreads, smem, stream>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (stages & 4) {
-        bwd_post_kernel<<<ew_grid, 256, 0, stream>>>(a);
+        bwd_post_kernel<D><<<ew_grid, 256, 0, stream>>>(a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_bwd(const BwdLaunch& L, int stages, cudaStream_t stream) {
+    if (L.d == 64) return launch_bwd_d<64>(L, stages, stream);
+    if (L.d == 128) return launch_bwd_d<128>(L, stages, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace fa

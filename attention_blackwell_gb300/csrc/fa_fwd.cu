@@ -1,7 +1,7 @@
 // fa_fwd.cu -- forward attention kernel for sm_103a (tcgen05 / TMEM / TMA).
 //
-// Computes O = softmax(alpha Q K^T [+ causal]) V and LSE for d = 128 with an
-// online softmax (FlashAttention-4 blog, "Forward pass: a new softmax pipeline
+// Computes O = softmax(alpha Q K^T [+ causal]) V and LSE for d = 128 or 64
+// (a template parameter D) with an online softmax (FlashAttention-4 blog, "Forward pass: a new softmax pipeline
 // with conditional rescaling"; FlashAttention-4 paper summary §3.1.2-§3.1.4).
 //
 // One persistent CTA per SM walks a list of work units.  A unit is two query
@@ -17,7 +17,7 @@
 //
 // Tensor memory (512 columns x 128 lanes, fp32 cells), per the paper
 // summary's "2 x O + 2 x S, P overlapping S" layout:
-//   cols   0-127  O of tile 0      cols 128-255  O of tile 1
+//   cols   0-127  O of tile 0      cols 128-255  O of tile 1 (D columns used)
 //   cols 256-383  S/P of tile 0    cols 384-511  S/P of tile 1
 // P (bf16, two per 32-bit cell) overwrites the first 64 columns of its S.
 //
@@ -36,12 +36,17 @@
 namespace fa {
 namespace {
 
-constexpr int kStages = 4;                     // K/V ring depth (32 KB slots)
+constexpr int kStages = 4;                     // K/V ring depth (one tile per slot)
 constexpr int kThreads = 384;
-constexpr uint32_t kTileBytes = 32768;         // 128 x 128 bf16
 constexpr uint32_t kBoxBytes = 16384;          // 128 rows x 64 bf16 (one TMA box)
-constexpr uint32_t kSmemTiles = 2 * kTileBytes + kStages * kTileBytes;
-constexpr uint32_t kSmemBytes = 1024 + kSmemTiles + kTableInts * 4;
+// Per head dim D: a 128-row tile of Q, K or V is D / 64 boxes.
+template <int D> struct Geo {
+    static_assert(D == 64 || D == 128, "head dim");
+    static constexpr int kBoxes = D / 64;
+    static constexpr uint32_t kTileBytes = 128u * D * 2u;
+    static constexpr uint32_t kSmemTiles = 2 * kTileBytes + kStages * kTileBytes;
+    static constexpr uint32_t kSmemBytes = 1024 + kSmemTiles + kTableInts * 4;
+};
 
 // TMEM column bases of O and S/P for tile x.
 __device__ __forceinline__ uint32_t col_o(int x) { return (uint32_t)x * 128u; }
@@ -70,21 +75,24 @@ struct FwdShared {
     Sched sched;
 };
 
-// S = Q K^T for one 128x128 tile: 8 UMMAs of K = 16 over d = 128.  Both
-// operands K-major; k-step k reads 32 bytes at column (k % 4) * 16 of box k / 4.
+// S = Q K^T for one 128x128 tile: D / 16 UMMAs of K = 16 over the head dim.
+// Both operands K-major; k-step k reads 32 bytes at column (k % 4) * 16 of box k / 4.
+template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
     const uint64_t qd = sdesc_sw128(q_smem, 16, 1024), kd = sdesc_sw128(k_smem, 16, 1024);
-    static_for<8>([&](auto kc) {
+    static_for<D / 16>([&](auto kc) {
         constexpr uint32_t k = kc, off = ((k >> 2) * kBoxBytes + (k & 3) * 32) >> 4;  // 16-byte units
         umma_ss_k<off, off>(d_tmem, qd, kd, idesc, k > 0);
     });
 }
 
 // O (+)= P V: A = P (bf16 in TMEM, 8 columns per k-step of 16 keys),
-// B = V MN-major (k-step k = 16 key rows = 2048 bytes further).
+// B = V MN-major (k-step k = 16 key rows = 2048 bytes further; N = D, the
+// 64-column boxes kBoxBytes apart).
+template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, uint32_t acc) {
-    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+    constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
     const uint64_t vd = sdesc_sw128(v_smem, kBoxBytes, 1024);
     static_for<8>([&](auto kc) {
         constexpr uint32_t k = kc;
@@ -92,19 +100,21 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
     });
 }
 
-template <int kEmuEighths>
+template <int kEmuEighths, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
            const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
     extern __shared__ uint8_t dsmem[];
     __shared__ FwdShared sh;
 
+    using G = Geo<D>;
+    constexpr uint32_t kTileBytes = G::kTileBytes;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
     uint8_t* gbase = dsmem + (base - smem_u32(dsmem));
     const uint32_t sQ = base;                        // 2 tiles
     const uint32_t sRing = base + 2 * kTileBytes;    // kStages tiles
-    int* s_cu = reinterpret_cast<int*>(gbase + kSmemTiles);
+    int* s_cu = reinterpret_cast<int*>(gbase + G::kSmemTiles);
     int* s_order = s_cu + (kMaxVarlenSeqs + 1);
     int* s_pref = s_order + kMaxVarlenSeqs;
 
@@ -140,7 +150,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         sh.sched.B = a.B; sh.sched.Hq = a.Hq; sh.sched.N = a.N; sh.sched.causal = a.causal;
         sh.sched.varlen = a.varlen; sh.sched.num_m = sh.maxm; sh.sched.maxm = sh.maxm;
         sh.sched.sec = a.l2_section; sh.sched.total = sh.total;
-            sh.sched.zz = a.causal && !a.varlen && sh.maxm % 2 == 0;
+        sh.sched.zz = a.causal && !a.varlen && sh.maxm % 2 == 0;
         sh.sched.s_cu = s_cu; sh.sched.s_order = s_order; sh.sched.s_pref = s_pref;
     }
     __syncthreads();
@@ -170,7 +180,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 if (!(ok = mbar_wait(&sh.q_empty, (uc & 1) ^ 1, wc, kSiteQEmpty))) break;
                 mbar_arrive_expect_tx(&sh.q_full, 2 * kTileBytes);
                 for (int x = 0; x < 2; ++x)
-                    for (int c = 0; c < 2; ++c)
+                    for (int c = 0; c < G::kBoxes; ++c)
                         tma_load_3d(sQ + x * kTileBytes + c * kBoxBytes, &tq, &sh.q_full, c * 64, U.h,
                                     U.tok0 + U.m * kUnitRows + x * kTileM);
                 const int n = kv_tiles(U, 1, a.causal);
@@ -180,7 +190,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         if (!(ok = mbar_wait(&sh.empty[slot], ((it / kStages) & 1) ^ 1, wc, kSiteRingEmpty))) break;
                         mbar_arrive_expect_tx(&sh.full[slot], kTileBytes);
                         const CUtensorMap* map = kv ? &tv : &tk;
-                        for (int c = 0; c < 2; ++c)
+                        for (int c = 0; c < G::kBoxes; ++c)
                             tma_load_3d(sRing + slot * kTileBytes + c * kBoxBytes, map, &sh.full[slot], c * 64,
                                         hk, U.tok0 + j * kTileN);
                         ++it;
@@ -221,9 +231,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 if (!(ok = mbar_wait_w(&sh.full[slot_k], (it / kStages) & 1, wc, kSiteRingFull))) break;
                 ++it;
                 tc_fence_after();  // S of the previous unit's epilogue (O) is in order
-                issue_qk(tmem + col_s(0), sQ, sRing + slot_k * kTileBytes);
+                issue_qk<D>(tmem + col_s(0), sQ, sRing + slot_k * kTileBytes);
                 umma_commit_w(&sh.s_full[0]);
-                issue_qk(tmem + col_s(1), sQ + kTileBytes, sRing + slot_k * kTileBytes);
+                issue_qk<D>(tmem + col_s(1), sQ + kTileBytes, sRing + slot_k * kTileBytes);
                 umma_commit_w(&sh.s_full[1]);
                 umma_commit_w(&sh.empty[slot_k]);
                 for (int j = 0; j < n1; ++j) {
@@ -240,21 +250,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         if (!(ok = mbar_wait_w(&sh.p_ready[0], pc[0] & 1, wc, kSiteP0))) break;
                         ++pc[0];
                         tc_fence_after();
-                        issue_pv(tmem + col_o(0), tmem + col_s(0), sRing + slot_v * kTileBytes, j > 0);
+                        issue_pv<D>(tmem + col_o(0), tmem + col_s(0), sRing + slot_v * kTileBytes, j > 0);
                         if (j == n0 - 1) umma_commit_w(&sh.o_done[0]);
                         if (more && j + 1 < n0) {
-                            issue_qk(tmem + col_s(0), sQ, sRing + slot_k * kTileBytes);
+                            issue_qk<D>(tmem + col_s(0), sQ, sRing + slot_k * kTileBytes);
                             umma_commit_w(&sh.s_full[0]);
                         }
                     }
                     if (!(ok = mbar_wait_w(&sh.p_ready[1], pc[1] & 1, wc, kSiteP1))) break;
                     ++pc[1];
                     tc_fence_after();
-                    issue_pv(tmem + col_o(1), tmem + col_s(1), sRing + slot_v * kTileBytes, j > 0);
+                    issue_pv<D>(tmem + col_o(1), tmem + col_s(1), sRing + slot_v * kTileBytes, j > 0);
                     umma_commit_w(&sh.empty[slot_v]);
                     if (j == n1 - 1) umma_commit_w(&sh.o_done[1]);
                     if (more) {
-                        issue_qk(tmem + col_s(1), sQ + kTileBytes, sRing + slot_k * kTileBytes);
+                        issue_qk<D>(tmem + col_s(1), sQ + kTileBytes, sRing + slot_k * kTileBytes);
                         umma_commit_w(&sh.s_full[1]);
                         umma_commit_w(&sh.empty[slot_k]);
                     }
@@ -331,7 +341,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     l *= fac;
                     if (j > 0) {
 #pragma unroll
-                        for (int c0 = 0; c0 < 128; c0 += 32) {
+                        for (int c0 = 0; c0 < D; c0 += 32) {
                             uint32_t o[32];
                             tmem_ld32(tO + c0, o);
                             tmem_wait_ld();
@@ -373,9 +383,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             const bool valid = qi < U.len;
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
             uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) +
-                                                   ((size_t)(U.tok0 + qi) * a.Hq + U.h) * kHeadDim);
+                                                   ((size_t)(U.tok0 + qi) * a.Hq + U.h) * D);
 #pragma unroll
-            for (int c0 = 0; c0 < 128; c0 += 32) {
+            for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t o[32];
                 tmem_ld32(tO + c0, o);
                 tmem_wait_ld();
@@ -411,13 +421,24 @@ __global__ void exp2_emu_kernel(const float* __restrict__ x, float* __restrict__
         y[i] = exp2_fma(x[i]);
 }
 
-template <int E>
+template <int E, int D>
 cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream, int grid) {
-    auto kern = fwd_kernel<E>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    auto kern = fwd_kernel<E, D>;
+    constexpr uint32_t smem = Geo<D>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(L.tq, L.tk, L.tv, L.a);
+    kern<<<grid, kThreads, smem, stream>>>(L.tq, L.tk, L.tv, L.a);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdLaunch& L, cudaStream_t stream, int grid) {
+    switch (L.emu_eighths) {
+        case 0: return launch_fwd_t<0, D>(L, stream, grid);
+        case 1: return launch_fwd_t<1, D>(L, stream, grid);
+        case 2: return launch_fwd_t<2, D>(L, stream, grid);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -431,12 +452,9 @@ cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream) {
         units = (long long)L.a.B * L.a.Hq * ((L.a.N + kUnitRows - 1) / kUnitRows);
     int grid = (int)(units < L.num_sms ? units : L.num_sms);
     if (grid < 1) grid = 1;
-    switch (L.emu_eighths) {
-        case 0: return launch_fwd_t<0>(L, stream, grid);
-        case 1: return launch_fwd_t<1>(L, stream, grid);
-        case 2: return launch_fwd_t<2>(L, stream, grid);
-        default: return cudaErrorInvalidValue;
-    }
+    if (L.d == 64) return launch_fwd_d<64>(L, stream, grid);
+    if (L.d == 128) return launch_fwd_d<128>(L, stream, grid);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_exp2_emu(const float* x, float* y, int64_t n, cudaStream_t stream) {

@@ -37,6 +37,7 @@ struct FwdLaunch {
     FwdArgs a;
     int emu_eighths;         // 0..4: share of exp2 pairs on the FMA pipe, in eighths
     int num_sms;
+    int d = 128;             // head dim (128 or 64; 64 runs on the ping-pong kernel only)
 };
 
 // ---------------------------------------------------------------- backward
@@ -44,7 +45,7 @@ struct FwdLaunch {
 // Workspace layout (caller-allocated, sized by fa_bwd_workspace_size):
 //   [0, 256)           BwdHeader (status word, unit count)
 //   D                  float [Hq][T]            rowsum(dO * O)
-//   dQacc              float [Hq][T][128]       fp32 dQ accumulator
+//   dQacc              float [Hq][T][d]         fp32 dQ accumulator
 //   semaphores         int   [Hq][T/128 + B + 1] (deterministic mode)
 //   units              int4  [Hkv * (T/128 + B)] (varlen work list)
 // T = B*N for fixed length, the packed token count for varlen.
@@ -64,13 +65,13 @@ struct WsLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-inline WsLayout ws_layout(long long T, int B, int Hq, int deterministic, int varlen) {
+inline WsLayout ws_layout(long long T, int B, int Hq, int deterministic, int varlen, int d = kHeadDim) {
     WsLayout w;
     const long long tiles = (T + kTileN - 1) / kTileN;
     w.sem_stride = tiles + B + 1;
     w.d_off = align256(sizeof(BwdHeader));
     w.dq_off = align256(w.d_off + (size_t)Hq * T * 4);
-    w.sem_off = align256(w.dq_off + (size_t)Hq * T * kHeadDim * 4);
+    w.sem_off = align256(w.dq_off + (size_t)Hq * T * d * 4);
     w.unit_off = align256(w.sem_off + (deterministic ? (size_t)Hq * w.sem_stride * 4 : 0));
     w.total = align256(w.unit_off + (varlen ? (size_t)Hq * (tiles + B) * 16 : 0));
     return w;
@@ -99,12 +100,13 @@ struct BwdArgs {
 
 struct BwdLaunch {
     CUtensorMap tq, tk, tv, tdo;
-    CUtensorMap tdq;         // dQacc as fp32 [Hq*T, 128], box {32, 128}, 128-B swizzle
+    CUtensorMap tdq;         // dQacc as fp32 [Hq*T, d], box {32, 128}, 128-B swizzle
     // CTA-pair main kernel only: Q and dO with 64-row boxes, dQacc with 64-row boxes.
     CUtensorMap tq64, tdo64, tdq64;
     BwdArgs a;
     int num_sms;
-    int pair;                // stage 2 runs the CTA-pair kernel (fa_bwd_pair.cu)
+    int pair;                // stage 2 runs the CTA-pair kernel (fa_bwd_pair.cu; d = 128 only)
+    int d = 128;             // head dim (128 or 64)
 };
 
 // CTA-pair backward main kernel (fa_bwd_pair.cu): fixed length, atomic mode.

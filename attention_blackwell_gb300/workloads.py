@@ -18,6 +18,8 @@ the workloads the pages' analysis is about: d = 128, BF16, long sequences):
 * varlen: 16 packed sequences, lengths uniform integers in [512, 8192],
   Hq=32, Hkv=1 (multi-query), causal.
 * causal_bwd: B=2, Hq=Hkv=16, N=8192, causal, Q, K, V, dO ~ N(0, 1).
+* large_d64, causal_bwd_d64: large and causal_bwd at head dim 64 (the
+  exponential-bound end of the balance between MUFU and tensor work).
 """
 from dataclasses import dataclass, field
 
@@ -54,6 +56,8 @@ WORKLOADS = {
     "varlen": Workload("varlen", B=16, Hq=32, Hkv=1, N=0, causal=True, varlen=True,
                        len_range=(512, 8192)),
     "causal_bwd": Workload("causal_bwd", B=2, Hq=16, Hkv=16, N=8192, causal=True, backward=True),
+    "large_d64": Workload("large_d64", B=4, Hq=16, Hkv=16, N=4096, causal=False, d=64),
+    "causal_bwd_d64": Workload("causal_bwd_d64", B=2, Hq=16, Hkv=16, N=8192, causal=True, backward=True, d=64),
 }
 
 

@@ -44,7 +44,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-bwd", action="store_true", help="time the forward only")
-    ap.add_argument("--workload", default=WORKLOAD, help="large (default), tiny, causal, varlen, causal_bwd")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="large (default), tiny, causal, varlen, causal_bwd, large_d64, causal_bwd_d64")
     ap.add_argument("--deterministic", action="store_true", help="backward in deterministic mode")
     ap.add_argument("--exp2-emu", type=int, default=0, help="forward: eighths of exp2 on the FMA pipe (0-2)")
     ap.add_argument("--tau", type=float, default=8.0, help="forward: conditional-rescale threshold (log2 units)")
@@ -178,6 +179,8 @@ def kernel_traffic(name):
 
 def traffic_key(args, w, kernel):
     """Record name in profiles/dram_traffic.json for a step kernel."""
+    if w.d != 128:   # the records are taken at d = 128
+        return "%s_d%d" % (kernel, w.d)
     if kernel == "bwd":
         return "bwd" if (w.varlen or args.deterministic or args.bwd_kernel == 0) else "bwd_pair"
     if kernel != "fwd":
@@ -212,10 +215,10 @@ def cpu_baseline(w, inp, with_bwd, budget_s):
         q, k, v, do = _slice(inp, w, b)
         L = q.shape[0]
         A.head_forward(q[:, h], k[:, h // g], v[:, h // g], w.alpha, w.causal)
-        flops += W.attention_flops(1, [L], w.causal)
+        flops += W.attention_flops(1, [L], w.causal, d=w.d)
         if with_bwd:
             A.head_backward(q[:, h], k[:, h // g], v[:, h // g], do[:, h], w.alpha, w.causal)
-            flops += W.attention_flops(1, [L], w.causal, backward=True)
+            flops += W.attention_flops(1, [L], w.causal, d=w.d, backward=True)
         done += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -231,7 +234,7 @@ def build_step(fa, w, dev_t, has_bwd, deterministic):
     q, k, v, o, lse = dev_t["q"], dev_t["k"], dev_t["v"], dev_t["o"], dev_t["lse"]
     cu, ms, lens = dev_t["cu"], dev_t["max_seqlen"], dev_t["lengths"]
     ks = [("fwd", lambda: fa.fwd(q, k, v, causal=w.causal, cu_seqlens=cu, max_seqlen=ms, out=o, lse=lse),
-           W.attention_flops(w.Hq, lens, w.causal), 1)]
+           W.attention_flops(w.Hq, lens, w.causal, d=w.d), 1)]
     if has_bwd:
         do, dq, dk, dv, ws = dev_t["do"], dev_t["dq"], dev_t["dk"], dev_t["dv"], dev_t["ws"]
 
@@ -240,7 +243,7 @@ def build_step(fa, w, dev_t, has_bwd, deterministic):
                                   deterministic=deterministic, workspace=ws, dq=dq, dk=dk, dv=dv, stages=s)
         # status reset + preprocess (+ the varlen work-list plan)
         ks.append(("bwd_pre", stage(1), 0.0, 2 + (cu is not None)))
-        ks.append(("bwd", stage(2), W.attention_flops(w.Hq, lens, w.causal, backward=True), 1))
+        ks.append(("bwd", stage(2), W.attention_flops(w.Hq, lens, w.causal, d=w.d, backward=True), 1))
         ks.append(("bwd_post", stage(4), 0.0, 1))
     return ks
 
@@ -273,7 +276,7 @@ def run_ours(args, rank, world):
         n_rows = w.N
     if has_bwd:
         t["dq"], t["dk"], t["dv"] = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
-        t["ws"] = fa.bwd_workspace(w.B, w.Hq, n_rows, deterministic=args.deterministic, varlen=w.varlen,
+        t["ws"] = fa.bwd_workspace(w.B, w.Hq, n_rows, deterministic=args.deterministic, varlen=w.varlen, d=w.d,
                                    device=dev)
     kernels = build_step(fa, w, t, has_bwd, args.deterministic)
     stream = torch.cuda.current_stream()
@@ -338,7 +341,7 @@ def run_ours(args, rank, world):
     for n in ins + outs:
         t2[n] = torch.empty_like(t[n])
     if has_bwd:
-        t2["ws"] = fa.bwd_workspace(w.B, w.Hq, n_rows, deterministic=args.deterministic, varlen=w.varlen,
+        t2["ws"] = fa.bwd_workspace(w.B, w.Hq, n_rows, deterministic=args.deterministic, varlen=w.varlen, d=w.d,
                                     device=dev)
     sets = [t, t2]
     kern = [kernels, build_step(fa, w, t2, has_bwd, args.deterministic)]
@@ -432,10 +435,10 @@ def main_ours(args):
         "config": {"workload": describe(w, r["inp"]),
             "step": step_name, "global_batch": w.B * world, "seq_len": w.N or max(r["inp"]["lengths"]),
             "deterministic_bwd": bool(args.deterministic), "exp2_emu_eighths": args.exp2_emu, "tau": args.tau,
-            "fwd_kernel": ("ping-pong 2x128" if args.exp2_emu or (w.varlen and args.fwd_kernel == 1) else
+            "fwd_kernel": ("ping-pong 2x128" if args.exp2_emu or w.d != 128 or (w.varlen and args.fwd_kernel == 1) else
                            {0: "ping-pong 2x128", 1: "256-key blocks", 2: "CTA pairs, 256-key blocks"}[args.fwd_kernel]),
             "fwd_pairs_resident": fa_pairs_resident(),
-            "bwd_kernel": ("one CTA per 128-key tile" if w.varlen or args.deterministic or args.bwd_kernel == 0
+            "bwd_kernel": ("one CTA per 128-key tile" if w.varlen or args.deterministic or args.bwd_kernel == 0 or w.d != 128
                            else "CTA pairs per 256-key block"),
             "bwd_pairs_resident": bwd_pairs_resident(),
             "parallelism": "replicas" if world > 1 else "single",
@@ -482,10 +485,10 @@ def main_reference(args):
         q, k, v, do = _slice(inp, w, b)
         L = q.shape[0]
         A.head_forward(q[:, h], k[:, hk], v[:, hk], w.alpha, w.causal)
-        f = W.attention_flops(1, [L], w.causal)
+        f = W.attention_flops(1, [L], w.causal, d=w.d)
         if with_bwd:
             A.head_backward(q[:, h], k[:, hk], v[:, hk], do[:, h], w.alpha, w.causal)
-            f += W.attention_flops(1, [L], w.causal, backward=True)
+            f += W.attention_flops(1, [L], w.causal, d=w.d, backward=True)
         return f
 
     for s in range(max(1, args.warmup)):

@@ -17,8 +17,9 @@
  * ---------------------------------------
  * - Element types: q, k, v, o, do, dq, dk, dv are bfloat16 (raw 16-bit
  *   storage, passed as void*); lse is float32; cu_seqlens is int32.
- * - Head dimension d must be 128.  Hq must be a multiple of Hkv; query head
- *   h reads key/value head h / (Hq / Hkv).
+ * - Head dimension d is 128 or 64 (the pages' balance point moves with d:
+ *   FlashAttention-4 paper summary, "Roofline" remarks).  Hq must be a
+ *   multiple of Hkv; query head h reads key/value head h / (Hq / Hkv).
  * - Fixed-length layout (cu_seqlens == NULL): q, o, do, dq are [B, N, Hq, d]
  *   row-major, k, v, dk, dv are [B, N, Hkv, d]; lse is [B, Hq, N].
  * - Variable-length layout (cu_seqlens != NULL): B sequences packed along
@@ -51,7 +52,7 @@ extern "C" {
 typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID = -1,      /* null pointer, bad size, bad scale           */
-    FA_ERR_UNSUPPORTED = -2,  /* legal but not built: d != 128, ...         */
+    FA_ERR_UNSUPPORTED = -2,  /* legal but not built: d not 64/128, ...     */
     FA_ERR_ALIGN = -3,        /* a tensor is not 16-byte aligned            */
     FA_ERR_LAUNCH = -4,       /* CUDA reported an error at launch           */
     FA_ERR_TIMEOUT = -5,      /* a device-side wait gave up (see status)    */
@@ -88,8 +89,9 @@ int fa_set_tuning(int exp2_emu_eighths, float tau);
  *        256-key blocks, each product one M = 256 UMMA over both SMs, so each
  *        SM loads and reads only half of every K and V block.
  * Kernel 2 serves fixed-length and packed varlen inputs, kernel 1 fixed-length
- * inputs, both with exp2_emu_eighths == 0; all other calls use kernel 0.  All
- * compute the same attention up to rounding.
+ * inputs, both with d = 128 and exp2_emu_eighths == 0; all other calls
+ * (d = 64 among them) use kernel 0.  All compute the same attention up to
+ * rounding.
  * Errors: FA_ERR_INVALID.
  */
 int fa_set_fwd_kernel(int kernel);
@@ -110,8 +112,8 @@ int fa_fwd_pairs_resident(void);
  *        M = 256 products over both SMs (each stages half of every B
  *        operand), dQ an M = 128 pair product after an exchange of half of
  *        dS through distributed shared memory.
- * Kernel 1 serves fixed-length inputs in atomic mode; packed varlen batches
- * and deterministic mode use kernel 0.  Both compute the same gradients up to
+ * Kernel 1 serves fixed-length d = 128 inputs in atomic mode; packed varlen
+ * batches, deterministic mode and d = 64 use kernel 0.  Both compute the same gradients up to
  * the order of the fp32 dQ additions.  Errors: FA_ERR_INVALID.
  */
 int fa_set_bwd_kernel(int kernel);
@@ -126,13 +128,13 @@ int fa_bwd_pairs_resident(void);
  * Forward: O and LSE of exact attention (FlashAttention-4 blog, "Forward
  * pass: a new softmax pipeline with conditional rescaling").
  *
- * q [B,N,Hq,128], k/v [B,N,Hkv,128] bf16 in; o [B,N,Hq,128] bf16 out,
+ * q [B,N,Hq,d], k/v [B,N,Hkv,d] bf16 in; o [B,N,Hq,d] bf16 out,
  * lse [B,Hq,N] float32 out (natural log, includes alpha).  Varlen: see
- * above.  alpha > 0 is the logit scale (normally 1/sqrt(128)).
+ * above.  alpha > 0 is the logit scale (normally 1/sqrt(d)).
  * causal: 0 or 1.  N == 0 (or T == 0) is a no-op returning FA_OK.
  * Errors: FA_ERR_INVALID (null pointer, B<1, N<0, Hq/Hkv<1, Hq % Hkv,
  * alpha not finite and > 0, varlen without max_seqlen>0),
- * FA_ERR_UNSUPPORTED (d != 128), FA_ERR_ALIGN, FA_ERR_LAUNCH.
+ * FA_ERR_UNSUPPORTED (d not 64 or 128), FA_ERR_ALIGN, FA_ERR_LAUNCH.
  */
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int Hq, int Hkv, int N, int d, float alpha, int causal,
@@ -143,7 +145,7 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  * D (rowsum(dO*O), fp32), the fp32 dQ accumulator, the deterministic-mode
  * semaphores and the varlen work list.  N is the sequence length (fixed
  * length) or the total token count T (varlen = 1).  Returns 0 for invalid
- * sizes.  About 516 * Hq * T bytes.
+ * sizes (d not 64 or 128 among them).  About (4 d + 4) * Hq * T bytes.
  */
 size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, int deterministic, int varlen);
 

@@ -65,7 +65,8 @@ def test_fwd_rejects_bad_arguments_on_the_host(lib):
     assert call(alpha=0.0) == -1
     assert call(alpha=float("inf")) == -1
     assert call(causal=2) == -1
-    assert call(d=64) == -2
+    assert call(d=96) == -2            # d is 64 or 128
+    assert call(d=256) == -2
     assert call(cu=P, ms=0) == -1      # varlen without max_seqlen
     assert call(cu=P, ms=1 << 20) == -2
     assert call(B=5000, cu=P, ms=128) == -2
@@ -98,3 +99,14 @@ def test_backward_kernel_selector(lib):
     assert lib.fa_set_bwd_kernel(2) == -1
     assert lib.fa_set_bwd_kernel(-1) == -1
     assert lib.fa_set_bwd_kernel(0) == 0
+
+
+def test_workspace_size_depends_on_head_dim(lib):
+    """Host arithmetic only: the fp32 dQ accumulator scales with d."""
+    f = lib.fa_bwd_workspace_size
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int] * 6
+    n64, n128 = f(2, 4, 1000, 64, 0, 0), f(2, 4, 1000, 128, 0, 0)
+    assert 0 < n64 < n128
+    assert n128 - n64 >= 2 * 4 * 1000 * 64 * 4        # B*N*Hq rows of 64 more floats
+    assert f(2, 4, 1000, 96, 0, 0) == 0 and f(2, 4, 1000, 256, 0, 0) == 0

@@ -207,7 +207,7 @@ def test_status_and_bad_arguments(fa):
     lse = torch.empty(1, 2, 128, device="cuda")
     p = lambda t: t.data_ptr()
     s = torch.cuda.current_stream().cuda_stream
-    assert L.fa_fwd(p(q), p(q), p(q), p(o), p(lse), 1, 2, 2, 128, 64, 0.1, 0, None, 0, s) == -2  # d != 128
+    assert L.fa_fwd(p(q), p(q), p(q), p(o), p(lse), 1, 2, 2, 128, 96, 0.1, 0, None, 0, s) == -2  # d not 64 or 128
     assert L.fa_fwd(p(q), p(q), p(q), p(o), p(lse), 1, 3, 2, 128, 128, 0.1, 0, None, 0, s) == -1  # Hq % Hkv
     assert L.fa_fwd(p(q) + 2, p(q), p(q), p(o), p(lse), 1, 2, 2, 128, 128, 0.1, 0, None, 0, s) == -3
     assert L.fa_fwd(p(q), p(q), p(q), p(o), p(lse), 1, 2, 2, 0, 128, 0.1, 0, None, 0, s) == 0  # empty
