@@ -214,3 +214,14 @@ def test_claim_counter_rewinds(fa):
     torch.cuda.synchronize()
     assert fa.device_status(ws) == 0
     assert torch.equal(dk, first[0]) and torch.equal(dv, first[1])
+
+
+def test_varlen_many_short_sequences(fa):
+    """1000 packed sequences of 0-300 tokens (the limit is 1024): the
+    forward's per-CTA tables, the backward's plan kernel and the claim
+    counter over thousands of tiny units, causal, with GQA."""
+    rng = np.random.default_rng(77)
+    lengths = [int(x) for x in rng.integers(0, 301, size=1000)]
+    inp = inputs(0, 0, 4, 2, seed=51, lengths=lengths)
+    got = gpu_grads(fa, inp, True)[0]
+    check(got, oracle(inp, True))

@@ -163,3 +163,12 @@ def test_bwd_many_tiles_one_head(fa):
                           ALPHA, True)
     check_bwd([g[0, :, 0] for g in (dq, dk, dv)], ref)
 
+
+
+def test_varlen_many_short_sequences_d64(fa):
+    rng = np.random.default_rng(78)
+    lengths = [int(x) for x in rng.integers(0, 301, size=1000)]
+    inp = inputs(0, 0, 4, 2, seed=52, lengths=lengths)
+    check_fwd(*gpu_fwd(fa, inp, True)[5:], inp, True)
+    check_bwd(gpu_grads(fa, inp, True)[0],
+              A.backward(inp["q"], inp["k"], inp["v"], inp["do"], ALPHA, True, cu_seqlens=inp["cu_seqlens"]))
