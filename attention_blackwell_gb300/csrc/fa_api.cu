@@ -238,7 +238,19 @@ int fa_get_device_status(const void* workspace, cudaStream_t stream) {
     int rc = current_device_info(&dev);
     if (rc != FA_OK) return rc;
     int a = read_and_clear(dev->status);
-    int b = workspace ? read_and_clear(&static_cast<BwdHeader*>(const_cast<void*>(workspace))->status) : FA_OK;
+    int b = FA_OK;
+    if (workspace) {
+        BwdHeader* h = static_cast<BwdHeader*>(const_cast<void*>(workspace));
+        b = read_and_clear(&h->status);
+        if (b != FA_OK && b != FA_ERR_LAUNCH) {
+            // A main kernel that gave up may leave its unit claim counter
+            // mid-list: rewind it, so that a later main stage run without the
+            // preprocess starts from the first unit.
+            const int zero[2] = {0, 0};
+            if (cudaMemcpy(&h->next_unit, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+                return FA_ERR_LAUNCH;
+        }
+    }
     return a != FA_OK ? a : b;
 }
 

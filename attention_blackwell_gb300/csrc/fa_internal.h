@@ -3,6 +3,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "fa_prim.cuh"
@@ -53,10 +54,11 @@ struct BwdHeader {
     DevStatus status;
     int total_units;   // varlen: written by the plan kernel
     int next_unit;     // main kernel: units claimed past the first wave
-    int done_ctas;     // main kernel: CTAs that found the list exhausted
+    int done_ctas;     // main kernel: CTAs that found the list exhausted (follows next_unit)
     int pad[57];
 };
 static_assert(sizeof(BwdHeader) == 256, "backward workspace header");
+static_assert(offsetof(BwdHeader, done_ctas) == offsetof(BwdHeader, next_unit) + sizeof(int), "claim counters");
 
 struct WsLayout {
     size_t d_off, dq_off, sem_off, unit_off, total;

@@ -217,7 +217,9 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
  * kernel's bounded wait gave up (the kernel then skipped its remaining work,
  * drained its own copies, freed its tensor memory and returned).
  * `workspace` may be NULL; when it is a backward workspace its status word
- * is read (and cleared) too.
+ * is read (and cleared) too, and after a reported timeout the main stage's
+ * unit claim counter in the workspace is rewound, so that a later
+ * fa_bwd_stages call with stages == 2 alone starts from the first unit.
  */
 int fa_get_device_status(const void *workspace, cudaStream_t stream);
 
