@@ -12,7 +12,7 @@ import os
 
 import torch
 
-__all__ = ["fwd", "set_fwd_kernel", "fwd_pairs_resident", "set_bwd_kernel", "bwd_pairs_resident", "bwd", "bwd_workspace", "exp2_emu", "set_tuning", "device_status", "num_sms", "FAError", "library_path", "lib"]
+__all__ = ["fwd", "set_fwd_kernel", "fwd_pairs_resident", "set_bwd_kernel", "bwd_pairs_resident", "bwd", "bwd_workspace", "exp2_emu", "selftest_timeout", "set_tuning", "device_status", "num_sms", "FAError", "library_path", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libfa.so")
@@ -69,6 +69,8 @@ def lib():
         L.fa_get_device_status.argtypes = [vp, vp]
         L.fa_exp2_emu.restype = i
         L.fa_exp2_emu.argtypes = [vp, vp, i64, vp]
+        L.fa_selftest_timeout.restype = i
+        L.fa_selftest_timeout.argtypes = [vp]
         _lib = L
     return _lib
 
@@ -241,3 +243,9 @@ def exp2_emu(x, stream=None):
     y = torch.empty_like(x)
     _check(lib().fa_exp2_emu(_ptr(x), _ptr(y), x.numel(), _stream(stream)), "fa_exp2_emu")
     return y
+
+
+def selftest_timeout(stream=None):
+    """Enqueue the failure-detection diagnostic (a bounded wait on a barrier
+    nothing arrives at); device_status() afterwards reports the timeout."""
+    _check(lib().fa_selftest_timeout(_stream(stream)), "fa_selftest_timeout")

@@ -340,6 +340,13 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
                          max_seqlen, deterministic, workspace, workspace_bytes, stream);
 }
 
+int fa_selftest_timeout(cudaStream_t stream) {
+    DeviceInfo* dev = nullptr;
+    int rc = current_device_info(&dev);
+    if (rc != FA_OK) return rc;
+    return launch_selftest_timeout(dev->status, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 int fa_exp2_emu(const float* x, float* y, int64_t n, cudaStream_t stream) {
     if (n < 0 || (n > 0 && (!x || !y))) return FA_ERR_INVALID;
     return launch_exp2_emu(x, y, n, stream) == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;

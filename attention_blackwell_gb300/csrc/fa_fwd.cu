@@ -54,7 +54,7 @@ __device__ __forceinline__ uint32_t col_s(int x) { return 256u + (uint32_t)x * 1
 
 // Wait-site identifiers reported through the status word.
 enum : int { kSiteQEmpty = 1, kSiteRingEmpty, kSiteQFull, kSiteRingFull, kSiteP0, kSiteP1, kSiteS, kSiteO,
-             kSiteDrain };
+             kSiteDrain, kSiteSelftest = 990 };
 
 // Key tiles tile x (0/1) of a unit needs.
 __device__ __forceinline__ int kv_tiles(const Unit& U, int x, int causal) {
@@ -416,6 +416,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// One warp waits, through the bounded wait of every pipeline here, on an
+// mbarrier that no thread arrives at: the wait gives up after kWaitLimitNs,
+// records the timeout in the status word and returns false.
+__global__ void selftest_timeout_kernel(DevStatus* status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const WaitCtx wc{&abort_flag, status};
+    const bool ok = mbar_wait_w(&bar, 0, wc, kSiteSelftest);
+    if (ok && threadIdx.x == 0) atomicCAS(&status->code, 0, -1);   // the phase cannot complete
+}
+
 __global__ void exp2_emu_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         y[i] = exp2_fma(x[i]);
@@ -455,6 +472,11 @@ cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream) {
     if (L.d == 64) return launch_fwd_d<64>(L, stream, grid);
     if (L.d == 128) return launch_fwd_d<128>(L, stream, grid);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_selftest_timeout(DevStatus* status, cudaStream_t stream) {
+    selftest_timeout_kernel<<<1, 32, 0, stream>>>(status);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_exp2_emu(const float* x, float* y, int64_t n, cudaStream_t stream) {

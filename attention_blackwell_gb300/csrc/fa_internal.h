@@ -133,6 +133,7 @@ extern int g_pairs_resident;
 
 // Evaluate the FMA-pipe exp2 on n floats (fa_fwd.cu).
 cudaError_t launch_exp2_emu(const float* x, float* y, int64_t n, cudaStream_t stream);
+cudaError_t launch_selftest_timeout(DevStatus* status, cudaStream_t stream);
 
 // The library's device status word on the current device.
 DevStatus* device_status_ptr();

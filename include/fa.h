@@ -234,6 +234,17 @@ int fa_get_device_status(const void *workspace, cudaStream_t stream);
  */
 int fa_exp2_emu(const float *x, float *y, int64_t n, cudaStream_t stream);
 
+/*
+ * Diagnostic for the failure-detection path, for tests: enqueues a one-block
+ * kernel on `stream` whose warp waits, through the same bounded mbarrier
+ * wait every kernel here uses, on a barrier nothing ever arrives at.  After
+ * the wait limit (about 2 s) it records FA_ERR_TIMEOUT in the current
+ * device's status word and returns; the context stays usable, and
+ * fa_get_device_status(NULL, stream) then reports (and clears) the timeout.
+ * Errors: FA_ERR_LAUNCH.
+ */
+int fa_selftest_timeout(cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -212,3 +212,19 @@ def test_status_and_bad_arguments(fa):
     assert L.fa_fwd(p(q) + 2, p(q), p(q), p(o), p(lse), 1, 2, 2, 128, 128, 0.1, 0, None, 0, s) == -3
     assert L.fa_fwd(p(q), p(q), p(q), p(o), p(lse), 1, 2, 2, 0, 128, 0.1, 0, None, 0, s) == 0  # empty
     assert fa.device_status() == 0
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(fa):
+    """The failure-detection path on the GPU, without a fault: a wait on a
+    barrier nothing arrives at gives up after its limit, the status word
+    reports FA_ERR_TIMEOUT once (reading clears it), and the same context
+    then computes a forward that matches the oracle."""
+    import time
+    t0 = time.time()
+    fa.selftest_timeout()
+    assert fa.device_status() == -5
+    assert time.time() - t0 >= 1.0          # the wait ran to its limit
+    assert fa.device_status() == 0          # cleared by the read
+    inp = small_inputs(1, 300, 2, 2, seed=61)
+    o, lse = run(fa, inp, True)
+    check(o, lse, *oracle(inp, True))
