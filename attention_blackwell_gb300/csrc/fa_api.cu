@@ -146,12 +146,13 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     if (B < 1 || N < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return FA_ERR_INVALID;
     if (!(alpha > 0.0f) || !isfinite(alpha)) return FA_ERR_INVALID;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID;
-    if (d != 128 && d != 64) return FA_ERR_UNSUPPORTED;
+    if (d != 128 && d != 64 && d != 256) return FA_ERR_UNSUPPORTED;
     const bool varlen = cu_seqlens != nullptr;
     if (varlen) {
         if (max_seqlen < 1) return FA_ERR_INVALID;
         if (B > kMaxVarlenSeqs || (max_seqlen + kUnitRows - 1) / kUnitRows > kMaxUnitLevels)
             return FA_ERR_UNSUPPORTED;
+        if (d == 256) return FA_ERR_UNSUPPORTED;   // the d = 256 kernel takes fixed-length inputs
     }
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGN;
     if (varlen && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FA_ERR_ALIGN;
@@ -170,11 +171,19 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     const bool pair = d == 128 && g_emu_eighths == 0 && g_fwd_kernel == 2;
     FwdLaunch L;
     L.d = d;
+    if (d == 256) {
+        // One 128-row query tile per CTA, 64-key blocks (fa_fwd256.cu).
+        if ((rc = make_map(&L.tq, q, Hq, T, kTileM, d)) != FA_OK) return rc;
+        if ((rc = make_map(&L.tk, k, Hkv, T, 64, d)) != FA_OK) return rc;
+        if ((rc = make_map(&L.tv, v, Hkv, T, 64, d)) != FA_OK) return rc;
+    }
     // K boxes: 256 rows (one block) for kernel 1, 128 (a block's half) for the
     // pair kernel; V boxes: 256 rows for both (the pair loads 64 columns of them).
-    if ((rc = make_map(&L.tq, q, Hq, T, kTileM, d)) != FA_OK) return rc;
-    if ((rc = make_map(&L.tk, k, Hkv, T, wide ? 256 : kTileM, d)) != FA_OK) return rc;
-    if ((rc = make_map(&L.tv, v, Hkv, T, (wide || pair) ? 256 : kTileM, d)) != FA_OK) return rc;
+    if (d != 256) {
+        if ((rc = make_map(&L.tq, q, Hq, T, kTileM, d)) != FA_OK) return rc;
+        if ((rc = make_map(&L.tk, k, Hkv, T, wide ? 256 : kTileM, d)) != FA_OK) return rc;
+        if ((rc = make_map(&L.tv, v, Hkv, T, (wide || pair) ? 256 : kTileM, d)) != FA_OK) return rc;
+    }
     if (pair && (rc = make_map(&L.to, o, Hq, T)) != FA_OK) return rc;
     L.a.o = o;
     L.a.lse = lse;
@@ -201,7 +210,10 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     L.a.tau = g_tau;
     L.emu_eighths = g_emu_eighths;
     L.num_sms = dev->num_sms;
-    cudaError_t e = pair ? launch_fwd_pair(L, stream) : wide ? launch_fwd_wide(L, stream) : launch_fwd(L, stream);
+    cudaError_t e = d == 256 ? launch_fwd256(L, stream)
+                    : pair    ? launch_fwd_pair(L, stream)
+                    : wide    ? launch_fwd_wide(L, stream)
+                              : launch_fwd(L, stream);
     return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

@@ -1,0 +1,367 @@
+// fa_fwd256.cu -- forward attention for head dim d = 256 (sm_103a).
+//
+// The same O = softmax(alpha Q K^T [+ causal]) V and LSE as fa_fwd.cu
+// (FlashAttention-4 blog, "Forward pass"), for the head dim at which the
+// products, not the exponentials, set the pace (FlashAttention-4 paper
+// summary, roofline remarks: the balance point moves with d).  At d = 256 a
+// 128-row tile of Q, K or V is 64 KB, so the layout differs from the d = 128
+// kernels: one CTA per SM owns one 128-row query tile at a time and streams
+// 64-key blocks of K and V.
+//
+//   warps 0-3  softmax: one thread per query row (TMEM lane), 64 scores per
+//              block; conditional rescale of its O row (tau), P as bf16 into
+//              tensor memory over the scores it read, the epilogue;
+//   warp  4    TMA loader: Q once per unit, then a K ring and a V ring;
+//   warp  5    UMMA issuer: S = Q K^T (M 128, N 64, K 256: 16 steps) and
+//              O += P V (M 128, N 256, K 64: 4 steps, P from tensor memory).
+//
+// Tensor memory (512 columns): O 0-255; S/P of block j in 256 + 64 (j % 2)
+// (two regions, so S of block j+1 is computed while the softmax of block j
+// runs; P of block j overwrites the first 32 columns of its region and is
+// read by the P V of block j before S of block j+2 is written there -- the
+// issuer emits both, in that order).
+//
+// Shared memory: Q 64 KB (four 128-row x 64-column boxes), K ring 2 x 32 KB
+// and V ring 2 x 32 KB (four 64-row x 64-column boxes each).
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kD = 256;
+constexpr int kBlk = 64;                         // keys per block
+constexpr int kThreads256 = 192;
+constexpr int kKS = 2, kVS = 2;
+constexpr uint32_t kQBox = 16384;                // 128 rows x 128 B
+constexpr uint32_t kKVBox = 8192;                // 64 rows x 128 B
+constexpr uint32_t kQBytes = 4 * kQBox, kKVBytes = 4 * kKVBox;
+constexpr uint32_t kOffQ = 0, kOffK = kQBytes, kOffV = kOffK + kKS * kKVBytes;
+constexpr uint32_t kSmem256 = 1024 + kOffV + kVS * kKVBytes;   // + alignment slack
+static_assert(kSmem256 <= 232448, "shared memory plan");
+constexpr uint32_t kColO = 0, kColS = 256;
+
+enum : int { k6QEmpty = 41, k6KEmpty, k6VEmpty, k6QFull, k6KFull, k6VFull, k6S, k6P, k6PV, k6O, k6OFree };
+
+struct Shared256 {
+    uint64_t q_full, q_empty, kfull[kKS], kempty[kKS], vfull[kVS], vempty[kVS];
+    uint64_t s_full[2], p_ready, pv_done, o_done, o_free, drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+struct Unit256 {
+    int seq, h, m, tok0, len, nb;
+};
+
+// Unit u: one 128-row query tile of one (batch, head).  Non-causal:
+// (batch, head) major; causal: query tiles from the last (longest first),
+// (batch, head) minor.
+__device__ __forceinline__ bool unit256(const FwdArgs& a, int u, Unit256& U) {
+    const int nm = (a.N + kTileM - 1) / kTileM, bh_all = a.B * a.Hq;
+    if (u < 0 || u >= bh_all * nm) return false;
+    int bh;
+    if (a.causal) {
+        U.m = nm - 1 - u / bh_all;
+        bh = u % bh_all;
+    } else {
+        bh = u / nm;
+        U.m = u - bh * nm;
+    }
+    U.seq = bh / a.Hq;
+    U.h = bh - U.seq * a.Hq;
+    U.tok0 = U.seq * a.N;
+    U.len = a.N;
+    const int all = (U.len + kBlk - 1) / kBlk;
+    const int diag = (U.m * kTileM + kTileM - 1) / kBlk + 1;   // blocks holding keys <= the tile's last row
+    U.nb = a.causal && diag < all ? diag : all;
+    return true;
+}
+
+// S = Q K^T: both K-major; k-step k (16 of the 256 head-dim columns) is box
+// k / 4, bytes (k % 4) * 32 of each 128-byte row.
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, kBlk, 0, 0);
+    const uint64_t qd = sdesc_sw128(q_smem, 16, 1024), kd = sdesc_sw128(k_smem, 16, 1024);
+    static_for<16>([&](auto kc) {
+        constexpr uint32_t k = kc;
+        constexpr uint32_t ao = ((k >> 2) * kQBox + (k & 3) * 32) >> 4, bo = ((k >> 2) * kKVBox + (k & 3) * 32) >> 4;
+        umma_ss_k<ao, bo>(d_tmem, qd, kd, idesc, k > 0);
+    });
+}
+
+// O (+)= P V: A = P (bf16 in tensor memory, 8 columns per 16 keys); B = V
+// MN-major, N = 256 over four 64-column boxes kKVBox apart, a 16-key step
+// 16 rows x 128 B = 2048 bytes further.
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, uint32_t acc) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, kD, 0, 1);
+    const uint64_t vd = sdesc_sw128(v_smem, kKVBox, 1024);
+    static_for<kBlk / 16>([&](auto kc) {
+        constexpr uint32_t k = kc;
+        umma_ts_k<k * 8, ((k * 2048) >> 4)>(d_tmem, p_tmem, vd, idesc, (acc | k) != 0);
+    });
+}
+
+__global__ void __launch_bounds__(kThreads256, 1)
+fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+              const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
+    extern __shared__ uint8_t dsmem[];
+    __shared__ Shared256 sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
+    const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
+
+    if (tid == 0) {
+        mbar_init(&sh.q_full, 1);
+        mbar_init(&sh.q_empty, 1);
+        for (int i = 0; i < kKS; ++i) { mbar_init(&sh.kfull[i], 1); mbar_init(&sh.kempty[i], 1); }
+        for (int i = 0; i < kVS; ++i) { mbar_init(&sh.vfull[i], 1); mbar_init(&sh.vempty[i], 1); }
+        mbar_init(&sh.s_full[0], 1);
+        mbar_init(&sh.s_full[1], 1);
+        mbar_init(&sh.p_ready, 128);
+        mbar_init(&sh.pv_done, 1);
+        mbar_init(&sh.o_done, 1);
+        mbar_init(&sh.o_free, 128);
+        mbar_init(&sh.drain, 1);
+        sh.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+    }
+    if (warp == 0) {
+        tmem_alloc(&sh.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const WaitCtx wc{&sh.abort_flag, a.status};
+    const uint32_t tmem = sh.tmem_base;
+    const int group = a.Hq / a.Hkv;
+
+    if (warp == 4) {
+        // ---------------------------------------------------------------- loader
+        if (lane == 0) {
+            uint32_t kit = 0, vit = 0, uc = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok; u += gridDim.x) {
+                Unit256 U;
+                if (!unit256(a, u, U)) break;
+                const int hk = U.h / group;
+                if (!(ok = mbar_wait(&sh.q_empty, (uc & 1) ^ 1, wc, k6QEmpty))) break;
+                mbar_arrive_expect_tx(&sh.q_full, kQBytes);
+                for (int c = 0; c < 4; ++c)
+                    tma_load_3d(sQ + c * kQBox, &tq, &sh.q_full, c * 64, U.h, U.tok0 + U.m * kTileM);
+                for (int j = 0; j < U.nb && ok; ++j) {
+                    const uint32_t ks = kit % kKS, vs = vit % kVS;
+                    if (!(ok = mbar_wait(&sh.kempty[ks], ((kit / kKS) & 1) ^ 1, wc, k6KEmpty))) break;
+                    mbar_arrive_expect_tx(&sh.kfull[ks], kKVBytes);
+                    for (int c = 0; c < 4; ++c)
+                        tma_load_3d(sK + ks * kKVBytes + c * kKVBox, &tk, &sh.kfull[ks], c * 64, hk, U.tok0 + j * kBlk);
+                    ++kit;
+                    if (!(ok = mbar_wait(&sh.vempty[vs], ((vit / kVS) & 1) ^ 1, wc, k6VEmpty))) break;
+                    mbar_arrive_expect_tx(&sh.vfull[vs], kKVBytes);
+                    for (int c = 0; c < 4; ++c)
+                        tma_load_3d(sV + vs * kKVBytes + c * kKVBox, &tv, &sh.vfull[vs], c * 64, hk, U.tok0 + j * kBlk);
+                    ++vit;
+                }
+                ++uc;
+            }
+            // Every copy this thread issued lands before teardown.
+            const uint64_t t0 = globaltimer_ns();
+            for (uint32_t i = (kit > kKS ? kit - kKS : 0); i < kit; ++i)
+                while (!mbar_try_wait(smem_u32(&sh.kfull[i % kKS]), (i / kKS) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+            for (uint32_t i = (vit > kVS ? vit - kVS : 0); i < vit; ++i)
+                while (!mbar_try_wait(smem_u32(&sh.vfull[i % kVS]), (i / kVS) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+            if (uc > 0)
+                while (!mbar_try_wait(smem_u32(&sh.q_full), (uc - 1) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ---------------------------------------------------------- UMMA issuer
+        uint32_t kit = 0, vit = 0, uc = 0, gs = 0, gp = 0;   // K, V slots; S and P V blocks so far
+        bool ok = true;
+        auto issue_s_block = [&](bool last_of_unit) -> bool {
+            const uint32_t ks = kit % kKS;
+            if (!mbar_wait_w(&sh.kfull[ks], (kit / kKS) & 1, wc, k6KFull)) return false;
+            ++kit;
+            tc_fence_after();
+            issue_s(tmem + kColS + 64 * (gs & 1), sQ, sK + ks * kKVBytes);
+            umma_commit_w(&sh.s_full[gs & 1]);
+            umma_commit_w(&sh.kempty[ks]);
+            if (last_of_unit) umma_commit_w(&sh.q_empty);   // Q read by the unit's last S
+            ++gs;
+            return true;
+        };
+        for (int u = blockIdx.x; ok; u += gridDim.x) {
+            Unit256 U;
+            if (!unit256(a, u, U)) break;
+            if (!(ok = mbar_wait_w(&sh.q_full, uc & 1, wc, k6QFull))) break;
+            if (!(ok = issue_s_block(U.nb == 1))) break;
+            if (U.nb > 1 && !(ok = issue_s_block(U.nb == 2))) break;
+            for (int j = 0; j < U.nb; ++j) {
+                if (!(ok = mbar_wait_w(&sh.p_ready, gp & 1, wc, k6P))) break;
+                if (j == 0 && uc > 0 && !(ok = mbar_wait_w(&sh.o_free, (uc - 1) & 1, wc, k6OFree))) break;
+                const uint32_t vs = vit % kVS;
+                if (!(ok = mbar_wait_w(&sh.vfull[vs], (vit / kVS) & 1, wc, k6VFull))) break;
+                ++vit;
+                tc_fence_after();
+                issue_pv(tmem + kColO, tmem + kColS + 64 * (gp & 1), sV + vs * kKVBytes, j > 0);
+                umma_commit_w(&sh.vempty[vs]);
+                umma_commit_w(&sh.pv_done);
+                ++gp;
+                // S of block j + 2 into the region P of block j was just read from.
+                if (j + 2 < U.nb && !(ok = issue_s_block(j + 3 == U.nb))) break;
+            }
+            if (!ok) break;
+            umma_commit_w(&sh.o_done);
+            ++uc;
+        }
+        umma_commit_w(&sh.drain);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_u32(&sh.drain), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------- softmax
+        const int r = warp * 32 + lane;                       // query row in the tile == TMEM lane
+        const uint32_t lane_bits = (uint32_t)(warp * 32) << 16;
+        const uint32_t tO = tmem + lane_bits + kColO;
+        const float scale = a.scale_log2;
+        uint32_t gs = 0, pvc = 0, uc = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok; u += gridDim.x) {
+            Unit256 U;
+            if (!unit256(a, u, U)) break;
+            const int q_first = U.m * kTileM, qi = q_first + r;
+            float m_ref = -INFINITY, l = 0.f;
+            for (int j = 0; j < U.nb; ++j) {
+                const uint32_t tS = tmem + lane_bits + kColS + 64 * (gs & 1);
+                if (!(ok = mbar_wait(&sh.s_full[gs & 1], (gs >> 1) & 1, wc, k6S))) break;
+                ++gs;
+                tc_fence_after();
+                float s[kBlk];
+                {
+                    uint32_t* su = reinterpret_cast<uint32_t*>(s);
+                    tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(su));
+                    tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
+                    tmem_wait_ld();
+                }
+                const int k0 = j * kBlk;
+                if (k0 + kBlk > U.len || (a.causal && k0 + kBlk - 1 > q_first)) {
+                    const int lim_len = U.len - k0;
+                    const int lim_causal = a.causal ? qi - k0 + 1 : kBlk;
+                    const int lim = lim_len < lim_causal ? lim_len : lim_causal;
+#pragma unroll
+                    for (int c = 0; c < kBlk; ++c)
+                        if (c >= lim) s[c] = -INFINITY;
+                }
+                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int c = 4; c < kBlk; c += 4) {
+                    mx0 = fmaxf(mx0, s[c]);
+                    mx1 = fmaxf(mx1, s[c + 1]);
+                    mx2 = fmaxf(mx2, s[c + 2]);
+                    mx3 = fmaxf(mx3, s[c + 3]);
+                }
+                const float m_new = fmaxf(m_ref, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale);
+                // The previous block's P V must be done before O is touched;
+                // every phase is waited for, in order.
+                if (j > 0) {
+                    if (!(ok = mbar_wait(&sh.pv_done, pvc & 1, wc, k6PV))) break;
+                    ++pvc;
+                    tc_fence_after();
+                }
+                // Conditional rescale (blog, "Forward pass"): move to the new
+                // maximum only when some row of this warp jumped by more than tau.
+                const bool jump = (m_ref == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_ref > a.tau);
+                if (__any_sync(0xffffffffu, jump)) {
+                    const float fac = (m_ref == -INFINITY) ? 0.f : ex2_mufu(m_ref - m_new);
+                    l *= fac;
+                    if (j > 0) {
+#pragma unroll 1
+                        for (int c0 = 0; c0 < kD; c0 += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + c0, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * fac);
+                            tmem_st32(tO + c0, o);
+                        }
+                    }
+                    m_ref = m_new;
+                }
+                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+                for (int st = 0; st < 2; ++st) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int c = st * 32 + 2 * i;
+                        const float p0 = ex2_mufu(fmaf(s[c], scale, -m_use)), p1 = ex2_mufu(fmaf(s[c + 1], scale, -m_use));
+                        l0 += p0;
+                        l1 += p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(tS + st * 16, pk);   // P over the scores just read
+                }
+                l += l0 + l1;
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&sh.p_ready);
+            }
+            if (!ok) break;
+            // Epilogue: O / l -> bf16, LSE = (m + log2 l) ln 2.
+            if (!(ok = mbar_wait(&sh.o_done, uc & 1, wc, k6O))) break;
+            ++uc;
+            ++pvc;   // the unit's last P V phase, covered by o_done
+            tc_fence_after();
+            const bool valid = qi < U.len;
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.o) +
+                                                   ((size_t)(U.tok0 + qi) * a.Hq + U.h) * kD);
+#pragma unroll 1
+            for (int c0 = 0; c0 < kD; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld32(tO + c0, o);
+                tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float* f = reinterpret_cast<const float*>(o + 8 * q);
+                        orow[c0 / 8 + q] = make_uint4(pack_bf16x2(f[0] * inv_l, f[1] * inv_l), pack_bf16x2(f[2] * inv_l, f[3] * inv_l),
+                                                      pack_bf16x2(f[4] * inv_l, f[5] * inv_l), pack_bf16x2(f[6] * inv_l, f[7] * inv_l));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&sh.o_free);
+            if (valid)
+                a.lse[((size_t)U.seq * a.Hq + U.h) * a.N + qi] =
+                    l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd256(const FwdLaunch& L, cudaStream_t stream) {
+    const FwdArgs& a = L.a;
+    const long long units = (long long)a.B * a.Hq * ((a.N + kTileM - 1) / kTileM);
+    int grid = (int)(units < L.num_sms ? units : L.num_sms);
+    if (grid < 1) grid = 1;
+    cudaError_t e = cudaFuncSetAttribute(fwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem256);
+    if (e != cudaSuccess) return e;
+    fwd256_kernel<<<grid, kThreads256, kSmem256, stream>>>(L.tq, L.tk, L.tv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -38,7 +38,7 @@ struct FwdLaunch {
     FwdArgs a;
     int emu_eighths;         // 0..4: share of exp2 pairs on the FMA pipe, in eighths
     int num_sms;
-    int d = 128;             // head dim (128 or 64; 64 runs on the ping-pong kernel only)
+    int d = 128;             // head dim (128; 64 on the ping-pong kernel; 256 on fa_fwd256.cu)
 };
 
 // ---------------------------------------------------------------- backward
@@ -134,6 +134,9 @@ extern int g_pairs_resident;
 // Evaluate the FMA-pipe exp2 on n floats (fa_fwd.cu).
 cudaError_t launch_exp2_emu(const float* x, float* y, int64_t n, cudaStream_t stream);
 cudaError_t launch_selftest_timeout(DevStatus* status, cudaStream_t stream);
+// Forward for head dim 256 (fa_fwd256.cu): fixed length; tq with 128-row
+// boxes, tk and tv with 64-row boxes.
+cudaError_t launch_fwd256(const FwdLaunch& L, cudaStream_t stream);
 
 // The library's device status word on the current device.
 DevStatus* device_status_ptr();

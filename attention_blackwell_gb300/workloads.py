@@ -20,6 +20,7 @@ the workloads the pages' analysis is about: d = 128, BF16, long sequences):
 * causal_bwd: B=2, Hq=Hkv=16, N=8192, causal, Q, K, V, dO ~ N(0, 1).
 * large_d64, causal_bwd_d64: large and causal_bwd at head dim 64 (the
   exponential-bound end of the balance between MUFU and tensor work).
+* large_d256, causal_d256: forward at head dim 256 (the product-bound end).
 """
 from dataclasses import dataclass, field
 
@@ -58,6 +59,8 @@ WORKLOADS = {
     "causal_bwd": Workload("causal_bwd", B=2, Hq=16, Hkv=16, N=8192, causal=True, backward=True),
     "large_d64": Workload("large_d64", B=4, Hq=16, Hkv=16, N=4096, causal=False, d=64),
     "causal_bwd_d64": Workload("causal_bwd_d64", B=2, Hq=16, Hkv=16, N=8192, causal=True, backward=True, d=64),
+    "large_d256": Workload("large_d256", B=4, Hq=16, Hkv=16, N=4096, causal=False, d=256),
+    "causal_d256": Workload("causal_d256", B=2, Hq=16, Hkv=16, N=8192, causal=True, d=256),
 }
 
 

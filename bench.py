@@ -45,7 +45,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-bwd", action="store_true", help="time the forward only")
     ap.add_argument("--workload", default=WORKLOAD,
-                    help="large (default), tiny, causal, varlen, causal_bwd, large_d64, causal_bwd_d64")
+                    help="large (default), tiny, causal, varlen, causal_bwd, large_d64, causal_bwd_d64, "
+                         "large_d256, causal_d256 (forward only)")
     ap.add_argument("--deterministic", action="store_true", help="backward in deterministic mode")
     ap.add_argument("--exp2-emu", type=int, default=0, help="forward: eighths of exp2 on the FMA pipe (0-2)")
     ap.add_argument("--tau", type=float, default=8.0, help="forward: conditional-rescale threshold (log2 units)")
@@ -261,7 +262,7 @@ def run_ours(args, rank, world):
     fa.set_tuning(args.exp2_emu, args.tau)
     fa.set_fwd_kernel(args.fwd_kernel)
     fa.set_bwd_kernel(args.bwd_kernel)
-    has_bwd = hasattr(fa, "bwd") and not args.no_bwd
+    has_bwd = hasattr(fa, "bwd") and not args.no_bwd and w.d != 256   # no d = 256 backward
     inp = W.make_inputs(w, with_grad=True)
     t = {n: inp[n].to(dev) for n in ("q", "k", "v", "do")}
     t["o"] = torch.empty_like(t["q"])
@@ -435,7 +436,8 @@ def main_ours(args):
         "config": {"workload": describe(w, r["inp"]),
             "step": step_name, "global_batch": w.B * world, "seq_len": w.N or max(r["inp"]["lengths"]),
             "deterministic_bwd": bool(args.deterministic), "exp2_emu_eighths": args.exp2_emu, "tau": args.tau,
-            "fwd_kernel": ("ping-pong 2x128" if args.exp2_emu or w.d != 128 or (w.varlen and args.fwd_kernel == 1) else
+            "fwd_kernel": ("one 128-row tile, 64-key blocks (d = 256)" if w.d == 256 else
+                           "ping-pong 2x128" if args.exp2_emu or w.d != 128 or (w.varlen and args.fwd_kernel == 1) else
                            {0: "ping-pong 2x128", 1: "256-key blocks", 2: "CTA pairs, 256-key blocks"}[args.fwd_kernel]),
             "fwd_pairs_resident": fa_pairs_resident(),
             "bwd_kernel": ("one CTA per 128-key tile" if w.varlen or args.deterministic or args.bwd_kernel == 0 or w.d != 128
@@ -476,7 +478,7 @@ def main_reference(args):
     from oracle import attention as A
 
     w = W.WORKLOADS[args.workload]
-    with_bwd = not args.no_bwd
+    with_bwd = not args.no_bwd and w.d != 256   # the same step as ours
     inp = W.make_inputs(w, with_grad=True)
 
     def step(s):  # one (sequence, head) slice of the workload per step

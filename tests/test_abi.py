@@ -65,8 +65,9 @@ def test_fwd_rejects_bad_arguments_on_the_host(lib):
     assert call(alpha=0.0) == -1
     assert call(alpha=float("inf")) == -1
     assert call(causal=2) == -1
-    assert call(d=96) == -2            # d is 64 or 128
-    assert call(d=256) == -2
+    assert call(d=96) == -2            # d is 64, 128 or 256
+    assert call(d=512) == -2
+    assert call(d=256, cu=P, ms=128) == -2   # d = 256: fixed length only
     assert call(cu=P, ms=0) == -1      # varlen without max_seqlen
     assert call(cu=P, ms=1 << 20) == -2
     assert call(B=5000, cu=P, ms=128) == -2
@@ -109,4 +110,4 @@ def test_workspace_size_depends_on_head_dim(lib):
     n64, n128 = f(2, 4, 1000, 64, 0, 0), f(2, 4, 1000, 128, 0, 0)
     assert 0 < n64 < n128
     assert n128 - n64 >= 2 * 4 * 1000 * 64 * 4        # B*N*Hq rows of 64 more floats
-    assert f(2, 4, 1000, 96, 0, 0) == 0 and f(2, 4, 1000, 256, 0, 0) == 0
+    assert f(2, 4, 1000, 96, 0, 0) == 0 and f(2, 4, 1000, 256, 0, 0) == 0   # no d = 256 backward
