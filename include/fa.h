@@ -17,9 +17,10 @@
  * ---------------------------------------
  * - Element types: q, k, v, o, do, dq, dk, dv are bfloat16 (raw 16-bit
  *   storage, passed as void*); lse is float32; cu_seqlens is int32.
- * - Head dimension d is 128 or 64 (the pages' balance point moves with d:
- *   FlashAttention-4 paper summary, "Roofline" remarks).  Hq must be a
- *   multiple of Hkv; query head h reads key/value head h / (Hq / Hkv).
+ * - Head dimension d is 128 or 64, or 256 for the fixed-length forward only
+ *   (the pages' balance point moves with d: FlashAttention-4 paper summary,
+ *   "Roofline" remarks).  Hq must be a multiple of Hkv; query head h reads
+ *   key/value head h / (Hq / Hkv).
  * - Fixed-length layout (cu_seqlens == NULL): q, o, do, dq are [B, N, Hq, d]
  *   row-major, k, v, dk, dv are [B, N, Hkv, d]; lse is [B, Hq, N].
  * - Variable-length layout (cu_seqlens != NULL): B sequences packed along
@@ -52,7 +53,7 @@ extern "C" {
 typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID = -1,      /* null pointer, bad size, bad scale           */
-    FA_ERR_UNSUPPORTED = -2,  /* legal but not built: d not 64/128, ...     */
+    FA_ERR_UNSUPPORTED = -2,  /* legal but not built: d not 64/128/256, ... */
     FA_ERR_ALIGN = -3,        /* a tensor is not 16-byte aligned            */
     FA_ERR_LAUNCH = -4,       /* CUDA reported an error at launch           */
     FA_ERR_TIMEOUT = -5,      /* a device-side wait gave up (see status)    */
@@ -134,7 +135,9 @@ int fa_bwd_pairs_resident(void);
  * causal: 0 or 1.  N == 0 (or T == 0) is a no-op returning FA_OK.
  * Errors: FA_ERR_INVALID (null pointer, B<1, N<0, Hq/Hkv<1, Hq % Hkv,
  * alpha not finite and > 0, varlen without max_seqlen>0),
- * FA_ERR_UNSUPPORTED (d not 64 or 128), FA_ERR_ALIGN, FA_ERR_LAUNCH.
+ * FA_ERR_UNSUPPORTED (d not 64, 128 or 256; d = 256 with cu_seqlens),
+ * FA_ERR_ALIGN, FA_ERR_LAUNCH.  d = 256 runs on a kernel of its own (one
+ * 128-row query tile per CTA, 64-key blocks) whatever fa_set_fwd_kernel says.
  */
 int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int Hq, int Hkv, int N, int d, float alpha, int causal,
@@ -145,7 +148,8 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  * D (rowsum(dO*O), fp32), the fp32 dQ accumulator, the deterministic-mode
  * semaphores and the varlen work list.  N is the sequence length (fixed
  * length) or the total token count T (varlen = 1).  Returns 0 for invalid
- * sizes (d not 64 or 128 among them).  About (4 d + 4) * Hq * T bytes.
+ * sizes (d not 64 or 128 among them: there is no d = 256 backward).  About
+ * (4 d + 4) * Hq * T bytes.
  */
 size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, int deterministic, int varlen);
 
