@@ -44,7 +44,7 @@ enum : int { k6QEmpty = 41, k6KEmpty, k6VEmpty, k6QFull, k6KFull, k6VFull, k6S, 
 
 struct Shared256 {
     uint64_t q_full, q_empty, kfull[kKS], kempty[kKS], vfull[kVS], vempty[kVS];
-    uint64_t s_full[2], p_ready, pv_done, o_done, o_free, drain;
+    uint64_t s_full[2], p_ready, pv_done[2], o_done, o_free, drain;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -118,7 +118,8 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         mbar_init(&sh.s_full[0], 1);
         mbar_init(&sh.s_full[1], 1);
         mbar_init(&sh.p_ready, 128);
-        mbar_init(&sh.pv_done, 1);
+        mbar_init(&sh.pv_done[0], 1);
+        mbar_init(&sh.pv_done[1], 1);
         mbar_init(&sh.o_done, 1);
         mbar_init(&sh.o_free, 128);
         mbar_init(&sh.drain, 1);
@@ -211,7 +212,7 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 tc_fence_after();
                 issue_pv(tmem + kColO, tmem + kColS + 64 * (gp & 1), sV + vs * kKVBytes, j > 0);
                 umma_commit_w(&sh.vempty[vs]);
-                umma_commit_w(&sh.pv_done);
+                umma_commit_w(&sh.pv_done[gp & 1]);
                 ++gp;
                 // S of block j + 2 into the region P of block j was just read from.
                 if (j + 2 < U.nb && !(ok = issue_s_block(j + 3 == U.nb))) break;
@@ -230,7 +231,7 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         const uint32_t lane_bits = (uint32_t)(warp * 32) << 16;
         const uint32_t tO = tmem + lane_bits + kColO;
         const float scale = a.scale_log2;
-        uint32_t gs = 0, pvc = 0, uc = 0;
+        uint32_t gs = 0, uc = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok; u += gridDim.x) {
             Unit256 U;
@@ -238,8 +239,9 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             const int q_first = U.m * kTileM, qi = q_first + r;
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < U.nb; ++j) {
-                const uint32_t tS = tmem + lane_bits + kColS + 64 * (gs & 1);
-                if (!(ok = mbar_wait(&sh.s_full[gs & 1], (gs >> 1) & 1, wc, k6S))) break;
+                const uint32_t g = gs;   // this block's global index (S and P V alike)
+                const uint32_t tS = tmem + lane_bits + kColS + 64 * (g & 1);
+                if (!(ok = mbar_wait(&sh.s_full[g & 1], (g >> 1) & 1, wc, k6S))) break;
                 ++gs;
                 tc_fence_after();
                 float s[kBlk];
@@ -267,13 +269,6 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                     mx3 = fmaxf(mx3, s[c + 3]);
                 }
                 const float m_new = fmaxf(m_ref, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale);
-                // The previous block's P V must be done before O is touched;
-                // every phase is waited for, in order.
-                if (j > 0) {
-                    if (!(ok = mbar_wait(&sh.pv_done, pvc & 1, wc, k6PV))) break;
-                    ++pvc;
-                    tc_fence_after();
-                }
                 // Conditional rescale (blog, "Forward pass"): move to the new
                 // maximum only when some row of this warp jumped by more than tau.
                 const bool jump = (m_ref == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_ref > a.tau);
@@ -281,6 +276,14 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                     const float fac = (m_ref == -INFINITY) ? 0.f : ex2_mufu(m_ref - m_new);
                     l *= fac;
                     if (j > 0) {
+                        // O is touched only after the previous block's P V is
+                        // done.  Its barrier (of two, alternating) has at that
+                        // point completed every earlier phase -- S of block g-1,
+                        // observed, was issued after P V g-3 -- and cannot have
+                        // completed the next one (P V g+1 needs this block's P),
+                        // so the parity identifies the phase.
+                        if (!(ok = mbar_wait(&sh.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, wc, k6PV))) break;
+                        tc_fence_after();
 #pragma unroll 1
                         for (int c0 = 0; c0 < kD; c0 += 32) {
                             uint32_t o[32];
@@ -317,7 +320,6 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             // Epilogue: O / l -> bf16, LSE = (m + log2 l) ln 2.
             if (!(ok = mbar_wait(&sh.o_done, uc & 1, wc, k6O))) break;
             ++uc;
-            ++pvc;   // the unit's last P V phase, covered by o_done
             tc_fence_after();
             const bool valid = qi < U.len;
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
