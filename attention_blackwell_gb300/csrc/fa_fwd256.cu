@@ -11,7 +11,9 @@
 //   warps 0-3  softmax: one thread per query row (TMEM lane), 64 scores per
 //              block; conditional rescale of its O row (tau), P as bf16 into
 //              tensor memory over the scores it read, the epilogue;
-//   warp  4    TMA loader: Q once per unit, then a K ring and a V ring;
+//   warp  4    TMA loader: Q once per unit, then K and V blocks through one
+//              ring in the order the products read them (K0, K1, V0, K2,
+//              V1, K3, ...), so a K block is requested ~2.5 blocks ahead;
 //   warp  5    UMMA issuer: S = Q K^T (M 128, N 64, K 256: 16 steps) and
 //              O += P V (M 128, N 256, K 64: 4 steps, P from tensor memory).
 //
@@ -21,8 +23,8 @@
 // read by the P V of block j before S of block j+2 is written there -- the
 // issuer emits both, in that order).
 //
-// Shared memory: Q 64 KB (four 128-row x 64-column boxes), K ring 2 x 32 KB
-// and V ring 2 x 32 KB (four 64-row x 64-column boxes each).
+// Shared memory: Q 64 KB (four 128-row x 64-column boxes) and a ring of five
+// 32 KB slots, each one 64-key block of K or V (four 64-row x 64-column boxes).
 #include "fa_internal.h"
 
 namespace fa {
@@ -31,19 +33,19 @@ namespace {
 constexpr int kD = 256;
 constexpr int kBlk = 64;                         // keys per block
 constexpr int kThreads256 = 192;
-constexpr int kKS = 2, kVS = 2;
+constexpr int kRing = 5;                         // K and V blocks in consumption order
 constexpr uint32_t kQBox = 16384;                // 128 rows x 128 B
 constexpr uint32_t kKVBox = 8192;                // 64 rows x 128 B
 constexpr uint32_t kQBytes = 4 * kQBox, kKVBytes = 4 * kKVBox;
-constexpr uint32_t kOffQ = 0, kOffK = kQBytes, kOffV = kOffK + kKS * kKVBytes;
-constexpr uint32_t kSmem256 = 1024 + kOffV + kVS * kKVBytes;   // + alignment slack
+constexpr uint32_t kOffQ = 0, kOffR = kQBytes;
+constexpr uint32_t kSmem256 = 1024 + kOffR + kRing * kKVBytes;   // + alignment slack
 static_assert(kSmem256 <= 232448, "shared memory plan");
 constexpr uint32_t kColO = 0, kColS = 256;
 
 enum : int { k6QEmpty = 41, k6KEmpty, k6VEmpty, k6QFull, k6KFull, k6VFull, k6S, k6P, k6PV, k6O, k6OFree };
 
 struct Shared256 {
-    uint64_t q_full, q_empty, kfull[kKS], kempty[kKS], vfull[kVS], vempty[kVS];
+    uint64_t q_full, q_empty, full[kRing], empty[kRing];
     uint64_t s_full[2], p_ready, pv_done[2], o_done, o_free, drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -108,13 +110,12 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     __shared__ Shared256 sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
-    const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
+    const uint32_t sQ = base + kOffQ, sR = base + kOffR;
 
     if (tid == 0) {
         mbar_init(&sh.q_full, 1);
         mbar_init(&sh.q_empty, 1);
-        for (int i = 0; i < kKS; ++i) { mbar_init(&sh.kfull[i], 1); mbar_init(&sh.kempty[i], 1); }
-        for (int i = 0; i < kVS; ++i) { mbar_init(&sh.vfull[i], 1); mbar_init(&sh.vempty[i], 1); }
+        for (int i = 0; i < kRing; ++i) { mbar_init(&sh.full[i], 1); mbar_init(&sh.empty[i], 1); }
         mbar_init(&sh.s_full[0], 1);
         mbar_init(&sh.s_full[1], 1);
         mbar_init(&sh.p_ready, 128);
@@ -146,8 +147,18 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     if (warp == 4) {
         // ---------------------------------------------------------------- loader
         if (lane == 0) {
-            uint32_t kit = 0, vit = 0, uc = 0;
+            uint32_t it = 0, uc = 0;
             bool ok = true;
+            // One block of K or V (64 keys x 256) into the next ring slot.
+            auto load = [&](const CUtensorMap* m, int hk, int row) -> bool {
+                const uint32_t rs = it % kRing;
+                if (!mbar_wait(&sh.empty[rs], ((it / kRing) & 1) ^ 1, wc, k6KEmpty)) return false;
+                mbar_arrive_expect_tx(&sh.full[rs], kKVBytes);
+                for (int c = 0; c < 4; ++c)
+                    tma_load_3d(sR + rs * kKVBytes + c * kKVBox, m, &sh.full[rs], c * 64, hk, row);
+                ++it;
+                return true;
+            };
             for (int u = blockIdx.x; ok; u += gridDim.x) {
                 Unit256 U;
                 if (!unit256(a, u, U)) break;
@@ -156,43 +167,35 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 mbar_arrive_expect_tx(&sh.q_full, kQBytes);
                 for (int c = 0; c < 4; ++c)
                     tma_load_3d(sQ + c * kQBox, &tq, &sh.q_full, c * 64, U.h, U.tok0 + U.m * kTileM);
+                // The issuer's order: K0, K1, then V j followed by K j+2.
+                if (!(ok = load(&tk, hk, U.tok0))) break;
+                if (U.nb > 1 && !(ok = load(&tk, hk, U.tok0 + kBlk))) break;
                 for (int j = 0; j < U.nb && ok; ++j) {
-                    const uint32_t ks = kit % kKS, vs = vit % kVS;
-                    if (!(ok = mbar_wait(&sh.kempty[ks], ((kit / kKS) & 1) ^ 1, wc, k6KEmpty))) break;
-                    mbar_arrive_expect_tx(&sh.kfull[ks], kKVBytes);
-                    for (int c = 0; c < 4; ++c)
-                        tma_load_3d(sK + ks * kKVBytes + c * kKVBox, &tk, &sh.kfull[ks], c * 64, hk, U.tok0 + j * kBlk);
-                    ++kit;
-                    if (!(ok = mbar_wait(&sh.vempty[vs], ((vit / kVS) & 1) ^ 1, wc, k6VEmpty))) break;
-                    mbar_arrive_expect_tx(&sh.vfull[vs], kKVBytes);
-                    for (int c = 0; c < 4; ++c)
-                        tma_load_3d(sV + vs * kKVBytes + c * kKVBox, &tv, &sh.vfull[vs], c * 64, hk, U.tok0 + j * kBlk);
-                    ++vit;
+                    if (!(ok = load(&tv, hk, U.tok0 + j * kBlk))) break;
+                    if (j + 2 < U.nb && !(ok = load(&tk, hk, U.tok0 + (j + 2) * kBlk))) break;
                 }
                 ++uc;
             }
             // Every copy this thread issued lands before teardown.
             const uint64_t t0 = globaltimer_ns();
-            for (uint32_t i = (kit > kKS ? kit - kKS : 0); i < kit; ++i)
-                while (!mbar_try_wait(smem_u32(&sh.kfull[i % kKS]), (i / kKS) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
-            for (uint32_t i = (vit > kVS ? vit - kVS : 0); i < vit; ++i)
-                while (!mbar_try_wait(smem_u32(&sh.vfull[i % kVS]), (i / kVS) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+            for (uint32_t i = (it > kRing ? it - kRing : 0); i < it; ++i)
+                while (!mbar_try_wait(smem_u32(&sh.full[i % kRing]), (i / kRing) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
             if (uc > 0)
                 while (!mbar_try_wait(smem_u32(&sh.q_full), (uc - 1) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
         }
         __syncwarp();
     } else if (warp == 5) {
         // ---------------------------------------------------------- UMMA issuer
-        uint32_t kit = 0, vit = 0, uc = 0, gs = 0, gp = 0;   // K, V slots; S and P V blocks so far
+        uint32_t it = 0, uc = 0, gs = 0, gp = 0;   // ring slots taken; S and P V blocks so far
         bool ok = true;
         auto issue_s_block = [&](bool last_of_unit) -> bool {
-            const uint32_t ks = kit % kKS;
-            if (!mbar_wait_w(&sh.kfull[ks], (kit / kKS) & 1, wc, k6KFull)) return false;
-            ++kit;
+            const uint32_t ks = it % kRing;
+            if (!mbar_wait_w(&sh.full[ks], (it / kRing) & 1, wc, k6KFull)) return false;
+            ++it;
             tc_fence_after();
-            issue_s(tmem + kColS + 64 * (gs & 1), sQ, sK + ks * kKVBytes);
+            issue_s(tmem + kColS + 64 * (gs & 1), sQ, sR + ks * kKVBytes);
             umma_commit_w(&sh.s_full[gs & 1]);
-            umma_commit_w(&sh.kempty[ks]);
+            umma_commit_w(&sh.empty[ks]);
             if (last_of_unit) umma_commit_w(&sh.q_empty);   // Q read by the unit's last S
             ++gs;
             return true;
@@ -206,12 +209,12 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             for (int j = 0; j < U.nb; ++j) {
                 if (!(ok = mbar_wait_w(&sh.p_ready, gp & 1, wc, k6P))) break;
                 if (j == 0 && uc > 0 && !(ok = mbar_wait_w(&sh.o_free, (uc - 1) & 1, wc, k6OFree))) break;
-                const uint32_t vs = vit % kVS;
-                if (!(ok = mbar_wait_w(&sh.vfull[vs], (vit / kVS) & 1, wc, k6VFull))) break;
-                ++vit;
+                const uint32_t vs = it % kRing;
+                if (!(ok = mbar_wait_w(&sh.full[vs], (it / kRing) & 1, wc, k6VFull))) break;
+                ++it;
                 tc_fence_after();
-                issue_pv(tmem + kColO, tmem + kColS + 64 * (gp & 1), sV + vs * kKVBytes, j > 0);
-                umma_commit_w(&sh.vempty[vs]);
+                issue_pv(tmem + kColO, tmem + kColS + 64 * (gp & 1), sR + vs * kKVBytes, j > 0);
+                umma_commit_w(&sh.empty[vs]);
                 umma_commit_w(&sh.pv_done[gp & 1]);
                 ++gp;
                 // S of block j + 2 into the region P of block j was just read from.
