@@ -10,21 +10,30 @@
 //
 //   warps 0-3  softmax: one thread per query row (TMEM lane), 64 scores per
 //              block; conditional rescale of its O row (tau), P as bf16 into
-//              tensor memory over the scores it read, the epilogue;
-//   warp  4    TMA loader: Q once per unit, then K and V blocks through one
-//              ring in the order the products read them (K0, K1, V0, K2,
-//              V1, K3, ...), so a K block is requested ~2.5 blocks ahead;
-//   warp  5    UMMA issuer: S = Q K^T (M 128, N 64, K 256: 16 steps) and
-//              O += P V (M 128, N 256, K 64: 4 steps, P from tensor memory).
+//              tensor memory over the scores it read, the epilogue; between
+//              units, the copy of the next query tile from shared into
+//              tensor memory;
+//   warp  4    TMA loader: K and V blocks through one ring in the order the
+//              products read them (K0, K1, V0, K2, V1, K3, ...), so a K block
+//              is requested ~2.5 blocks ahead; the next unit's Q after this
+//              unit's K0 and K1;
+//   warp  5    UMMA issuer: S = Q K^T (M 128, N 64, K 256: 16 steps, Q from
+//              tensor memory) and O += P V (M 128, N 256, K 64: 4 steps, P
+//              from tensor memory).
 //
 // Tensor memory (512 columns): O 0-255; S/P of block j in 256 + 64 (j % 2)
 // (two regions, so S of block j+1 is computed while the softmax of block j
 // runs; P of block j overwrites the first 32 columns of its region and is
 // read by the P V of block j before S of block j+2 is written there -- the
-// issuer emits both, in that order).
+// issuer emits both, in that order); the query tile, bf16 pairs, in 384-511.
+// With Q in tensor memory an S step reads only its 2 KB of K from shared
+// memory: a 128 x 64 x 16 product with both operands in shared memory reads
+// 6 KB and runs at two thirds of the tensor rate, bound by shared-memory
+// bandwidth (measured on GB300: 48 instead of 32 cycles).
 //
-// Shared memory: Q 64 KB (four 128-row x 64-column boxes) and a ring of five
-// 32 KB slots, each one 64-key block of K or V (four 64-row x 64-column boxes).
+// Shared memory: a 64 KB landing area for Q (four 128-row x 64-column boxes)
+// and a ring of five 32 KB slots, each one 64-key block of K or V (four 64-row
+// x 64-column boxes).
 #include "fa_internal.h"
 
 namespace fa {
@@ -40,13 +49,13 @@ constexpr uint32_t kQBytes = 4 * kQBox, kKVBytes = 4 * kKVBox;
 constexpr uint32_t kOffQ = 0, kOffR = kQBytes;
 constexpr uint32_t kSmem256 = 1024 + kOffR + kRing * kKVBytes;   // + alignment slack
 static_assert(kSmem256 <= 232448, "shared memory plan");
-constexpr uint32_t kColO = 0, kColS = 256;
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;
 
 enum : int { k6QEmpty = 41, k6KEmpty, k6VEmpty, k6QFull, k6KFull, k6VFull, k6S, k6P, k6PV, k6O, k6OFree };
 
 struct Shared256 {
     uint64_t q_full, q_empty, full[kRing], empty[kRing];
-    uint64_t s_full[2], p_ready, pv_done[2], o_done, o_free, drain;
+    uint64_t qt_full, s_full[2], p_ready, pv_done[2], o_done, o_free, drain;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -81,13 +90,13 @@ __device__ __forceinline__ bool unit256(const FwdArgs& a, int u, Unit256& U) {
 
 // S = Q K^T: both K-major; k-step k (16 of the 256 head-dim columns) is box
 // k / 4, bytes (k % 4) * 32 of each 128-byte row.
-__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_tmem, uint32_t k_smem) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, kBlk, 0, 0);
-    const uint64_t qd = sdesc_sw128(q_smem, 16, 1024), kd = sdesc_sw128(k_smem, 16, 1024);
+    const uint64_t kd = sdesc_sw128(k_smem, 16, 1024);
     static_for<16>([&](auto kc) {
         constexpr uint32_t k = kc;
-        constexpr uint32_t ao = ((k >> 2) * kQBox + (k & 3) * 32) >> 4, bo = ((k >> 2) * kKVBox + (k & 3) * 32) >> 4;
-        umma_ss_k<ao, bo>(d_tmem, qd, kd, idesc, k > 0);
+        constexpr uint32_t bo = ((k >> 2) * kKVBox + (k & 3) * 32) >> 4;
+        umma_ts_k<k * 8, bo>(d_tmem, q_tmem, kd, idesc, k > 0);
     });
 }
 
@@ -114,7 +123,8 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 
     if (tid == 0) {
         mbar_init(&sh.q_full, 1);
-        mbar_init(&sh.q_empty, 1);
+        mbar_init(&sh.q_empty, 128);
+        mbar_init(&sh.qt_full, 128);
         for (int i = 0; i < kRing; ++i) { mbar_init(&sh.full[i], 1); mbar_init(&sh.empty[i], 1); }
         mbar_init(&sh.s_full[0], 1);
         mbar_init(&sh.s_full[1], 1);
@@ -147,7 +157,7 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
     if (warp == 4) {
         // ---------------------------------------------------------------- loader
         if (lane == 0) {
-            uint32_t it = 0, uc = 0;
+            uint32_t it = 0, qc = 0;
             bool ok = true;
             // One block of K or V (64 keys x 256) into the next ring slot.
             auto load = [&](const CUtensorMap* m, int hk, int row) -> bool {
@@ -159,53 +169,63 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 ++it;
                 return true;
             };
-            for (int u = blockIdx.x; ok; u += gridDim.x) {
-                Unit256 U;
-                if (!unit256(a, u, U)) break;
-                const int hk = U.h / group;
-                if (!(ok = mbar_wait(&sh.q_empty, (uc & 1) ^ 1, wc, k6QEmpty))) break;
+            auto load_q = [&](const Unit256& U) -> bool {
+                if (!mbar_wait(&sh.q_empty, (qc & 1) ^ 1, wc, k6QEmpty)) return false;
                 mbar_arrive_expect_tx(&sh.q_full, kQBytes);
                 for (int c = 0; c < 4; ++c)
                     tma_load_3d(sQ + c * kQBox, &tq, &sh.q_full, c * 64, U.h, U.tok0 + U.m * kTileM);
-                // The issuer's order: K0, K1, then V j followed by K j+2.
+                ++qc;
+                return true;
+            };
+            {
+                Unit256 U;
+                if (unit256(a, blockIdx.x, U)) ok = load_q(U);
+            }
+            for (int u = blockIdx.x; ok; u += gridDim.x) {
+                Unit256 U, Un;
+                if (!unit256(a, u, U)) break;
+                const int hk = U.h / group;
+                // The issuer's order: K0, K1, then V j followed by K j+2; Q of
+                // the next unit goes out early (its slot is free once this
+                // unit's Q is in tensor memory).
                 if (!(ok = load(&tk, hk, U.tok0))) break;
                 if (U.nb > 1 && !(ok = load(&tk, hk, U.tok0 + kBlk))) break;
+                if (unit256(a, u + gridDim.x, Un) && !(ok = load_q(Un))) break;
                 for (int j = 0; j < U.nb && ok; ++j) {
                     if (!(ok = load(&tv, hk, U.tok0 + j * kBlk))) break;
                     if (j + 2 < U.nb && !(ok = load(&tk, hk, U.tok0 + (j + 2) * kBlk))) break;
                 }
-                ++uc;
             }
             // Every copy this thread issued lands before teardown.
             const uint64_t t0 = globaltimer_ns();
             for (uint32_t i = (it > kRing ? it - kRing : 0); i < it; ++i)
                 while (!mbar_try_wait(smem_u32(&sh.full[i % kRing]), (i / kRing) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
-            if (uc > 0)
-                while (!mbar_try_wait(smem_u32(&sh.q_full), (uc - 1) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+            if (qc > 0)
+                while (!mbar_try_wait(smem_u32(&sh.q_full), (qc - 1) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {}
         }
         __syncwarp();
     } else if (warp == 5) {
         // ---------------------------------------------------------- UMMA issuer
         uint32_t it = 0, uc = 0, gs = 0, gp = 0;   // ring slots taken; S and P V blocks so far
         bool ok = true;
-        auto issue_s_block = [&](bool last_of_unit) -> bool {
+        auto issue_s_block = [&]() -> bool {
             const uint32_t ks = it % kRing;
             if (!mbar_wait_w(&sh.full[ks], (it / kRing) & 1, wc, k6KFull)) return false;
             ++it;
             tc_fence_after();
-            issue_s(tmem + kColS + 64 * (gs & 1), sQ, sR + ks * kKVBytes);
+            issue_s(tmem + kColS + 64 * (gs & 1), tmem + kColQ, sR + ks * kKVBytes);
             umma_commit_w(&sh.s_full[gs & 1]);
             umma_commit_w(&sh.empty[ks]);
-            if (last_of_unit) umma_commit_w(&sh.q_empty);   // Q read by the unit's last S
             ++gs;
             return true;
         };
         for (int u = blockIdx.x; ok; u += gridDim.x) {
             Unit256 U;
             if (!unit256(a, u, U)) break;
-            if (!(ok = mbar_wait_w(&sh.q_full, uc & 1, wc, k6QFull))) break;
-            if (!(ok = issue_s_block(U.nb == 1))) break;
-            if (U.nb > 1 && !(ok = issue_s_block(U.nb == 2))) break;
+            if (!(ok = mbar_wait_w(&sh.qt_full, uc & 1, wc, k6QFull))) break;
+            tc_fence_after();
+            if (!(ok = issue_s_block())) break;
+            if (U.nb > 1 && !(ok = issue_s_block())) break;
             for (int j = 0; j < U.nb; ++j) {
                 if (!(ok = mbar_wait_w(&sh.p_ready, gp & 1, wc, k6P))) break;
                 if (j == 0 && uc > 0 && !(ok = mbar_wait_w(&sh.o_free, (uc - 1) & 1, wc, k6OFree))) break;
@@ -218,7 +238,7 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 umma_commit_w(&sh.pv_done[gp & 1]);
                 ++gp;
                 // S of block j + 2 into the region P of block j was just read from.
-                if (j + 2 < U.nb && !(ok = issue_s_block(j + 3 == U.nb))) break;
+                if (j + 2 < U.nb && !(ok = issue_s_block())) break;
             }
             if (!ok) break;
             umma_commit_w(&sh.o_done);
@@ -234,10 +254,37 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         const uint32_t lane_bits = (uint32_t)(warp * 32) << 16;
         const uint32_t tO = tmem + lane_bits + kColO;
         const float scale = a.scale_log2;
-        uint32_t gs = 0, uc = 0;
+        uint32_t gs = 0, uc = 0, qc = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok; u += gridDim.x) {
+        // This row of the next unit's Q tile, shared memory (128 B per row and
+        // 64-column box, 16-byte chunks swizzled by row % 8) -> tensor memory
+        // columns kColQ + 0..127 (bf16 pairs, the A operand of S).
+        auto copy_q = [&]() -> bool {
+            if (!mbar_wait(&sh.q_full, qc & 1, wc, k6QFull)) return false;
+            ++qc;
+#pragma unroll 1
+            for (int b = 0; b < 4; ++b) {
+                uint32_t v[32];
+                const uint32_t row = sQ + b * kQBox + r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(v[4 * c]), "=r"(v[4 * c + 1]), "=r"(v[4 * c + 2]), "=r"(v[4 * c + 3])
+                                 : "r"(row + ((c ^ (r & 7)) << 4)) : "memory");
+                tmem_st32(tmem + lane_bits + kColQ + 32 * b, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&sh.q_empty);
+            mbar_arrive(&sh.qt_full);
+            return true;
+        };
+        {
             Unit256 U;
+            if (unit256(a, blockIdx.x, U)) ok = copy_q();
+        }
+        for (int u = blockIdx.x; ok; u += gridDim.x) {
+            Unit256 U, Un;
             if (!unit256(a, u, U)) break;
             const int q_first = U.m * kTileM, qi = q_first + r;
             float m_ref = -INFINITY, l = 0.f;
@@ -320,6 +367,8 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 mbar_arrive(&sh.p_ready);
             }
             if (!ok) break;
+            // Every S of this unit has been read: its Q columns take the next tile.
+            if (unit256(a, u + gridDim.x, Un) && !(ok = copy_q())) break;
             // Epilogue: O / l -> bf16, LSE = (m + log2 l) ln 2.
             if (!(ok = mbar_wait(&sh.o_done, uc & 1, wc, k6O))) break;
             ++uc;
