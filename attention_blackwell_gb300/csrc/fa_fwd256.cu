@@ -55,7 +55,7 @@ enum : int { k6QEmpty = 41, k6KEmpty, k6VEmpty, k6QFull, k6KFull, k6VFull, k6S, 
 
 struct Shared256 {
     uint64_t q_full, q_empty, full[kRing], empty[kRing];
-    uint64_t qt_full, s_full[2], p_ready, pv_done[2], o_done, o_free, drain;
+    uint64_t qt_full, s_full[2], p_ready[2], pv_done[2], o_done, o_free, drain;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -128,7 +128,8 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         for (int i = 0; i < kRing; ++i) { mbar_init(&sh.full[i], 1); mbar_init(&sh.empty[i], 1); }
         mbar_init(&sh.s_full[0], 1);
         mbar_init(&sh.s_full[1], 1);
-        mbar_init(&sh.p_ready, 128);
+        mbar_init(&sh.p_ready[0], 128);
+        mbar_init(&sh.p_ready[1], 128);
         mbar_init(&sh.pv_done[0], 1);
         mbar_init(&sh.pv_done[1], 1);
         mbar_init(&sh.o_done, 1);
@@ -227,11 +228,14 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             if (!(ok = issue_s_block())) break;
             if (U.nb > 1 && !(ok = issue_s_block())) break;
             for (int j = 0; j < U.nb; ++j) {
-                if (!(ok = mbar_wait_w(&sh.p_ready, gp & 1, wc, k6P))) break;
-                if (j == 0 && uc > 0 && !(ok = mbar_wait_w(&sh.o_free, (uc - 1) & 1, wc, k6OFree))) break;
                 const uint32_t vs = it % kRing;
                 if (!(ok = mbar_wait_w(&sh.full[vs], (it / kRing) & 1, wc, k6VFull))) break;
                 ++it;
+                if (j == 0 && uc > 0 && !(ok = mbar_wait_w(&sh.o_free, (uc - 1) & 1, wc, k6OFree))) break;
+                // P of block gp.  Two barriers, alternating: the softmax can
+                // finish block gp + 1 (its S was issued above) before this
+                // wait, never block gp + 2 (its S comes after this P V).
+                if (!(ok = mbar_wait_w(&sh.p_ready[gp & 1], (gp >> 1) & 1, wc, k6P))) break;
                 tc_fence_after();
                 issue_pv(tmem + kColO, tmem + kColS + 64 * (gp & 1), sR + vs * kKVBytes, j > 0);
                 umma_commit_w(&sh.empty[vs]);
@@ -254,6 +258,7 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         const uint32_t lane_bits = (uint32_t)(warp * 32) << 16;
         const uint32_t tO = tmem + lane_bits + kColO;
         const float scale = a.scale_log2;
+        const bool o32 = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0;
         uint32_t gs = 0, uc = 0, qc = 0;
         bool ok = true;
         // This row of the next unit's Q tile, shared memory (128 B per row and
@@ -364,7 +369,7 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 l += l0 + l1;
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(&sh.p_ready);
+                mbar_arrive(&sh.p_ready[g & 1]);
             }
             if (!ok) break;
             // Every S of this unit has been read: its Q columns take the next tile.
@@ -383,11 +388,24 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 tmem_ld32(tO + c0, o);
                 tmem_wait_ld();
                 if (valid) {
+                    if (o32) {   // whole 32-byte sectors
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float* f = reinterpret_cast<const float*>(o + 8 * q);
-                        orow[c0 / 8 + q] = make_uint4(pack_bf16x2(f[0] * inv_l, f[1] * inv_l), pack_bf16x2(f[2] * inv_l, f[3] * inv_l),
-                                                      pack_bf16x2(f[4] * inv_l, f[5] * inv_l), pack_bf16x2(f[6] * inv_l, f[7] * inv_l));
+                        for (int q = 0; q < 2; ++q) {
+                            const float* f = reinterpret_cast<const float*>(o + 16 * q);
+                            uint32_t w[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) w[e] = pack_bf16x2(f[2 * e] * inv_l, f[2 * e + 1] * inv_l);
+                            asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                                         :: "l"(orow + c0 / 8 + 2 * q), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]),
+                                            "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]) : "memory");
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float* f = reinterpret_cast<const float*>(o + 8 * q);
+                            orow[c0 / 8 + q] = make_uint4(pack_bf16x2(f[0] * inv_l, f[1] * inv_l), pack_bf16x2(f[2] * inv_l, f[3] * inv_l),
+                                                          pack_bf16x2(f[4] * inv_l, f[5] * inv_l), pack_bf16x2(f[6] * inv_l, f[7] * inv_l));
+                        }
                     }
                 }
             }
