@@ -74,7 +74,9 @@ int fa_num_sms(void);
  *     (0, 1 or 2; FlashAttention-4 paper summary §3.1.3 uses 10-25 %).
  *   tau: conditional-rescale threshold in log2 units, 0 <= tau <= 64
  *     (default log2(256) = 8; tau = 0 rescales whenever the max grows).
- * Every setting gives the same attention up to rounding.  Not thread-safe
+ * At d = 256 only tau applies: that forward evaluates every exponential on
+ * MUFU (its exponentials are off the critical path; the products set the
+ * pace).  Every setting gives the same attention up to rounding.  Not thread-safe
  * with concurrent fa_fwd calls.  Errors: FA_ERR_UNSUPPORTED, FA_ERR_INVALID.
  */
 int fa_set_tuning(int exp2_emu_eighths, float tau);
