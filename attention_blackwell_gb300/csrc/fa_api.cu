@@ -152,7 +152,6 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
         if (max_seqlen < 1) return FA_ERR_INVALID;
         if (B > kMaxVarlenSeqs || (max_seqlen + kUnitRows - 1) / kUnitRows > kMaxUnitLevels)
             return FA_ERR_UNSUPPORTED;
-        if (d == 256) return FA_ERR_UNSUPPORTED;   // the d = 256 kernel takes fixed-length inputs
     }
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA_ERR_ALIGN;
     if (varlen && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FA_ERR_ALIGN;

@@ -6,7 +6,7 @@
 // summary, roofline remarks: the balance point moves with d).  At d = 256 a
 // 128-row tile of Q, K or V is 64 KB, so the layout differs from the d = 128
 // kernels: one CTA per SM owns one 128-row query tile at a time and streams
-// 64-key blocks of K and V.
+// 64-key blocks of K and V.  Fixed-length and packed variable-length inputs.
 //
 //   warps 0-3  softmax: one thread per query row (TMEM lane), 64 scores per
 //              block; conditional rescale of its O row (tau), P as bf16 into
@@ -64,9 +64,17 @@ struct Unit256 {
     int seq, h, m, tok0, len, nb;
 };
 
-// Unit u: one 128-row query tile of one (batch, head).  Non-causal:
-// (batch, head) major; causal: query tiles from the last (longest first),
-// (batch, head) minor.
+// Blocks of 64 keys a query tile visits: all of its sequence's, or under the
+// causal mask those holding keys up to the tile's last row.
+__device__ __forceinline__ void set_blocks(const FwdArgs& a, Unit256& U) {
+    const int all = (U.len + kBlk - 1) / kBlk;
+    const int diag = (U.m * kTileM + kTileM - 1) / kBlk + 1;
+    U.nb = a.causal && diag < all ? diag : all;
+}
+
+// Fixed length, unit u: one 128-row query tile of one (batch, head).
+// Non-causal: (batch, head) major; causal: query tiles from the last
+// (longest first), (batch, head) minor.
 __device__ __forceinline__ bool unit256(const FwdArgs& a, int u, Unit256& U) {
     const int nm = (a.N + kTileM - 1) / kTileM, bh_all = a.B * a.Hq;
     if (u < 0 || u >= bh_all * nm) return false;
@@ -82,11 +90,49 @@ __device__ __forceinline__ bool unit256(const FwdArgs& a, int u, Unit256& U) {
     U.h = bh - U.seq * a.Hq;
     U.tok0 = U.seq * a.N;
     U.len = a.N;
-    const int all = (U.len + kBlk - 1) / kBlk;
-    const int diag = (U.m * kTileM + kTileM - 1) / kBlk + 1;   // blocks holding keys <= the tile's last row
-    U.nb = a.causal && diag < all ? diag : all;
+    set_blocks(a, U);
     return true;
 }
+
+// Units of packed variable-length sequences (cu_seqlens).  Level k holds
+// every sequence's k-th query tile counted from its last one (under the
+// causal mask the last tile is the most expensive, so the costliest units
+// come first); within a level, sequences in order, heads minor.  Each role
+// asks for its units in non-decreasing order, so one cursor per thread walks
+// the levels and sequences once: O(levels x B) reads of cu_seqlens per CTA.
+struct Walk256 {
+    int k = -1, lvl_start = 0, lvl_count = 0, b = 0, idx_b = 0;
+
+    __device__ __forceinline__ static int tiles(const FwdArgs& a, int s) {
+        return (a.cu_seqlens[s + 1] - a.cu_seqlens[s] + kTileM - 1) / kTileM;
+    }
+    __device__ bool get(const FwdArgs& a, int u, Unit256& U) {
+        if (!a.varlen) return unit256(a, u, U);
+        if (u < 0) return false;
+        while (k < 0 || u >= lvl_start + lvl_count) {
+            lvl_start += lvl_count;
+            ++k;
+            int n = 0;
+            for (int s = 0; s < a.B; ++s) n += tiles(a, s) > k;
+            lvl_count = n * a.Hq;
+            if (n == 0) return false;                    // past the last level
+            for (b = 0; tiles(a, b) <= k; ++b) {}
+            idx_b = 0;
+        }
+        const int i = u - lvl_start;
+        while (i >= idx_b + a.Hq) {                      // a later sequence of this level
+            idx_b += a.Hq;
+            do ++b; while (tiles(a, b) <= k);
+        }
+        U.seq = b;
+        U.h = i - idx_b;
+        U.tok0 = a.cu_seqlens[b];
+        U.len = a.cu_seqlens[b + 1] - U.tok0;
+        U.m = (U.len + kTileM - 1) / kTileM - 1 - k;
+        set_blocks(a, U);
+        return true;
+    }
+};
 
 // S = Q K^T: both K-major; k-step k (16 of the 256 head-dim columns) is box
 // k / 4, bytes (k % 4) * 32 of each 128-byte row.
@@ -178,20 +224,21 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 ++qc;
                 return true;
             };
+            Walk256 walk;
             {
                 Unit256 U;
-                if (unit256(a, blockIdx.x, U)) ok = load_q(U);
+                if (walk.get(a, blockIdx.x, U)) ok = load_q(U);
             }
             for (int u = blockIdx.x; ok; u += gridDim.x) {
                 Unit256 U, Un;
-                if (!unit256(a, u, U)) break;
+                if (!walk.get(a, u, U)) break;
                 const int hk = U.h / group;
                 // The issuer's order: K0, K1, then V j followed by K j+2; Q of
                 // the next unit goes out early (its slot is free once this
                 // unit's Q is in tensor memory).
                 if (!(ok = load(&tk, hk, U.tok0))) break;
                 if (U.nb > 1 && !(ok = load(&tk, hk, U.tok0 + kBlk))) break;
-                if (unit256(a, u + gridDim.x, Un) && !(ok = load_q(Un))) break;
+                if (walk.get(a, u + gridDim.x, Un) && !(ok = load_q(Un))) break;
                 for (int j = 0; j < U.nb && ok; ++j) {
                     if (!(ok = load(&tv, hk, U.tok0 + j * kBlk))) break;
                     if (j + 2 < U.nb && !(ok = load(&tk, hk, U.tok0 + (j + 2) * kBlk))) break;
@@ -220,9 +267,10 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             ++gs;
             return true;
         };
+        Walk256 walk;
         for (int u = blockIdx.x; ok; u += gridDim.x) {
             Unit256 U;
-            if (!unit256(a, u, U)) break;
+            if (!walk.get(a, u, U)) break;
             if (!(ok = mbar_wait_w(&sh.qt_full, uc & 1, wc, k6QFull))) break;
             tc_fence_after();
             if (!(ok = issue_s_block())) break;
@@ -284,13 +332,14 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             mbar_arrive(&sh.qt_full);
             return true;
         };
+        Walk256 walk;
         {
             Unit256 U;
-            if (unit256(a, blockIdx.x, U)) ok = copy_q();
+            if (walk.get(a, blockIdx.x, U)) ok = copy_q();
         }
         for (int u = blockIdx.x; ok; u += gridDim.x) {
             Unit256 U, Un;
-            if (!unit256(a, u, U)) break;
+            if (!walk.get(a, u, U)) break;
             const int q_first = U.m * kTileM, qi = q_first + r;
             float m_ref = -INFINITY, l = 0.f;
             for (int j = 0; j < U.nb; ++j) {
@@ -373,7 +422,7 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             }
             if (!ok) break;
             // Every S of this unit has been read: its Q columns take the next tile.
-            if (unit256(a, u + gridDim.x, Un) && !(ok = copy_q())) break;
+            if (walk.get(a, u + gridDim.x, Un) && !(ok = copy_q())) break;
             // Epilogue: O / l -> bf16, LSE = (m + log2 l) ln 2.
             if (!(ok = mbar_wait(&sh.o_done, uc & 1, wc, k6O))) break;
             ++uc;
@@ -411,9 +460,11 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             }
             tc_fence_before();
             mbar_arrive(&sh.o_free);
-            if (valid)
-                a.lse[((size_t)U.seq * a.Hq + U.h) * a.N + qi] =
-                    l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            if (valid) {
+                const size_t li = a.varlen ? (size_t)U.h * a.N + U.tok0 + qi     // [Hq, T]
+                                           : ((size_t)U.seq * a.Hq + U.h) * a.N + qi;
+                a.lse[li] = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            }
         }
     }
 
@@ -427,7 +478,9 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 
 cudaError_t launch_fwd256(const FwdLaunch& L, cudaStream_t stream) {
     const FwdArgs& a = L.a;
-    const long long units = (long long)a.B * a.Hq * ((a.N + kTileM - 1) / kTileM);
+    // Varlen: sum over sequences of ceil(len / 128) <= ceil(T / 128) + B.
+    const long long units = a.varlen ? (long long)a.Hq * ((a.N + kTileM - 1) / kTileM + a.B)
+                                     : (long long)a.B * a.Hq * ((a.N + kTileM - 1) / kTileM);
     int grid = (int)(units < L.num_sms ? units : L.num_sms);
     if (grid < 1) grid = 1;
     cudaError_t e = cudaFuncSetAttribute(fwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem256);

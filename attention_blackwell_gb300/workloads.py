@@ -21,6 +21,8 @@ the workloads the pages' analysis is about: d = 128, BF16, long sequences):
 * large_d64, causal_bwd_d64: large and causal_bwd at head dim 64 (the
   exponential-bound end of the balance between MUFU and tensor work).
 * large_d256, causal_d256: forward at head dim 256 (the product-bound end).
+* varlen_d256: the varlen workload's sequences and heads at head dim 256,
+  forward.
 """
 from dataclasses import dataclass, field
 
@@ -61,6 +63,8 @@ WORKLOADS = {
     "causal_bwd_d64": Workload("causal_bwd_d64", B=2, Hq=16, Hkv=16, N=8192, causal=True, backward=True, d=64),
     "large_d256": Workload("large_d256", B=4, Hq=16, Hkv=16, N=4096, causal=False, d=256),
     "causal_d256": Workload("causal_d256", B=2, Hq=16, Hkv=16, N=8192, causal=True, d=256),
+    "varlen_d256": Workload("varlen_d256", B=16, Hq=32, Hkv=1, N=0, causal=True, varlen=True,
+                            len_range=(512, 8192), d=256),
 }
 
 

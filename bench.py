@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--no-bwd", action="store_true", help="time the forward only")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="large (default), tiny, causal, varlen, causal_bwd, large_d64, causal_bwd_d64, "
-                         "large_d256, causal_d256 (forward only)")
+                         "large_d256, causal_d256, varlen_d256 (forward only)")
     ap.add_argument("--deterministic", action="store_true", help="backward in deterministic mode")
     ap.add_argument("--exp2-emu", type=int, default=0, help="forward: eighths of exp2 on the FMA pipe (0-2)")
     ap.add_argument("--tau", type=float, default=8.0, help="forward: conditional-rescale threshold (log2 units)")
@@ -158,16 +158,17 @@ def measured_peaks():
         return None
 
 
-def kernel_traffic(name):
+def kernel_traffic(name, workload):
     """dram bytes per launch from the committed ncu summary, or None when the
-    kernel's sources changed since the counters were taken."""
+    counters were taken on another workload or the kernel's sources changed
+    since."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         rec = json.load(open(path)).get(name)
     except (OSError, ValueError):
         return None
-    if not rec:
+    if not rec or rec.get("workload", "").split(":")[0] != workload:
         return None
     h = hashlib.sha256()
     try:
@@ -456,7 +457,7 @@ def main_ours(args):
                      "peak_source": peak_src,
                      "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4)
                      if achieved and peaks and peaks.get("bf16_tflops_sustained") else None,
-                     "traffic": kernel_traffic(traffic_key(args, w, dom["kernel"]))},
+                     "traffic": kernel_traffic(traffic_key(args, w, dom["kernel"]), w.name)},
         "e2e": {"value": round(r["e2e_value"], 2), "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "steps": r["E"],
                 "note": "public API, pinned host buffers, copies of step s overlap compute of step s-1"},

@@ -17,7 +17,7 @@
  * ---------------------------------------
  * - Element types: q, k, v, o, do, dq, dk, dv are bfloat16 (raw 16-bit
  *   storage, passed as void*); lse is float32; cu_seqlens is int32.
- * - Head dimension d is 128 or 64, or 256 for the fixed-length forward only
+ * - Head dimension d is 128 or 64, or 256 for the forward only
  *   (the pages' balance point moves with d: FlashAttention-4 paper summary,
  *   "Roofline" remarks).  Hq must be a multiple of Hkv; query head h reads
  *   key/value head h / (Hq / Hkv).
@@ -137,7 +137,8 @@ int fa_bwd_pairs_resident(void);
  * causal: 0 or 1.  N == 0 (or T == 0) is a no-op returning FA_OK.
  * Errors: FA_ERR_INVALID (null pointer, B<1, N<0, Hq/Hkv<1, Hq % Hkv,
  * alpha not finite and > 0, varlen without max_seqlen>0),
- * FA_ERR_UNSUPPORTED (d not 64, 128 or 256; d = 256 with cu_seqlens),
+ * FA_ERR_UNSUPPORTED (d not 64, 128 or 256; varlen with B > 1024 or
+ * max_seqlen > 131072),
  * FA_ERR_ALIGN, FA_ERR_LAUNCH.  d = 256 runs on a kernel of its own (one
  * 128-row query tile per CTA, 64-key blocks) whatever fa_set_fwd_kernel says.
  */

@@ -67,7 +67,8 @@ def test_fwd_rejects_bad_arguments_on_the_host(lib):
     assert call(causal=2) == -1
     assert call(d=96) == -2            # d is 64, 128 or 256
     assert call(d=512) == -2
-    assert call(d=256, cu=P, ms=128) == -2   # d = 256: fixed length only
+    assert call(d=256, cu=P, ms=1 << 20) == -2   # d = 256 varlen: the same limits
+    assert call(d=256, B=5000, cu=P, ms=128) == -2
     assert call(cu=P, ms=0) == -1      # varlen without max_seqlen
     assert call(cu=P, ms=1 << 20) == -2
     assert call(B=5000, cu=P, ms=128) == -2
