@@ -81,6 +81,21 @@ def test_large_q_logits(fa):
     check(*run(fa, inp, True), inp, True)
 
 
+@pytest.mark.parametrize("tau", [0.0, 64.0])
+def test_rescale_threshold_extremes(fa, tau):
+    """tau = 0 rescales O whenever a row maximum grows (the wait for the
+    previous block's P V on almost every block); tau = 64 keeps the first
+    maximum unless it is beaten by 2^64.  Both give the same attention."""
+    fa.set_tuning(0, tau)
+    try:
+        inp = inputs(1, 1000, 4, 2, seed=17, q_std=3.0)
+        check(*run(fa, inp, True), inp, True)
+        inp = inputs(0, 0, 2, 1, seed=18, q_std=3.0, lengths=[700, 5, 257])
+        check(*run(fa, inp, False), inp, False)
+    finally:
+        fa.set_tuning(0, 8.0)
+
+
 def test_many_units_sampled_rows(fa):
     """B=2, Hq=8, N=4096, causal: more units than CTAs, rows checked one by one."""
     inp = inputs(2, 4096, 8, 8, seed=33)
