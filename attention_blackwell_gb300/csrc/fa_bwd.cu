@@ -802,8 +802,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         auto release_pending = [&]() {
             if (r == 0 && sem_pend) {
                 bulk_wait0();          // the tile's additions are complete
-                fence_async_global();
-                __threadfence();
+                fence_async_global();  // ... and ordered before the release
                 red_release_add(sem_pend, 1);
             }
             sem_pend = nullptr;
@@ -840,8 +839,11 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     release_pending();
                     // Key tiles add into this query tile in ascending order;
                     // wait (bounded) until the previous one has released it.
+                    // The wait runs in another warp than the releasing thread,
+                    // so the two round trips to L2 overlap; the barrier below
+                    // then orders the acquire before this tile's reductions.
                     bool gave_up = false;
-                    if (r == 0) {
+                    if (r == 32) {
                         const uint64_t t0 = globaltimer_ns();
                         uint32_t spins = 0;
                         while (ld_acquire(sem) != U.k) {
@@ -856,9 +858,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                                 break;
                             }
                         }
-                        fence_async_global();  // our bulk reduction follows the acquire
                     }
                     if (named_bar_or(1, 128, gave_up)) { ok = false; break; }
+                    if (r == 0) fence_async_global();  // our bulk reduction follows the acquire
                 }
                 // Add dQ_i into the fp32 accumulator with TMA bulk tensor
                 // reductions of whole 128-byte lines, staged in shared memory
