@@ -145,7 +145,7 @@ def fwd(q, k, v, causal=False, alpha=None, cu_seqlens=None, max_seqlen=None, out
     Fixed length: q [B,N,Hq,d], k/v [B,N,Hkv,d] bf16 -> o like q,
     lse float32 [B,Hq,N].  Varlen: q [T,Hq,d], k/v [T,Hkv,d],
     cu_seqlens int32 [B+1] on the device, max_seqlen -> o [T,Hq,d],
-    lse [Hq,T].  d = 128 or 64.
+    lse [Hq,T].  d = 128, 64 or 256.
     """
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, n, torch.bfloat16)
@@ -201,7 +201,8 @@ def bwd_workspace(B, Hq, N, deterministic=False, varlen=False, device=None, d=HE
 
 def bwd(q, k, v, o, lse, do, causal=False, alpha=None, cu_seqlens=None, max_seqlen=None, deterministic=False,
         workspace=None, dq=None, dk=None, dv=None, stages=7, stream=None):
-    """Backward attention.  Returns (dq, dk, dv); layouts as in fwd.
+    """Backward attention.  Returns (dq, dk, dv); layouts as in fwd, d = 128
+    or 64.
 
     ``stages`` selects the launches (1 preprocess, 2 main, 4 postprocess);
     the default runs all three.
