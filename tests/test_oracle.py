@@ -63,7 +63,8 @@ def test_causal_row0_is_v0():
 
 
 @pytest.mark.parametrize("N,d,causal", [(1, 4, False), (2, 4, True), (17, 8, False), (17, 8, True),
-                                        (64, 8, True), (9, 128, False), (9, 64, True), (33, 64, False)])
+                                        (64, 8, True), (9, 128, False), (9, 64, True), (33, 64, False),
+                                        (7, 256, True), (12, 256, False)])
 def test_bruteforce_agrees(N, d, causal):
     alpha = 1 / math.sqrt(d)
     q, k, v = rnd((N, d), 10), rnd((N, d), 11), rnd((N, d), 12)
