@@ -256,10 +256,15 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         // ---------------------------------------------------------- UMMA issuer
         uint32_t it = 0, uc = 0, gs = 0, gp = 0;   // ring slots taken; S and P V blocks so far
         bool ok = true;
-        auto issue_s_block = [&]() -> bool {
+        bool v_ready = false;   // the next V block's full wait already taken
+        auto issue_s_block = [&](bool then_v) -> bool {
             const uint32_t ks = it % kRing;
             if (!mbar_wait_w(&sh.full[ks], (it / kRing) & 1, wc, k6KFull)) return false;
             ++it;
+            if (then_v) {   // the next ring item is the V of the next P V
+                if (!mbar_wait_w(&sh.full[it % kRing], (it / kRing) & 1, wc, k6VFull)) return false;
+                v_ready = true;
+            }
             tc_fence_after();
             issue_s(tmem + kColS + 64 * (gs & 1), tmem + kColQ, sR + ks * kKVBytes);
             umma_commit_w(&sh.s_full[gs & 1]);
@@ -273,11 +278,12 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             if (!walk.get(a, u, U)) break;
             if (!(ok = mbar_wait_w(&sh.qt_full, uc & 1, wc, k6QFull))) break;
             tc_fence_after();
-            if (!(ok = issue_s_block())) break;
-            if (U.nb > 1 && !(ok = issue_s_block())) break;
+            if (!(ok = issue_s_block(false))) break;
+            if (U.nb > 1 && !(ok = issue_s_block(false))) break;
             for (int j = 0; j < U.nb; ++j) {
                 const uint32_t vs = it % kRing;
-                if (!(ok = mbar_wait_w(&sh.full[vs], (it / kRing) & 1, wc, k6VFull))) break;
+                if (!v_ready && !(ok = mbar_wait_w(&sh.full[vs], (it / kRing) & 1, wc, k6VFull))) break;
+                v_ready = false;
                 ++it;
                 if (j == 0 && uc > 0 && !(ok = mbar_wait_w(&sh.o_free, (uc - 1) & 1, wc, k6OFree))) break;
                 // P of block gp.  Two barriers, alternating: the softmax can
@@ -290,7 +296,8 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 umma_commit_w(&sh.pv_done[gp & 1]);
                 ++gp;
                 // S of block j + 2 into the region P of block j was just read from.
-                if (j + 2 < U.nb && !(ok = issue_s_block())) break;
+                // V of block j + 1 directly follows K of block j + 2 in the ring.
+                if (j + 2 < U.nb && !(ok = issue_s_block(true))) break;
             }
             if (!ok) break;
             umma_commit_w(&sh.o_done);
