@@ -100,11 +100,21 @@ __device__ __forceinline__ bool unit256(const FwdArgs& a, int u, Unit256& U) {
 // come first); within a level, sequences in order, heads minor.  Each role
 // asks for its units in non-decreasing order, so one cursor per thread walks
 // the levels and sequences once: O(levels x B) reads of cu_seqlens per CTA.
+// Offsets are clamped to [0, T] and a sequence's end to at least its start,
+// so malformed offsets cannot move a row outside the tensors.
 struct Walk256 {
     int k = -1, lvl_start = 0, lvl_count = 0, b = 0, idx_b = 0;
 
+    __device__ __forceinline__ static int start(const FwdArgs& a, int s) {
+        const int c = a.cu_seqlens[s];
+        return c < 0 ? 0 : (c > a.N ? a.N : c);
+    }
+    __device__ __forceinline__ static int length(const FwdArgs& a, int s) {
+        const int c0 = start(a, s), c1 = a.cu_seqlens[s + 1];
+        return c1 <= c0 ? 0 : (c1 > a.N ? a.N : c1) - c0;
+    }
     __device__ __forceinline__ static int tiles(const FwdArgs& a, int s) {
-        return (a.cu_seqlens[s + 1] - a.cu_seqlens[s] + kTileM - 1) / kTileM;
+        return (length(a, s) + kTileM - 1) / kTileM;
     }
     __device__ bool get(const FwdArgs& a, int u, Unit256& U) {
         if (!a.varlen) return unit256(a, u, U);
@@ -126,8 +136,8 @@ struct Walk256 {
         }
         U.seq = b;
         U.h = i - idx_b;
-        U.tok0 = a.cu_seqlens[b];
-        U.len = a.cu_seqlens[b + 1] - U.tok0;
+        U.tok0 = start(a, b);
+        U.len = length(a, b);
         U.m = (U.len + kTileM - 1) / kTileM - 1 - k;
         set_blocks(a, U);
         return true;
