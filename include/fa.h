@@ -27,7 +27,10 @@
  *   the token axis; N is then the TOTAL token count T; q, o are [T, Hq, d],
  *   k, v are [T, Hkv, d], lse is [Hq, T].  cu_seqlens is a DEVICE array of
  *   B+1 non-decreasing offsets with cu_seqlens[0] = 0 and cu_seqlens[B] = T;
- *   max_seqlen is an upper bound on every sequence length.
+ *   max_seqlen is an upper bound on every sequence length.  The kernels
+ *   clamp offsets outside [0, T] and ends below their starts (the results
+ *   for such offsets are unspecified, but no row outside the tensors is
+ *   read or written).
  * - Causal masks are top-left aligned within each sequence (query and key
  *   lengths are equal).
  * - Pointers are device pointers owned by the caller; the library allocates
