@@ -134,8 +134,8 @@ def set_tuning(exp2_emu_eighths=0, tau=8.0):
 
 
 def set_fwd_kernel(kernel=2):
-    """Forward kernel for later calls: 0 ping-pong 128x128 tiles, 1 256-key
-    blocks, 2 CTA pairs with 256-key blocks (the default)."""
+    """Forward kernel for later calls: 0 ping-pong 128x128 tiles, 2 CTA pairs
+    with 256-key blocks (the default)."""
     _check(lib().fa_set_fwd_kernel(int(kernel)), "fa_set_fwd_kernel")
 
 

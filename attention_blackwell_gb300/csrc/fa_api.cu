@@ -31,7 +31,7 @@ std::mutex g_dev_mu;
 
 int g_emu_eighths = 0;         // share of exp2 pairs on the FMA pipe (eighths)
 int g_bwd_kernel = 0;          // 0: one CTA per 128-key tile; 1: CTA pairs per 256-key block
-int g_fwd_kernel = 2;          // 0: ping-pong of two 128-row query tiles; 1: 256-key blocks; 2: CTA pairs
+int g_fwd_kernel = 2;          // 0: ping-pong of two 128-row query tiles; 2: CTA pairs
 float g_tau = 8.0f;            // conditional-rescale threshold, log2(256)
 
 int current_device_info(DeviceInfo** out) {
@@ -163,10 +163,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     int rc = current_device_info(&dev);
     if (rc != FA_OK) return rc;
 
-    // The 256-key kernels use the MUFU-only exp2 (the FMA-exp2 variants run on
-    // the ping-pong kernel); the single-CTA one serves fixed-length inputs
-    // only; d = 64 runs on the ping-pong kernel.
-    const bool wide = d == 128 && !varlen && g_emu_eighths == 0 && g_fwd_kernel == 1;
+    // The pair kernel uses the MUFU-only exp2 (the FMA-exp2 variants run on
+    // the ping-pong kernel); d = 64 runs on the ping-pong kernel.
     const bool pair = d == 128 && g_emu_eighths == 0 && g_fwd_kernel == 2;
     FwdLaunch L;
     L.d = d;
@@ -176,12 +174,12 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
         if ((rc = make_map(&L.tk, k, Hkv, T, 64, d)) != FA_OK) return rc;
         if ((rc = make_map(&L.tv, v, Hkv, T, 64, d)) != FA_OK) return rc;
     }
-    // K boxes: 256 rows (one block) for kernel 1, 128 (a block's half) for the
-    // pair kernel; V boxes: 256 rows for both (the pair loads 64 columns of them).
+    // K boxes: 128 rows (the pair kernel loads a block's half); V boxes: 256
+    // rows for the pair kernel (it loads 64 columns of each block's 256 keys).
     if (d != 256) {
         if ((rc = make_map(&L.tq, q, Hq, T, kTileM, d)) != FA_OK) return rc;
-        if ((rc = make_map(&L.tk, k, Hkv, T, wide ? 256 : kTileM, d)) != FA_OK) return rc;
-        if ((rc = make_map(&L.tv, v, Hkv, T, (wide || pair) ? 256 : kTileM, d)) != FA_OK) return rc;
+        if ((rc = make_map(&L.tk, k, Hkv, T, kTileM, d)) != FA_OK) return rc;
+        if ((rc = make_map(&L.tv, v, Hkv, T, pair ? 256 : kTileM, d)) != FA_OK) return rc;
     }
     if (pair && (rc = make_map(&L.to, o, Hq, T)) != FA_OK) return rc;
     L.a.o = o;
@@ -211,7 +209,6 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     L.num_sms = dev->num_sms;
     cudaError_t e = d == 256 ? launch_fwd256(L, stream)
                     : pair    ? launch_fwd_pair(L, stream)
-                    : wide    ? launch_fwd_wide(L, stream)
                               : launch_fwd(L, stream);
     return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
@@ -227,7 +224,7 @@ int fa_set_bwd_kernel(int kernel) {
 int fa_bwd_pairs_resident(void) { return g_bwd_pairs_resident; }
 
 int fa_set_fwd_kernel(int kernel) {
-    if (kernel < 0 || kernel > 2) return FA_ERR_INVALID;
+    if (kernel != 0 && kernel != 2) return FA_ERR_INVALID;
     g_fwd_kernel = kernel;
     return FA_OK;
 }
@@ -243,26 +240,32 @@ static int read_and_clear(DevStatus* where) {
     return s.code;
 }
 
+// A backward workspace's status word; after a reported failure the main
+// stage's unit claim counter is rewound too (a main kernel that gave up may
+// leave it mid-list), so that a later main stage run without the preprocess
+// starts from the first unit.
+static int read_and_clear_ws(BwdHeader* h) {
+    const int b = read_and_clear(&h->status);
+    if (b != FA_OK && b != FA_ERR_LAUNCH) {
+        const int zero[2] = {0, 0};
+        if (cudaMemcpy(&h->next_unit, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return FA_ERR_LAUNCH;
+    }
+    return b;
+}
+
 int fa_get_device_status(const void* workspace, cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_LAUNCH;
     DeviceInfo* dev = nullptr;
     int rc = current_device_info(&dev);
     if (rc != FA_OK) return rc;
     int a = read_and_clear(dev->status);
-    int b = FA_OK;
-    if (workspace) {
-        BwdHeader* h = static_cast<BwdHeader*>(const_cast<void*>(workspace));
-        b = read_and_clear(&h->status);
-        if (b != FA_OK && b != FA_ERR_LAUNCH) {
-            // A main kernel that gave up may leave its unit claim counter
-            // mid-list: rewind it, so that a later main stage run without the
-            // preprocess starts from the first unit.
-            const int zero[2] = {0, 0};
-            if (cudaMemcpy(&h->next_unit, zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
-                return FA_ERR_LAUNCH;
-        }
-    }
-    return a != FA_OK ? a : b;
+    int b = FA_OK, c = FA_OK;
+    if (workspace) b = read_and_clear_ws(static_cast<BwdHeader*>(const_cast<void*>(workspace)));
+    // fa_bwd_noalloc's scratch area on this device, once a call has set it up.
+    BwdHeader* nh = noalloc_header_current_device();
+    if (nh && nh != workspace) c = read_and_clear_ws(nh);
+    return a != FA_OK ? a : (b != FA_OK ? b : c);
 }
 
 size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, int deterministic, int varlen) {
@@ -271,12 +274,14 @@ size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, int deterministic, int
     return ws_layout(T, B, Hq, deterministic ? 1 : 0, varlen ? 1 : 0, d).total;
 }
 
-int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const void* o, const float* lse,
-                  const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, float alpha,
-                  int causal, const int* cu_seqlens, int max_seqlen, int deterministic, void* workspace,
-                  size_t workspace_bytes, cudaStream_t stream) {
-    if (stages < 1 || stages > 7) return FA_ERR_INVALID;
-    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FA_ERR_INVALID;
+}  // extern "C"
+
+namespace fa {
+
+int bwd_validate(const void* const ptrs[9], int B, int Hq, int Hkv, int N, int d, float alpha, int causal,
+                 const int* cu_seqlens, int max_seqlen, int deterministic, long long* T_out) {
+    for (int i = 0; i < 9; ++i)
+        if (!ptrs[i]) return FA_ERR_INVALID;
     if (B < 1 || N < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return FA_ERR_INVALID;
     if (!(alpha > 0.0f) || !isfinite(alpha)) return FA_ERR_INVALID;
     if ((causal != 0 && causal != 1) || (deterministic != 0 && deterministic != 1)) return FA_ERR_INVALID;
@@ -286,20 +291,36 @@ int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const
         if (max_seqlen < 1) return FA_ERR_INVALID;
         if (B > kMaxVarlenSeqs || max_seqlen > 131072) return FA_ERR_UNSUPPORTED;
     }
-    const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
-    for (const void* p : ptrs)
-        if (!aligned16(p)) return FA_ERR_ALIGN;
+    for (int i = 0; i < 9; ++i)
+        if (!aligned16(ptrs[i])) return FA_ERR_ALIGN;
     if (varlen && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FA_ERR_ALIGN;
     const long long T = varlen ? (long long)N : (long long)B * N;
-    if (T == 0) return FA_OK;
     if (T > 0x7fffffffLL || (long long)Hq * T > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    *T_out = T;
+    return FA_OK;
+}
+
+}  // namespace fa
+
+extern "C" {
+
+int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d, float alpha,
+                  int causal, const int* cu_seqlens, int max_seqlen, int deterministic, void* workspace,
+                  size_t workspace_bytes, cudaStream_t stream) {
+    if (stages < 1 || stages > 7) return FA_ERR_INVALID;
+    const void* ptrs[9] = {q, k, v, o, lse, dout, dq, dk, dv};
+    long long T = 0;
+    int rc = bwd_validate(ptrs, B, Hq, Hkv, N, d, alpha, causal, cu_seqlens, max_seqlen, deterministic, &T);
+    if (rc != FA_OK) return rc;
+    if (T == 0) return FA_OK;
+    const bool varlen = cu_seqlens != nullptr;
     const WsLayout w = ws_layout(T, B, Hq, deterministic, varlen ? 1 : 0, d);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < w.total)
         return FA_ERR_WORKSPACE;
 
     DeviceInfo* dev = nullptr;
-    int rc = current_device_info(&dev);
-    if (rc != FA_OK) return rc;
+    if ((rc = current_device_info(&dev)) != FA_OK) return rc;
     BwdLaunch L;
     L.d = d;
     if ((rc = make_map(&L.tq, q, Hq, T, kTileM, d)) != FA_OK) return rc;
@@ -321,6 +342,7 @@ int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const
     a.dqacc = reinterpret_cast<float*>(ws + w.dq_off);
     a.sem = reinterpret_cast<int*>(ws + w.sem_off);
     a.units = reinterpret_cast<int4*>(ws + w.unit_off);
+    a.cu_s = reinterpret_cast<int*>(ws + w.cu_off);
     a.sem_stride = w.sem_stride;
     a.B = B;
     a.Hq = Hq;

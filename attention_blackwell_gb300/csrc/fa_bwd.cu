@@ -121,6 +121,9 @@ __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a) {
     if (tid == 0)
         for (int i = 1; i <= B; ++i) s_cu[i] = s_cu[i] > s_cu[i - 1] ? s_cu[i] : s_cu[i - 1];
     __syncthreads();
+    // The main kernel reads the units' bounds from this copy, so that plan
+    // and main kernel agree on every sequence whatever the offsets were.
+    for (int i = tid; i <= B; i += blockDim.x) a.cu_s[i] = s_cu[i];
     auto nkv = [&](int s) { return (s_cu[s + 1] - s_cu[s] + kTileN - 1) / kTileN; };
     for (int i = tid; i < B; i += blockDim.x) {
         const int ni = nkv(i);
@@ -317,11 +320,9 @@ __device__ __forceinline__ bool bwd_unit(const BwdArgs& a, int total, int u, BUn
         U.seq = e.x;
         U.hk = e.y;
         U.k = e.z;
-        int c0 = a.cu_seqlens[U.seq], c1 = a.cu_seqlens[U.seq + 1];
-        c0 = c0 < 0 ? 0 : (c0 > a.N ? a.N : c0);
-        c1 = c1 < c0 ? c0 : (c1 > a.N ? a.N : c1);
+        const int c0 = a.cu_s[U.seq];   // sanitised by the plan kernel
         U.tok0 = c0;
-        U.len = c1 - c0;
+        U.len = a.cu_s[U.seq + 1] - c0;
     }
     U.nq = (U.len + kTileM - 1) / kTileM;
     U.i0 = a.causal ? U.k : 0;

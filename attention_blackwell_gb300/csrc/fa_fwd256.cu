@@ -100,22 +100,29 @@ __device__ __forceinline__ bool unit256(const FwdArgs& a, int u, Unit256& U) {
 // come first); within a level, sequences in order, heads minor.  Each role
 // asks for its units in non-decreasing order, so one cursor per thread walks
 // the levels and sequences once: O(levels x B) reads of cu_seqlens per CTA.
-// Offsets are clamped to [0, T] and a sequence's end to at least its start,
-// so malformed offsets cannot move a row outside the tensors.
+// Offsets are sanitised by the rule every kernel here applies: each is
+// clamped to [0, T] and raised to at least the one before it (a running
+// maximum the cursor carries along), so malformed offsets give empty
+// sequences, never rows outside the tensors or overlapping sequences.
 struct Walk256 {
     int k = -1, lvl_start = 0, lvl_count = 0, b = 0, idx_b = 0;
+    int c0 = 0, c1 = 0;   // sanitised offsets of sequence b
 
-    __device__ __forceinline__ static int start(const FwdArgs& a, int s) {
-        const int c = a.cu_seqlens[s];
+    __device__ __forceinline__ static int clamp_t(const FwdArgs& a, int c) {
         return c < 0 ? 0 : (c > a.N ? a.N : c);
     }
-    __device__ __forceinline__ static int length(const FwdArgs& a, int s) {
-        const int c0 = start(a, s), c1 = a.cu_seqlens[s + 1];
-        return c1 <= c0 ? 0 : (c1 > a.N ? a.N : c1) - c0;
+    __device__ __forceinline__ void first(const FwdArgs& a) {
+        b = 0;
+        c0 = clamp_t(a, a.cu_seqlens[0]);
+        c1 = max(c0, clamp_t(a, a.cu_seqlens[1]));
     }
-    __device__ __forceinline__ static int tiles(const FwdArgs& a, int s) {
-        return (length(a, s) + kTileM - 1) / kTileM;
+    __device__ __forceinline__ void next(const FwdArgs& a) {   // sequence b + 1 (b + 1 < B)
+        ++b;
+        c0 = c1;
+        c1 = max(c1, clamp_t(a, a.cu_seqlens[b + 1]));
     }
+    __device__ __forceinline__ int tiles() const { return (c1 - c0 + kTileM - 1) / kTileM; }
+
     __device__ bool get(const FwdArgs& a, int u, Unit256& U) {
         if (!a.varlen) return unit256(a, u, U);
         if (u < 0) return false;
@@ -123,21 +130,25 @@ struct Walk256 {
             lvl_start += lvl_count;
             ++k;
             int n = 0;
-            for (int s = 0; s < a.B; ++s) n += tiles(a, s) > k;
+            first(a);
+            for (int s = 0; s < a.B; ++s) {
+                n += tiles() > k;
+                if (s + 1 < a.B) next(a);
+            }
             lvl_count = n * a.Hq;
             if (n == 0) return false;                    // past the last level
-            for (b = 0; tiles(a, b) <= k; ++b) {}
+            for (first(a); tiles() <= k; next(a)) {}     // stops at a sequence of this level
             idx_b = 0;
         }
         const int i = u - lvl_start;
         while (i >= idx_b + a.Hq) {                      // a later sequence of this level
             idx_b += a.Hq;
-            do ++b; while (tiles(a, b) <= k);
+            do next(a); while (tiles() <= k);
         }
         U.seq = b;
         U.h = i - idx_b;
-        U.tok0 = start(a, b);
-        U.len = length(a, b);
+        U.tok0 = c0;
+        U.len = c1 - c0;
         U.m = (U.len + kTileM - 1) / kTileM - 1 - k;
         set_blocks(a, U);
         return true;

@@ -49,7 +49,13 @@ struct FwdLaunch {
 //   dQacc              float [Hq][T][d]         fp32 dQ accumulator
 //   semaphores         int   [Hq][T/128 + B + 1] (deterministic mode)
 //   units              int4  [Hkv * (T/128 + B)] (varlen work list)
+//   cu                 int   [B+1]              (varlen: sanitised offsets)
 // T = B*N for fixed length, the packed token count for varlen.
+//
+// Sanitised offsets (the one rule every kernel applies to cu_seqlens):
+// c'_0 = clamp(c_0, 0, T), c'_s = max(c'_{s-1}, clamp(c_s, 0, T)); sequence
+// s owns rows [c'_s, c'_{s+1}).  Malformed offsets therefore give empty
+// sequences, never rows outside the tensors or overlapping sequences.
 struct BwdHeader {
     DevStatus status;
     int total_units;   // varlen: written by the plan kernel
@@ -61,7 +67,7 @@ static_assert(sizeof(BwdHeader) == 256, "backward workspace header");
 static_assert(offsetof(BwdHeader, done_ctas) == offsetof(BwdHeader, next_unit) + sizeof(int), "claim counters");
 
 struct WsLayout {
-    size_t d_off, dq_off, sem_off, unit_off, total;
+    size_t d_off, dq_off, sem_off, unit_off, cu_off, total;
     long long sem_stride;  // semaphores per query head
 };
 
@@ -75,7 +81,8 @@ inline WsLayout ws_layout(long long T, int B, int Hq, int deterministic, int var
     w.dq_off = align256(w.d_off + (size_t)Hq * T * 4);
     w.sem_off = align256(w.dq_off + (size_t)Hq * T * d * 4);
     w.unit_off = align256(w.sem_off + (deterministic ? (size_t)Hq * w.sem_stride * 4 : 0));
-    w.total = align256(w.unit_off + (varlen ? (size_t)Hq * (tiles + B) * 16 : 0));
+    w.cu_off = align256(w.unit_off + (varlen ? (size_t)Hq * (tiles + B) * 16 : 0));
+    w.total = align256(w.cu_off + (varlen ? (size_t)(B + 1) * 4 : 0));
     return w;
 }
 
@@ -92,6 +99,7 @@ struct BwdArgs {
     float* dqacc;
     int* sem;
     int4* units;
+    int* cu_s;               // varlen: sanitised offsets [B+1], written by the plan kernel
     long long sem_stride;
     int B, Hq, Hkv;
     int N;                   // fixed: sequence length; varlen: T
@@ -123,9 +131,6 @@ cudaError_t launch_bwd(const BwdLaunch& L, int stages, cudaStream_t stream);
 // Launch the forward kernel (fa_fwd.cu).  Returns a cudaError_t.
 cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream);
 
-// Launch the 256-key-block forward kernel (fa_fwd_wide.cu; fixed length
-// only).  Its K and V maps use boxes of 256 rows.
-cudaError_t launch_fwd_wide(const FwdLaunch& L, cudaStream_t stream);
 // CTA-pair kernel (clusters of two), fixed length, MUFU exp2.
 cudaError_t launch_fwd_pair(const FwdLaunch& L, cudaStream_t stream);
 // CTA pairs the pair kernel keeps resident (0 until its first launch).
@@ -140,5 +145,15 @@ cudaError_t launch_fwd256(const FwdLaunch& L, cudaStream_t stream);
 
 // The library's device status word on the current device.
 DevStatus* device_status_ptr();
+
+// fa_bwd's host-side argument checks (everything but the workspace), in the
+// order fa_bwd applies them; on FA_OK *T_out is the token count.  ptrs: q,
+// k, v, o, lse, dout, dq, dk, dv.
+int bwd_validate(const void* const ptrs[9], int B, int Hq, int Hkv, int N, int d, float alpha, int causal,
+                 const int* cu_seqlens, int max_seqlen, int deterministic, long long* T_out);
+
+// Header of fa_bwd_noalloc's scratch area on the current device, or nullptr
+// while no call has set the area up there (fa_noalloc.cu).
+BwdHeader* noalloc_header_current_device();
 
 }  // namespace fa

@@ -47,13 +47,28 @@ int scratch_address(void** out) {
 }
 
 }  // namespace
+
+BwdHeader* noalloc_header_current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    return static_cast<BwdHeader*>(g_scratch_addr[dev]);
+}
+
 }  // namespace fa
 
 extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
                               const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
                               float alpha, int causal, const int* cu_seqlens, int max_seqlen, int deterministic,
                               cudaStream_t stream) {
-    const size_t need = fa_bwd_workspace_size(B, Hq, N, d, deterministic ? 1 : 0, cu_seqlens ? 1 : 0);
+    // fa_bwd's own checks first, so that both entry points return the same
+    // code for the same arguments; then the size limit of the scratch area.
+    const void* ptrs[9] = {q, k, v, o, lse, dout, dq, dk, dv};
+    long long T = 0;
+    const int vrc = fa::bwd_validate(ptrs, B, Hq, Hkv, N, d, alpha, causal, cu_seqlens, max_seqlen, deterministic, &T);
+    if (vrc != FA_OK) return vrc;
+    if (T == 0) return FA_OK;
+    const size_t need = fa_bwd_workspace_size(B, Hq, N, d, deterministic, cu_seqlens ? 1 : 0);
     if (need == 0) return FA_ERR_INVALID;
     if (need > fa::kNoAllocScratchBytes) return FA_ERR_WORKSPACE;
     void* scratch = nullptr;

@@ -52,8 +52,8 @@ def parse():
     ap.add_argument("--tau", type=float, default=8.0, help="forward: conditional-rescale threshold (log2 units)")
     ap.add_argument("--bwd-kernel", type=int, default=0,
                     help="backward main kernel: 0 one CTA per 128-key tile, 1 CTA pairs per 256-key block")
-    ap.add_argument("--fwd-kernel", type=int, default=2,
-                    help="forward kernel: 0 ping-pong 128x128, 1 256-key blocks, 2 CTA pairs with 256-key blocks")
+    ap.add_argument("--fwd-kernel", type=int, default=2, choices=[0, 2],
+                    help="forward kernel: 0 ping-pong 128x128, 2 CTA pairs with 256-key blocks")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
     return ap.parse_args()
@@ -187,9 +187,9 @@ def traffic_key(args, w, kernel):
         return "bwd" if (w.varlen or args.deterministic or args.bwd_kernel == 0) else "bwd_pair"
     if kernel != "fwd":
         return kernel
-    if args.exp2_emu or args.fwd_kernel == 0 or (w.varlen and args.fwd_kernel == 1):
+    if args.exp2_emu or args.fwd_kernel == 0:
         return "fwd_pingpong"
-    return {1: "fwd_wide", 2: "fwd_pair"}[args.fwd_kernel]
+    return "fwd_pair"
 
 
 def _slice(inp, w, b):
@@ -438,8 +438,8 @@ def main_ours(args):
             "step": step_name, "global_batch": w.B * world, "seq_len": w.N or max(r["inp"]["lengths"]),
             "deterministic_bwd": bool(args.deterministic), "exp2_emu_eighths": args.exp2_emu, "tau": args.tau,
             "fwd_kernel": ("one 128-row tile, 64-key blocks (d = 256)" if w.d == 256 else
-                           "ping-pong 2x128" if args.exp2_emu or w.d != 128 or (w.varlen and args.fwd_kernel == 1) else
-                           {0: "ping-pong 2x128", 1: "256-key blocks", 2: "CTA pairs, 256-key blocks"}[args.fwd_kernel]),
+                           "ping-pong 2x128" if args.exp2_emu or w.d != 128 or args.fwd_kernel == 0 else
+                           "CTA pairs, 256-key blocks"),
             "fwd_pairs_resident": fa_pairs_resident(),
             "bwd_kernel": ("one CTA per 128-key tile" if w.varlen or args.deterministic or args.bwd_kernel == 0 or w.d != 128
                            else "CTA pairs per 256-key block"),

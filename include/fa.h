@@ -27,10 +27,15 @@
  *   the token axis; N is then the TOTAL token count T; q, o are [T, Hq, d],
  *   k, v are [T, Hkv, d], lse is [Hq, T].  cu_seqlens is a DEVICE array of
  *   B+1 non-decreasing offsets with cu_seqlens[0] = 0 and cu_seqlens[B] = T;
- *   max_seqlen is an upper bound on every sequence length.  The kernels
- *   clamp offsets outside [0, T] and ends below their starts (the results
- *   for such offsets are unspecified, but no row outside the tensors is
- *   read or written).
+ *   max_seqlen is an upper bound on every sequence length.  Malformed
+ *   offsets are sanitised by one rule in every kernel: c'_0 = clamp(c_0, 0,
+ *   T), c'_s = max(c'_{s-1}, clamp(c_s, 0, T)), and sequence s is rows
+ *   [c'_s, c'_{s+1}).  Sequences thus never overlap and never leave the
+ *   tensors; rows outside every sequence are not written (o, lse, dk, dv)
+ *   or written as zero (dq).  A sanitised sequence longer than 131072
+ *   tokens (possible only when max_seqlen understates the lengths) makes a
+ *   d = 64/128 call compute nothing and report FA_ERR_INVALID through
+ *   fa_get_device_status; the d = 256 forward has no such limit.
  * - Causal masks are top-left aligned within each sequence (query and key
  *   lengths are equal).
  * - Pointers are device pointers owned by the caller; the library allocates
@@ -88,17 +93,13 @@ int fa_set_tuning(int exp2_emu_eighths, float tau);
  * Process-wide choice of the forward kernel (affects later fa_fwd calls):
  *   0 -- two 128-row query tiles per CTA in ping-pong, 128-key tiles: the
  *        pipeline of the FlashAttention-4 blog, "Forward pass";
- *   1 -- one 128-row query tile per CTA, 256-key blocks, so the S = Q K^T
- *        product is a 128x256 UMMA, which runs at the tensor core's full
- *        rate on GB300 (the 128x128 shape does not);
  *   2 -- (default) CTA pairs (clusters of two): 256 query rows per pair and
  *        256-key blocks, each product one M = 256 UMMA over both SMs, so each
  *        SM loads and reads only half of every K and V block.
- * Kernel 2 serves fixed-length and packed varlen inputs, kernel 1 fixed-length
- * inputs, both with d = 128 and exp2_emu_eighths == 0; all other calls
- * (d = 64 among them) use kernel 0.  All compute the same attention up to
- * rounding.
- * Errors: FA_ERR_INVALID.
+ * Kernel 2 serves fixed-length and packed varlen inputs with d = 128 and
+ * exp2_emu_eighths == 0; all other calls (d = 64 among them) use kernel 0.
+ * Both compute the same attention up to rounding.
+ * Errors: FA_ERR_INVALID (any other value).
  */
 int fa_set_fwd_kernel(int kernel);
 
@@ -213,8 +214,12 @@ int fa_bwd_stages(int stages, const void *q, const void *k, const void *v, const
  *   call's contents (each call re-zeroes what must start at zero).  Calls
  *   that overlap on the GPU (different streams, or concurrent host threads)
  *   race on it and produce wrong gradients: serialise them.
- * - A device-side wait timeout is recorded in the scratch area's own status
- *   word, which callers cannot read; fa_get_device_status does not see it.
+ * - A device-side wait timeout (or an offset table the plan stage rejects)
+ *   is recorded in the scratch area's own status word;
+ *   fa_get_device_status reports and clears it on this device, as it does
+ *   for a workspace passed to it.
+ * Argument errors are fa_bwd's, checked in fa_bwd's order (FA_ERR_UNSUPPORTED
+ * for d = 256, ...); a call with no tokens returns FA_OK.
  */
 int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const float *lse,
                    const void *dout, void *dq, void *dk, void *dv,
@@ -225,11 +230,18 @@ int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, c
  * Reads (and clears) the library's device status word on the current
  * device after synchronising `stream`: FA_OK, or FA_ERR_TIMEOUT when a
  * kernel's bounded wait gave up (the kernel then skipped its remaining work,
- * drained its own copies, freed its tensor memory and returned).
+ * drained its own copies, freed its tensor memory and returned), or
+ * FA_ERR_INVALID when a kernel rejected a device-side table (a varlen batch
+ * whose sanitised offsets hold a sequence longer than the 131072-token
+ * limit: nothing is computed for that call).
  * `workspace` may be NULL; when it is a backward workspace its status word
- * is read (and cleared) too, and after a reported timeout the main stage's
+ * is read (and cleared) too, and after a reported failure the main stage's
  * unit claim counter in the workspace is rewound, so that a later
  * fa_bwd_stages call with stages == 2 alone starts from the first unit.
+ * The status word of fa_bwd_noalloc's scratch area on this device is read,
+ * cleared and rewound the same way once a no-allocation call has run here.
+ * The first non-OK code found is returned (device word, then workspace,
+ * then scratch area); all of them are cleared.
  */
 int fa_get_device_status(const void *workspace, cudaStream_t stream);
 

@@ -31,8 +31,20 @@ cu[s] .. cu[s+1]-1).  LSE is [B, Hq, N] (fixed length) or [Hq, T] (varlen).
 Rows of S are independent, so the forward and the dQ part of the backward are
 evaluated over chunks of query rows only to bound memory; no other blocking,
 fusion or reordering is applied.
+
+``workers`` (forward / backward): the (sequence, head) problems are
+independent, so they may be evaluated by a pool of processes (started with
+``spawn``, safe after CUDA has been initialised in the caller).  Each task
+runs the same per-head function on the same inputs; the results are
+assembled in the serial loop's order (dK/dV group sums included).  The output
+equals ``workers=None`` up to the BLAS library's own summation order inside
+each matrix product, which depends on its thread count (each worker runs it
+single-threaded).
 """
 import math
+import multiprocessing as mp
+import os
+from concurrent.futures import ProcessPoolExecutor
 
 import numpy as np
 
@@ -103,12 +115,66 @@ def head_forward(qh, kh, vh, alpha, causal=False):
     return o, lse
 
 
-def forward(q, k, v, alpha, causal=False, cu_seqlens=None, heads=None):
+_ONE_THREAD = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def _pool(workers):
+    """A spawn pool whose workers each run single-threaded BLAS (the pool
+    itself supplies the parallelism)."""
+    saved = {k: os.environ.get(k) for k in _ONE_THREAD}
+    os.environ.update({k: "1" for k in _ONE_THREAD})
+    try:
+        ex = ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn"))
+        # Start every worker now, while the variables are set.
+        list(ex.map(int, range(workers)))
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return ex
+
+
+def _head_tasks(shape, cu_seqlens, heads, Hq, Hkv):
+    """(b, off, L, hq, hk) in the serial loop's order, empty sequences skipped."""
+    return [(b, off, L, hq, kv_head_of(hq, Hq, Hkv))
+            for b, off, L in _sequences(shape, cu_seqlens) if L > 0 for hq in heads]
+
+
+def _run_heads(fn, tasks, operands, extra, workers):
+    """fn(*[t[seq][:, head] for each operand], *extra) for every task, in order.
+
+    operands: list of (tensor, 'q' | 'k') -- the head index used is hq or hk.
+    """
+    def args(task):  # contiguous copies in both modes, so both see identical inputs
+        b, off, L, hq, hk = task
+        return [np.ascontiguousarray(_seq_slice(t, b, off, L)[:, hq if which == "q" else hk])
+                for t, which in operands] + list(extra)
+
+    if not workers or workers <= 1 or len(tasks) <= 1:
+        for task in tasks:
+            yield task, fn(*args(task))
+        return
+    with _pool(min(workers, len(tasks))) as ex:
+        # Bounded look-ahead keeps at most ~2 tasks per worker in flight.
+        pending = []
+        for task in tasks:
+            pending.append((task, ex.submit(fn, *args(task))))
+            if len(pending) >= 2 * workers:
+                t0, f0 = pending.pop(0)
+                yield t0, f0.result()
+        for t0, f0 in pending:
+            yield t0, f0.result()
+
+
+def forward(q, k, v, alpha, causal=False, cu_seqlens=None, heads=None, workers=None):
     """O and LSE of exact attention.
 
     q: [B,N,Hq,d] or packed [T,Hq,d]; k, v: same with Hkv heads.
     heads: optional iterable of query heads to compute (others are left 0 /
     -inf), used to sample large workloads head by head (heads are independent).
+    workers: evaluate the (sequence, head) problems in that many processes.
     Returns (o float64 like q, lse float64 [B,Hq,N] or [Hq,T]).
     """
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
@@ -122,19 +188,14 @@ def forward(q, k, v, alpha, causal=False, cu_seqlens=None, heads=None):
         lse = np.full((q.shape[0], Hq, q.shape[1]), -np.inf)
         shape = q.shape[:2]
     heads = range(Hq) if heads is None else list(heads)
-    for b, off, L in _sequences(shape, cu_seqlens):
-        if L == 0:
-            continue
-        qs, ks, vs = (_seq_slice(t, b, off, L) for t in (q, k, v))
-        os_ = _seq_slice(o, b, off, L)
-        for hq in heads:
-            hk = kv_head_of(hq, Hq, Hkv)
-            oh, lh = head_forward(qs[:, hq], ks[:, hk], vs[:, hk], alpha, causal)
-            os_[:, hq] = oh
-            if varlen:
-                lse[hq, off:off + L] = lh
-            else:
-                lse[b, hq] = lh
+    tasks = _head_tasks(shape, cu_seqlens, heads, Hq, Hkv)
+    ops = [(q, "q"), (k, "k"), (v, "k")]
+    for (b, off, L, hq, hk), (oh, lh) in _run_heads(head_forward, tasks, ops, (alpha, causal), workers):
+        _seq_slice(o, b, off, L)[:, hq] = oh
+        if varlen:
+            lse[hq, off:off + L] = lh
+        else:
+            lse[b, hq] = lh
     return o, lse
 
 
@@ -182,28 +243,24 @@ def head_backward(qh, kh, vh, doh, alpha, causal=False):
     return dq, dk, dv
 
 
-def backward(q, k, v, do, alpha, causal=False, cu_seqlens=None, heads=None):
+def backward(q, k, v, do, alpha, causal=False, cu_seqlens=None, heads=None, workers=None):
     """dQ, dK, dV of L = sum(O * dO) for exact attention, float64.
 
     heads: optional query heads to include (for sampling whole heads of large
     workloads); dK/dV of a key/value head then sum only the included heads.
+    workers: evaluate the (sequence, head) problems in that many processes.
     """
     q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(do)
     Hq, Hkv = q.shape[-2], k.shape[-2]
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     shape = None if cu_seqlens is not None else q.shape[:2]
     heads = range(Hq) if heads is None else list(heads)
-    for b, off, L in _sequences(shape, cu_seqlens):
-        if L == 0:
-            continue
-        qs, ks, vs, dos = (_seq_slice(t, b, off, L) for t in (q, k, v, do))
-        dqs, dks, dvs = (_seq_slice(t, b, off, L) for t in (dq, dk, dv))
-        for hq in heads:
-            hk = kv_head_of(hq, Hq, Hkv)
-            a, bb, c = head_backward(qs[:, hq], ks[:, hk], vs[:, hk], dos[:, hq], alpha, causal)
-            dqs[:, hq] = a
-            dks[:, hk] += bb
-            dvs[:, hk] += c
+    tasks = _head_tasks(shape, cu_seqlens, heads, Hq, Hkv)
+    ops = [(q, "q"), (k, "k"), (v, "k"), (do, "q")]
+    for (b, off, L, hq, hk), (a, bb, c) in _run_heads(head_backward, tasks, ops, (alpha, causal), workers):
+        _seq_slice(dq, b, off, L)[:, hq] = a
+        _seq_slice(dk, b, off, L)[:, hk] += bb
+        _seq_slice(dv, b, off, L)[:, hk] += c
     return dq, dk, dv
 
 

@@ -83,11 +83,12 @@ def test_set_tuning_validation(lib):
 
 
 def test_forward_kernel_selector(lib):
-    """Kernels 0-2 are accepted, others rejected; no GPU call is made and the
-    pair kernel reports no resident pairs before it has ever been launched."""
+    """Kernels 0 and 2 are accepted, others rejected; no GPU call is made and
+    the pair kernel reports no resident pairs before it has ever been launched."""
     assert lib.fa_fwd_pairs_resident() == 0
-    for k in (0, 1, 2):
+    for k in (0, 2):
         assert lib.fa_set_fwd_kernel(k) == 0
+    assert lib.fa_set_fwd_kernel(1) == -1
     assert lib.fa_set_fwd_kernel(3) == -1
     assert lib.fa_set_fwd_kernel(-1) == -1
     assert lib.fa_set_fwd_kernel(2) == 0
@@ -112,3 +113,28 @@ def test_workspace_size_depends_on_head_dim(lib):
     assert 0 < n64 < n128
     assert n128 - n64 >= 2 * 4 * 1000 * 64 * 4        # B*N*Hq rows of 64 more floats
     assert f(2, 4, 1000, 96, 0, 0) == 0 and f(2, 4, 1000, 256, 0, 0) == 0   # no d = 256 backward
+
+
+def test_noalloc_returns_fa_bwd_codes_on_the_host(lib):
+    """fa_bwd_noalloc runs fa_bwd's argument checks first, so both entry
+    points give the same code for the same bad arguments (d = 256 and other
+    unbuilt head dims: FA_ERR_UNSUPPORTED); none of these calls reaches the
+    GPU."""
+    vp, i, fl, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    na, bw = lib.fa_bwd_noalloc, lib.fa_bwd
+    na.restype = bw.restype = i
+    na.argtypes = [vp] * 9 + [i, i, i, i, i, fl, i, vp, i, i, vp]
+    bw.argtypes = [vp] * 9 + [i, i, i, i, i, fl, i, vp, i, i, vp, sz, vp]
+    P = 0x10000
+    ok = dict(p=P, B=1, Hq=2, Hkv=2, N=128, d=128, alpha=0.1, causal=0, cu=None, ms=0, det=0)
+    cases = [dict(d=256), dict(d=96), dict(p=None), dict(B=0), dict(Hq=3), dict(alpha=0.0), dict(causal=2),
+             dict(det=2), dict(cu=P, ms=0), dict(cu=P, ms=1 << 20), dict(p=P + 8), dict(d=256, p=P + 8)]
+    for kw in cases:
+        a = dict(ok, **kw)
+        ptrs = [a["p"]] * 9
+        args = ptrs + [a["B"], a["Hq"], a["Hkv"], a["N"], a["d"], a["alpha"], a["causal"], a["cu"], a["ms"], a["det"]]
+        r_na = na(*args, None)
+        r_bw = bw(*args, P, 1 << 40, None)
+        assert r_na == r_bw and r_na < 0, (kw, r_na, r_bw)
+    a = dict(ok, d=256)
+    assert na(*([P] * 9 + [1, 2, 2, 128, 256, 0.1, 0, None, 0, 0]), None) == -2

@@ -54,9 +54,9 @@ def test_traffic_dropped_once_the_sources_change(fake_root):
 def test_traffic_key_follows_the_kernel_that_runs():
     large, varlen = W.WORKLOADS["large"], W.WORKLOADS["varlen"]
     assert bench.traffic_key(_args(), large, "fwd") == "fwd_pair"
-    assert bench.traffic_key(_args(fwd_kernel=1), large, "fwd") == "fwd_wide"
+    assert bench.traffic_key(_args(fwd_kernel=0), large, "fwd") == "fwd_pingpong"
     assert bench.traffic_key(_args(exp2_emu=1), large, "fwd") == "fwd_pingpong"
-    assert bench.traffic_key(_args(fwd_kernel=1), varlen, "fwd") == "fwd_pingpong"
+    assert bench.traffic_key(_args(), varlen, "fwd") == "fwd_pair"
     assert bench.traffic_key(_args(), large, "bwd") == "bwd"
     assert bench.traffic_key(_args(bwd_kernel=1), large, "bwd") == "bwd_pair"
     assert bench.traffic_key(_args(bwd_kernel=1, deterministic=True), large, "bwd") == "bwd"

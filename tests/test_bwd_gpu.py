@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import full_size as FS
 from attention_blackwell_gb300 import workloads as W
 from oracle import attention as A
 
@@ -64,8 +65,8 @@ def gpu_grads(fa, inp, causal, deterministic=False, repeats=1):
 
 def check(got, ref):
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
-        scale = np.abs(r).max()
-        err = np.abs(g - r).max()
+        scale = FS.max_abs(r)
+        err, _ = FS.abs_err_stats(g, r)
         assert np.isfinite(g).all(), name
         assert err <= REL * scale, (name, err, scale)
 
@@ -127,28 +128,25 @@ def test_large_q_logits(fa):
     check(gpu_grads(fa, inp, True)[0], oracle(inp, True))
 
 
-# --------------------------------------------- full-size causal backward
+# ------------------------------------ full-size workloads, every element
 
 @pytest.fixture(scope="module")
 def full(fa):
-    w = W.WORKLOADS["causal_bwd"]
-    inp = W.make_inputs(w)
+    """causal_bwd: atomic mode on this fixture's main kernel, and 10 runs of
+    deterministic mode."""
+    w, inp = FS.inputs("causal_bwd")
     atomic = gpu_grads(fa, inp, True, deterministic=False)[0]
     det = gpu_grads(fa, inp, True, deterministic=True, repeats=10)
     return w, inp, atomic, det
 
 
-def _head_ref(inp, w, b, h):
-    q, k, v, do = (inp[n][b, :, h].float().numpy().astype(np.float64) for n in ("q", "k", "v", "do"))
-    return A.head_backward(q, k, v, do, w.alpha, True)
-
-
-@pytest.mark.parametrize("b,h", [(0, 0), (1, 15)])
-def test_full_size_atomic_and_deterministic(full, b, h):
-    w, inp, atomic, det = full
-    ref = _head_ref(inp, w, b, h)
+def test_full_size_atomic_and_deterministic(full):
+    """Every element of dQ, dK, dV of the full causal backward, both modes,
+    against the float64 oracle over the whole workload."""
+    _, _, atomic, det = full
+    ref = FS.backward_reference("causal_bwd")
     for got in (atomic, det[0]):
-        check([g[b, :, h] for g in got], ref)
+        check(got, ref)
 
 
 def test_full_size_deterministic_bit_identical(full):
@@ -158,6 +156,29 @@ def test_full_size_deterministic_bit_identical(full):
             assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
     for a, b in zip(det[0], atomic):  # the two modes agree up to summation order
         assert np.abs(a - b).max() <= 1e-2 * max(np.abs(b).max(), 1e-6)
+
+
+def test_full_size_headline_every_element(fa):
+    """The headline step's backward (large: B=4, H=16, N=4096, non-causal,
+    atomic -- the work-unit order and claim counter the bench times, over
+    many waves of CTAs): every element against the whole-workload oracle."""
+    w, inp = FS.inputs("large")
+    check(gpu_grads(fa, inp, w.causal)[0], FS.backward_reference("large"))
+
+
+def test_varlen_full_size_every_sequence(fa):
+    """The packed causal MQA workload at full size (16 sequences of 512-8192
+    tokens, 32 query heads on one key/value head): every element of every
+    sequence, with the tolerance applied to the whole tensors and to each
+    sequence's own gradient scale."""
+    w, inp = FS.inputs("varlen")
+    got = gpu_grads(fa, inp, True)[0]
+    ref = FS.backward_reference("varlen")
+    check(got, ref)
+    cu = inp["cu_seqlens"]
+    for s in range(w.B):
+        c0, c1 = int(cu[s]), int(cu[s + 1])
+        check([g[c0:c1] for g in got], [r[c0:c1] for r in ref])
 
 
 # ------------------------------------------- work-list order and claiming
@@ -175,21 +196,6 @@ def test_varlen_deterministic_many_units(fa, causal):
         for a_, b_ in zip(runs[0], r):
             assert np.array_equal(a_.view(np.uint32), b_.view(np.uint32))
     check(runs[0], oracle(inp, causal))
-
-
-def test_varlen_full_size_mqa_sampled(fa):
-    """The packed causal workload at full size (16 sequences of 512-8192
-    tokens, 32 query heads on one key/value head): the two shortest
-    sequences checked whole, all 32 heads, against the oracle."""
-    w = W.WORKLOADS["varlen"]
-    inp = W.make_inputs(w, with_grad=True)
-    dq, dk, dv = gpu_grads(fa, inp, True)[0]
-    cu = inp["cu_seqlens"]
-    for s in np.argsort(inp["lengths"])[:2]:
-        c0, c1 = int(cu[s]), int(cu[s + 1])
-        sl = {n: inp[n][c0:c1].unsqueeze(0) for n in ("q", "k", "v", "do")}
-        ref = A.backward(sl["q"], sl["k"], sl["v"], sl["do"], w.alpha, True)
-        check([g[c0:c1] for g in (dq, dk, dv)], [r[0] for r in ref])
 
 
 def test_claim_counter_rewinds(fa):
