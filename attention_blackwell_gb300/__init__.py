@@ -12,7 +12,7 @@ import os
 
 import torch
 
-__all__ = ["fwd", "set_fwd_kernel", "fwd_pairs_resident", "set_bwd_kernel", "bwd_pairs_resident", "bwd", "bwd_workspace", "exp2_emu", "selftest_timeout", "set_tuning", "device_status", "num_sms", "FAError", "library_path", "lib"]
+__all__ = ["fwd", "set_fwd_kernel", "fwd_pairs_resident", "set_bwd_kernel", "bwd_pairs_resident", "bwd", "bwd_workspace", "exp2_emu", "selftest_timeout", "set_tuning", "set_debug_counters", "device_status", "num_sms", "FAError", "library_path", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libfa.so")
@@ -71,6 +71,8 @@ def lib():
         L.fa_exp2_emu.argtypes = [vp, vp, i64, vp]
         L.fa_selftest_timeout.restype = i
         L.fa_selftest_timeout.argtypes = [vp]
+        L.fa_set_debug_counters.restype = i
+        L.fa_set_debug_counters.argtypes = [vp, vp, vp]
         _lib = L
     return _lib
 
@@ -128,9 +130,10 @@ def num_sms():
     return n
 
 
-def set_tuning(exp2_emu_eighths=0, tau=8.0):
-    """Process-wide forward tuning (share of exp2 on the FMA pipe, rescale tau)."""
-    _check(lib().fa_set_tuning(int(exp2_emu_eighths), float(tau)), "fa_set_tuning")
+def set_tuning(exp2_emu_sixteenths=0, tau=8.0):
+    """Process-wide forward tuning (sixteenths of exp2 on the FMA pipe, 0-4;
+    rescale threshold tau)."""
+    _check(lib().fa_set_tuning(int(exp2_emu_sixteenths), float(tau)), "fa_set_tuning")
 
 
 def set_fwd_kernel(kernel=2):
@@ -201,8 +204,8 @@ def bwd_workspace(B, Hq, N, deterministic=False, varlen=False, device=None, d=HE
 
 def bwd(q, k, v, o, lse, do, causal=False, alpha=None, cu_seqlens=None, max_seqlen=None, deterministic=False,
         workspace=None, dq=None, dk=None, dv=None, stages=7, stream=None):
-    """Backward attention.  Returns (dq, dk, dv); layouts as in fwd, d = 128
-    or 64.
+    """Backward attention.  Returns (dq, dk, dv); layouts as in fwd, d = 128,
+    64 or 256.
 
     ``stages`` selects the launches (1 preprocess, 2 main, 4 postprocess);
     the default runs all three.
@@ -231,6 +234,15 @@ def bwd(q, k, v, o, lse, do, causal=False, alpha=None, cu_seqlens=None, max_seql
                              workspace.numel(), _stream(stream))
     _check(rc, "fa_bwd")
     return dq, dk, dv
+
+
+def set_debug_counters(visits=None, inner=None, rescales=None):
+    """Arm (tensors) or disarm (None) the kernels' debug counters: int32
+    visits / inner and int64 rescales[2] CUDA tensors the caller zeroes."""
+    for t, n, dt in ((visits, "visits", torch.int32), (inner, "inner", torch.int32), (rescales, "rescales", torch.int64)):
+        if t is not None:
+            _need(t, n, dt)
+    _check(lib().fa_set_debug_counters(_ptr(visits), _ptr(inner), _ptr(rescales)), "fa_set_debug_counters")
 
 
 def device_status(workspace=None, stream=None):

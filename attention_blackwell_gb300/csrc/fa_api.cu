@@ -29,10 +29,13 @@ struct DeviceInfo {
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
-int g_emu_eighths = 0;         // share of exp2 pairs on the FMA pipe (eighths)
+int g_emu16 = 0;               // share of exp2 pairs on the FMA pipe (sixteenths)
 int g_bwd_kernel = 0;          // 0: one CTA per 128-key tile; 1: CTA pairs per 256-key block
 int g_fwd_kernel = 2;          // 0: ping-pong of two 128-row query tiles; 2: CTA pairs
 float g_tau = 8.0f;            // conditional-rescale threshold, log2(256)
+int* g_dbg_visits = nullptr;   // debug counters (fa_set_debug_counters)
+int* g_dbg_inner = nullptr;
+unsigned long long* g_dbg_rescale = nullptr;
 
 int current_device_info(DeviceInfo** out) {
     int dev = 0;
@@ -132,10 +135,10 @@ int fa_num_sms(void) {
     return rc == FA_OK ? d->num_sms : rc;
 }
 
-int fa_set_tuning(int exp2_emu_eighths, float tau) {
-    if (exp2_emu_eighths < 0 || exp2_emu_eighths > 2) return FA_ERR_UNSUPPORTED;
+int fa_set_tuning(int exp2_emu_sixteenths, float tau) {
+    if (exp2_emu_sixteenths < 0 || exp2_emu_sixteenths > 4) return FA_ERR_UNSUPPORTED;
     if (!(tau >= 0.0f) || !(tau <= 64.0f)) return FA_ERR_INVALID;
-    g_emu_eighths = exp2_emu_eighths;
+    g_emu16 = exp2_emu_sixteenths;
     g_tau = tau;
     return FA_OK;
 }
@@ -163,9 +166,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     int rc = current_device_info(&dev);
     if (rc != FA_OK) return rc;
 
-    // The pair kernel uses the MUFU-only exp2 (the FMA-exp2 variants run on
-    // the ping-pong kernel); d = 64 runs on the ping-pong kernel.
-    const bool pair = d == 128 && g_emu_eighths == 0 && g_fwd_kernel == 2;
+    // d = 64 runs on the ping-pong kernel.
+    const bool pair = d == 128 && g_fwd_kernel == 2;
     FwdLaunch L;
     L.d = d;
     if (d == 256) {
@@ -205,7 +207,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     }
     L.a.scale_log2 = alpha * 1.4426950408889634f;
     L.a.tau = g_tau;
-    L.emu_eighths = g_emu_eighths;
+    L.a.dbg_visits = g_dbg_visits;
+    L.a.dbg_rescale = g_dbg_rescale;
+    L.emu16 = g_emu16;
     L.num_sms = dev->num_sms;
     cudaError_t e = d == 256 ? launch_fwd256(L, stream)
                     : pair    ? launch_fwd_pair(L, stream)
@@ -214,6 +218,16 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 }
 
 int fa_fwd_pairs_resident(void) { return g_pairs_resident; }
+
+int fa_set_debug_counters(int* visits, int* inner, unsigned long long* rescales) {
+    if ((reinterpret_cast<uintptr_t>(visits) & 3u) || (reinterpret_cast<uintptr_t>(inner) & 3u) ||
+        (reinterpret_cast<uintptr_t>(rescales) & 7u))
+        return FA_ERR_ALIGN;
+    g_dbg_visits = visits;
+    g_dbg_inner = inner;
+    g_dbg_rescale = rescales;
+    return FA_OK;
+}
 
 int fa_set_bwd_kernel(int kernel) {
     if (kernel < 0 || kernel > 1) return FA_ERR_INVALID;
@@ -269,7 +283,7 @@ int fa_get_device_status(const void* workspace, cudaStream_t stream) {
 }
 
 size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, int deterministic, int varlen) {
-    if (B < 1 || Hq < 1 || N < 0 || (d != 128 && d != 64)) return 0;
+    if (B < 1 || Hq < 1 || N < 0 || (d != 128 && d != 64 && d != 256)) return 0;
     const long long T = varlen ? (long long)N : (long long)B * N;
     return ws_layout(T, B, Hq, deterministic ? 1 : 0, varlen ? 1 : 0, d).total;
 }
@@ -285,7 +299,7 @@ int bwd_validate(const void* const ptrs[9], int B, int Hq, int Hkv, int N, int d
     if (B < 1 || N < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return FA_ERR_INVALID;
     if (!(alpha > 0.0f) || !isfinite(alpha)) return FA_ERR_INVALID;
     if ((causal != 0 && causal != 1) || (deterministic != 0 && deterministic != 1)) return FA_ERR_INVALID;
-    if (d != 128 && d != 64) return FA_ERR_UNSUPPORTED;
+    if (d != 128 && d != 64 && d != 256) return FA_ERR_UNSUPPORTED;
     const bool varlen = cu_seqlens != nullptr;
     if (varlen) {
         if (max_seqlen < 1) return FA_ERR_INVALID;
@@ -323,12 +337,15 @@ int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const
     if ((rc = current_device_info(&dev)) != FA_OK) return rc;
     BwdLaunch L;
     L.d = d;
-    if ((rc = make_map(&L.tq, q, Hq, T, kTileM, d)) != FA_OK) return rc;
+    // Q and dO boxes: 128 rows (d = 256: 64-row query steps).
+    const int qbox = d == 256 ? 64 : kTileM;
+    if ((rc = make_map(&L.tq, q, Hq, T, qbox, d)) != FA_OK) return rc;
     if ((rc = make_map(&L.tk, k, Hkv, T, kTileM, d)) != FA_OK) return rc;
     if ((rc = make_map(&L.tv, v, Hkv, T, kTileM, d)) != FA_OK) return rc;
-    if ((rc = make_map(&L.tdo, dout, Hq, T, kTileM, d)) != FA_OK) return rc;
+    if ((rc = make_map(&L.tdo, dout, Hq, T, qbox, d)) != FA_OK) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    if ((rc = make_map_acc(&L.tdq, ws + w.dq_off, (long long)Hq * T, kTileM, d)) != FA_OK) return rc;
+    // The fp32 dQ accumulator's map (TMA reductions; d = 256 adds per thread).
+    if (d != 256 && (rc = make_map_acc(&L.tdq, ws + w.dq_off, (long long)Hq * T, kTileM, d)) != FA_OK) return rc;
     BwdArgs& a = L.a;
     a.o = o;
     a.dO = dout;
@@ -355,6 +372,8 @@ int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const
     a.max_seqlen = varlen ? max_seqlen : N;
     a.alpha = alpha;
     a.scale_log2 = alpha * 1.4426950408889634f;
+    a.dbg_visits = g_dbg_visits;
+    a.dbg_inner = g_dbg_inner;
     L.num_sms = dev->num_sms;
     L.pair = d == 128 && g_bwd_kernel == 1 && bwd_pair_supported(a) ? 1 : 0;
     if (L.pair) {

@@ -35,6 +35,8 @@ __device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u &
 
 // Per lane of a warp on one row of D elements: D / 32 consecutive elements.
 template <int D> struct LaneVec;
+struct float8v { float4 lo, hi; };
+template <> struct LaneVec<256> { using bf = uint4; using f = float8v; };
 template <> struct LaneVec<128> { using bf = uint2; using f = float4; };
 template <> struct LaneVec<64> { using bf = uint32_t; using f = float2; };
 
@@ -44,12 +46,23 @@ __device__ __forceinline__ float dot_bf16(uint2 a, uint2 b) {
 __device__ __forceinline__ float dot_bf16(uint32_t a, uint32_t b) {
     return bf16lo(a) * bf16lo(b) + bf16hi(a) * bf16hi(b);
 }
+__device__ __forceinline__ float dot_bf16(uint4 a, uint4 b) {
+    return dot_bf16(make_uint2(a.x, a.y), make_uint2(b.x, b.y)) + dot_bf16(make_uint2(a.z, a.w), make_uint2(b.z, b.w));
+}
+__device__ __forceinline__ void zero_vec(float8v& v) {
+    v.lo = make_float4(0.f, 0.f, 0.f, 0.f);
+    v.hi = v.lo;
+}
 __device__ __forceinline__ void zero_vec(float4& v) { v = make_float4(0.f, 0.f, 0.f, 0.f); }
 __device__ __forceinline__ void zero_vec(float2& v) { v = make_float2(0.f, 0.f); }
 __device__ __forceinline__ uint2 pack_scaled(float4 g, float s) {
     return make_uint2(pack_bf16x2(g.x * s, g.y * s), pack_bf16x2(g.z * s, g.w * s));
 }
 __device__ __forceinline__ uint32_t pack_scaled(float2 g, float s) { return pack_bf16x2(g.x * s, g.y * s); }
+__device__ __forceinline__ uint4 pack_scaled(float8v g, float s) {
+    const uint2 a = pack_scaled(g.lo, s), b = pack_scaled(g.hi, s);
+    return make_uint4(a.x, a.y, b.x, b.y);
+}
 
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
@@ -87,8 +100,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
             }
         }
     }
-    if (a.deterministic) {
-        const long long n = (long long)a.Hq * a.sem_stride;
+    if (a.deterministic) {   // d = 256: one set per head-dim half
+        const long long n = (D == 256 ? 2LL : 1LL) * a.Hq * a.sem_stride;
         for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
              i += (long long)gridDim.x * blockDim.x)
             a.sem[i] = 0;
@@ -893,6 +906,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     }
                 }
                 sem_pend = sem;
+                if (r == 0) dbg_count(a.dbg_inner, (long long)h * a.T + U.tok0 + i * kTileM);
             }
             if (!ok) break;
             release_pending();   // before the dK/dV epilogue: the next key tile is waiting
@@ -923,6 +937,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     }
                 }
             }
+            if (r == 0) dbg_count(a.dbg_visits, (long long)U.hk * a.T + U.tok0 + U.k * kTileN);
             tc_fence_before();
             mbar_arrive(&sh.acc_free);
         }
@@ -956,7 +971,12 @@ cudaError_t launch_bwd_d(const BwdLaunch& L, int stages, cudaStream_t stream) {
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if ((stages & 2) && L.pair) {
+    if constexpr (D == 256) {
+        if (stages & 2) {
+            cudaError_t e = launch_bwd256_main(L, stream);
+            if (e != cudaSuccess) return e;
+        }
+    } else if ((stages & 2) && L.pair) {
         cudaError_t e = launch_bwd_pair_main(L, stream);
         if (e != cudaSuccess) return e;
     } else if (stages & 2) {
@@ -982,6 +1002,7 @@ cudaError_t launch_bwd_d(const BwdLaunch& L, int stages, cudaStream_t stream) {
 cudaError_t launch_bwd(const BwdLaunch& L, int stages, cudaStream_t stream) {
     if (L.d == 64) return launch_bwd_d<64>(L, stages, stream);
     if (L.d == 128) return launch_bwd_d<128>(L, stages, stream);
+    if (L.d == 256) return launch_bwd_d<256>(L, stages, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -1,0 +1,678 @@
+// fa_bwd256.cu -- backward main kernel for head dim d = 256 (sm_103a).
+//
+// The same gradients as fa_bwd.cu (FlashAttention-4 blog, "Backward pass":
+// S, dP, dV, dK, dQ plus the elementwise P and dS), at the head dim where the
+// products, not the exponentials, set the pace (paper summary, roofline
+// remarks).  At d = 256 neither of the one-CTA kernel's resources fits:
+//   * tensor memory: the dK and dV accumulators of a 128-key tile are
+//     128 x 256 fp32 each, i.e. all 512 columns together;
+//   * shared memory: a 128-row tile of K, V, Q or dO is 64 KB.
+// So each work unit (one 128-key tile of one key/value head) runs twice, once
+// per head-dim half h of the outputs: pass h keeps dK[:, h], dV[:, h] (128
+// columns each) in tensor memory and produces dQ[:, h].  Both passes recompute
+// S^T and dP^T over the full head dim (the price of the split: 14 instead of
+// 10 product units per tile).  K and V stay resident (128 KB); queries stream
+// in steps of 64 rows (Q and dO 32 KB each), and each step's Q and dO arrive
+// as two head-dim halves: the half the pass does not keep is free as soon as
+// S^T (dP^T) has read it, so the next step's copy starts early.
+//
+// Per step (128 keys x 64 queries), keys on the tensor-memory lanes:
+//   S^T  = K Q^T        M 128, N 64, K 256 (both K-major, shared memory)
+//   dP^T = V dO^T       M 128, N 64, K 256
+//   P^T  = 2^(alpha log2e S^T - LSE log2e)  -> bf16 into tensor memory
+//   dS^T = P^T (dP^T - D)                   -> bf16 into shared memory
+//   dV_h += P^T dO_h    M 128, N 128, K 64  (A = P^T from tensor memory)
+//   dK_h += dS^T Q_h    M 128, N 128, K 64
+//   dQ_h^T = K_h^T dS^T M 128 (head-dim half), N 64 (queries), K 128 (keys)
+// dQ is produced transposed so that the 128 drain threads each own one
+// head-dim column: their fp32 additions into the accumulator (red.global)
+// touch 32 consecutive floats per warp instruction, a whole 128-B line.
+//
+// Warp roles (512 threads): warps 0-3 and 12-15 key rows (P^T, dS^T; 32 of
+// the step's 64 queries each); warps 4-7 the dQ drain and the dK/dV epilogue;
+// warp 8 loader; warp 9 issues dP^T, dV, dQ^T, dK; warp 10 issues S^T.
+// Deterministic mode orders the dQ additions per (half, head, 64-row query
+// step) by key tile with the semaphores of the one-CTA kernel.
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kD6 = 256;
+constexpr int kStep = 64;                        // query rows per step
+constexpr int kThreads6 = 512;
+constexpr uint32_t kKBox6 = 16384;               // 128 rows x 128 B (K, V, dS^T)
+constexpr uint32_t kQBox6 = 8192;                // 64 rows x 128 B (Q, dO)
+constexpr uint32_t kOffK6 = 0, kOffV6 = 4 * kKBox6, kOffQ6 = 8 * kKBox6, kOffDO6 = kOffQ6 + 4 * kQBox6,
+                   kOffDS6 = kOffDO6 + 4 * kQBox6, kOffStat6 = kOffDS6 + kKBox6,
+                   kOffBar6 = kOffStat6 + 2 * kStep * 4;
+constexpr uint32_t kSmem6 = kOffBar6 + 1024;
+static_assert(kSmem6 <= 232448, "shared memory plan");
+constexpr uint32_t kColDK6 = 0, kColDV6 = 128, kColS6 = 256, kColDP6 = 320, kColDQ6 = 384;
+
+enum : int { k6SiteKvEmpty = 81, k6SiteQEmpty, k6SiteDoEmpty, k6SiteKvFull, k6SiteAcc, k6SiteQFull, k6SiteDoFull,
+             k6SiteP, k6SiteDs, k6SiteDqFree, k6SiteS, k6SiteDp, k6SiteDsFree, k6SiteDq, k6SiteDkdv, k6SiteSem,
+             k6SiteUnit };
+
+struct Shared6 {
+    uint64_t kv_full, kv_empty;
+    // Q and dO of a step arrive as two head-dim halves: "a" is the half this
+    // pass does not keep (read by S^T / dP^T only), "b" the pass's own half
+    // (read again by dK / dV).
+    uint64_t qa_full, qa_empty, qb_full, qb_empty, da_full, da_empty, db_full, db_empty;
+    uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dq_full, dq_free, dkdv_done, acc_free, r0_free, drain;
+    uint64_t unit_full[4], unit_empty[4];
+    int unit_id[4];
+    uint32_t tmem_base;
+    int abort_flag;
+    int total;
+};
+static_assert(sizeof(Shared6) <= 1024, "barrier block");
+
+constexpr uint32_t kUnitReaders6 = 2 + 256 + 128;
+
+struct Unit6 {
+    int seq, hk, k, tok0, len, n, nq, i0, pass;
+};
+
+// Work unit u: base unit u / 2 (one 128-key tile of one key/value head, in
+// the one-CTA kernel's order: head-major for non-causal atomic runs,
+// key-tile-major otherwise, the planned list for varlen), head-dim half
+// u % 2.  The two halves of a tile are neighbours in the list, so the CTAs
+// running them read the same K and V from L2 at about the same time.
+__device__ __forceinline__ bool unit6(const BwdArgs& a, int total, int u, Unit6& U) {
+    if (u < 0 || u >= total) return false;
+    const int ub = u >> 1;
+    U.pass = u & 1;
+    if (!a.varlen) {
+        const int bh = a.B * a.Hkv;
+        int r;
+        if (a.deterministic || a.causal) {
+            U.k = ub / bh;
+            r = ub - U.k * bh;
+        } else {
+            const int nk = (a.N + kTileN - 1) / kTileN;
+            r = ub / nk;
+            U.k = ub - r * nk;
+        }
+        U.seq = r / a.Hkv;
+        U.hk = r - U.seq * a.Hkv;
+        U.tok0 = U.seq * a.N;
+        U.len = a.N;
+    } else {
+        const int4 e = a.units[ub];
+        U.seq = e.x;
+        U.hk = e.y;
+        U.k = e.z;
+        U.tok0 = a.cu_s[U.seq];           // sanitised by the plan kernel
+        U.len = a.cu_s[U.seq + 1] - U.tok0;
+    }
+    U.nq = (U.len + kStep - 1) / kStep;
+    U.i0 = a.causal ? 2 * U.k : 0;        // first 64-row step that sees key tile k
+    if (U.i0 > U.nq) U.i0 = U.nq;
+    U.n = (a.Hq / a.Hkv) * (U.nq - U.i0);
+    return true;
+}
+
+// S^T / dP^T, the 8 K-steps over head-dim half HALF (boxes 2 HALF, 2 HALF + 1
+// of both operands): M = 128 keys, N = 64 queries, both K-major.
+template <int HALF>
+__device__ __forceinline__ void mma6_kq_half(uint32_t d, uint32_t a_smem, uint32_t b_smem, uint32_t first) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+    const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, 16, 1024);
+    static_for<8>([&](auto kc) {
+        constexpr uint32_t k = (uint32_t)kc + 8 * HALF;
+        constexpr uint32_t ao = ((k >> 2) * kKBox6 + (k & 3) * 32) >> 4;
+        constexpr uint32_t bo = ((k >> 2) * kQBox6 + (k & 3) * 32) >> 4;
+        umma_ss_k<ao, bo>(d, ad, bd, idesc, (first != 0 && kc == 0) ? 0u : 1u);
+    });
+}
+
+__device__ __forceinline__ void mma6_kq(uint32_t d, uint32_t a_smem, uint32_t b_smem, int half, uint32_t first) {
+    if (half) mma6_kq_half<1>(d, a_smem, b_smem, first);
+    else mma6_kq_half<0>(d, a_smem, b_smem, first);
+}
+
+// dV_h += P^T dO_h: M = 128 keys, N = 128 (the half's head-dim columns, two
+// 64-wide boxes), K = 64 queries.  A is bf16 in tensor memory: queries 0-31
+// in columns 0-15 of the S region, queries 32-63 in columns 32-47 (each key-
+// row warpgroup packs over the first half of the 32 columns it read).
+__device__ __forceinline__ void mma6_dv(uint32_t d, uint32_t p_tmem, uint32_t b_smem, uint32_t acc) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+    const uint64_t bd = sdesc_sw128(b_smem, kQBox6, 1024);
+    static_for<4>([&](auto kc) {
+        constexpr uint32_t k = kc, col = k * 8 + (k >= 2 ? 16 : 0);
+        umma_ts_k<col, ((k * 2048) >> 4)>(d, p_tmem, bd, idesc, (acc | k) != 0);
+    });
+}
+
+// dK_h += dS^T Q_h: A = dS^T K-major ([key][query], one 128 x 64 box), B = the
+// half's Q boxes MN-major.  M = 128, N = 128, K = 64.
+__device__ __forceinline__ void mma6_dk(uint32_t d, uint32_t a_smem, uint32_t b_smem, uint32_t acc) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+    const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, kQBox6, 1024);
+    static_for<4>([&](auto kc) {
+        constexpr uint32_t k = kc, ao = (k * 32) >> 4, bo = (k * 2048) >> 4;
+        umma_ss_k<ao, bo>(d, ad, bd, idesc, (acc | k) != 0);
+    });
+}
+
+// dQ_h^T = K_h^T dS^T: A = K's boxes of half h read MN-major (head dim
+// contiguous, the two 64-wide boxes one box apart), B = dS^T MN-major (the
+// queries contiguous in each key row).  M = 128, N = 64, K = 128 keys.
+__device__ __forceinline__ void mma6_dqt(uint32_t d, uint32_t a_smem, uint32_t b_smem) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 64, 1, 1);
+    const uint64_t ad = sdesc_sw128(a_smem, kKBox6, 1024), bd = sdesc_sw128(b_smem, kKBox6, 1024);
+    static_for<8>([&](auto kc) {
+        constexpr uint32_t k = kc, off = (k * 2048) >> 4;
+        umma_ss_k<off, off>(d, ad, bd, idesc, k > 0);
+    });
+}
+
+__device__ __forceinline__ void fence6_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void bar6(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ bool bar6_or(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(n) : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ int ld6_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red6_release_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void drain6(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(smem_u32(bar), parity) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+}
+
+__global__ void __launch_bounds__(kThreads6, 1)
+bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const BwdArgs a) {
+    extern __shared__ __align__(1024) uint8_t dsm[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t base = smem_u32(dsm);
+    if (base & 1023u) {  // the swizzled tiles need a 1024-byte aligned window
+        if (tid == 0 && atomicCAS(&a.hdr->status.code, 0, -1) == 0) a.hdr->status.where = 310;
+        return;
+    }
+    Shared6& sh = *reinterpret_cast<Shared6*>(dsm + kOffBar6);
+    float* s_lse = reinterpret_cast<float*>(dsm + kOffStat6);   // [64], LSE * log2(e)
+    float* s_D = s_lse + kStep;                                  // [64]
+    const uint32_t sK = base + kOffK6, sV = base + kOffV6, sQ = base + kOffQ6, sDO = base + kOffDO6,
+                   sDS = base + kOffDS6;
+
+    if (tid == 0) {
+        mbar_init(&sh.kv_full, 1);
+        mbar_init(&sh.kv_empty, 1);
+        mbar_init(&sh.qa_full, 1);
+        mbar_init(&sh.qa_empty, 1);
+        mbar_init(&sh.qb_full, 1);
+        mbar_init(&sh.qb_empty, 1);
+        mbar_init(&sh.da_full, 1);
+        mbar_init(&sh.da_empty, 1);
+        mbar_init(&sh.db_full, 1);
+        mbar_init(&sh.db_empty, 1);
+        mbar_init(&sh.s_full, 1);
+        mbar_init(&sh.dp_full, 1);
+        mbar_init(&sh.p_ready, 256);
+        mbar_init(&sh.ds_ready, 256);
+        mbar_init(&sh.ds_free, 1);
+        mbar_init(&sh.dq_full, 1);
+        mbar_init(&sh.dq_free, 128);
+        mbar_init(&sh.dkdv_done, 1);
+        mbar_init(&sh.acc_free, 128);
+        mbar_init(&sh.r0_free, 1);
+        mbar_init(&sh.drain, 2);   // both issuers
+        for (int s = 0; s < 4; ++s) { mbar_init(&sh.unit_full[s], 1); mbar_init(&sh.unit_empty[s], kUnitReaders6); }
+        sh.abort_flag = 0;
+        sh.total = 2 * (a.varlen ? a.hdr->total_units : a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN));
+        fence_mbar_init();
+    }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_desc(&tq);
+        tma_prefetch_desc(&tk);
+        tma_prefetch_desc(&tv);
+        tma_prefetch_desc(&tdo);
+    }
+    if (warp == 0) {
+        tmem_alloc(&sh.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const WaitCtx wc{&sh.abort_flag, &a.hdr->status};
+    const uint32_t tmem = sh.tmem_base;
+    const int total = sh.total;
+    const int g = a.Hq / a.Hkv;
+    const float scale = a.scale_log2;
+
+    // Register split (launch 512 x 128 = 65536): key-row warpgroups 144 each,
+    // dQ / epilogue warpgroup 168, loader / issuer warpgroup 56.
+    if (warp >= 8 && warp < 12) {
+        regs_dec<56>();
+        if (warp == 8) {
+            // ------------------------------------------------------------ loader
+            uint32_t jj = 0, uc = 0;
+            // Loads issued on each full barrier, for the drain at the end.
+            uint32_t n_qa = 0, n_da = 0, n_qb = 0, n_db = 0, n_kv = 0;
+            bool ok = true;
+            for (uint32_t n = 0; ok; ++n) {
+                int u = -1;
+                if (lane == 0) {
+                    ok = mbar_wait(&sh.unit_empty[n & 3], ((n >> 2) & 1) ^ 1, wc, k6SiteUnit);
+                    if (ok) {
+                        // The first unit by block index, later ones in list
+                        // order from the workspace counter; the last CTA to
+                        // find the list exhausted rewinds it.
+                        u = n == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&a.hdr->next_unit, 1);
+                        if (u >= total) {
+                            u = -1;
+                            if (atomicAdd(&a.hdr->done_ctas, 1) == (int)gridDim.x - 1) {
+                                atomicExch(&a.hdr->next_unit, 0);
+                                atomicExch(&a.hdr->done_ctas, 0);
+                            }
+                        }
+                        sh.unit_id[n & 3] = u;
+                        mbar_arrive(&sh.unit_full[n & 3]);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                u = __shfl_sync(0xffffffffu, u, 0);
+                if (!ok) break;
+                Unit6 U;
+                if (!unit6(a, total, u, U)) break;
+                if (lane == 0) ok = mbar_wait(&sh.kv_empty, (uc & 1) ^ 1, wc, k6SiteKvEmpty);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&sh.kv_full, 8 * kKBox6);
+                    for (int c = 0; c < 4; ++c) {
+                        tma_load_3d(sK + c * kKBox6, &tk, &sh.kv_full, c * 64, U.hk, U.tok0 + U.k * kTileN);
+                        tma_load_3d(sV + c * kKBox6, &tv, &sh.kv_full, c * 64, U.hk, U.tok0 + U.k * kTileN);
+                    }
+                }
+                ++n_kv;
+                const int span = U.nq - U.i0;
+                const int ca = 2 * (1 - U.pass), cb = 2 * U.pass;   // first box of each head-dim half
+                // LSE and D of a step, loaded one step ahead into registers.
+                float nl[2], nd[2];
+                auto load_stats = [&](int t) {
+                    const int h = U.hk * g + t / span, i = U.i0 + t % span;
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int q = i * kStep + 2 * lane + e;
+                        nl[e] = 0.f;
+                        nd[e] = 0.f;
+                        if (q < U.len) {
+                            const size_t li = a.varlen ? (size_t)h * a.T + U.tok0 + q
+                                                       : ((size_t)U.seq * a.Hq + h) * a.N + q;
+                            nl[e] = a.lse[li] * 1.4426950408889634f;
+                            nd[e] = a.D[(size_t)h * a.T + U.tok0 + q];
+                        }
+                    }
+                };
+                load_stats(0);
+                for (int t = 0; t < U.n; ++t, ++jj) {
+                    const int h = U.hk * g + t / span, i = U.i0 + t % span, row = U.tok0 + i * kStep;
+                    const uint32_t ep = (jj & 1) ^ 1;
+                    if (lane == 0) {
+                        // The half the pass does not keep: free once S^T / dP^T read it.
+                        ok = mbar_wait(&sh.qa_empty, ep, wc, k6SiteQEmpty);
+                        if (ok) {
+                            mbar_arrive_expect_tx(&sh.qa_full, 2 * kQBox6);
+                            for (int c = ca; c < ca + 2; ++c)
+                                tma_load_3d(sQ + c * kQBox6, &tq, &sh.qa_full, c * 64, h, row);
+                            ++n_qa;
+                        }
+                        if (ok) ok = mbar_wait(&sh.da_empty, ep, wc, k6SiteDoEmpty);
+                        if (ok) {
+                            mbar_arrive_expect_tx(&sh.da_full, 2 * kQBox6);
+                            for (int c = ca; c < ca + 2; ++c)
+                                tma_load_3d(sDO + c * kQBox6, &tdo, &sh.da_full, c * 64, h, row);
+                            ++n_da;
+                        }
+                        // The pass's own half (and the step's LSE / D): free
+                        // once dK (Q) and dV (dO) of the previous step are done.
+                        if (ok) ok = mbar_wait(&sh.qb_empty, ep, wc, k6SiteQEmpty);
+                        if (ok) {
+                            mbar_expect_tx(&sh.qb_full, 2 * kQBox6);
+                            for (int c = cb; c < cb + 2; ++c)
+                                tma_load_3d(sQ + c * kQBox6, &tq, &sh.qb_full, c * 64, h, row);
+                        }
+                    }
+                    n_qb += ok ? 1 : 0;
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    // qb_full's one arrival follows the LSE / D stores.
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        s_lse[2 * lane + e] = nl[e];
+                        s_D[2 * lane + e] = nd[e];
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&sh.qb_full);
+                        ok = mbar_wait(&sh.db_empty, ep, wc, k6SiteDoEmpty);
+                        if (ok) {
+                            mbar_arrive_expect_tx(&sh.db_full, 2 * kQBox6);
+                            for (int c = cb; c < cb + 2; ++c)
+                                tma_load_3d(sDO + c * kQBox6, &tdo, &sh.db_full, c * 64, h, row);
+                            ++n_db;
+                        }
+                    }
+                    if (t + 1 < U.n) load_stats(t + 1);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                }
+                ++uc;
+            }
+            if (lane == 0) {  // every copy this thread issued has landed before teardown
+                if (n_qa) drain6(&sh.qa_full, (n_qa - 1) & 1);
+                if (n_da) drain6(&sh.da_full, (n_da - 1) & 1);
+                if (n_qb) drain6(&sh.qb_full, (n_qb - 1) & 1);
+                if (n_db) drain6(&sh.db_full, (n_db - 1) & 1);
+                if (n_kv) drain6(&sh.kv_full, (n_kv - 1) & 1);
+            }
+            __syncwarp();
+        } else if (warp == 10) {
+            // ------------------------------------------------------- S issuer
+            uint32_t jj = 0, uc = 0;
+            bool ok = true;
+            for (uint32_t n = 0; ok; ++n) {
+                if (!(ok = mbar_wait_w(&sh.unit_full[n & 3], (n >> 2) & 1, wc, k6SiteUnit))) break;
+                const int u = *(volatile int*)&sh.unit_id[n & 3];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.unit_empty[n & 3]);
+                Unit6 U;
+                if (!unit6(a, total, u, U)) break;
+                if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, k6SiteKvFull))) break;
+                for (int t = 0; t < U.n; ++t, ++jj) {
+                    // dV of the previous step has read P^T out of the S region.
+                    if (jj > 0 && !(ok = mbar_wait_w(&sh.r0_free, (jj - 1) & 1, wc, k6SiteP))) break;
+                    if (!(ok = mbar_wait_w(&sh.qa_full, jj & 1, wc, k6SiteQFull))) break;
+                    tc_fence_after();
+                    mma6_kq(tmem + kColS6, sK, sQ, 1 - U.pass, 1);
+                    umma_commit_w(&sh.qa_empty);
+                    if (!(ok = mbar_wait_w(&sh.qb_full, jj & 1, wc, k6SiteQFull))) break;
+                    tc_fence_after();
+                    mma6_kq(tmem + kColS6, sK, sQ, U.pass, 0);
+                    umma_commit_w(&sh.s_full);
+                }
+                ++uc;
+            }
+            umma_commit_w(&sh.drain);
+            drain6(&sh.drain, 0);
+            __syncwarp();
+        } else if (warp == 9) {
+            // --------------------------------------- dP^T, dV, dQ^T, dK issuer
+            uint32_t jj = 0, uc = 0;
+            bool ok = true;
+            for (uint32_t n = 0; ok; ++n) {
+                if (!(ok = mbar_wait_w(&sh.unit_full[n & 3], (n >> 2) & 1, wc, k6SiteUnit))) break;
+                const int u = *(volatile int*)&sh.unit_id[n & 3];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.unit_empty[n & 3]);
+                Unit6 U;
+                if (!unit6(a, total, u, U)) break;
+                if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, k6SiteKvFull))) break;
+                if (!(ok = mbar_wait_w(&sh.acc_free, (uc & 1) ^ 1, wc, k6SiteAcc))) break;
+                const uint32_t oK = U.pass * 2 * kKBox6, oQ = U.pass * 2 * kQBox6;   // the pass's half
+                for (int t = 0; t < U.n; ++t, ++jj) {
+                    if (!(ok = mbar_wait_w(&sh.da_full, jj & 1, wc, k6SiteDoFull))) break;
+                    tc_fence_after();
+                    mma6_kq(tmem + kColDP6, sV, sDO, 1 - U.pass, 1);
+                    umma_commit_w(&sh.da_empty);
+                    if (!(ok = mbar_wait_w(&sh.db_full, jj & 1, wc, k6SiteDoFull))) break;
+                    tc_fence_after();
+                    mma6_kq(tmem + kColDP6, sV, sDO, U.pass, 0);
+                    umma_commit_w(&sh.dp_full);
+                    if (!(ok = mbar_wait_w(&sh.p_ready, jj & 1, wc, k6SiteP))) break;
+                    tc_fence_after();
+                    mma6_dv(tmem + kColDV6, tmem + kColS6, sDO + oQ, t > 0);
+                    umma_commit_w(&sh.db_empty);    // dO read by dP^T and dV
+                    umma_commit_w(&sh.r0_free);     // P^T read: the next S^T may overwrite it
+                    if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, k6SiteDs))) break;
+                    if (jj > 0 && !(ok = mbar_wait_w(&sh.dq_free, (jj - 1) & 1, wc, k6SiteDqFree))) break;
+                    tc_fence_after();
+                    mma6_dqt(tmem + kColDQ6, sK + oK, sDS);
+                    umma_commit_w(&sh.dq_full);
+                    mma6_dk(tmem + kColDK6, sDS, sQ + oQ, t > 0);
+                    umma_commit_w(&sh.qb_empty);    // Q (and the step's LSE / D) consumed
+                    umma_commit_w(&sh.ds_free);     // dS^T read by dQ^T and dK
+                }
+                if (!ok) break;
+                umma_commit_w(&sh.dkdv_done);
+                umma_commit_w(&sh.kv_empty);
+                ++uc;
+            }
+            umma_commit_w(&sh.drain);
+            drain6(&sh.drain, 0);
+            __syncwarp();
+        }
+    } else if (warp < 4 || warp >= 12) {
+        regs_inc<144>();
+        // ------------------------------------------------ P^T and dS^T (key rows)
+        const int hc = warp >= 12 ? 1 : 0;                   // which 32 of the step's 64 queries
+        const int cb = hc * 32;
+        const int r = (warp & 3) * 32 + lane;                // key row in the tile == TMEM lane
+        const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lb + kColS6 + cb, tDP = tmem + lb + kColDP6 + cb;
+        uint8_t* ds_row = dsm + kOffDS6 + r * 128;
+        const int sw = r & 7;
+        uint32_t jj = 0;
+        bool ok = true;
+        for (uint32_t n = 0; ok; ++n) {
+            if (!(ok = mbar_wait(&sh.unit_full[n & 3], (n >> 2) & 1, wc, k6SiteUnit))) break;
+            const int u = *(volatile int*)&sh.unit_id[n & 3];
+            mbar_arrive(&sh.unit_empty[n & 3]);
+            Unit6 U;
+            if (!unit6(a, total, u, U)) break;
+            const int key = U.k * kTileN + r;
+            const int span = U.nq - U.i0;
+            for (int t = 0; t < U.n; ++t, ++jj) {
+                const int i = U.i0 + t % span;
+                if (!(ok = mbar_wait(&sh.qb_full, jj & 1, wc, k6SiteQFull))) break;   // LSE / D stored
+                if (!(ok = mbar_wait(&sh.s_full, jj & 1, wc, k6SiteS))) break;
+                tc_fence_after();
+                float p[32];
+                tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(p));
+                tmem_wait_ld();
+                // visible columns c: query 64 i + cb + c < len, key < len, key <= query if causal
+                const int c_lo = (a.causal ? key - i * kStep : 0) - cb;
+                const int c_hi = (key >= U.len ? 0 : U.len - i * kStep) - cb;
+                const float4* l4v = reinterpret_cast<const float4*>(s_lse + cb);
+                if (c_lo <= 0 && c_hi >= 32) {
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 l4 = l4v[c4];
+                        p[4 * c4] = ex2_mufu(fmaf(p[4 * c4], scale, -l4.x));
+                        p[4 * c4 + 1] = ex2_mufu(fmaf(p[4 * c4 + 1], scale, -l4.y));
+                        p[4 * c4 + 2] = ex2_mufu(fmaf(p[4 * c4 + 2], scale, -l4.z));
+                        p[4 * c4 + 3] = ex2_mufu(fmaf(p[4 * c4 + 3], scale, -l4.w));
+                    }
+                } else {
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 l4 = l4v[c4];
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = 4 * c4 + e;
+                            const float pe = ex2_mufu(fmaf(p[c], scale, -lv[e]));
+                            p[c] = (c >= c_lo && c < c_hi) ? pe : 0.f;
+                        }
+                    }
+                }
+                {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int m = 0; m < 16; ++m) pk[m] = pack_bf16x2(p[2 * m], p[2 * m + 1]);
+                    tmem_st16(tS, pk);   // P^T: two bf16 per column, over this half's first 16 columns
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&sh.p_ready);
+
+                // dS^T from this half's dP^T columns, into shared memory.
+                if (!(ok = mbar_wait(&sh.dp_full, jj & 1, wc, k6SiteDp))) break;
+                if (!(ok = mbar_wait(&sh.ds_free, (jj & 1) ^ 1, wc, k6SiteDsFree))) break;
+                tc_fence_after();
+                uint32_t dp[32];
+                tmem_ld32(tDP, dp);
+                tmem_wait_ld();
+                const float4* d4v = reinterpret_cast<const float4*>(s_D + cb);
+                uint32_t pk[16];
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const float4 d4 = d4v[m];
+                    const int c = 4 * m;
+                    pk[2 * m] = pack_bf16x2(p[c] * (__uint_as_float(dp[c]) - d4.x),
+                                            p[c + 1] * (__uint_as_float(dp[c + 1]) - d4.y));
+                    pk[2 * m + 1] = pack_bf16x2(p[c + 2] * (__uint_as_float(dp[c + 2]) - d4.z),
+                                                p[c + 3] * (__uint_as_float(dp[c + 3]) - d4.w));
+                }
+                // 32 queries = four 16-byte chunks; chunk q of the row holds
+                // queries 8q .. 8q+7 at position q ^ (row % 8) (128-B swizzle).
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int q = hc * 4 + m;
+                    *reinterpret_cast<uint4*>(ds_row + ((q ^ sw) << 4)) =
+                        make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
+                }
+                fence6_async_smem();   // dS^T is read by the dQ^T and dK products
+                tc_fence_before();
+                mbar_arrive(&sh.ds_ready);
+            }
+        }
+    } else {
+        regs_inc<168>();
+        // -------------------------------------------- dQ drain, dK/dV epilogue
+        const int r = tid - 128;                             // head-dim column (dQ^T) / key row (dK, dV)
+        const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tDQ = tmem + lb + kColDQ6;
+        uint32_t jj = 0, uc = 0;
+        bool ok = true;
+        for (uint32_t n = 0; ok; ++n) {
+            ok = mbar_wait(&sh.unit_full[n & 3], (n >> 2) & 1, wc, k6SiteUnit);
+            if (bar6_or(1, 128, !ok)) { ok = false; break; }
+            const int u = *(volatile int*)&sh.unit_id[n & 3];
+            mbar_arrive(&sh.unit_empty[n & 3]);
+            Unit6 U;
+            if (!unit6(a, total, u, U)) break;
+            const int span = U.nq - U.i0;
+            for (int t = 0; t < U.n; ++t, ++jj) {
+                const int h = U.hk * g + t / span, i = U.i0 + t % span;
+                ok = mbar_wait(&sh.dq_full, jj & 1, wc, k6SiteDq);
+                ok = !bar6_or(1, 128, !ok);
+                if (!ok) break;
+                tc_fence_after();
+                float v[64];
+                tmem_ld32(tDQ, *reinterpret_cast<uint32_t(*)[32]>(v));
+                tmem_ld32(tDQ + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(&sh.dq_free);
+                int* sem = a.deterministic
+                               ? a.sem + ((size_t)U.pass * a.Hq + h) * a.sem_stride + U.seq + (U.tok0 + i * kStep) / kStep
+                               : nullptr;
+                if (sem) {
+                    // Key tiles add into this query step in ascending order.
+                    bool gave_up = false;
+                    if (r == 0) {
+                        const uint64_t t0 = globaltimer_ns();
+                        uint32_t spins = 0;
+                        while (ld6_acquire(sem) != U.k) {
+                            if ((++spins & 255u) == 0 &&
+                                (*(volatile int*)&sh.abort_flag || globaltimer_ns() - t0 > kWaitLimitNs)) {
+                                if (atomicCAS(&a.hdr->status.code, 0, kStatusTimeout) == 0) {
+                                    a.hdr->status.where = k6SiteSem;
+                                    a.hdr->status.block = blockIdx.x;
+                                }
+                                *(volatile int*)&sh.abort_flag = 1;
+                                gave_up = true;
+                                break;
+                            }
+                        }
+                    }
+                    if (bar6_or(1, 128, gave_up)) { ok = false; break; }
+                }
+                // Column r of this half for the step's valid rows: a warp
+                // instruction adds one query row's 32 consecutive floats.
+                const int rows = U.len - i * kStep < kStep ? U.len - i * kStep : kStep;
+                float* dst = a.dqacc + ((size_t)h * a.T + U.tok0 + i * kStep) * kD6 + U.pass * 128 + r;
+#pragma unroll
+                for (int q = 0; q < kStep; ++q)
+                    if (q < rows) atomicAdd(dst + (size_t)q * kD6, v[q]);
+                if (sem) {
+                    __threadfence();   // this thread's additions are performed ...
+                    bar6(1, 128);      // ... by every thread of the group ...
+                    if (r == 0) red6_release_add(sem, 1);   // ... before the next key tile may add
+                }
+                if (r == 0 && U.pass == 0) dbg_count(a.dbg_inner, (long long)h * a.T + U.tok0 + i * kStep);
+            }
+            if (!ok) break;
+            ok = mbar_wait(&sh.dkdv_done, uc & 1, wc, k6SiteDkdv);
+            if (bar6_or(1, 128, !ok)) { ok = false; break; }
+            ++uc;
+            tc_fence_after();
+            const int key = U.k * kTileN + r;
+            const bool kvalid = key < U.len;
+            const size_t orow = ((size_t)(U.tok0 + key) * a.Hkv + U.hk) * kD6 + U.pass * 128;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t tacc = tmem + lb + (which ? kColDV6 : kColDK6);
+                const float mul = which ? 1.f : a.alpha;
+                uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which ? a.dv : a.dk) + orow);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t w[32];
+                    tmem_ld32(tacc + cc * 32, w);
+                    tmem_wait_ld();
+                    if (kvalid) {
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const float* f = reinterpret_cast<const float*>(w + 8 * m);
+                            out[cc * 4 + m] = make_uint4(pack_bf16x2(f[0] * mul, f[1] * mul), pack_bf16x2(f[2] * mul, f[3] * mul),
+                                                         pack_bf16x2(f[4] * mul, f[5] * mul), pack_bf16x2(f[6] * mul, f[7] * mul));
+                        }
+                    }
+                }
+            }
+            if (r == 0 && U.pass == 0) dbg_count(a.dbg_visits, (long long)U.hk * a.T + U.tok0 + U.k * kTileN);
+            tc_fence_before();
+            mbar_arrive(&sh.acc_free);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd256_main(const BwdLaunch& L, cudaStream_t stream) {
+    const BwdArgs& a = L.a;
+    cudaError_t e = cudaFuncSetAttribute(bwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem6);
+    if (e != cudaSuccess) return e;
+    const long long units = 2 * (a.varlen ? (long long)a.Hkv * ((a.T + kTileN - 1) / kTileN + a.B)
+                                          : (long long)a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN));
+    int grid = (int)(units < L.num_sms ? units : L.num_sms);
+    if (grid < 1) grid = 1;
+    bwd256_kernel<<<grid, kThreads6, kSmem6, stream>>>(L.tq, L.tk, L.tv, L.tdo, a);
+    return cudaGetLastError();
+}
+
+}  // namespace fa

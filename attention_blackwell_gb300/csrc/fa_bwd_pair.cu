@@ -656,6 +656,11 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                         pb_bulk_commit();
                     }
                 }
+                // This CTA's key tile contributed to query tile i unless it
+                // lies past the sequence or (causal) after the tile's rows.
+                const int kt = 2 * U.kb + PB_RANK;
+                if (r == 0 && kt * kTileN < U.len && (!a.causal || i >= kt))
+                    dbg_count(a.dbg_inner, (long long)h * a.T + U.tok0 + i * kTileM);
             }
             if (!ok) break;
             if (!(ok = mbar_wait(&sh.dkdv_done, uc & 1, wc, kPBSiteDkdv))) break;
@@ -688,6 +693,8 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     }
                 }
             }
+            if (r == 0 && (2 * U.kb + PB_RANK) * kTileN < U.len)
+                dbg_count(a.dbg_visits, (long long)U.hk * a.T + U.tok0 + (2 * U.kb + PB_RANK) * kTileN);
             tc_fence_before();
             mbar_arrive_remote_w(lead(&sh.acc_free));
         }

@@ -23,6 +23,8 @@
 #pragma once
 #include <stdint.h>
 
+#include "fa_prim.cuh"
+
 namespace fa {
 
 constexpr float kExp2P1 = 0x1.63e66ap-1f;  // 0.69511729
@@ -36,6 +38,26 @@ __device__ __forceinline__ float exp2_fma(float x) {
     const float f = x - n;                      // [0, 1), exact
     const float p = fmaf(f, fmaf(f, fmaf(f, kExp2P3, kExp2P2), kExp2P1), 1.0f);
     return __int_as_float(__float_as_int(p) + (__float_as_int(j) << 23));
+}
+
+// The same function on two lanes of a packed fp32 pair (sm_100 family f32x2
+// arithmetic: one instruction per step for both elements); every step rounds
+// exactly as in exp2_fma, so each element equals exp2_fma's result.
+__device__ __forceinline__ void exp2_fma_x2(float x0, float x1, float& y0, float& y1) {
+    uint64_t x, j, n, f, p;
+    x = f2_pack(fmaxf(x0, -127.0f), fmaxf(x1, -127.0f));
+    const uint64_t magic = f2_pack(12582912.0f, 12582912.0f);
+    asm("add.rm.f32x2 %0, %1, %2;" : "=l"(j) : "l"(x), "l"(magic));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(n) : "l"(j), "l"(magic));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(f) : "l"(x), "l"(n));
+    p = f2_fma(f, f2_pack(kExp2P3, kExp2P3), f2_pack(kExp2P2, kExp2P2));
+    p = f2_fma(f, p, f2_pack(kExp2P1, kExp2P1));
+    p = f2_fma(f, p, f2_pack(1.0f, 1.0f));
+    float p0, p1, j0, j1;
+    f2_unpack(p, p0, p1);
+    f2_unpack(j, j0, j1);
+    y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(j0) << 23));
+    y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(j1) << 23));
 }
 
 }  // namespace fa

@@ -100,7 +100,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
     });
 }
 
-template <int kEmuEighths, int D>
+template <int kEmu16, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
            const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
@@ -336,7 +336,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 // equation): move to the new max only if some row of this warp
                 // jumped by more than tau; the first tile always initialises.
                 const bool jump = (m_ref == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_ref > a.tau);
-                if (__any_sync(0xffffffffu, jump)) {
+                const bool rescale = __any_sync(0xffffffffu, jump);
+                if (lane == 0) dbg_count_rescale(a.dbg_rescale, j > 0, rescale);
+                if (rescale) {
                     const float fac = (m_ref == -INFINITY) ? 0.f : ex2_mufu(m_ref - m_new);
                     l *= fac;
                     if (j > 0) {
@@ -362,7 +364,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         const int c = st * 32 + 2 * i;
                         const float x0 = fmaf(s[c], scale, -m_use), x1 = fmaf(s[c + 1], scale, -m_use);
                         float p0, p1;
-                        if ((i & 7) < kEmuEighths) { p0 = exp2_fma(x0); p1 = exp2_fma(x1); }
+                        if (i < kEmu16) { p0 = exp2_fma(x0); p1 = exp2_fma(x1); }   // kEmu16 of 16 pairs
                         else { p0 = ex2_mufu(x0); p1 = ex2_mufu(x1); }
                         l0 += p0;
                         l1 += p1;
@@ -407,6 +409,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                                            : ((size_t)U.seq * a.Hq + U.h) * a.N + qi;
                 a.lse[li] = lse;
             }
+            if (r == 0 && q_first < U.len)
+                dbg_count(a.dbg_visits, (long long)U.h * (a.varlen ? a.N : (long long)a.B * a.N) + U.tok0 + q_first);
         }
     }
 
@@ -433,9 +437,21 @@ __global__ void selftest_timeout_kernel(DevStatus* status) {
     if (ok && threadIdx.x == 0) atomicCAS(&status->code, 0, -1);   // the phase cannot complete
 }
 
+// Both forms the forward kernels use: the scalar one (ping-pong kernel) and
+// the packed pair (CTA-pair kernel).  They must agree bit for bit; an element
+// where they do not is returned as NaN, so a test of y checks both.
 __global__ void exp2_emu_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-        y[i] = exp2_fma(x[i]);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        // The second lane gets the neighbouring element, so both lanes of
+        // the packed form are checked.
+        const int64_t nb = (i ^ 1) < n ? (i ^ 1) : i;
+        const float xi = x[i], xn = x[nb];
+        const float ys = exp2_fma(xi), yn = exp2_fma(xn);
+        float yp, yq;
+        exp2_fma_x2(xi, xn, yp, yq);
+        const bool same = __float_as_uint(ys) == __float_as_uint(yp) && __float_as_uint(yn) == __float_as_uint(yq);
+        y[i] = same ? ys : __int_as_float(0x7fc00000);
+    }
 }
 
 template <int E, int D>
@@ -450,10 +466,12 @@ cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream, int grid) {
 
 template <int D>
 cudaError_t launch_fwd_d(const FwdLaunch& L, cudaStream_t stream, int grid) {
-    switch (L.emu_eighths) {
+    switch (L.emu16) {
         case 0: return launch_fwd_t<0, D>(L, stream, grid);
         case 1: return launch_fwd_t<1, D>(L, stream, grid);
         case 2: return launch_fwd_t<2, D>(L, stream, grid);
+        case 3: return launch_fwd_t<3, D>(L, stream, grid);
+        case 4: return launch_fwd_t<4, D>(L, stream, grid);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -404,7 +404,9 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 // Conditional rescale (blog, "Forward pass"): move to the new
                 // maximum only when some row of this warp jumped by more than tau.
                 const bool jump = (m_ref == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_ref > a.tau);
-                if (__any_sync(0xffffffffu, jump)) {
+                const bool rescale = __any_sync(0xffffffffu, jump);
+                if (lane == 0) dbg_count_rescale(a.dbg_rescale, j > 0, rescale);
+                if (rescale) {
                     const float fac = (m_ref == -INFINITY) ? 0.f : ex2_mufu(m_ref - m_new);
                     l *= fac;
                     if (j > 0) {
@@ -493,6 +495,8 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                                            : ((size_t)U.seq * a.Hq + U.h) * a.N + qi;
                 a.lse[li] = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             }
+            if (r == 0 && q_first < U.len)
+                dbg_count(a.dbg_visits, (long long)U.h * (a.varlen ? a.N : (long long)a.B * a.N) + U.tok0 + q_first);
         }
     }
 

@@ -29,6 +29,7 @@
 // and softmax arrivals count there.
 //
 // Fixed-length and packed varlen inputs.
+#include "fa_exp2.cuh"
 #include "fa_internal.h"
 #include "fa_sched.cuh"
 
@@ -127,6 +128,10 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     while (!mbar_try_wait(smem_u32(bar), parity) && globaltimer_ns() - t0 < kWaitLimitNs) {}
 }
 
+// kEmu16: of every 16 column pairs of a row half, how many take their exp2
+// from the FMA-pipe polynomial (fa_exp2.cuh) instead of MUFU.EX2
+// (FlashAttention-4 blog, "Faster exponential").
+template <int kEmu16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
 fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, const FwdArgs a) {
@@ -434,6 +439,8 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 const size_t li = a.varlen ? (size_t)U.h * a.N + U.tok0 + qi : ((size_t)U.seq * a.Hq + U.h) * a.N + qi;
                 a.lse[li] = lt > 0.f ? (mp + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
             }
+            if (x == 0 && r == 0 && m * kTileM < U.len)
+                dbg_count(a.dbg_visits, (long long)U.h * (a.varlen ? a.N : (long long)a.B * a.N) + U.tok0 + m * kTileM);
             tc_fence_before();
             mbar_arrive_remote_w(lead(&sh.o_free));
             return true;
@@ -491,6 +498,7 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 // both halves see the same row maxima, so their warp votes agree.
                 const bool jump = (m_ref == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_ref > a.tau);
                 const bool rescale = __any_sync(0xffffffffu, jump);
+                if (lane == 0 && x == 0) dbg_count_rescale(a.dbg_rescale, j > 0, rescale);
                 float fac = 1.f;
                 if (rescale) {
                     fac = (m_ref == -INFINITY) ? 0.f : ex2_mufu(m_ref - m_new);
@@ -498,8 +506,9 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     m_ref = m_new;
                 }
                 const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-                // Exponents two at a time (packed fp32 FMA), exp2 on MUFU,
-                // row sum in two packed accumulators.
+                // Exponents two at a time (packed fp32 FMA), exp2 on MUFU
+                // (kEmu16 of every 16 pairs on the FMA pipe), row sum in two
+                // packed accumulators.
                 uint32_t pk[64];
                 const uint64_t sc2 = f2_pack(scale, scale), nm2 = f2_pack(-m_use, -m_use);
                 uint64_t la = f2_pack(0.f, 0.f), lb = la;
@@ -507,7 +516,13 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 for (int i = 0; i < 64; ++i) {
                     float x0, x1;
                     f2_unpack(f2_fma(f2_pack(s[2 * i], s[2 * i + 1]), sc2, nm2), x0, x1);
-                    const float p0 = ex2_mufu(x0), p1 = ex2_mufu(x1);
+                    float p0, p1;
+                    if ((i & 15) < kEmu16) {
+                        exp2_fma_x2(x0, x1, p0, p1);
+                    } else {
+                        p0 = ex2_mufu(x0);
+                        p1 = ex2_mufu(x1);
+                    }
                     if (i & 1) lb = f2_add(lb, f2_pack(p0, p1));
                     else la = f2_add(la, f2_pack(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
@@ -586,8 +601,12 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
 int g_pairs_resident = 0;
 
-cudaError_t launch_fwd_pair(const FwdLaunch& L, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmem);
+namespace {
+
+template <int E>
+cudaError_t launch_fwd_pair_t(const FwdLaunch& L, cudaStream_t stream) {
+    auto kern = fwd_pair_kernel<E>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmem);
     if (e != cudaSuccess) return e;
     // Persistent: as many pairs as can be resident at once (clusters must fit
     // inside one GPC, so this can be below half the SM count).
@@ -605,7 +624,7 @@ cudaError_t launch_fwd_pair(const FwdLaunch& L, cudaStream_t stream) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, fwd_pair_kernel, &cfg) != cudaSuccess || n < 1) n = L.num_sms / 2;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) n = L.num_sms / 2;
         max_pairs = g_pairs_resident = n;
     }
     // Upper bound on the unit count (varlen: the kernel computes the exact one).
@@ -613,8 +632,21 @@ cudaError_t launch_fwd_pair(const FwdLaunch& L, cudaStream_t stream) {
                                        : (long long)L.a.B * L.a.Hq * ((L.a.N + kBlockN - 1) / kBlockN);
     int pairs = (int)(units < max_pairs ? units : max_pairs);
     if (pairs < 1) pairs = 1;
-    fwd_pair_kernel<<<2 * pairs, kPThreads, kPSmem, stream>>>(L.tq, L.tk, L.tv, L.to, L.a);
+    kern<<<2 * pairs, kPThreads, kPSmem, stream>>>(L.tq, L.tk, L.tv, L.to, L.a);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_pair(const FwdLaunch& L, cudaStream_t stream) {
+    switch (L.emu16) {
+        case 0: return launch_fwd_pair_t<0>(L, stream);
+        case 1: return launch_fwd_pair_t<1>(L, stream);
+        case 2: return launch_fwd_pair_t<2>(L, stream);
+        case 3: return launch_fwd_pair_t<3>(L, stream);
+        case 4: return launch_fwd_pair_t<4>(L, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace fa

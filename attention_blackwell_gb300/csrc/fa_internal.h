@@ -30,13 +30,19 @@ struct FwdArgs {
     int l2_section;          // causal fixed-length: (batch, head) pairs per L2 section
     float scale_log2;        // alpha * log2(e)
     float tau;               // conditional-rescale threshold (log2 units)
+    // Debug counters (nullptr unless fa_set_debug_counters armed them):
+    // visits[h * T + first row of a 128-row query tile] += 1 per finished
+    // tile; rescale[0] += 1 per warp that takes the rescale branch after a
+    // row block's first key block, rescale[1] += 1 per such warp decision.
+    int* dbg_visits;
+    unsigned long long* dbg_rescale;
 };
 
 struct FwdLaunch {
     CUtensorMap tq, tk, tv;  // 3-D maps {128, H, T}, box {64, 1, 128}, 128-B swizzle
     CUtensorMap to;          // O, same shape as tq (pair kernel: TMA stores of full tiles)
     FwdArgs a;
-    int emu_eighths;         // 0..4: share of exp2 pairs on the FMA pipe, in eighths
+    int emu16;               // 0..4: share of exp2 pairs on the FMA pipe, in sixteenths
     int num_sms;
     int d = 128;             // head dim (128; 64 on the ping-pong kernel; 256 on fa_fwd256.cu)
 };
@@ -47,7 +53,8 @@ struct FwdLaunch {
 //   [0, 256)           BwdHeader (status word, unit count)
 //   D                  float [Hq][T]            rowsum(dO * O)
 //   dQacc              float [Hq][T][d]         fp32 dQ accumulator
-//   semaphores         int   [Hq][T/128 + B + 1] (deterministic mode)
+//   semaphores         int   [Hq][T/128 + B + 1] (deterministic mode;
+//                                                d = 256: [2][Hq][T/64 + B + 1])
 //   units              int4  [Hkv * (T/128 + B)] (varlen work list)
 //   cu                 int   [B+1]              (varlen: sanitised offsets)
 // T = B*N for fixed length, the packed token count for varlen.
@@ -76,11 +83,15 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 inline WsLayout ws_layout(long long T, int B, int Hq, int deterministic, int varlen, int d = kHeadDim) {
     WsLayout w;
     const long long tiles = (T + kTileN - 1) / kTileN;
-    w.sem_stride = tiles + B + 1;
+    // Semaphores per query head: one per 128-row query tile (d = 256: per
+    // 64-row query step, and a set for each head-dim half).
+    const long long steps = d == 256 ? (T + 63) / 64 : tiles;
+    const size_t sem_sets = d == 256 ? 2 : 1;
+    w.sem_stride = steps + B + 1;
     w.d_off = align256(sizeof(BwdHeader));
     w.dq_off = align256(w.d_off + (size_t)Hq * T * 4);
     w.sem_off = align256(w.dq_off + (size_t)Hq * T * d * 4);
-    w.unit_off = align256(w.sem_off + (deterministic ? (size_t)Hq * w.sem_stride * 4 : 0));
+    w.unit_off = align256(w.sem_off + (deterministic ? sem_sets * Hq * w.sem_stride * 4 : 0));
     w.cu_off = align256(w.unit_off + (varlen ? (size_t)Hq * (tiles + B) * 16 : 0));
     w.total = align256(w.cu_off + (varlen ? (size_t)(B + 1) * 4 : 0));
     return w;
@@ -106,6 +117,12 @@ struct BwdArgs {
     long long T;
     int causal, varlen, deterministic, max_seqlen;
     float alpha, scale_log2;
+    // Debug counters (nullptr unless fa_set_debug_counters armed them):
+    // visits[hk * T + first row of a 128-key tile] += 1 per finished work
+    // unit (key tile of one key/value head); inner[h * T + first row of a
+    // 128-row query tile] += 1 per (key tile, query tile) product chain.
+    int* dbg_visits;
+    int* dbg_inner;
 };
 
 struct BwdLaunch {
@@ -116,8 +133,12 @@ struct BwdLaunch {
     BwdArgs a;
     int num_sms;
     int pair;                // stage 2 runs the CTA-pair kernel (fa_bwd_pair.cu; d = 128 only)
-    int d = 128;             // head dim (128 or 64)
+    int d = 128;             // head dim (128, 64 or 256)
 };
+
+// Head-dim 256 backward main kernel (fa_bwd256.cu): Q and dO maps with 64-row
+// boxes, K and V with 128-row boxes; dQ is added with per-thread reductions.
+cudaError_t launch_bwd256_main(const BwdLaunch& L, cudaStream_t stream);
 
 // CTA-pair backward main kernel (fa_bwd_pair.cu): fixed length, atomic mode.
 bool bwd_pair_supported(const BwdArgs& a);
@@ -145,6 +166,17 @@ cudaError_t launch_fwd256(const FwdLaunch& L, cudaStream_t stream);
 
 // The library's device status word on the current device.
 DevStatus* device_status_ptr();
+
+// Debug counter increment (no-op while the counters are off).
+__device__ __forceinline__ void dbg_count(int* counts, long long idx) {
+    if (counts) atomicAdd(counts + idx, 1);
+}
+__device__ __forceinline__ void dbg_count_rescale(unsigned long long* c, bool after_first, bool taken) {
+    if (c && after_first) {
+        atomicAdd(c + 1, 1ull);
+        if (taken) atomicAdd(c, 1ull);
+    }
+}
 
 // fa_bwd's host-side argument checks (everything but the workspace), in the
 // order fa_bwd applies them; on FA_OK *T_out is the token count.  ptrs: q,

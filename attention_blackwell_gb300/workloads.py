@@ -20,9 +20,9 @@ the workloads the pages' analysis is about: d = 128, BF16, long sequences):
 * causal_bwd: B=2, Hq=Hkv=16, N=8192, causal, Q, K, V, dO ~ N(0, 1).
 * large_d64, causal_bwd_d64: large and causal_bwd at head dim 64 (the
   exponential-bound end of the balance between MUFU and tensor work).
-* large_d256, causal_d256: forward at head dim 256 (the product-bound end).
-* varlen_d256: the varlen workload's sequences and heads at head dim 256,
-  forward.
+* large_d256, causal_d256: large and causal at head dim 256 (the
+  product-bound end).
+* varlen_d256: the varlen workload's sequences and heads at head dim 256.
 """
 from dataclasses import dataclass, field
 

@@ -46,9 +46,9 @@ def parse():
     ap.add_argument("--no-bwd", action="store_true", help="time the forward only")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="large (default), tiny, causal, varlen, causal_bwd, large_d64, causal_bwd_d64, "
-                         "large_d256, causal_d256, varlen_d256 (forward only)")
+                         "large_d256, causal_d256, varlen_d256")
     ap.add_argument("--deterministic", action="store_true", help="backward in deterministic mode")
-    ap.add_argument("--exp2-emu", type=int, default=0, help="forward: eighths of exp2 on the FMA pipe (0-2)")
+    ap.add_argument("--exp2-emu", type=int, default=0, help="forward: sixteenths of exp2 on the FMA pipe (0-4)")
     ap.add_argument("--tau", type=float, default=8.0, help="forward: conditional-rescale threshold (log2 units)")
     ap.add_argument("--bwd-kernel", type=int, default=0,
                     help="backward main kernel: 0 one CTA per 128-key tile, 1 CTA pairs per 256-key block")
@@ -187,7 +187,7 @@ def traffic_key(args, w, kernel):
         return "bwd" if (w.varlen or args.deterministic or args.bwd_kernel == 0) else "bwd_pair"
     if kernel != "fwd":
         return kernel
-    if args.exp2_emu or args.fwd_kernel == 0:
+    if args.fwd_kernel == 0:
         return "fwd_pingpong"
     return "fwd_pair"
 
@@ -263,7 +263,7 @@ def run_ours(args, rank, world):
     fa.set_tuning(args.exp2_emu, args.tau)
     fa.set_fwd_kernel(args.fwd_kernel)
     fa.set_bwd_kernel(args.bwd_kernel)
-    has_bwd = hasattr(fa, "bwd") and not args.no_bwd and w.d != 256   # no d = 256 backward
+    has_bwd = hasattr(fa, "bwd") and not args.no_bwd
     inp = W.make_inputs(w, with_grad=True)
     t = {n: inp[n].to(dev) for n in ("q", "k", "v", "do")}
     t["o"] = torch.empty_like(t["q"])
@@ -436,12 +436,13 @@ def main_ours(args):
         "data": "synthetic",
         "config": {"workload": describe(w, r["inp"]),
             "step": step_name, "global_batch": w.B * world, "seq_len": w.N or max(r["inp"]["lengths"]),
-            "deterministic_bwd": bool(args.deterministic), "exp2_emu_eighths": args.exp2_emu, "tau": args.tau,
+            "deterministic_bwd": bool(args.deterministic), "exp2_emu_sixteenths": args.exp2_emu, "tau": args.tau,
             "fwd_kernel": ("one 128-row tile, 64-key blocks (d = 256)" if w.d == 256 else
-                           "ping-pong 2x128" if args.exp2_emu or w.d != 128 or args.fwd_kernel == 0 else
+                           "ping-pong 2x128" if w.d != 128 or args.fwd_kernel == 0 else
                            "CTA pairs, 256-key blocks"),
             "fwd_pairs_resident": fa_pairs_resident(),
-            "bwd_kernel": ("one CTA per 128-key tile" if w.varlen or args.deterministic or args.bwd_kernel == 0 or w.d != 128
+            "bwd_kernel": ("128-key tile per head-dim half, 64-row query steps (d = 256)" if w.d == 256 else
+                           "one CTA per 128-key tile" if w.varlen or args.deterministic or args.bwd_kernel == 0 or w.d != 128
                            else "CTA pairs per 256-key block"),
             "bwd_pairs_resident": bwd_pairs_resident(),
             "parallelism": "replicas" if world > 1 else "single",
@@ -479,7 +480,7 @@ def main_reference(args):
     from oracle import attention as A
 
     w = W.WORKLOADS[args.workload]
-    with_bwd = not args.no_bwd and w.d != 256   # the same step as ours
+    with_bwd = not args.no_bwd   # the same step as ours
     inp = W.make_inputs(w, with_grad=True)
 
     def step(s):  # one (sequence, head) slice of the workload per step

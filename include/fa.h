@@ -17,9 +17,8 @@
  * ---------------------------------------
  * - Element types: q, k, v, o, do, dq, dk, dv are bfloat16 (raw 16-bit
  *   storage, passed as void*); lse is float32; cu_seqlens is int32.
- * - Head dimension d is 128 or 64, or 256 for the forward only
- *   (the pages' balance point moves with d: FlashAttention-4 paper summary,
- *   "Roofline" remarks).  Hq must be a multiple of Hkv; query head h reads
+ * - Head dimension d is 64, 128 or 256 (the pages' balance point moves with
+ *   d: FlashAttention-4 paper summary, "Roofline" remarks).  Hq must be a multiple of Hkv; query head h reads
  *   key/value head h / (Hq / Hkv).
  * - Fixed-length layout (cu_seqlens == NULL): q, o, do, dq are [B, N, Hq, d]
  *   row-major, k, v, dk, dv are [B, N, Hkv, d]; lse is [B, Hq, N].
@@ -77,9 +76,11 @@ int fa_num_sms(void);
 
 /*
  * Process-wide tuning of the forward kernel (affects later fa_fwd calls):
- *   exp2_emu_eighths: share of the softmax exponentials evaluated on the FMA
- *     pipe by the polynomial (fa_exp2_emu) instead of MUFU.EX2, in eighths
- *     (0, 1 or 2; FlashAttention-4 paper summary §3.1.3 uses 10-25 %).
+ *   exp2_emu_sixteenths: share of the softmax exponentials evaluated on the
+ *     FMA pipe by the polynomial (fa_exp2_emu) instead of MUFU.EX2, in
+ *     sixteenths (0 to 4, i.e. up to 25 %; FlashAttention-4 paper summary
+ *     §3.1.3 uses 10-25 %).  Both d = 128 forward kernels and the d = 64 one
+ *     apply it.
  *   tau: conditional-rescale threshold in log2 units, 0 <= tau <= 64
  *     (default log2(256) = 8; tau = 0 rescales whenever the max grows).
  * At d = 256 only tau applies: that forward evaluates every exponential on
@@ -87,7 +88,7 @@ int fa_num_sms(void);
  * pace).  Every setting gives the same attention up to rounding.  Not thread-safe
  * with concurrent fa_fwd calls.  Errors: FA_ERR_UNSUPPORTED, FA_ERR_INVALID.
  */
-int fa_set_tuning(int exp2_emu_eighths, float tau);
+int fa_set_tuning(int exp2_emu_sixteenths, float tau);
 
 /*
  * Process-wide choice of the forward kernel (affects later fa_fwd calls):
@@ -96,8 +97,8 @@ int fa_set_tuning(int exp2_emu_eighths, float tau);
  *   2 -- (default) CTA pairs (clusters of two): 256 query rows per pair and
  *        256-key blocks, each product one M = 256 UMMA over both SMs, so each
  *        SM loads and reads only half of every K and V block.
- * Kernel 2 serves fixed-length and packed varlen inputs with d = 128 and
- * exp2_emu_eighths == 0; all other calls (d = 64 among them) use kernel 0.
+ * Kernel 2 serves fixed-length and packed varlen inputs with d = 128; d = 64
+ * calls use kernel 0.
  * Both compute the same attention up to rounding.
  * Errors: FA_ERR_INVALID (any other value).
  */
@@ -132,6 +133,33 @@ int fa_set_bwd_kernel(int kernel);
 int fa_bwd_pairs_resident(void);
 
 /*
+ * Debug counters for the scheduler's exactly-once property (FlashAttention-4
+ * blog, "Scheduling": every work tile is handed out once) and for the
+ * conditional rescale (paper summary §3.1.4: how often tau = 8 skips).
+ * Process-wide; affects later fa_fwd / fa_bwd calls; all NULL (the default)
+ * turns counting off.  The caller owns and zeroes the device buffers; the
+ * kernels only add to them (atomically), so calls accumulate.  With T the
+ * token count (B * N fixed length, the packed total for varlen):
+ *   visits (int [Hq * T] for fa_fwd, [Hkv * T] for fa_bwd; may be NULL):
+ *     fa_fwd adds 1 at [h * T + r] when it finishes the 128-row query tile
+ *     of head h starting at token row r; fa_bwd adds 1 at [hk * T + r] when
+ *     it finishes the work unit of key/value head hk whose 128-key tile
+ *     starts at row r (its dK, dV written);
+ *   inner (int [Hq * T], fa_bwd; may be NULL): 1 at [h * T + r] each time a
+ *     128-key tile's dQ contribution to the query tile of head h starting at
+ *     row r has been added (so the count is the number of key tiles that see
+ *     the query tile; at d = 256 the query tiles are the kernel's 64-row
+ *     steps, counted by the first head-dim half's pass);
+ *   rescales (unsigned long long [2], fa_fwd; may be NULL): [1] counts the
+ *     per-warp rescale decisions after each row block's first key block,
+ *     [0] those that took the rescale branch (tau exceeded).
+ * Tile starts are the sequence start plus multiples of 128.  Counting costs
+ * an atomic per tile (and per warp decision): a debugging aid, not for
+ * timed runs.  Errors: FA_ERR_ALIGN (misaligned pointer).
+ */
+int fa_set_debug_counters(int *visits, int *inner, unsigned long long *rescales);
+
+/*
  * Forward: O and LSE of exact attention (FlashAttention-4 blog, "Forward
  * pass: a new softmax pipeline with conditional rescaling").
  *
@@ -155,8 +183,7 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  * D (rowsum(dO*O), fp32), the fp32 dQ accumulator, the deterministic-mode
  * semaphores and the varlen work list.  N is the sequence length (fixed
  * length) or the total token count T (varlen = 1).  Returns 0 for invalid
- * sizes (d not 64 or 128 among them: there is no d = 256 backward).  About
- * (4 d + 4) * Hq * T bytes.
+ * sizes (d not 64, 128 or 256 among them).  About (4 d + 4) * Hq * T bytes.
  */
 size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, int deterministic, int varlen);
 
@@ -171,6 +198,10 @@ size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, int deterministic, int
  * 256-byte aligned, owned by the caller; its contents need no
  * initialisation and are overwritten.  Calls that share a workspace must not
  * overlap on the GPU.
+ * d = 256 runs on a kernel of its own: the dK / dV accumulators of a
+ * 128-key tile would fill all of tensor memory, so each tile is processed
+ * once per head-dim half of the gradients (recomputing S and dP for each),
+ * with queries in 64-row steps (fa_set_bwd_kernel does not apply).
  * Errors: as fa_fwd, plus FA_ERR_WORKSPACE (NULL, misaligned or too small)
  * and FA_ERR_UNSUPPORTED (varlen with max_seqlen > 131072 or B > 1024).
  */
@@ -219,7 +250,7 @@ int fa_bwd_stages(int stages, const void *q, const void *k, const void *v, const
  *   fa_get_device_status reports and clears it on this device, as it does
  *   for a workspace passed to it.
  * Argument errors are fa_bwd's, checked in fa_bwd's order (FA_ERR_UNSUPPORTED
- * for d = 256, ...); a call with no tokens returns FA_OK.
+ * for an unbuilt head dim, ...); a call with no tokens returns FA_OK.
  */
 int fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o, const float *lse,
                    const void *dout, void *dq, void *dk, void *dv,
@@ -251,8 +282,11 @@ int fa_get_device_status(const void *workspace, cudaStream_t stream);
  * degree-3 Horner polynomial in f with p0 = 1, scaled by adding n to the
  * exponent bits (FlashAttention-4 blog, "Faster exponential" section;
  * paper summary §3.1.3: max relative error 8.77e-5 on [0,1)).  Inputs below
- * -127 (and -inf) give 0 or a value below 2^-126.  x, y: device float32
- * arrays of n elements.  Errors: FA_ERR_INVALID, FA_ERR_LAUNCH.
+ * -127 (and -inf) give 0 or a value below 2^-126.  Each element is
+ * evaluated both in the scalar form (ping-pong forward) and in the packed
+ * two-lane form (CTA-pair forward); where the two differ in any bit, y[i] is
+ * NaN.  x, y: device float32 arrays of n elements.
+ * Errors: FA_ERR_INVALID, FA_ERR_LAUNCH.
  */
 int fa_exp2_emu(const float *x, float *y, int64_t n, cudaStream_t stream);
 

@@ -77,7 +77,9 @@ def test_fwd_rejects_bad_arguments_on_the_host(lib):
 
 def test_set_tuning_validation(lib):
     lib.fa_set_tuning.argtypes = [ctypes.c_int, ctypes.c_float]
-    assert lib.fa_set_tuning(7, 8.0) == -2
+    assert lib.fa_set_tuning(5, 8.0) == -2
+    assert lib.fa_set_tuning(-1, 8.0) == -2
+    assert lib.fa_set_tuning(4, 8.0) == 0
     assert lib.fa_set_tuning(0, -1.0) == -1
     assert lib.fa_set_tuning(0, 8.0) == 0
 
@@ -109,17 +111,19 @@ def test_workspace_size_depends_on_head_dim(lib):
     f = lib.fa_bwd_workspace_size
     f.restype = ctypes.c_size_t
     f.argtypes = [ctypes.c_int] * 6
-    n64, n128 = f(2, 4, 1000, 64, 0, 0), f(2, 4, 1000, 128, 0, 0)
-    assert 0 < n64 < n128
+    n64, n128, n256 = f(2, 4, 1000, 64, 0, 0), f(2, 4, 1000, 128, 0, 0), f(2, 4, 1000, 256, 0, 0)
+    assert 0 < n64 < n128 < n256
     assert n128 - n64 >= 2 * 4 * 1000 * 64 * 4        # B*N*Hq rows of 64 more floats
-    assert f(2, 4, 1000, 96, 0, 0) == 0 and f(2, 4, 1000, 256, 0, 0) == 0   # no d = 256 backward
+    assert n256 - n128 >= 2 * 4 * 1000 * 128 * 4
+    # d = 256 deterministic: two semaphore sets of one per 64-row query step
+    assert f(2, 4, 1000, 256, 1, 0) - n256 >= 2 * 4 * (2000 // 64) * 4
+    assert f(2, 4, 1000, 96, 0, 0) == 0 and f(2, 4, 1000, 512, 0, 0) == 0
 
 
 def test_noalloc_returns_fa_bwd_codes_on_the_host(lib):
     """fa_bwd_noalloc runs fa_bwd's argument checks first, so both entry
-    points give the same code for the same bad arguments (d = 256 and other
-    unbuilt head dims: FA_ERR_UNSUPPORTED); none of these calls reaches the
-    GPU."""
+    points give the same code for the same bad arguments (unbuilt head dims:
+    FA_ERR_UNSUPPORTED); none of these calls reaches the GPU."""
     vp, i, fl, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     na, bw = lib.fa_bwd_noalloc, lib.fa_bwd
     na.restype = bw.restype = i
@@ -127,8 +131,8 @@ def test_noalloc_returns_fa_bwd_codes_on_the_host(lib):
     bw.argtypes = [vp] * 9 + [i, i, i, i, i, fl, i, vp, i, i, vp, sz, vp]
     P = 0x10000
     ok = dict(p=P, B=1, Hq=2, Hkv=2, N=128, d=128, alpha=0.1, causal=0, cu=None, ms=0, det=0)
-    cases = [dict(d=256), dict(d=96), dict(p=None), dict(B=0), dict(Hq=3), dict(alpha=0.0), dict(causal=2),
-             dict(det=2), dict(cu=P, ms=0), dict(cu=P, ms=1 << 20), dict(p=P + 8), dict(d=256, p=P + 8)]
+    cases = [dict(d=512), dict(d=96), dict(p=None), dict(B=0), dict(Hq=3), dict(alpha=0.0), dict(causal=2),
+             dict(det=2), dict(cu=P, ms=0), dict(cu=P, ms=1 << 20), dict(p=P + 8), dict(d=96, p=P + 8)]
     for kw in cases:
         a = dict(ok, **kw)
         ptrs = [a["p"]] * 9
@@ -136,5 +140,4 @@ def test_noalloc_returns_fa_bwd_codes_on_the_host(lib):
         r_na = na(*args, None)
         r_bw = bw(*args, P, 1 << 40, None)
         assert r_na == r_bw and r_na < 0, (kw, r_na, r_bw)
-    a = dict(ok, d=256)
-    assert na(*([P] * 9 + [1, 2, 2, 128, 256, 0.1, 0, None, 0, 0]), None) == -2
+    assert na(*([P] * 9 + [1, 2, 2, 128, 96, 0.1, 0, None, 0, 0]), None) == -2

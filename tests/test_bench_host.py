@@ -55,7 +55,7 @@ def test_traffic_key_follows_the_kernel_that_runs():
     large, varlen = W.WORKLOADS["large"], W.WORKLOADS["varlen"]
     assert bench.traffic_key(_args(), large, "fwd") == "fwd_pair"
     assert bench.traffic_key(_args(fwd_kernel=0), large, "fwd") == "fwd_pingpong"
-    assert bench.traffic_key(_args(exp2_emu=1), large, "fwd") == "fwd_pingpong"
+    assert bench.traffic_key(_args(exp2_emu=1), large, "fwd") == "fwd_pair"
     assert bench.traffic_key(_args(), varlen, "fwd") == "fwd_pair"
     assert bench.traffic_key(_args(), large, "bwd") == "bwd"
     assert bench.traffic_key(_args(bwd_kernel=1), large, "bwd") == "bwd_pair"

@@ -1,9 +1,9 @@
-"""Head dim d = 256: forward parity against the fp64 oracle.
+"""Head dim d = 256: forward and backward parity against the fp64 oracle.
 
 The d = 256 forward (one 128-row query tile per CTA, 64-key blocks, O in
-256 tensor-memory columns, the query tile in 128 more) takes
-fixed-length and packed variable-length inputs; the backward is not built for
-d = 256 (dK and dV alone would fill the 512 tensor-memory columns).
+256 tensor-memory columns, the query tile in 128 more) and backward (each
+128-key unit once per head-dim half of the gradients, 64-row query steps)
+take fixed-length and packed variable-length inputs.
 Tolerances as for d = 128: O max |err| <= 2e-2, mean |err| <= 1e-3, LSE abs
 err <= 1e-3.  alpha = 1/sqrt(256).
 """
@@ -140,6 +140,126 @@ def test_varlen_mqa_full_size_sampled_rows(fa):
         assert abs(lse[h, cu[b] + i] - rl[n]) <= LSE_ABS
 
 
+# ------------------------------------------------------------------ backward
+#
+# The d = 256 backward (fa_bwd256.cu): each 128-key unit runs once per
+# head-dim half of dK / dV / dQ, queries in 64-row steps.  Tolerance as for
+# d = 128: max |err| <= 2e-2 * max |grad| for each of dQ, dK, dV.
+
+REL = 2e-2
+
+
+def bwd_inputs(B, N, Hq, Hkv, seed=0, lengths=None, q_std=1.0):
+    inp = inputs(B, N, Hq, Hkv, seed=seed, q_std=q_std, lengths=lengths)
+    inp["do"] = W.normal_bf16(inp["q"].shape, seed + 3)
+    if lengths is None:
+        inp["lengths"] = [N] * B
+    return inp
+
+
+def gpu_grads(fa, inp, causal, deterministic=False, repeats=1):
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    cu = inp["cu_seqlens"].cuda() if inp.get("cu_seqlens") is not None else None
+    ms = max(inp["lengths"]) if cu is not None else None
+    o, lse = fa.fwd(q, k, v, causal=causal, cu_seqlens=cu, max_seqlen=ms)
+    B = len(inp["lengths"])
+    N = q.shape[0] if cu is not None else q.shape[1]
+    ws = fa.bwd_workspace(B, q.shape[-2], N, deterministic, cu is not None, d=D)
+    outs = []
+    for _ in range(repeats):
+        g = fa.bwd(q, k, v, o, lse, do, causal=causal, cu_seqlens=cu, max_seqlen=ms, deterministic=deterministic,
+                   workspace=ws)
+        assert fa.device_status(ws) == 0
+        outs.append(tuple(t.float().cpu().numpy() for t in g))
+    return outs
+
+
+def check_bwd(got, ref):
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert np.isfinite(g).all(), name
+        err, scale = np.abs(g - r).max(), np.abs(r).max()
+        assert err <= REL * scale, (name, err, scale)
+
+
+def oracle_bwd(inp, causal):
+    return A.backward(inp["q"], inp["k"], inp["v"], inp["do"], ALPHA, causal, cu_seqlens=inp.get("cu_seqlens"))
+
+
+@pytest.mark.parametrize("N", [1, 63, 64, 65, 128, 200, 513])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_ragged(fa, N, causal):
+    inp = bwd_inputs(2, N, 2, 2, seed=N + 100)
+    check_bwd(gpu_grads(fa, inp, causal)[0], oracle_bwd(inp, causal))
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (8, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_grouped_heads(fa, Hq, Hkv, causal):
+    inp = bwd_inputs(1, 300, Hq, Hkv, seed=5)
+    check_bwd(gpu_grads(fa, inp, causal)[0], oracle_bwd(inp, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_varlen(fa, causal):
+    inp = bwd_inputs(0, 0, 4, 2, seed=9, lengths=[130, 1, 0, 300, 64, 257, 63])
+    check_bwd(gpu_grads(fa, inp, causal)[0], oracle_bwd(inp, causal))
+
+
+def test_bwd_large_q_logits(fa):
+    inp = bwd_inputs(1, 384, 2, 2, seed=17, q_std=3.0)
+    check_bwd(gpu_grads(fa, inp, True)[0], oracle_bwd(inp, True))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_deterministic_bit_identical(fa, causal):
+    inp = bwd_inputs(2, 640, 4, 2, seed=13)
+    runs = gpu_grads(fa, inp, causal, deterministic=True, repeats=10)
+    for r in runs[1:]:
+        for a_, b_ in zip(runs[0], r):
+            assert np.array_equal(a_.view(np.uint32), b_.view(np.uint32))
+    check_bwd(runs[0], oracle_bwd(inp, causal))
+
+
+def test_bwd_deterministic_many_waves(fa):
+    """More units (2 x 40 key tiles x heads) than two waves of CTAs: the
+    fixed-order semaphores must never wait on a unit that has not started."""
+    import attention_blackwell_gb300 as fa_mod
+    N = 128 * 40
+    H = max(4, (2 * fa_mod.num_sms()) // 80 + 1)
+    inp = bwd_inputs(1, N, H, H, seed=31)
+    runs = gpu_grads(fa, inp, False, deterministic=True, repeats=2)
+    for a_, b_ in zip(runs[0], runs[1]):
+        assert np.array_equal(a_.view(np.uint32), b_.view(np.uint32))
+    ref = A.head_backward(*(inp[n][0, :, 0].float().numpy().astype(np.float64) for n in ("q", "k", "v", "do")),
+                          ALPHA, False)
+    check_bwd([g[0, :, 0] for g in runs[0]], ref)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_varlen_deterministic_many_units(fa, causal):
+    lengths = [2500, 2000, 1500, 1000, 700, 300, 129, 0, 1]
+    inp = bwd_inputs(0, 0, 8, 8, seed=41, lengths=lengths)
+    runs = gpu_grads(fa, inp, causal, deterministic=True, repeats=3)
+    for r in runs[1:]:
+        for a_, b_ in zip(runs[0], r):
+            assert np.array_equal(a_.view(np.uint32), b_.view(np.uint32))
+    check_bwd(runs[0], oracle_bwd(inp, causal))
+
+
+@pytest.mark.parametrize("name", ["large_d256", "varlen_d256"])
+def test_bwd_full_size_every_element(fa, name):
+    """The benchmarked d = 256 shapes: every element of dQ, dK, dV against the
+    float64 oracle over the whole workload."""
+    import full_size as FS
+    w, inp = FS.inputs(name)
+    got = gpu_grads(fa, inp, w.causal)[0]
+    ref = FS.backward_reference(name)
+    for name_, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert np.isfinite(g).all(), name_
+        err, _ = FS.abs_err_stats(g, r)
+        assert err <= REL * FS.max_abs(r), (name_, err)
+
+
 def test_unsupported_forms_are_rejected_on_the_host(fa):
-    with pytest.raises(ValueError):
-        fa.bwd_workspace(1, 2, 300, d=D)                        # no d = 256 backward
+    import attention_blackwell_gb300 as fa_mod
+    assert fa_mod.lib().fa_bwd_workspace_size(1, 2, 300, 96, 0, 0) == 0   # d = 96 is not built

@@ -101,7 +101,7 @@ def test_fwd_grouped_and_varlen(fa, causal):
     check_fwd(*gpu_fwd(fa, inp, causal)[5:], inp, causal)
 
 
-@pytest.mark.parametrize("emu", [1, 2])
+@pytest.mark.parametrize("emu", [1, 2, 3, 4])
 def test_fwd_exp2_split(fa, emu):
     fa.set_tuning(emu, 8.0)
     try:
