@@ -175,10 +175,15 @@ def gpu_grads(fa, inp, causal, deterministic=False, repeats=1):
 
 
 def check_bwd(got, ref):
+    """max |err| <= 2e-2 * max |grad|.  Where a gradient is exactly zero in
+    exact arithmetic (N = 1: P = 1, so dS = dP - D = 0 and dQ = dK = 0) the
+    relative bound has no scale; there it is read with the scale floored at
+    1e-3 (2e-5 absolute, rounding noise of the fp32 dP and D against O(1)
+    inputs)."""
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
         assert np.isfinite(g).all(), name
         err, scale = np.abs(g - r).max(), np.abs(r).max()
-        assert err <= REL * scale, (name, err, scale)
+        assert err <= REL * max(scale, 1e-3), (name, err, scale)
 
 
 def oracle_bwd(inp, causal):
