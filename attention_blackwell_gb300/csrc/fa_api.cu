@@ -344,8 +344,9 @@ int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const
     if ((rc = make_map(&L.tv, v, Hkv, T, kTileM, d)) != FA_OK) return rc;
     if ((rc = make_map(&L.tdo, dout, Hq, T, qbox, d)) != FA_OK) return rc;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    // The fp32 dQ accumulator's map (TMA reductions; d = 256 adds per thread).
-    if (d != 256 && (rc = make_map_acc(&L.tdq, ws + w.dq_off, (long long)Hq * T, kTileM, d)) != FA_OK) return rc;
+    // The fp32 dQ accumulator's map for the TMA reductions: boxes of 32
+    // columns x 128 rows (d = 256: 32 rows).
+    if ((rc = make_map_acc(&L.tdq, ws + w.dq_off, (long long)Hq * T, d == 256 ? 32 : kTileM, d)) != FA_OK) return rc;
     BwdArgs& a = L.a;
     a.o = o;
     a.dO = dout;

@@ -24,9 +24,12 @@
 //   dV_h += P^T dO_h    M 128, N 128, K 64  (A = P^T from tensor memory)
 //   dK_h += dS^T Q_h    M 128, N 128, K 64
 //   dQ_h^T = K_h^T dS^T M 128 (head-dim half), N 64 (queries), K 128 (keys)
-// dQ is produced transposed so that the 128 drain threads each own one
-// head-dim column: their fp32 additions into the accumulator (red.global)
-// touch 32 consecutive floats per warp instruction, a whole 128-B line.
+// dQ is produced transposed: each of the 128 drain threads owns one head-dim
+// column, so each drain warp holds a 32-column strip -- exactly one 128-B
+// box of the fp32 accumulator -- and adds it with its own TMA bulk tensor
+// reductions, staged 32 query rows at a time (per-thread red.global
+// additions of the same data measured far slower: L2 absorbs bulk
+// reductions much faster).
 //
 // Warp roles (512 threads): warps 0-3 and 12-15 key rows (P^T, dS^T; 32 of
 // the step's 64 queries each); warps 4-7 the dQ drain and the dK/dV epilogue;
@@ -43,9 +46,11 @@ constexpr int kStep = 64;                        // query rows per step
 constexpr int kThreads6 = 512;
 constexpr uint32_t kKBox6 = 16384;               // 128 rows x 128 B (K, V, dS^T)
 constexpr uint32_t kQBox6 = 8192;                // 64 rows x 128 B (Q, dO)
+constexpr uint32_t kStgBox6 = 4096;              // dQ staging: 32 query rows x 32 fp32 (128 B)
 constexpr uint32_t kOffK6 = 0, kOffV6 = 4 * kKBox6, kOffQ6 = 8 * kKBox6, kOffDO6 = kOffQ6 + 4 * kQBox6,
                    kOffDS6 = kOffDO6 + 4 * kQBox6, kOffStat6 = kOffDS6 + kKBox6,
-                   kOffBar6 = kOffStat6 + 2 * kStep * 4;
+                   kOffStg6 = (kOffStat6 + 2 * kStep * 4 + 1023) & ~1023u,   // one box per drain warp
+                   kOffBar6 = kOffStg6 + 4 * kStgBox6;
 constexpr uint32_t kSmem6 = kOffBar6 + 1024;
 static_assert(kSmem6 <= 232448, "shared memory plan");
 constexpr uint32_t kColDK6 = 0, kColDV6 = 128, kColS6 = 256, kColDP6 = 320, kColDQ6 = 384;
@@ -189,6 +194,14 @@ __device__ __forceinline__ int ld6_acquire(const int* p) {
 __device__ __forceinline__ void red6_release_add(int* p, int v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ void tma6_reduce_add(const CUtensorMap* map, uint32_t src, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void bulk6_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk6_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk6_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence6_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 __device__ __forceinline__ void drain6(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(smem_u32(bar), parity) && globaltimer_ns() - t0 < kWaitLimitNs) {}
@@ -196,7 +209,8 @@ __device__ __forceinline__ void drain6(uint64_t* bar, uint32_t parity) {
 
 __global__ void __launch_bounds__(kThreads6, 1)
 bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, const BwdArgs a) {
+              const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+              const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
     extern __shared__ __align__(1024) uint8_t dsm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t base = smem_u32(dsm);
@@ -242,6 +256,7 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         tma_prefetch_desc(&tk);
         tma_prefetch_desc(&tv);
         tma_prefetch_desc(&tdo);
+        tma_prefetch_desc(&tdq);
     }
     if (warp == 0) {
         tmem_alloc(&sh.tmem_base, 512);
@@ -606,18 +621,39 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                         }
                     }
                     if (bar6_or(1, 128, gave_up)) { ok = false; break; }
+                    if (lane == 0) fence6_async_global();   // our bulk reductions follow the acquire
                 }
-                // Column r of this half for the step's valid rows: a warp
-                // instruction adds one query row's 32 consecutive floats.
-                const int rows = U.len - i * kStep < kStep ? U.len - i * kStep : kStep;
-                float* dst = a.dqacc + ((size_t)h * a.T + U.tok0 + i * kStep) * kD6 + U.pass * 128 + r;
+                // This warp's strip (head-dim columns 32 (warp % 4) .. +31 of
+                // the half) in two boxes of 32 query rows, staged in the
+                // 128-B swizzled layout of the accumulator's tensor map (row e
+                // of a box: 16-byte chunk c at position c ^ (e % 8)).  Rows
+                // past the sequence hold exact zeros (their dS is zero), so
+                // adding them to the neighbouring rows changes nothing.
+                const int y0 = h * (int)a.T + U.tok0 + i * kStep, x0 = U.pass * 128 + (warp & 3) * 32;
+                uint8_t* box = dsm + kOffStg6 + (warp & 3) * kStgBox6;
+                const uint32_t box_s = base + kOffStg6 + (warp & 3) * kStgBox6;
 #pragma unroll
-                for (int q = 0; q < kStep; ++q)
-                    if (q < rows) atomicAdd(dst + (size_t)q * kD6, v[q]);
+                for (int qh = 0; qh < 2; ++qh) {
+                    if (lane == 0) bulk6_wait_read0();   // the box's previous reduction has read it
+                    __syncwarp();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        *reinterpret_cast<float*>(box + e * 128 + ((((lane >> 2) ^ (e & 7)) << 4) | ((lane & 3) << 2))) =
+                            v[qh * 32 + e];
+                    fence6_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma6_reduce_add(&tdq, box_s, x0, y0 + qh * 32);
+                        bulk6_commit();
+                    }
+                }
                 if (sem) {
-                    __threadfence();   // this thread's additions are performed ...
-                    bar6(1, 128);      // ... by every thread of the group ...
-                    if (r == 0) red6_release_add(sem, 1);   // ... before the next key tile may add
+                    if (lane == 0) {
+                        bulk6_wait0();          // this warp's additions are complete ...
+                        fence6_async_global();  // ... and ordered before the release
+                    }
+                    bar6(1, 128);               // ... for every warp of the group
+                    if (r == 0) red6_release_add(sem, 1);
                 }
                 if (r == 0 && U.pass == 0) dbg_count(a.dbg_inner, (long long)h * a.T + U.tok0 + i * kStep);
             }
@@ -653,6 +689,7 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             tc_fence_before();
             mbar_arrive(&sh.acc_free);
         }
+        if (lane == 0) bulk6_wait0();   // every bulk reduction this warp issued has completed
     }
 
     tc_fence_before();
@@ -671,7 +708,7 @@ cudaError_t launch_bwd256_main(const BwdLaunch& L, cudaStream_t stream) {
                                           : (long long)a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN));
     int grid = (int)(units < L.num_sms ? units : L.num_sms);
     if (grid < 1) grid = 1;
-    bwd256_kernel<<<grid, kThreads6, kSmem6, stream>>>(L.tq, L.tk, L.tv, L.tdo, a);
+    bwd256_kernel<<<grid, kThreads6, kSmem6, stream>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, a);
     return cudaGetLastError();
 }
 

@@ -137,7 +137,7 @@ struct BwdLaunch {
 };
 
 // Head-dim 256 backward main kernel (fa_bwd256.cu): Q and dO maps with 64-row
-// boxes, K and V with 128-row boxes; dQ is added with per-thread reductions.
+// boxes, K and V with 128-row boxes, the dQ accumulator with 32 x 32 boxes.
 cudaError_t launch_bwd256_main(const BwdLaunch& L, cudaStream_t stream);
 
 // CTA-pair backward main kernel (fa_bwd_pair.cu): fixed length, atomic mode.
