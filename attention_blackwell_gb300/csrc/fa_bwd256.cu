@@ -11,19 +11,28 @@
 // per head-dim half h of the outputs: pass h keeps dK[:, h], dV[:, h] (128
 // columns each) in tensor memory and produces dQ[:, h].  Both passes recompute
 // S^T and dP^T over the full head dim (the price of the split: 14 instead of
-// 10 product units per tile).  K and V stay resident (128 KB); queries stream
-// in steps of 64 rows (Q and dO 32 KB each), and each step's Q and dO arrive
-// as two head-dim halves: the half the pass does not keep is free as soon as
-// S^T (dP^T) has read it, so the next step's copy starts early.
+// 10 product units per tile).
+//
+// V is only ever the A operand of dP^T = V dO^T, so it lives in tensor memory
+// (128 columns of bf16 pairs, copied there once per unit through the dO ring);
+// K stays in shared memory (64 KB: S^T reads it K-major, dQ^T head-dim-major).
+// That leaves room for two full steps of Q and of dO (64 queries x 256, 32 KB
+// each): the next step's copies land while the current step still reads its
+// own, instead of waiting for the last product of the step (dK reads Q, dV
+// reads dO) and then for a whole L2 round trip.  It also takes V's 64 KB per
+// step off the shared-memory operand reads, the bound of these products.
 //
 // Per step (128 keys x 64 queries), keys on the tensor-memory lanes:
 //   S^T  = K Q^T        M 128, N 64, K 256 (both K-major, shared memory)
-//   dP^T = V dO^T       M 128, N 64, K 256
+//   dP^T = V dO^T       M 128, N 64, K 256 (A = V from tensor memory)
 //   P^T  = 2^(alpha log2e S^T - LSE log2e)  -> bf16 into tensor memory
 //   dS^T = P^T (dP^T - D)                   -> bf16 into shared memory
 //   dV_h += P^T dO_h    M 128, N 128, K 64  (A = P^T from tensor memory)
 //   dK_h += dS^T Q_h    M 128, N 128, K 64
 //   dQ_h^T = K_h^T dS^T M 128 (head-dim half), N 64 (queries), K 128 (keys)
+// Tensor memory: dK_h 0-127, dV_h 128-255, V 256-383, S^T / P^T 384-447, and
+// dP^T 448-511, which dQ^T reuses once the key rows have read dP^T (the next
+// dP^T waits until the dQ drain has read dQ^T out).
 // dQ is produced transposed: each of the 128 drain threads owns one head-dim
 // column, so each drain warp holds a 32-column strip -- exactly one 128-B
 // box of the fp32 accumulator -- and adds it with its own TMA bulk tensor
@@ -31,11 +40,12 @@
 // additions of the same data measured far slower: L2 absorbs bulk
 // reductions much faster).
 //
-// Warp roles (512 threads): warps 0-3 and 12-15 key rows (P^T, dS^T; 32 of
-// the step's 64 queries each); warps 4-7 the dQ drain and the dK/dV epilogue;
-// warp 8 loader; warp 9 issues dP^T, dV, dQ^T, dK; warp 10 issues S^T.
-// Deterministic mode orders the dQ additions per (half, head, 64-row query
-// step) by key tile with the semaphores of the one-CTA kernel.
+// Warp roles (512 threads): warps 0-3 and 12-15 key rows (V into tensor
+// memory, P^T, dS^T; 32 of the step's 64 queries each); warps 4-7 the dQ
+// drain and the dK/dV epilogue; warp 8 loader; warp 9 issues dP^T, dV, dQ^T,
+// dK; warp 10 issues S^T.  Deterministic mode orders the dQ additions per
+// (half, head, 64-row query step) by key tile with the semaphores of the
+// one-CTA kernel.
 #include "fa_internal.h"
 
 namespace fa {
@@ -44,27 +54,28 @@ namespace {
 constexpr int kD6 = 256;
 constexpr int kStep = 64;                        // query rows per step
 constexpr int kThreads6 = 512;
-constexpr uint32_t kKBox6 = 16384;               // 128 rows x 128 B (K, V, dS^T)
+constexpr uint32_t kKBox6 = 16384;               // 128 rows x 128 B (K, V staging, dS^T)
 constexpr uint32_t kQBox6 = 8192;                // 64 rows x 128 B (Q, dO)
+constexpr uint32_t kStage6 = 4 * kQBox6;         // one step of Q or dO, all 256 columns
 constexpr uint32_t kStgBox6 = 4096;              // dQ staging: 32 query rows x 32 fp32 (128 B)
-constexpr uint32_t kOffK6 = 0, kOffV6 = 4 * kKBox6, kOffQ6 = 8 * kKBox6, kOffDO6 = kOffQ6 + 4 * kQBox6,
-                   kOffDS6 = kOffDO6 + 4 * kQBox6, kOffStat6 = kOffDS6 + kKBox6,
-                   kOffStg6 = (kOffStat6 + 2 * kStep * 4 + 1023) & ~1023u,   // one box per drain warp
+constexpr uint32_t kOffK6 = 0, kOffQ6 = 4 * kKBox6, kOffDO6 = kOffQ6 + 2 * kStage6,
+                   kOffDS6 = kOffDO6 + 2 * kStage6, kOffStat6 = kOffDS6 + kKBox6,   // [2][LSE 64, D 64]
+                   kOffStg6 = kOffStat6 + 1024,                                     // one box per drain warp
                    kOffBar6 = kOffStg6 + 4 * kStgBox6;
 constexpr uint32_t kSmem6 = kOffBar6 + 1024;
 static_assert(kSmem6 <= 232448, "shared memory plan");
-constexpr uint32_t kColDK6 = 0, kColDV6 = 128, kColS6 = 256, kColDP6 = 320, kColDQ6 = 384;
+static_assert(kOffStat6 % 1024 == 0 && kOffStg6 % 1024 == 0, "swizzled boxes need 1024-byte alignment");
+static_assert(2 * kStage6 == 4 * kKBox6, "V is staged in the two dO stages");
+constexpr uint32_t kColDK6 = 0, kColDV6 = 128, kColV6 = 256, kColS6 = 384, kColDP6 = 448;
 
 enum : int { k6SiteKvEmpty = 81, k6SiteQEmpty, k6SiteDoEmpty, k6SiteKvFull, k6SiteAcc, k6SiteQFull, k6SiteDoFull,
              k6SiteP, k6SiteDs, k6SiteDqFree, k6SiteS, k6SiteDp, k6SiteDsFree, k6SiteDq, k6SiteDkdv, k6SiteSem,
-             k6SiteUnit };
+             k6SiteUnit, k6SiteVFull, k6SiteVReady };
 
 struct Shared6 {
-    uint64_t kv_full, kv_empty;
-    // Q and dO of a step arrive as two head-dim halves: "a" is the half this
-    // pass does not keep (read by S^T / dP^T only), "b" the pass's own half
-    // (read again by dK / dV).
-    uint64_t qa_full, qa_empty, qb_full, qb_empty, da_full, da_empty, db_full, db_empty;
+    uint64_t kv_full, kv_empty;     // K (and V's staging) of a unit; empty once the unit's products are done
+    uint64_t v_full, v_ready;       // V staged in the dO ring; V copied into tensor memory
+    uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];   // two steps of Q (with LSE, D) and of dO
     uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dq_full, dq_free, dkdv_done, acc_free, r0_free, drain;
     uint64_t unit_full[4], unit_empty[4];
     int unit_id[4];
@@ -119,23 +130,30 @@ __device__ __forceinline__ bool unit6(const BwdArgs& a, int total, int u, Unit6&
     return true;
 }
 
-// S^T / dP^T, the 8 K-steps over head-dim half HALF (boxes 2 HALF, 2 HALF + 1
-// of both operands): M = 128 keys, N = 64 queries, both K-major.
-template <int HALF>
-__device__ __forceinline__ void mma6_kq_half(uint32_t d, uint32_t a_smem, uint32_t b_smem, uint32_t first) {
+// S^T = K Q^T: M = 128 keys, N = 64 queries, K = 256 in 16 steps over the
+// four 64-column boxes of both operands (both K-major).
+__device__ __forceinline__ void mma6_s(uint32_t d, uint32_t a_smem, uint32_t b_smem) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
     const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, 16, 1024);
-    static_for<8>([&](auto kc) {
-        constexpr uint32_t k = (uint32_t)kc + 8 * HALF;
+    static_for<16>([&](auto kc) {
+        constexpr uint32_t k = kc;
         constexpr uint32_t ao = ((k >> 2) * kKBox6 + (k & 3) * 32) >> 4;
         constexpr uint32_t bo = ((k >> 2) * kQBox6 + (k & 3) * 32) >> 4;
-        umma_ss_k<ao, bo>(d, ad, bd, idesc, (first != 0 && kc == 0) ? 0u : 1u);
+        umma_ss_k<ao, bo>(d, ad, bd, idesc, k > 0 ? 1u : 0u);
     });
 }
 
-__device__ __forceinline__ void mma6_kq(uint32_t d, uint32_t a_smem, uint32_t b_smem, int half, uint32_t first) {
-    if (half) mma6_kq_half<1>(d, a_smem, b_smem, first);
-    else mma6_kq_half<0>(d, a_smem, b_smem, first);
+// dP^T = V dO^T: A = V from tensor memory (lane = key row; K-step k, head-dim
+// columns 16k .. 16k+15, in tensor-memory columns 8k .. 8k+7 as bf16 pairs),
+// B = dO K-major from shared memory.  M = 128, N = 64, K = 256.
+__device__ __forceinline__ void mma6_dp(uint32_t d, uint32_t v_tmem, uint32_t b_smem) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+    const uint64_t bd = sdesc_sw128(b_smem, 16, 1024);
+    static_for<16>([&](auto kc) {
+        constexpr uint32_t k = kc;
+        constexpr uint32_t bo = ((k >> 2) * kQBox6 + (k & 3) * 32) >> 4;
+        umma_ts_k<8 * k, bo>(d, v_tmem, bd, idesc, k > 0 ? 1u : 0u);
+    });
 }
 
 // dV_h += P^T dO_h: M = 128 keys, N = 128 (the half's head-dim columns, two
@@ -219,22 +237,20 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         return;
     }
     Shared6& sh = *reinterpret_cast<Shared6*>(dsm + kOffBar6);
-    float* s_lse = reinterpret_cast<float*>(dsm + kOffStat6);   // [64], LSE * log2(e)
-    float* s_D = s_lse + kStep;                                  // [64]
-    const uint32_t sK = base + kOffK6, sV = base + kOffV6, sQ = base + kOffQ6, sDO = base + kOffDO6,
-                   sDS = base + kOffDS6;
+    float* s_stat = reinterpret_cast<float*>(dsm + kOffStat6);   // stage s: [LSE * log2(e) 64, D 64]
+    const uint32_t sK = base + kOffK6, sQ = base + kOffQ6, sDO = base + kOffDO6, sDS = base + kOffDS6;
 
     if (tid == 0) {
         mbar_init(&sh.kv_full, 1);
         mbar_init(&sh.kv_empty, 1);
-        mbar_init(&sh.qa_full, 1);
-        mbar_init(&sh.qa_empty, 1);
-        mbar_init(&sh.qb_full, 1);
-        mbar_init(&sh.qb_empty, 1);
-        mbar_init(&sh.da_full, 1);
-        mbar_init(&sh.da_empty, 1);
-        mbar_init(&sh.db_full, 1);
-        mbar_init(&sh.db_empty, 1);
+        mbar_init(&sh.v_full, 1);
+        mbar_init(&sh.v_ready, 256);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sh.q_full[s], 1);
+            mbar_init(&sh.q_empty[s], 1);
+            mbar_init(&sh.do_full[s], 1);
+            mbar_init(&sh.do_empty[s], 1);
+        }
         mbar_init(&sh.s_full, 1);
         mbar_init(&sh.dp_full, 1);
         mbar_init(&sh.p_ready, 256);
@@ -280,7 +296,7 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             // ------------------------------------------------------------ loader
             uint32_t jj = 0, uc = 0;
             // Loads issued on each full barrier, for the drain at the end.
-            uint32_t n_qa = 0, n_da = 0, n_qb = 0, n_db = 0, n_kv = 0;
+            uint32_t n_q0 = 0, n_q1 = 0, n_do0 = 0, n_do1 = 0, n_kv = 0;
             bool ok = true;
             for (uint32_t n = 0; ok; ++n) {
                 int u = -1;
@@ -307,19 +323,20 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 if (!ok) break;
                 Unit6 U;
                 if (!unit6(a, total, u, U)) break;
+                // K, and V into the dO ring, once the previous unit's products are done.
                 if (lane == 0) ok = mbar_wait(&sh.kv_empty, (uc & 1) ^ 1, wc, k6SiteKvEmpty);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&sh.kv_full, 8 * kKBox6);
+                    mbar_arrive_expect_tx(&sh.kv_full, 4 * kKBox6);
+                    mbar_arrive_expect_tx(&sh.v_full, 4 * kKBox6);
                     for (int c = 0; c < 4; ++c) {
                         tma_load_3d(sK + c * kKBox6, &tk, &sh.kv_full, c * 64, U.hk, U.tok0 + U.k * kTileN);
-                        tma_load_3d(sV + c * kKBox6, &tv, &sh.kv_full, c * 64, U.hk, U.tok0 + U.k * kTileN);
+                        tma_load_3d(sDO + c * kKBox6, &tv, &sh.v_full, c * 64, U.hk, U.tok0 + U.k * kTileN);
                     }
                 }
                 ++n_kv;
                 const int span = U.nq - U.i0;
-                const int ca = 2 * (1 - U.pass), cb = 2 * U.pass;   // first box of each head-dim half
                 // LSE and D of a step, loaded one step ahead into registers.
                 float nl[2], nd[2];
                 auto load_stats = [&](int t) {
@@ -340,50 +357,50 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 load_stats(0);
                 for (int t = 0; t < U.n; ++t, ++jj) {
                     const int h = U.hk * g + t / span, i = U.i0 + t % span, row = U.tok0 + i * kStep;
-                    const uint32_t ep = (jj & 1) ^ 1;
-                    if (lane == 0) {
-                        // The half the pass does not keep: free once S^T / dP^T read it.
-                        ok = mbar_wait(&sh.qa_empty, ep, wc, k6SiteQEmpty);
+                    const uint32_t s = jj & 1, ep = ((jj >> 1) & 1) ^ 1;
+                    const uint32_t sq = sQ + s * kStage6, sdo = sDO + s * kStage6;
+                    // dO before Q: its slot frees first (dV reads dO, dK reads Q
+                    // last) -- except on the unit's first step, where dO waits
+                    // for V to leave the ring.
+                    if (t > 0 && lane == 0) {
+                        ok = mbar_wait(&sh.do_empty[s], ep, wc, k6SiteDoEmpty);
                         if (ok) {
-                            mbar_arrive_expect_tx(&sh.qa_full, 2 * kQBox6);
-                            for (int c = ca; c < ca + 2; ++c)
-                                tma_load_3d(sQ + c * kQBox6, &tq, &sh.qa_full, c * 64, h, row);
-                            ++n_qa;
-                        }
-                        if (ok) ok = mbar_wait(&sh.da_empty, ep, wc, k6SiteDoEmpty);
-                        if (ok) {
-                            mbar_arrive_expect_tx(&sh.da_full, 2 * kQBox6);
-                            for (int c = ca; c < ca + 2; ++c)
-                                tma_load_3d(sDO + c * kQBox6, &tdo, &sh.da_full, c * 64, h, row);
-                            ++n_da;
-                        }
-                        // The pass's own half (and the step's LSE / D): free
-                        // once dK (Q) and dV (dO) of the previous step are done.
-                        if (ok) ok = mbar_wait(&sh.qb_empty, ep, wc, k6SiteQEmpty);
-                        if (ok) {
-                            mbar_expect_tx(&sh.qb_full, 2 * kQBox6);
-                            for (int c = cb; c < cb + 2; ++c)
-                                tma_load_3d(sQ + c * kQBox6, &tq, &sh.qb_full, c * 64, h, row);
+                            mbar_arrive_expect_tx(&sh.do_full[s], kStage6);
+                            for (int c = 0; c < 4; ++c) tma_load_3d(sdo + c * kQBox6, &tdo, &sh.do_full[s], c * 64, h, row);
+                            if (s) ++n_do1; else ++n_do0;
                         }
                     }
-                    n_qb += ok ? 1 : 0;
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
-                    // qb_full's one arrival follows the LSE / D stores.
+                    if (lane == 0) {
+                        ok = mbar_wait(&sh.q_empty[s], ep, wc, k6SiteQEmpty);
+                        if (ok) {
+                            mbar_expect_tx(&sh.q_full[s], kStage6);
+                            for (int c = 0; c < 4; ++c) tma_load_3d(sq + c * kQBox6, &tq, &sh.q_full[s], c * 64, h, row);
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    if (s) ++n_q1; else ++n_q0;
+                    // q_full's one arrival follows the LSE / D stores.
+                    float* st = s_stat + s * 2 * kStep;
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        s_lse[2 * lane + e] = nl[e];
-                        s_D[2 * lane + e] = nd[e];
+                        st[2 * lane + e] = nl[e];
+                        st[kStep + 2 * lane + e] = nd[e];
                     }
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(&sh.qb_full);
-                        ok = mbar_wait(&sh.db_empty, ep, wc, k6SiteDoEmpty);
-                        if (ok) {
-                            mbar_arrive_expect_tx(&sh.db_full, 2 * kQBox6);
-                            for (int c = cb; c < cb + 2; ++c)
-                                tma_load_3d(sDO + c * kQBox6, &tdo, &sh.db_full, c * 64, h, row);
-                            ++n_db;
+                        mbar_arrive(&sh.q_full[s]);
+                        if (t == 0) {
+                            ok = mbar_wait(&sh.v_ready, uc & 1, wc, k6SiteVReady);
+                            if (ok) ok = mbar_wait(&sh.do_empty[s], ep, wc, k6SiteDoEmpty);
+                            if (ok) {
+                                mbar_arrive_expect_tx(&sh.do_full[s], kStage6);
+                                for (int c = 0; c < 4; ++c)
+                                    tma_load_3d(sdo + c * kQBox6, &tdo, &sh.do_full[s], c * 64, h, row);
+                                if (s) ++n_do1; else ++n_do0;
+                            }
                         }
                     }
                     if (t + 1 < U.n) load_stats(t + 1);
@@ -393,11 +410,14 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 ++uc;
             }
             if (lane == 0) {  // every copy this thread issued has landed before teardown
-                if (n_qa) drain6(&sh.qa_full, (n_qa - 1) & 1);
-                if (n_da) drain6(&sh.da_full, (n_da - 1) & 1);
-                if (n_qb) drain6(&sh.qb_full, (n_qb - 1) & 1);
-                if (n_db) drain6(&sh.db_full, (n_db - 1) & 1);
-                if (n_kv) drain6(&sh.kv_full, (n_kv - 1) & 1);
+                if (n_q0) drain6(&sh.q_full[0], (n_q0 - 1) & 1);
+                if (n_q1) drain6(&sh.q_full[1], (n_q1 - 1) & 1);
+                if (n_do0) drain6(&sh.do_full[0], (n_do0 - 1) & 1);
+                if (n_do1) drain6(&sh.do_full[1], (n_do1 - 1) & 1);
+                if (n_kv) {
+                    drain6(&sh.kv_full, (n_kv - 1) & 1);
+                    drain6(&sh.v_full, (n_kv - 1) & 1);
+                }
             }
             __syncwarp();
         } else if (warp == 10) {
@@ -413,15 +433,12 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 if (!unit6(a, total, u, U)) break;
                 if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, k6SiteKvFull))) break;
                 for (int t = 0; t < U.n; ++t, ++jj) {
+                    const uint32_t s = jj & 1;
                     // dV of the previous step has read P^T out of the S region.
                     if (jj > 0 && !(ok = mbar_wait_w(&sh.r0_free, (jj - 1) & 1, wc, k6SiteP))) break;
-                    if (!(ok = mbar_wait_w(&sh.qa_full, jj & 1, wc, k6SiteQFull))) break;
+                    if (!(ok = mbar_wait_w(&sh.q_full[s], (jj >> 1) & 1, wc, k6SiteQFull))) break;
                     tc_fence_after();
-                    mma6_kq(tmem + kColS6, sK, sQ, 1 - U.pass, 1);
-                    umma_commit_w(&sh.qa_empty);
-                    if (!(ok = mbar_wait_w(&sh.qb_full, jj & 1, wc, k6SiteQFull))) break;
-                    tc_fence_after();
-                    mma6_kq(tmem + kColS6, sK, sQ, U.pass, 0);
+                    mma6_s(tmem + kColS6, sK, sQ + s * kStage6);
                     umma_commit_w(&sh.s_full);
                 }
                 ++uc;
@@ -441,30 +458,30 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 Unit6 U;
                 if (!unit6(a, total, u, U)) break;
                 if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, k6SiteKvFull))) break;
-                if (!(ok = mbar_wait_w(&sh.acc_free, (uc & 1) ^ 1, wc, k6SiteAcc))) break;
+                if (!(ok = mbar_wait_w(&sh.v_ready, uc & 1, wc, k6SiteVReady))) break;
                 const uint32_t oK = U.pass * 2 * kKBox6, oQ = U.pass * 2 * kQBox6;   // the pass's half
                 for (int t = 0; t < U.n; ++t, ++jj) {
-                    if (!(ok = mbar_wait_w(&sh.da_full, jj & 1, wc, k6SiteDoFull))) break;
-                    tc_fence_after();
-                    mma6_kq(tmem + kColDP6, sV, sDO, 1 - U.pass, 1);
-                    umma_commit_w(&sh.da_empty);
-                    if (!(ok = mbar_wait_w(&sh.db_full, jj & 1, wc, k6SiteDoFull))) break;
-                    tc_fence_after();
-                    mma6_kq(tmem + kColDP6, sV, sDO, U.pass, 0);
-                    umma_commit_w(&sh.dp_full);
-                    if (!(ok = mbar_wait_w(&sh.p_ready, jj & 1, wc, k6SiteP))) break;
-                    tc_fence_after();
-                    mma6_dv(tmem + kColDV6, tmem + kColS6, sDO + oQ, t > 0);
-                    umma_commit_w(&sh.db_empty);    // dO read by dP^T and dV
-                    umma_commit_w(&sh.r0_free);     // P^T read: the next S^T may overwrite it
-                    if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, k6SiteDs))) break;
+                    const uint32_t s = jj & 1, sq = sQ + s * kStage6, sdo = sDO + s * kStage6;
+                    if (!(ok = mbar_wait_w(&sh.do_full[s], (jj >> 1) & 1, wc, k6SiteDoFull))) break;
+                    // dQ^T of the previous step (in the dP^T columns) has been drained.
                     if (jj > 0 && !(ok = mbar_wait_w(&sh.dq_free, (jj - 1) & 1, wc, k6SiteDqFree))) break;
                     tc_fence_after();
-                    mma6_dqt(tmem + kColDQ6, sK + oK, sDS);
+                    mma6_dp(tmem + kColDP6, tmem + kColV6, sdo);
+                    umma_commit_w(&sh.dp_full);
+                    if (!(ok = mbar_wait_w(&sh.p_ready, jj & 1, wc, k6SiteP))) break;
+                    // The previous unit's epilogue has read dK_h, dV_h out.
+                    if (t == 0 && !(ok = mbar_wait_w(&sh.acc_free, (uc & 1) ^ 1, wc, k6SiteAcc))) break;
+                    tc_fence_after();
+                    mma6_dv(tmem + kColDV6, tmem + kColS6, sdo + oQ, t > 0);
+                    umma_commit_w(&sh.do_empty[s]);  // dO read by dP^T and dV
+                    umma_commit_w(&sh.r0_free);      // P^T read: the next S^T may overwrite it
+                    if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, k6SiteDs))) break;
+                    tc_fence_after();
+                    mma6_dqt(tmem + kColDP6, sK + oK, sDS);   // every key row has read dP^T
                     umma_commit_w(&sh.dq_full);
-                    mma6_dk(tmem + kColDK6, sDS, sQ + oQ, t > 0);
-                    umma_commit_w(&sh.qb_empty);    // Q (and the step's LSE / D) consumed
-                    umma_commit_w(&sh.ds_free);     // dS^T read by dQ^T and dK
+                    mma6_dk(tmem + kColDK6, sDS, sq + oQ, t > 0);
+                    umma_commit_w(&sh.q_empty[s]);   // Q (and the step's LSE / D) consumed
+                    umma_commit_w(&sh.ds_free);      // dS^T read by dQ^T and dK
                 }
                 if (!ok) break;
                 umma_commit_w(&sh.dkdv_done);
@@ -477,15 +494,15 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         }
     } else if (warp < 4 || warp >= 12) {
         regs_inc<144>();
-        // ------------------------------------------------ P^T and dS^T (key rows)
-        const int hc = warp >= 12 ? 1 : 0;                   // which 32 of the step's 64 queries
+        // ------------------------------------ V into tensor memory, P^T, dS^T (key rows)
+        const int hc = warp >= 12 ? 1 : 0;                   // which 32 of the step's 64 queries (V: head-dim half)
         const int cb = hc * 32;
         const int r = (warp & 3) * 32 + lane;                // key row in the tile == TMEM lane
         const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lb + kColS6 + cb, tDP = tmem + lb + kColDP6 + cb;
         uint8_t* ds_row = dsm + kOffDS6 + r * 128;
         const int sw = r & 7;
-        uint32_t jj = 0;
+        uint32_t jj = 0, uc = 0;
         bool ok = true;
         for (uint32_t n = 0; ok; ++n) {
             if (!(ok = mbar_wait(&sh.unit_full[n & 3], (n >> 2) & 1, wc, k6SiteUnit))) break;
@@ -493,11 +510,41 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
             mbar_arrive(&sh.unit_empty[n & 3]);
             Unit6 U;
             if (!unit6(a, total, u, U)) break;
+            // V of the unit, staged by TMA in the dO ring (four 64-column
+            // boxes, 128-B swizzled rows), into tensor memory: this thread's
+            // key row, head-dim half hc.  Chunk q of box c (columns 64c+8q ..
+            // +7) sits at position q ^ (row % 8) and becomes columns
+            // 32c+4q .. +3 of the A operand (bf16 pairs).  The loader issued
+            // these copies after every product of the previous unit had
+            // completed, so V's old columns are no longer read.
+            if (!(ok = mbar_wait(&sh.v_full, uc & 1, wc, k6SiteVFull))) break;
+            tc_fence_after();
+#pragma unroll 1   // one box at a time: 32 registers
+            for (int b = 0; b < 2; ++b) {
+                const int c = 2 * hc + b;
+                const uint8_t* src = dsm + kOffDO6 + c * kKBox6 + r * 128;
+                uint32_t w[32];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint4 x = *reinterpret_cast<const uint4*>(src + ((q ^ sw) << 4));
+                    w[4 * q] = x.x;
+                    w[4 * q + 1] = x.y;
+                    w[4 * q + 2] = x.z;
+                    w[4 * q + 3] = x.w;
+                }
+                tmem_st32(tmem + lb + kColV6 + 32 * c, w);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&sh.v_ready);
+            ++uc;
             const int key = U.k * kTileN + r;
             const int span = U.nq - U.i0;
             for (int t = 0; t < U.n; ++t, ++jj) {
                 const int i = U.i0 + t % span;
-                if (!(ok = mbar_wait(&sh.qb_full, jj & 1, wc, k6SiteQFull))) break;   // LSE / D stored
+                const float* s_lse = s_stat + (jj & 1) * 2 * kStep;
+                const float* s_D = s_lse + kStep;
+                if (!(ok = mbar_wait(&sh.q_full[jj & 1], (jj >> 1) & 1, wc, k6SiteQFull))) break;   // LSE / D stored
                 if (!(ok = mbar_wait(&sh.s_full, jj & 1, wc, k6SiteS))) break;
                 tc_fence_after();
                 float p[32];
@@ -575,7 +622,7 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         // -------------------------------------------- dQ drain, dK/dV epilogue
         const int r = tid - 128;                             // head-dim column (dQ^T) / key row (dK, dV)
         const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tDQ = tmem + lb + kColDQ6;
+        const uint32_t tDQ = tmem + lb + kColDP6;
         uint32_t jj = 0, uc = 0;
         bool ok = true;
         for (uint32_t n = 0; ok; ++n) {
