@@ -42,8 +42,8 @@
 //
 // Warp roles (512 threads): warps 0-3 and 12-15 key rows (V into tensor
 // memory, P^T, dS^T; 32 of the step's 64 queries each); warps 4-7 the dQ
-// drain and the dK/dV epilogue; warp 8 loader; warp 9 issues dP^T, dV, dQ^T,
-// dK; warp 10 issues S^T.  Deterministic mode orders the dQ additions per
+// drain and the dK/dV epilogue; warp 8 loader; warp 9 issues every product
+// (warps 10-11 idle).  Deterministic mode orders the dQ additions per
 // (half, head, 64-row query step) by key tile with the semaphores of the
 // one-CTA kernel.
 #include "fa_internal.h"
@@ -76,7 +76,7 @@ struct Shared6 {
     uint64_t kv_full, kv_empty;     // K (and V's staging) of a unit; empty once the unit's products are done
     uint64_t v_full, v_ready;       // V staged in the dO ring; V copied into tensor memory
     uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];   // two steps of Q (with LSE, D) and of dO
-    uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dq_full, dq_free, dkdv_done, acc_free, r0_free, drain;
+    uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dq_full, dq_free, dkdv_done, acc_free, drain;
     uint64_t unit_full[4], unit_empty[4];
     int unit_id[4];
     uint32_t tmem_base;
@@ -85,7 +85,7 @@ struct Shared6 {
 };
 static_assert(sizeof(Shared6) <= 1024, "barrier block");
 
-constexpr uint32_t kUnitReaders6 = 2 + 256 + 128;
+constexpr uint32_t kUnitReaders6 = 1 + 256 + 128;
 
 struct Unit6 {
     int seq, hk, k, tok0, len, n, nq, i0, pass;
@@ -260,8 +260,7 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         mbar_init(&sh.dq_free, 128);
         mbar_init(&sh.dkdv_done, 1);
         mbar_init(&sh.acc_free, 128);
-        mbar_init(&sh.r0_free, 1);
-        mbar_init(&sh.drain, 2);   // both issuers
+        mbar_init(&sh.drain, 1);
         for (int s = 0; s < 4; ++s) { mbar_init(&sh.unit_full[s], 1); mbar_init(&sh.unit_empty[s], kUnitReaders6); }
         sh.abort_flag = 0;
         sh.total = 2 * (a.varlen ? a.hdr->total_units : a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN));
@@ -420,34 +419,8 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 }
             }
             __syncwarp();
-        } else if (warp == 10) {
-            // ------------------------------------------------------- S issuer
-            uint32_t jj = 0, uc = 0;
-            bool ok = true;
-            for (uint32_t n = 0; ok; ++n) {
-                if (!(ok = mbar_wait_w(&sh.unit_full[n & 3], (n >> 2) & 1, wc, k6SiteUnit))) break;
-                const int u = *(volatile int*)&sh.unit_id[n & 3];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.unit_empty[n & 3]);
-                Unit6 U;
-                if (!unit6(a, total, u, U)) break;
-                if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, k6SiteKvFull))) break;
-                for (int t = 0; t < U.n; ++t, ++jj) {
-                    const uint32_t s = jj & 1;
-                    // dV of the previous step has read P^T out of the S region.
-                    if (jj > 0 && !(ok = mbar_wait_w(&sh.r0_free, (jj - 1) & 1, wc, k6SiteP))) break;
-                    if (!(ok = mbar_wait_w(&sh.q_full[s], (jj >> 1) & 1, wc, k6SiteQFull))) break;
-                    tc_fence_after();
-                    mma6_s(tmem + kColS6, sK, sQ + s * kStage6);
-                    umma_commit_w(&sh.s_full);
-                }
-                ++uc;
-            }
-            umma_commit_w(&sh.drain);
-            drain6(&sh.drain, 0);
-            __syncwarp();
         } else if (warp == 9) {
-            // --------------------------------------- dP^T, dV, dQ^T, dK issuer
+            // ----------------------------------- S^T, dP^T, dV, dQ^T, dK issuer
             uint32_t jj = 0, uc = 0;
             bool ok = true;
             for (uint32_t n = 0; ok; ++n) {
@@ -460,6 +433,14 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, k6SiteKvFull))) break;
                 if (!(ok = mbar_wait_w(&sh.v_ready, uc & 1, wc, k6SiteVReady))) break;
                 const uint32_t oK = U.pass * 2 * kKBox6, oQ = U.pass * 2 * kQBox6;   // the pass's half
+                // S^T of the unit's first step.  Every S^T overwrites the
+                // columns the previous step's dV reads P^T from; this thread
+                // issued that dV earlier, and the tensor core runs one
+                // thread's products in issue order.
+                if (!(ok = mbar_wait_w(&sh.q_full[jj & 1], (jj >> 1) & 1, wc, k6SiteQFull))) break;
+                tc_fence_after();
+                mma6_s(tmem + kColS6, sK, sQ + (jj & 1) * kStage6);
+                umma_commit_w(&sh.s_full);
                 for (int t = 0; t < U.n; ++t, ++jj) {
                     const uint32_t s = jj & 1, sq = sQ + s * kStage6, sdo = sDO + s * kStage6;
                     if (!(ok = mbar_wait_w(&sh.do_full[s], (jj >> 1) & 1, wc, k6SiteDoFull))) break;
@@ -474,7 +455,13 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                     tc_fence_after();
                     mma6_dv(tmem + kColDV6, tmem + kColS6, sdo + oQ, t > 0);
                     umma_commit_w(&sh.do_empty[s]);  // dO read by dP^T and dV
-                    umma_commit_w(&sh.r0_free);      // P^T read: the next S^T may overwrite it
+                    if (t + 1 < U.n) {               // the next step's S^T, right behind dV (see above)
+                        const uint32_t s1 = (jj + 1) & 1;
+                        if (!(ok = mbar_wait_w(&sh.q_full[s1], ((jj + 1) >> 1) & 1, wc, k6SiteQFull))) break;
+                        tc_fence_after();
+                        mma6_s(tmem + kColS6, sK, sQ + s1 * kStage6);
+                        umma_commit_w(&sh.s_full);
+                    }
                     if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, k6SiteDs))) break;
                     tc_fence_after();
                     mma6_dqt(tmem + kColDP6, sK + oK, sDS);   // every key row has read dP^T
