@@ -464,10 +464,13 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                     }
                     if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, k6SiteDs))) break;
                     tc_fence_after();
-                    mma6_dqt(tmem + kColDP6, sK + oK, sDS);   // every key row has read dP^T
-                    umma_commit_w(&sh.dq_full);
+                    // dK before dQ^T: Q's slot is released, and the copy of
+                    // the step after next queued, ahead of dQ's reductions
+                    // (they share the copy engine).
                     mma6_dk(tmem + kColDK6, sDS, sq + oQ, t > 0);
                     umma_commit_w(&sh.q_empty[s]);   // Q (and the step's LSE / D) consumed
+                    mma6_dqt(tmem + kColDP6, sK + oK, sDS);   // every key row has read dP^T
+                    umma_commit_w(&sh.dq_full);
                     umma_commit_w(&sh.ds_free);      // dS^T read by dQ^T and dK
                 }
                 if (!ok) break;
