@@ -225,6 +225,9 @@ __device__ __forceinline__ void drain6(uint64_t* bar, uint32_t parity) {
     while (!mbar_try_wait(smem_u32(bar), parity) && globaltimer_ns() - t0 < kWaitLimitNs) {}
 }
 
+// kDbg: the debug counters are armed (a separate build of the kernel, so
+// that their tests cost nothing otherwise).
+template <bool kDbg>
 __global__ void __launch_bounds__(kThreads6, 1)
 bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -692,7 +695,7 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                     bar6(1, 128);               // ... for every warp of the group
                     if (r == 0) red6_release_add(sem, 1);
                 }
-                if (r == 0 && U.pass == 0) dbg_count(a.dbg_inner, (long long)h * a.T + U.tok0 + i * kStep);
+                if (kDbg && r == 0 && U.pass == 0) dbg_count(a.dbg_inner, (long long)h * a.T + U.tok0 + i * kStep);
             }
             if (!ok) break;
             ok = mbar_wait(&sh.dkdv_done, uc & 1, wc, k6SiteDkdv);
@@ -722,7 +725,7 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                     }
                 }
             }
-            if (r == 0 && U.pass == 0) dbg_count(a.dbg_visits, (long long)U.hk * a.T + U.tok0 + U.k * kTileN);
+            if (kDbg && r == 0 && U.pass == 0) dbg_count(a.dbg_visits, (long long)U.hk * a.T + U.tok0 + U.k * kTileN);
             tc_fence_before();
             mbar_arrive(&sh.acc_free);
         }
@@ -739,13 +742,14 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
 
 cudaError_t launch_bwd256_main(const BwdLaunch& L, cudaStream_t stream) {
     const BwdArgs& a = L.a;
-    cudaError_t e = cudaFuncSetAttribute(bwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem6);
+    auto kern = (a.dbg_visits || a.dbg_inner) ? bwd256_kernel<true> : bwd256_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem6);
     if (e != cudaSuccess) return e;
     const long long units = 2 * (a.varlen ? (long long)a.Hkv * ((a.T + kTileN - 1) / kTileN + a.B)
                                           : (long long)a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN));
     int grid = (int)(units < L.num_sms ? units : L.num_sms);
     if (grid < 1) grid = 1;
-    bwd256_kernel<<<grid, kThreads6, kSmem6, stream>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, a);
+    kern<<<grid, kThreads6, kSmem6, stream>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, a);
     return cudaGetLastError();
 }
 

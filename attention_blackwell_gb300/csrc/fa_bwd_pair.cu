@@ -211,6 +211,9 @@ __device__ __forceinline__ void pb_drain_wait(uint64_t* bar, uint32_t parity) {
 #define PB_NPAIRS ((int)(gridDim.x >> 1))
 #define PB_RANK ((int)(blockIdx.x & 1))
 
+// kDbg: the debug counters are armed (a separate build of the kernel, so
+// that their tests cost nothing otherwise).
+template <bool kDbg>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPBThreads, 1)
 bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tq64,
                 const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -659,7 +662,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 // This CTA's key tile contributed to query tile i unless it
                 // lies past the sequence or (causal) after the tile's rows.
                 const int kt = 2 * U.kb + PB_RANK;
-                if (r == 0 && kt * kTileN < U.len && (!a.causal || i >= kt))
+                if (kDbg && r == 0 && kt * kTileN < U.len && (!a.causal || i >= kt))
                     dbg_count(a.dbg_inner, (long long)h * a.T + U.tok0 + i * kTileM);
             }
             if (!ok) break;
@@ -693,7 +696,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     }
                 }
             }
-            if (r == 0 && (2 * U.kb + PB_RANK) * kTileN < U.len)
+            if (kDbg && r == 0 && (2 * U.kb + PB_RANK) * kTileN < U.len)
                 dbg_count(a.dbg_visits, (long long)U.hk * a.T + U.tok0 + (2 * U.kb + PB_RANK) * kTileN);
             tc_fence_before();
             mbar_arrive_remote_w(lead(&sh.acc_free));
@@ -722,7 +725,8 @@ int g_bwd_pairs_resident = 0;
 bool bwd_pair_supported(const BwdArgs& a) { return !a.varlen && !a.deterministic; }
 
 cudaError_t launch_bwd_pair_main(const BwdLaunch& L, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPBSmem);
+    auto kern = (L.a.dbg_visits || L.a.dbg_inner) ? bwd_pair_kernel<true> : bwd_pair_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPBSmem);
     if (e != cudaSuccess) return e;
     int max_pairs = g_bwd_pairs_resident;
     if (max_pairs == 0) {
@@ -738,14 +742,14 @@ cudaError_t launch_bwd_pair_main(const BwdLaunch& L, cudaStream_t stream) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, bwd_pair_kernel, &cfg) != cudaSuccess || n < 1) n = L.num_sms / 2;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) n = L.num_sms / 2;
         max_pairs = g_bwd_pairs_resident = n;
     }
     const BwdArgs& a = L.a;
     const long long units = (long long)a.B * a.Hkv * ((a.N + kKeyBlock - 1) / kKeyBlock);
     int pairs = (int)(units < max_pairs ? units : max_pairs);
     if (pairs < 1) pairs = 1;
-    bwd_pair_kernel<<<2 * pairs, kPBThreads, kPBSmem, stream>>>(L.tq, L.tq64, L.tk, L.tv, L.tdo, L.tdo64, L.tdq64, a);
+    kern<<<2 * pairs, kPBThreads, kPBSmem, stream>>>(L.tq, L.tq64, L.tk, L.tv, L.tdo, L.tdo64, L.tdq64, a);
     return cudaGetLastError();
 }
 

@@ -179,6 +179,9 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
     });
 }
 
+// kDbg: the debug counters are armed (a separate build of the kernel, so
+// that their tests cost nothing otherwise).
+template <bool kDbg>
 __global__ void __launch_bounds__(kThreads256, 1)
 fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
               const __grid_constant__ CUtensorMap tv, const FwdArgs a) {
@@ -405,7 +408,7 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                 // maximum only when some row of this warp jumped by more than tau.
                 const bool jump = (m_ref == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_ref > a.tau);
                 const bool rescale = __any_sync(0xffffffffu, jump);
-                if (lane == 0) dbg_count_rescale(a.dbg_rescale, j > 0, rescale);
+                if (kDbg && lane == 0) dbg_count_rescale(a.dbg_rescale, j > 0, rescale);
                 if (rescale) {
                     const float fac = (m_ref == -INFINITY) ? 0.f : ex2_mufu(m_ref - m_new);
                     l *= fac;
@@ -495,7 +498,7 @@ fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                                            : ((size_t)U.seq * a.Hq + U.h) * a.N + qi;
                 a.lse[li] = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
             }
-            if (r == 0 && q_first < U.len)
+            if (kDbg && r == 0 && q_first < U.len)
                 dbg_count(a.dbg_visits, (long long)U.h * (a.varlen ? a.N : (long long)a.B * a.N) + U.tok0 + q_first);
         }
     }
@@ -515,9 +518,10 @@ cudaError_t launch_fwd256(const FwdLaunch& L, cudaStream_t stream) {
                                      : (long long)a.B * a.Hq * ((a.N + kTileM - 1) / kTileM);
     int grid = (int)(units < L.num_sms ? units : L.num_sms);
     if (grid < 1) grid = 1;
-    cudaError_t e = cudaFuncSetAttribute(fwd256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem256);
+    auto kern = (a.dbg_visits || a.dbg_rescale) ? fwd256_kernel<true> : fwd256_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem256);
     if (e != cudaSuccess) return e;
-    fwd256_kernel<<<grid, kThreads256, kSmem256, stream>>>(L.tq, L.tk, L.tv, a);
+    kern<<<grid, kThreads256, kSmem256, stream>>>(L.tq, L.tk, L.tv, a);
     return cudaGetLastError();
 }
 

@@ -130,8 +130,10 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 // kEmu16: of every 16 column pairs of a row half, how many take their exp2
 // from the FMA-pipe polynomial (fa_exp2.cuh) instead of MUFU.EX2
-// (FlashAttention-4 blog, "Faster exponential").
-template <int kEmu16>
+// (FlashAttention-4 blog, "Faster exponential").  kDbg: the debug counters
+// are armed (a separate build of the kernel: their tests in the softmax loop
+// cost 1-4 % of the forward).
+template <int kEmu16, bool kDbg>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
 fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, const FwdArgs a) {
@@ -439,7 +441,7 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 const size_t li = a.varlen ? (size_t)U.h * a.N + U.tok0 + qi : ((size_t)U.seq * a.Hq + U.h) * a.N + qi;
                 a.lse[li] = lt > 0.f ? (mp + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
             }
-            if (x == 0 && r == 0 && m * kTileM < U.len)
+            if (kDbg && x == 0 && r == 0 && m * kTileM < U.len)
                 dbg_count(a.dbg_visits, (long long)U.h * (a.varlen ? a.N : (long long)a.B * a.N) + U.tok0 + m * kTileM);
             tc_fence_before();
             mbar_arrive_remote_w(lead(&sh.o_free));
@@ -498,7 +500,7 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 // both halves see the same row maxima, so their warp votes agree.
                 const bool jump = (m_ref == -INFINITY) ? (m_new != -INFINITY) : (m_new - m_ref > a.tau);
                 const bool rescale = __any_sync(0xffffffffu, jump);
-                if (lane == 0 && x == 0) dbg_count_rescale(a.dbg_rescale, j > 0, rescale);
+                if (kDbg && lane == 0 && x == 0) dbg_count_rescale(a.dbg_rescale, j > 0, rescale);
                 float fac = 1.f;
                 if (rescale) {
                     fac = (m_ref == -INFINITY) ? 0.f : ex2_mufu(m_ref - m_new);
@@ -603,9 +605,9 @@ int g_pairs_resident = 0;
 
 namespace {
 
-template <int E>
+template <int E, bool kDbg>
 cudaError_t launch_fwd_pair_t(const FwdLaunch& L, cudaStream_t stream) {
-    auto kern = fwd_pair_kernel<E>;
+    auto kern = fwd_pair_kernel<E, kDbg>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPSmem);
     if (e != cudaSuccess) return e;
     // Persistent: as many pairs as can be resident at once (clusters must fit
@@ -636,17 +638,22 @@ cudaError_t launch_fwd_pair_t(const FwdLaunch& L, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <bool kDbg>
+cudaError_t launch_fwd_pair_d(const FwdLaunch& L, cudaStream_t stream) {
+    switch (L.emu16) {
+        case 0: return launch_fwd_pair_t<0, kDbg>(L, stream);
+        case 1: return launch_fwd_pair_t<1, kDbg>(L, stream);
+        case 2: return launch_fwd_pair_t<2, kDbg>(L, stream);
+        case 3: return launch_fwd_pair_t<3, kDbg>(L, stream);
+        case 4: return launch_fwd_pair_t<4, kDbg>(L, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_fwd_pair(const FwdLaunch& L, cudaStream_t stream) {
-    switch (L.emu16) {
-        case 0: return launch_fwd_pair_t<0>(L, stream);
-        case 1: return launch_fwd_pair_t<1>(L, stream);
-        case 2: return launch_fwd_pair_t<2>(L, stream);
-        case 3: return launch_fwd_pair_t<3>(L, stream);
-        case 4: return launch_fwd_pair_t<4>(L, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    return (L.a.dbg_visits || L.a.dbg_rescale) ? launch_fwd_pair_d<true>(L, stream) : launch_fwd_pair_d<false>(L, stream);
 }
 
 }  // namespace fa

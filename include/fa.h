@@ -155,7 +155,10 @@ int fa_bwd_pairs_resident(void);
  *     [0] those that took the rescale branch (tau exceeded).
  * Tile starts are the sequence start plus multiples of 128.  Counting costs
  * an atomic per tile (and per warp decision): a debugging aid, not for
- * timed runs.  Errors: FA_ERR_ALIGN (misaligned pointer).
+ * timed runs.  While any counter is armed, the CTA-pair forward, the CTA-pair
+ * backward and both d = 256 kernels run a separate build that counts; the
+ * build without the counters has no trace of them.
+ * Errors: FA_ERR_ALIGN (misaligned pointer).
  */
 int fa_set_debug_counters(int *visits, int *inner, unsigned long long *rescales);
 
