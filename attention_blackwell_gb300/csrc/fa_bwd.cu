@@ -242,7 +242,8 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 //               of a unit stores dK (x alpha) and dV in bf16;
 //   warp  8     loader: K, V once per unit (TMA), then Q_i, dO_i (TMA) and
 //               LSE_i, D_i (plain loads) into a two-stage ring;
-//   warp  9     issues dV, dQ, dK, dP;  warp 10 issues S;  warp 11 idle.
+//   warp  9     issues dV, dQ, dK, dP (and, at d = 128, S);  warp 10 issues S
+//               at d = 64;  warp 11 idle.
 //
 // Tensor memory (512 columns): dK acc 0-127, dV acc 128-255 (d columns used),
 //   R0 256-383: S^T, then P^T (bf16; each key-row half packs its 64 queries
@@ -250,12 +251,18 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 //   R1 384-511: dP^T, then dQ_i (d columns) once the dS step has read dP^T (the
 //               paper's 1-CTA sharing of dP/dS/dQ columns; dS itself stays in
 //               shared memory).
-// Warp 10 issues each S^T as soon as its Q tile is loaded and dV has read
-// the previous P^T out of R0, so the next tile's S^T is computed while this
-// tile's dS is (FlashAttention-4 blog, "Backward pass": the next tile's
-// products overlap the elementwise work); warp 9 issues dV, dQ, dK and the
-// next dP in that order: dQ before dK, so that the hand-off of dQ out of R1
-// (which the next dP waits for) overlaps the dK product.
+// The next tile's S^T is computed while this tile's dS is (FlashAttention-4
+// blog, "Backward pass": the next tile's products overlap the elementwise
+// work).  At d = 128 one thread issues every product: dV(j), then S^T(j+1)
+// right behind it (S^T overwrites the R0 columns dV reads P^T from; one
+// thread's products run in issue order, so it need not wait for dV to
+// complete), then dK(j), so that Q's stage frees early for the copy two
+// tiles ahead, then dQ(j) and the next dP.  At d = 64, where the products
+// are short and the exponentials set the pace, warp 10 issues each S^T once
+// its Q tile is loaded and dV has completed, and warp 9 issues dV, dQ, dK and
+// the next dP, dQ before dK so that the hand-off of dQ out of R1 (which the
+// next dP waits for) overlaps the dK product (each order measured faster for
+// its head dim).
 //
 // Shared memory (dynamic, 1024-aligned; 232448 bytes at d = 128), a tile
 // being 128 rows x d bf16 (32K at d = 128, 16K at d = 64):
@@ -292,9 +299,12 @@ constexpr uint32_t kColDK = 0, kColDV = 128, kColR0 = 256, kColR1 = 384;
 enum : int { kBSiteKvEmpty = 11, kBSiteQEmpty, kBSiteKvFull, kBSiteAcc, kBSiteQFull, kBSiteP, kBSiteDs,
              kBSiteDqFree, kBSiteS, kBSiteDp, kBSiteDsFree, kBSiteDq, kBSiteDkdv, kBSiteSem, kBSiteUnit };
 
-// Readers of each claimed unit index: the two issuer warps (one arrival
-// each), the 256 key-row threads and the 128 dQ threads.
-constexpr uint32_t kUnitReaders = 2 + 256 + 128;
+// One thread issues every product at d = 128, two at d = 64 (see above).
+template <int D> constexpr int kIssuers = D == 128 ? 1 : 2;
+
+// Readers of each claimed unit index: the issuer warps (one arrival each),
+// the 256 key-row threads and the 128 dQ threads.
+template <int D> constexpr uint32_t kUnitReaders = kIssuers<D> + 256 + 128;
 
 struct BUnit {
     int seq, hk, k, tok0, len, n, nq, i0;
@@ -471,9 +481,9 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         mbar_init(&sh.dq_free, 128);
         mbar_init(&sh.dkdv_done, 1);
         mbar_init(&sh.acc_free, 128);
-        mbar_init(&sh.drain, 2);   // both issuers
+        mbar_init(&sh.drain, kIssuers<D>);
         mbar_init(&sh.r0_free, 1);
-        for (int s = 0; s < 4; ++s) { mbar_init(&sh.unit_full[s], 1); mbar_init(&sh.unit_empty[s], kUnitReaders); }
+        for (int s = 0; s < 4; ++s) { mbar_init(&sh.unit_full[s], 1); mbar_init(&sh.unit_empty[s], kUnitReaders<D>); }
         sh.abort_flag = 0;
         sh.total = a.varlen ? a.hdr->total_units : a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN);
         fence_mbar_init();
@@ -612,7 +622,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                            globaltimer_ns() - t0 < kWaitLimitNs) {}
             }
             __syncwarp();
-        } else if (warp == 10) {
+        } else if (warp == 10 && kIssuers<D> == 2) {
             // ------------------------------------------------------- S issuer
             // S^T(j) = K Q_j^T into R0 as soon as Q_j is loaded and dV(j-1)
             // has finished reading P^T(j-1) there; a warp of its own, so the
@@ -657,6 +667,14 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     if (!(ok = mbar_wait_w(&sh.dq_free, (jj - 1) & 1, wc, kBSiteDqFree))) break;
                     tc_fence_after();
                 }
+                if constexpr (kIssuers<D> == 1) {
+                    // S^T of the unit's first tile (R0 was last read by the
+                    // previous dV, which this thread issued earlier).
+                    if (!(ok = mbar_wait_w(&sh.q_full[jj & 1], (jj >> 1) & 1, wc, kBSiteQFull))) break;
+                    tc_fence_after();
+                    mma_kk<D>(tmem + kColR0, sK, base + kOffQ + (jj & 1) * kT32);
+                    umma_commit_w(&sh.s_full);
+                }
                 if (!(ok = mbar_wait_w(&sh.do_full, jj & 1, wc, kBSiteQFull))) break;
                 mma_kk<D>(tmem + kColR1, sV, base + kOffDO);
                 umma_commit_w(&sh.dp_full);
@@ -667,15 +685,32 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     tc_fence_after();
                     mma_tn<D>(tmem + kColDV, tmem + kColR0, base + kOffDO, t > 0);
                     umma_commit_w(&sh.do_empty);     // dO read by dP and dV: the next may load
-                    umma_commit_w(&sh.r0_free);      // P^T read: the next S^T may overwrite R0
+                    if constexpr (kIssuers<D> == 1) {
+                        if (more) {                  // the next S^T, right behind dV
+                            const uint32_t s1 = (jj + 1) & 1;
+                            if (!(ok = mbar_wait_w(&sh.q_full[s1], ((jj + 1) >> 1) & 1, wc, kBSiteQFull))) break;
+                            tc_fence_after();
+                            mma_kk<D>(tmem + kColR0, sK, base + kOffQ + s1 * kT32);
+                            umma_commit_w(&sh.s_full);
+                        }
+                    } else {
+                        umma_commit_w(&sh.r0_free);  // P^T read: the next S^T may overwrite R0
+                    }
                     if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, kBSiteDs))) break;
                     tc_fence_after();
-                    // dQ first (over dP^T, which the dS step has read), so its
-                    // drain overlaps dK; both read dS from shared memory.
-                    mma_nn<D>(tmem + kColR1, sDS, sK);
-                    umma_commit_w(&sh.dq_full);
-                    mma_ks<D>(tmem + kColDK, sDS, base + kOffQ + st * kT32, t > 0);
-                    umma_commit_w(&sh.q_empty[st]);  // Q and LSE/D of this stage are consumed
+                    // dQ goes over dP^T, which the dS step has read; both dQ
+                    // and dK read dS from shared memory.
+                    if constexpr (kIssuers<D> == 1) {
+                        mma_ks<D>(tmem + kColDK, sDS, base + kOffQ + st * kT32, t > 0);
+                        umma_commit_w(&sh.q_empty[st]);  // Q and LSE/D of this stage are consumed
+                        mma_nn<D>(tmem + kColR1, sDS, sK);
+                        umma_commit_w(&sh.dq_full);
+                    } else {
+                        mma_nn<D>(tmem + kColR1, sDS, sK);
+                        umma_commit_w(&sh.dq_full);
+                        mma_ks<D>(tmem + kColDK, sDS, base + kOffQ + st * kT32, t > 0);
+                        umma_commit_w(&sh.q_empty[st]);  // Q and LSE/D of this stage are consumed
+                    }
                     umma_commit_w(&sh.ds_free);      // dS read by dQ and dK
                     if (more) {
                         if (!(ok = mbar_wait_w(&sh.dq_free, jj & 1, wc, kBSiteDqFree))) break;
