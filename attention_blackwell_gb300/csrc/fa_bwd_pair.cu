@@ -30,9 +30,21 @@
 // query columns); warps 4-7 dQ drain (one thread per TMEM lane: 64 columns of
 // one dQ row) and the dK/dV epilogue; warp 8 loader; warp 11 relays "this
 // CTA's dS buffer is complete" to the even CTA.  In the even CTA warp 9
-// issues dP, dV, dK, dQ and warp 10 issues S.  Barriers an issuer waits on
-// live in the even CTA: the odd CTA's TMA bytes and warp arrivals count
+// issues dP, dV, S and dK, and warp 10 issues dQ.  Barriers an issuer waits
+// on live in the even CTA: the odd CTA's TMA bytes and warp arrivals count
 // there; commits go to both CTAs.
+//
+// Order (blog, "2-CTA backward": the previous tile's dQ before the current
+// dP, in the S columns next to P): the dQ product of tile j waits for the
+// exchange of dS(j), which takes about as long as a tile.  So dQ(j) is not
+// on the chain dS(j) -> dQ(j) -> dP(j+1): it is issued by a thread of its
+// own once the key rows have read S^T(j+1) out of R0 (its columns 64-127
+// hold dQ(j) from then until the drain has read it), and only S^T(j+2)
+// waits for that drain.  dP^T then has R1 to itself, and the dS exchange of
+// tile j overlaps the elementwise work of tile j+1.  Warp 9 issues, per tile
+// j: dP^T(j), dV(j) (when P^T(j) is ready), S^T(j+1) right behind dV (the
+// same thread's products run in order, so S^T(j+1) may overwrite the P^T
+// columns dV reads), then dK(j) (when dS^T(j) is ready).
 //
 // The dS exchange: the key-row half whose queries belong to this CTA writes
 // its rows into this CTA's dS buffer; the other half writes them into an
@@ -41,13 +53,14 @@
 // end, so no thread waits for remote stores to drain.
 //
 // Tensor memory (512 columns, both CTAs): dK 0-127, dV 128-255,
-//   R0 256-383: S^T, then P^T (bf16; each half packs its 64 queries into the
-//               first 32 of the 64 columns it read);
+//   R0 256-383: S^T(j), then P^T(j) in columns 0-63 (bf16; half 0 packs its
+//               64 queries into columns 0-31, half 1 into 32-63 once half 0
+//               has read them) and dQ(j-1) in columns 64-127 once half 1 has
+//               read S^T(j) there (an M = 128 pair product leaves each CTA's
+//               64 rows in 128 lanes x 64 columns: row m, column n at lane
+//               m + 64 (n / 64), column n % 64);
 //   R1 384-511: dP^T, then dS^T (bf16: half 0 in columns 0-31, half 1 in
-//               96-127, each over dP^T columns it has read) and dQ_i in columns
-//               32-95 (an M = 128 pair product leaves each CTA's 64 rows in 128
-//               lanes x 64 columns: row m, column n at lane m + 64 (n / 64),
-//               column n % 64).
+//               96-127, each over dP^T columns it has read).
 #include "fa_internal.h"
 
 namespace fa {
@@ -80,7 +93,11 @@ enum : int { kPBSiteKv = 81, kPBSiteQ, kPBSiteDo, kPBSiteS, kPBSiteP, kPBSiteDp,
 
 struct PBShared {
     uint64_t kv_full, kv_empty, qs_full, qs_empty, q_empty[2], qd_full, do_full, do_empty, st_full[2];
-    uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dq_full, dq_free, dkdv_done, acc_free, r0_free, drain;
+    uint64_t s_full, dp_full, p_ready, ds_ready, ds_free, dq_full, dkdv_done, acc_free, drain;
+    // Per tile parity: the waiters below skip tiles (a unit's last dQ does not
+    // wait for the next S^T), and a parity wait must never be more than one
+    // phase behind its barrier.
+    uint64_t s_read[2], dq_free[2];
     uint64_t dsx, dsx_ready;
     uint32_t tmem_base;
     int abort_flag;
@@ -130,7 +147,7 @@ __device__ __forceinline__ void pb_mma_kq(uint32_t d, uint32_t a_smem, uint32_t 
 
 // dV / dK: M = 256 (keys), N = d (64 per CTA, MN-major), K = 128 queries; A
 // (bf16) from TMEM: queries 0-63 in columns 0-31 of the region, queries
-// 64-127 kGap columns further than contiguous (P^T: 32, dS^T: 64).
+// 64-127 kGap columns further than contiguous (P^T: 0, dS^T: 64).
 template <uint32_t kGap>
 __device__ __forceinline__ void pb_mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b_smem, uint32_t acc) {
     constexpr uint32_t idesc = idesc_bf16_f32(256, 128, 0, 1);
@@ -173,6 +190,9 @@ __device__ __forceinline__ void pb_bulk_wait_read0() {
 __device__ __forceinline__ void pb_bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void pb_named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void pb_named_arrive(int id, int n) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 __device__ __forceinline__ bool pb_named_bar_or(int id, int n, bool pred) {
     uint32_t r;
@@ -234,7 +254,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
     if (tid == 0) {
         mbar_init(&sh.kv_full, 1);
-        mbar_init(&sh.kv_empty, 1);
+        mbar_init(&sh.kv_empty, 2);    // both issuers (dQ reads K too)
         mbar_init(&sh.qs_full, 1);
         mbar_init(&sh.qs_empty, 1);
         for (int s = 0; s < 2; ++s) {
@@ -247,15 +267,17 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         mbar_init(&sh.do_full, 1);
         mbar_init(&sh.do_empty, 1);
         mbar_init(&sh.s_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sh.s_read[s], 16);    // key-row warps of both CTAs have loaded S^T
+            mbar_init(&sh.dq_free[s], 8);    // drain warps of both CTAs
+        }
         mbar_init(&sh.dp_full, 1);
         mbar_init(&sh.p_ready, 16);    // key-row warps of both CTAs
         mbar_init(&sh.ds_ready, 16);
         mbar_init(&sh.ds_free, 1);
         mbar_init(&sh.dq_full, 1);
-        mbar_init(&sh.dq_free, 8);     // drain warps of both CTAs
         mbar_init(&sh.dkdv_done, 1);
         mbar_init(&sh.acc_free, 8);
-        mbar_init(&sh.r0_free, 1);
         mbar_init(&sh.drain, 2);       // both issuers
         sh.abort_flag = 0;
         fence_mbar_init();
@@ -342,20 +364,23 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive(&sh.st_full[st]);
-                        // Q columns of this CTA's head-dim half (dK) once dK of the previous tile is done.
-                        if (jj > 0) ok = mbar_wait(&sh.q_empty[(jj - 1) & 1], ((jj - 1) >> 1) & 1, wc, kPBSiteQ);
-                        if (ok) {
-                            if (leader) mbar_arrive_expect_tx(&sh.qd_full, 2 * kT16);
-                            tma_load_3d_pair(base + kOffQd, &tq, lead(&sh.qd_full), PB_RANK * 64, h, q0);
-                            // dO: both halves once dV of the previous tile is done.
-                            ok = mbar_wait(&sh.do_empty, (jj & 1) ^ 1, wc, kPBSiteDo);
-                        }
+                        // dO, both halves, once dV of the previous tile is done:
+                        // dP is the tile's first product after S, so its operand
+                        // goes ahead of Q's dK half below, which waits for the
+                        // previous tile's dK, a product later.
+                        ok = mbar_wait(&sh.do_empty, (jj & 1) ^ 1, wc, kPBSiteDo);
                         if (ok) {
                             if (leader) mbar_arrive_expect_tx(&sh.do_full, 2 * 2 * kT16);
                             for (int c = 0; c < 2; ++c)
                                 tma_load_3d_pair(base + kOffDOs + c * 8192, &tdo64, lead(&sh.do_full), c * 64, h,
                                                  q0 + PB_RANK * 64);
                             tma_load_3d_pair(base + kOffDOd, &tdo, lead(&sh.do_full), PB_RANK * 64, h, q0);
+                            // Q columns of this CTA's head-dim half (dK) once dK of the previous tile is done.
+                            if (jj > 0) ok = mbar_wait(&sh.q_empty[(jj - 1) & 1], ((jj - 1) >> 1) & 1, wc, kPBSiteQ);
+                        }
+                        if (ok) {
+                            if (leader) mbar_arrive_expect_tx(&sh.qd_full, 2 * kT16);
+                            tma_load_3d_pair(base + kOffQd, &tq, lead(&sh.qd_full), PB_RANK * 64, h, q0);
                         }
                     }
                     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -375,22 +400,34 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             }
             __syncwarp();
         } else if (warp == 10 && leader) {
-            // ------------------------------------------------------- S issuer
-            uint32_t jj = 0, uc = 0;
+            // ------------------------------------------------------ dQ issuer
+            // dQ(j) = dS K into R0 columns 64-127 once both CTAs' dS buffers
+            // are complete and those columns are free: the key rows have read
+            // S^T(j+1) there, or, for the unit's last tile (whose dQ reads
+            // this unit's K, so it cannot wait for the next unit's S^T), the
+            // drain has read dQ(j-1) and the key rows S^T(j).
+            uint32_t jj = 0;
             bool ok = true;
             for (int u = PB_PAIR; ok; u += PB_NPAIRS) {
                 PBUnit U;
                 if (!pb_unit(a, u, U)) break;
-                if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, kPBSiteKv))) break;
                 for (int t = 0; t < U.n; ++t, ++jj) {
-                    if (!(ok = mbar_wait_w(&sh.qs_full, jj & 1, wc, kPBSiteQ))) break;
-                    if (jj > 0 && !(ok = mbar_wait_w(&sh.r0_free, (jj - 1) & 1, wc, kPBSiteR0))) break;
+                    if (t + 1 < U.n) {
+                        const uint32_t n1 = jj + 1;
+                        if (!(ok = mbar_wait_w(&sh.s_read[n1 & 1], (n1 >> 1) & 1, wc, kPBSiteR0))) break;
+                    } else {
+                        if (!(ok = mbar_wait_w(&sh.s_read[jj & 1], (jj >> 1) & 1, wc, kPBSiteR0))) break;
+                        const uint32_t p1 = jj - 1;
+                        if (jj > 0 && !(ok = mbar_wait_w(&sh.dq_free[p1 & 1], (p1 >> 1) & 1, wc, kPBSiteDqFree))) break;
+                    }
+                    if (!(ok = pb_wait_cluster_w(&sh.dsx_ready, jj & 1, wc, kPBSiteDs))) break;
                     tc_fence_after();
-                    pb_mma_kq(tmem + kColR0, sK, base + kOffQs);
-                    umma_commit_pair_w(&sh.s_full, kBoth);
-                    umma_commit_pair_w(&sh.qs_empty, kBoth);   // the Q rows may reload
+                    pb_mma_dq(tmem + kColR0 + 64, sDS, sKdq);
+                    umma_commit_pair_w(&sh.dq_full, kBoth);
+                    umma_commit_pair_w(&sh.ds_free, kBoth);      // both CTAs' dS buffers read
                 }
-                ++uc;
+                if (!ok) break;
+                umma_commit_pair_w(&sh.kv_empty, kBoth);         // this unit's K (dQ's B) read
             }
             umma_commit_pair_w(&sh.drain, kLead);
             const uint64_t t0 = globaltimer_ns();
@@ -413,7 +450,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             }
             __syncwarp();
         } else if (warp == 9 && leader) {
-            // -------------------------------------------- dP, dV, dK, dQ issuer
+            // ---------------------------------------------- dP, dV, S, dK issuer
             uint32_t jj = 0, uc = 0;
             bool ok = true;
             for (int u = PB_PAIR; ok; u += PB_NPAIRS) {
@@ -429,39 +466,39 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 }
                 if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, kPBSiteKv))) break;
                 if (!(ok = mbar_wait_w(&sh.acc_free, (uc & 1) ^ 1, wc, kPBSiteAcc))) break;
-                if (jj > 0) {
-                    if (!(ok = mbar_wait_w(&sh.dq_free, (jj - 1) & 1, wc, kPBSiteDqFree))) break;
+                // S^T(j) into R0: both 64-column halves must be free.  The P^T
+                // half was read by dV(j-1), issued earlier by this thread.  The
+                // dQ half holds dQ(j-2) (written once the key rows had read
+                // S^T(j-1)) until the drain has read it -- or, for a unit's
+                // first tile, dQ(j-1): the previous unit's last dQ did not wait
+                // for this S^T.
+                auto issue_s = [&](uint32_t j, bool first) -> bool {
+                    const uint32_t lag = first ? 1u : 2u, jt = j - lag;
+                    if (j >= lag && !mbar_wait_w(&sh.dq_free[jt & 1], (jt >> 1) & 1, wc, kPBSiteDqFree)) return false;
+                    if (!mbar_wait_w(&sh.qs_full, j & 1, wc, kPBSiteQ)) return false;
                     tc_fence_after();
-                }
-                if (!(ok = mbar_wait_w(&sh.do_full, jj & 1, wc, kPBSiteDo))) break;
-                pb_mma_kq(tmem + kColR1, sV, base + kOffDOs);
-                umma_commit_pair_w(&sh.dp_full, kBoth);
+                    pb_mma_kq(tmem + kColR0, sK, base + kOffQs);
+                    umma_commit_pair_w(&sh.s_full, kBoth);
+                    umma_commit_pair_w(&sh.qs_empty, kBoth);   // the Q rows may reload
+                    return true;
+                };
+                if (!(ok = issue_s(jj, true))) break;
                 for (int t = 0; t < U.n; ++t, ++jj) {
                     const uint32_t st = jj & 1;
-                    const bool more = t + 1 < U.n;
+                    // dP^T(j) into R1, which dK(j-1) (issued earlier by this thread) has read.
+                    if (!(ok = mbar_wait_w(&sh.do_full, jj & 1, wc, kPBSiteDo))) break;
+                    pb_mma_kq(tmem + kColR1, sV, base + kOffDOs);
+                    umma_commit_pair_w(&sh.dp_full, kBoth);
                     if (!(ok = mbar_wait_w(&sh.p_ready, jj & 1, wc, kPBSiteP))) break;
                     tc_fence_after();
-                    pb_mma_tn<32>(tmem + kColDV, tmem + kColR0, base + kOffDOd, t > 0);
+                    pb_mma_tn<0>(tmem + kColDV, tmem + kColR0, base + kOffDOd, t > 0);
                     umma_commit_pair_w(&sh.do_empty, kBoth);   // dO read by dP and dV
-                    umma_commit_pair_w(&sh.r0_free, kLead);    // P^T read: the next S^T may overwrite R0
+                    if (t + 1 < U.n && !(ok = issue_s(jj + 1, false))) break;   // right behind dV
                     if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, kPBSiteDs))) break;
                     if (!(ok = mbar_wait_w(&sh.qd_full, jj & 1, wc, kPBSiteQ))) break;
                     tc_fence_after();
                     pb_mma_tn<64>(tmem + kColDK, tmem + kColR1, base + kOffQd, t > 0);
                     umma_commit_pair_w(&sh.q_empty[st], kBoth);  // Q columns and LSE/D of this tile consumed
-                    // dQ once both CTAs' dS buffers are complete (relayed below).
-                    if (!(ok = pb_wait_cluster_w(&sh.dsx_ready, jj & 1, wc, kPBSiteDs))) break;
-                    tc_fence_after();
-                    pb_mma_dq(tmem + kColR1 + 32, sDS, sKdq);
-                    umma_commit_pair_w(&sh.dq_full, kBoth);
-                    umma_commit_pair_w(&sh.ds_free, kBoth);      // both CTAs' dS buffers read
-                    if (more) {
-                        if (!(ok = mbar_wait_w(&sh.dq_free, jj & 1, wc, kPBSiteDqFree))) break;
-                        tc_fence_after();
-                        if (!(ok = mbar_wait_w(&sh.do_full, (jj + 1) & 1, wc, kPBSiteDo))) break;
-                        pb_mma_kq(tmem + kColR1, sV, base + kOffDOs);
-                        umma_commit_pair_w(&sh.dp_full, kBoth);
-                    }
                 }
                 if (!ok) break;
                 umma_commit_pair_w(&sh.dkdv_done, kBoth);
@@ -500,7 +537,6 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 const int st = jj & 1, i = U.i0 + t % span;
                 bool okw = mbar_wait(&sh.st_full[st], (jj >> 1) & 1, wc, kPBSiteSt);
                 okw = okw && mbar_wait(&sh.s_full, jj & 1, wc, kPBSiteS);
-                // The two halves meet at a named barrier below: both leave together.
                 float p[64];
                 if (okw) {
                     tc_fence_after();
@@ -508,6 +544,15 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     tmem_ld32(tR0 + cb, *reinterpret_cast<uint32_t(*)[32]>(pu + 0));
                     tmem_ld32(tR0 + cb + 32, *reinterpret_cast<uint32_t(*)[32]>(pu + 32));
                     tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive_remote_w(lead(&sh.s_read[jj & 1]));   // R0 columns 64-127 may take dQ(j-1)
+                    // Half 1 packs its P^T into columns 32-63, which half 0
+                    // reads: half 0 signals its loads done on the lane
+                    // quadrant's named barrier, half 1 waits there before its
+                    // stores.  Both do so in every tile, whatever their waits
+                    // returned (the else branch below).
+                    if (hc == 0) pb_named_arrive(2 + (warp & 3), 64);
+                    tc_fence_after();
                     const int c_lo = (a.causal ? key - i * kTileM : 0) - cb;
                     const int c_hi = (key >= U.len ? 0 : U.len - i * kTileM) - cb;
                     const float4* l2v = reinterpret_cast<const float4*>(s_lse + st * 128 + cb);
@@ -533,18 +578,26 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                             }
                         }
                     }
+                    if (hc == 1) {
+                        pb_named_bar(2 + (warp & 3), 64);
+                        tc_fence_after();
+                    }
 #pragma unroll
                     for (int stg = 0; stg < 2; ++stg) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int m = 0; m < 16; ++m) pk[m] = pack_bf16x2(p[stg * 32 + 2 * m], p[stg * 32 + 2 * m + 1]);
-                        tmem_st16(tR0 + cb + stg * 16, pk);   // P^T in this half's own columns
+                        tmem_st16(tR0 + hc * 32 + stg * 16, pk);   // P^T: columns 32 hc .. +31
                     }
                     tmem_wait_st();
                     tc_fence_before();
                     mbar_arrive_remote_w(lead(&sh.p_ready));
                     okw = mbar_wait(&sh.dp_full, jj & 1, wc, kPBSiteDp);
                     okw = okw && mbar_wait(&sh.ds_free, (jj & 1) ^ 1, wc, kPBSiteDsFree);
+                } else if (hc == 0) {
+                    pb_named_arrive(2 + (warp & 3), 64);
+                } else {
+                    pb_named_bar(2 + (warp & 3), 64);
                 }
                 // dS^T over the dP^T columns this thread has read: half 0 packs
                 // into R1 columns 0-31, half 1 into 96-127 (taking its second
@@ -586,7 +639,9 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                         chunk(std::integral_constant<int, 0>{});
                     }
                 }
-                if (!okw) { ok = false; break; }
+                // Both warps of the lane quadrant leave together (the P^T
+                // hand-off above needs both in every tile).
+                if (pb_named_bar_or(6 + (warp & 3), 64, !okw)) { ok = false; break; }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive_remote_w(lead(&sh.ds_ready));   // dS^T in TMEM: dK may start
@@ -617,7 +672,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         const int r = tid - 128;                             // TMEM lane
         const int wq = warp & 3;
         const uint32_t lb = (uint32_t)(wq * 32) << 16;
-        const uint32_t tDQ = tmem + lb + kColR1 + 32;
+        const uint32_t tDQ = tmem + lb + kColR0 + 64;
         const int qrow = r & 63, dh = r >> 6;                // dQ row of this CTA's 64 and head-dim half
         uint32_t jj = 0, uc = 0;
         bool ok = true;
@@ -636,7 +691,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 tmem_ld32(tDQ + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
                 tmem_wait_ld();
                 tc_fence_before();
-                mbar_arrive_remote_w(lead(&sh.dq_free));
+                mbar_arrive_remote_w(lead(&sh.dq_free[jj & 1]));
                 // Add this CTA's 64 x 128 slice of dQ_i into the fp32
                 // accumulator: two rounds, each two 64-row x 32-column boxes
                 // (one per head-dim half), staged like a 128-B TMA box.
