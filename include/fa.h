@@ -119,10 +119,13 @@ int fa_fwd_pairs_resident(void);
  *   1 -- CTA pairs per 256-key block: S^T, dP^T, dV and dK are
  *        M = 256 products over both SMs (each stages half of every B
  *        operand), dQ an M = 128 pair product after an exchange of half of
- *        dS through distributed shared memory.
+ *        dS through distributed shared memory; the dQ of a tile is computed
+ *        during the next tile, in the S columns beside P^T ("2-CTA
+ *        backward": the previous tile's dQ before the current dP).
  * Kernel 1 serves fixed-length d = 128 inputs in atomic mode; packed varlen
- * batches, deterministic mode and d = 64 use kernel 0.  Both compute the same gradients up to
- * the order of the fp32 dQ additions.  Errors: FA_ERR_INVALID.
+ * batches, deterministic mode and other head dims use kernel 0 (d = 256 its
+ * own kernel).  Both compute the same gradients up to the order of the fp32
+ * dQ additions; kernel 0 is the faster on GB300.  Errors: FA_ERR_INVALID.
  */
 int fa_set_bwd_kernel(int kernel);
 
