@@ -618,6 +618,26 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         const uint32_t tDQ = tmem + lb + kColDP6;
         uint32_t jj = 0, uc = 0;
         bool ok = true;
+        // Deterministic mode: a step's semaphore is released one step late,
+        // once the group reaches the next step's semaphore (or the unit's
+        // epilogue) -- by then its bulk reductions have long completed, so
+        // waiting for them costs nothing, where waiting at once stalled the
+        // drain every step.  Each warp's elected lane waits for its own
+        // reductions; one thread then releases.  A release always comes
+        // before the group's next wait, so no CTA holds one semaphore while
+        // it waits on another.
+        int* sem_pend = nullptr;
+        auto release_pending6 = [&]() {
+            if (sem_pend) {
+                if (lane == 0) {
+                    bulk6_wait0();          // this warp's additions are complete ...
+                    fence6_async_global();  // ... and ordered before the release
+                }
+                bar6(1, 128);               // ... for every warp of the group
+                if (r == 0) red6_release_add(sem_pend, 1);
+            }
+            sem_pend = nullptr;
+        };
         for (uint32_t n = 0; ok; ++n) {
             ok = mbar_wait(&sh.unit_full[n & 3], (n >> 2) & 1, wc, k6SiteUnit);
             if (bar6_or(1, 128, !ok)) { ok = false; break; }
@@ -642,6 +662,7 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                                ? a.sem + ((size_t)U.pass * a.Hq + h) * a.sem_stride + U.seq + (U.tok0 + i * kStep) / kStep
                                : nullptr;
                 if (sem) {
+                    release_pending6();
                     // Key tiles add into this query step in ascending order.
                     bool gave_up = false;
                     if (r == 0) {
@@ -687,17 +708,11 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
                         bulk6_commit();
                     }
                 }
-                if (sem) {
-                    if (lane == 0) {
-                        bulk6_wait0();          // this warp's additions are complete ...
-                        fence6_async_global();  // ... and ordered before the release
-                    }
-                    bar6(1, 128);               // ... for every warp of the group
-                    if (r == 0) red6_release_add(sem, 1);
-                }
+                if (sem) sem_pend = sem;
                 if (kDbg && r == 0 && U.pass == 0) dbg_count(a.dbg_inner, (long long)h * a.T + U.tok0 + i * kStep);
             }
             if (!ok) break;
+            release_pending6();   // the next key tile may be waiting for it
             ok = mbar_wait(&sh.dkdv_done, uc & 1, wc, k6SiteDkdv);
             if (bar6_or(1, 128, !ok)) { ok = false; break; }
             ++uc;
