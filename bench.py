@@ -158,6 +158,51 @@ def measured_peaks():
         return None
 
 
+def tile_budget(kind, M=128, N=128, d=128, mma_flop_per_clk=8192, exp_per_clk=16, smem_bytes_per_clk=128,
+                pair=False, ds_t_in_tmem=True, tma_writes=False):
+    """Per-SM cycles one M x N (query x key) tile costs each resource alone:
+    the feeds-and-speeds model of the FA4 blog ("Feeds and speeds") and the
+    FA4 paper summary (Tables 1 and 3), with B200's rates as defaults.
+
+    tensor core: 2 products of 2 M N d FLOP forward, 5 backward;
+    exponential unit: M N exponentials;
+    shared memory: the bytes the tensor core reads as operands, plus what
+    threads or copies move through it:
+      forward  -- Q, K and V tiles (P is read from tensor memory);
+      backward -- S^T = K Q^T reads K and Q, dP^T = V dO^T reads V and dO,
+                  dV += P^T dO reads dO (P^T from tensor memory), dK += dS^T Q
+                  reads Q (and dS^T unless it sits in tensor memory), dQ = dS K
+                  reads dS and K; the dS tile is stored, and the fp32 dQ tile
+                  is written to and read back from shared memory for its
+                  reduction.
+    pair: on CTA pairs each CTA stages half of every B operand (K in the
+    forward's S, V in P V; Q, dO, dO, Q, K in the backward's five products);
+    the dQ tile's round trip is counted whole, as the paper summary's Table 3
+    counts it.
+    ds_t_in_tmem=False and tma_writes=True give this build's one-CTA backward
+    (dK reads dS^T from shared memory; the Q and dO copies land there)."""
+    b = 2  # bf16 bytes
+    if kind == "fwd":
+        mma = 4 * M * N * d / mma_flop_per_clk
+        q, k, v = M * d * b, N * d * b, N * d * b
+        if pair:
+            k, v = k / 2, v / 2
+        smem = q + k + v + (q + k + v if tma_writes else 0)
+    elif kind == "bwd":
+        mma = 10 * M * N * d / mma_flop_per_clk
+        q = do = M * d * b
+        k = v = N * d * b
+        ds = M * N * b
+        half = 0.5 if pair else 1.0
+        reads = (k + q * half) + (v + do * half) + do * half + (q * half + (0 if ds_t_in_tmem else ds)) \
+            + (ds + k * half)
+        dq = M * d * 4
+        smem = reads + ds + 2 * dq + ((q + do) if tma_writes else 0)
+    else:
+        raise ValueError(kind)
+    return {"mma": mma, "exp": M * N / exp_per_clk, "smem": smem / smem_bytes_per_clk}
+
+
 def kernel_traffic(name, workload):
     """dram bytes per launch from the committed ncu summary, or None when the
     counters were taken on another workload or the kernel's sources changed
