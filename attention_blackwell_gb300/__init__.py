@@ -12,7 +12,7 @@ import os
 
 import torch
 
-__all__ = ["fwd", "set_fwd_kernel", "fwd_pairs_resident", "set_bwd_kernel", "bwd_pairs_resident", "bwd", "bwd_workspace", "exp2_emu", "selftest_timeout", "set_tuning", "set_debug_counters", "device_status", "num_sms", "FAError", "library_path", "lib"]
+__all__ = ["fwd", "set_fwd_kernel", "fwd_pairs_resident", "set_bwd_kernel", "bwd_pairs_resident", "set_schedule_order", "bwd", "bwd_workspace", "exp2_emu", "selftest_timeout", "set_tuning", "set_debug_counters", "device_status", "num_sms", "FAError", "library_path", "lib"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libfa.so")
@@ -56,6 +56,8 @@ def lib():
         L.fa_set_bwd_kernel.argtypes = [i]
         L.fa_bwd_pairs_resident.restype = i
         L.fa_bwd_pairs_resident.argtypes = []
+        L.fa_set_schedule_order.restype = i
+        L.fa_set_schedule_order.argtypes = [i]
         L.fa_fwd.restype = i
         L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, vp]
         sz = ctypes.c_size_t
@@ -111,6 +113,12 @@ def set_bwd_kernel(kernel=0):
     """Backward main kernel for later calls: 0 one CTA per 128-key tile (the
     default), 1 CTA pairs per 256-key block (fixed length, atomic mode)."""
     _check(lib().fa_set_bwd_kernel(int(kernel)), "fa_set_bwd_kernel")
+
+
+def set_schedule_order(order=0):
+    """Order of the work units for later calls: 0 the cost-ordered schedule
+    (the default), 1 plain enumeration (for testing the scheduler)."""
+    _check(lib().fa_set_schedule_order(int(order)), "fa_set_schedule_order")
 
 
 def bwd_pairs_resident():

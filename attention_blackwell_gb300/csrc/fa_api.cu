@@ -33,6 +33,7 @@ int g_emu16 = 0;               // share of exp2 pairs on the FMA pipe (sixteenth
 int g_bwd_kernel = 0;          // 0: one CTA per 128-key tile; 1: CTA pairs per 256-key block
 int g_fwd_kernel = 2;          // 0: ping-pong of two 128-row query tiles; 2: CTA pairs
 float g_tau = 8.0f;            // conditional-rescale threshold, log2(256)
+int g_naive = 0;               // 1: work units in plain enumeration order
 int* g_dbg_visits = nullptr;   // debug counters (fa_set_debug_counters)
 int* g_dbg_inner = nullptr;
 unsigned long long* g_dbg_rescale = nullptr;
@@ -207,6 +208,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     }
     L.a.scale_log2 = alpha * 1.4426950408889634f;
     L.a.tau = g_tau;
+    L.a.naive = g_naive;
     L.a.dbg_visits = g_dbg_visits;
     L.a.dbg_rescale = g_dbg_rescale;
     L.emu16 = g_emu16;
@@ -236,6 +238,12 @@ int fa_set_bwd_kernel(int kernel) {
 }
 
 int fa_bwd_pairs_resident(void) { return g_bwd_pairs_resident; }
+
+int fa_set_schedule_order(int order) {
+    if (order < 0 || order > 1) return FA_ERR_INVALID;
+    g_naive = order;
+    return FA_OK;
+}
 
 int fa_set_fwd_kernel(int kernel) {
     if (kernel != 0 && kernel != 2) return FA_ERR_INVALID;
@@ -373,6 +381,7 @@ int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const
     a.max_seqlen = varlen ? max_seqlen : N;
     a.alpha = alpha;
     a.scale_log2 = alpha * 1.4426950408889634f;
+    a.naive = g_naive;
     a.dbg_visits = g_dbg_visits;
     a.dbg_inner = g_dbg_inner;
     L.num_sms = dev->num_sms;

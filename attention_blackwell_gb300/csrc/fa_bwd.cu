@@ -121,6 +121,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
 //   non-causal: level L is sequence order[L] (longest first), key/value
 //     head major, key tiles ascending (the heads' Q and dO stay in L2 while
 //     their key tiles run).
+// The naive order (fa_set_schedule_order) lists every call like the
+// non-causal one, with the sequences in index order.
 // One CTA of 1024 threads.
 __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a) {
     __shared__ int s_cu[kMaxVarlenSeqs + 1], s_order[kMaxVarlenSeqs], s_pref[kLevelsMax + 1], s_cnt[kLevelsMax];
@@ -141,21 +143,24 @@ __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a) {
     for (int i = tid; i < B; i += blockDim.x) {
         const int ni = nkv(i);
         int rank = 0;
-        for (int j = 0; j < B; ++j) {
-            const int nj = nkv(j);
-            rank += (nj > ni) || (nj == ni && j < i);
-        }
-        s_order[rank] = i;   // tile count descending, index ascending among equals
+        if (!a.naive)
+            for (int j = 0; j < B; ++j) {
+                const int nj = nkv(j);
+                rank += (nj > ni) || (nj == ni && j < i);
+            }
+        s_order[a.naive ? i : rank] = i;   // tile count descending, index ascending among equals
     }
     __syncthreads();
+    const bool levels_by_cost = a.causal && !a.naive;
     if (tid == 0) {
-        int maxk = B > 0 ? nkv(s_order[0]) : 0;
+        int maxk = 0;
+        for (int i = 0; i < B; ++i) maxk = nkv(i) > maxk ? nkv(i) : maxk;
         if (maxk > kLevelsMax) {
             if (atomicCAS(&a.hdr->status.code, 0, -1) == 0) a.hdr->status.where = 200;
             maxk = 0;
         }
         int acc = 0, levels;
-        if (a.causal) {
+        if (levels_by_cost) {
             int p = 0;
             for (int L = 0; L < maxk; ++L) {
                 while (p < B && nkv(s_order[p]) >= maxk - L) ++p;   // sequences with >= c tiles
@@ -186,7 +191,7 @@ __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a) {
         }
         const int r = u - s_pref[lo];
         int seq, hk, k;
-        if (a.causal) {
+        if (levels_by_cost) {
             seq = s_order[s_cnt[lo] - 1 - r / a.Hkv];
             hk = r % a.Hkv;
             k = nkv(seq) - (maxk - lo);
@@ -319,14 +324,16 @@ struct BUnit {
 // mask, and in deterministic mode a key tile waits at its semaphores only on
 // tiles that are already claimed.  Both orders put every unit after the
 // ones it waits on, and CTAs claim units in list order, so the earliest
-// unfinished unit always runs.  Varlen: the planned work list.  u < 0 is the
-// end of the list.
+// unfinished unit always runs.  The naive order (fa_set_schedule_order) is
+// head-major with key tiles ascending in every mode, which also lists a
+// unit after those it waits on.  Varlen: the planned work list.  u < 0 is
+// the end of the list.
 __device__ __forceinline__ bool bwd_unit(const BwdArgs& a, int total, int u, BUnit& U) {
     if (u < 0 || u >= total) return false;
     if (!a.varlen) {
         const int bh = a.B * a.Hkv;
         int r;
-        if (a.deterministic || a.causal) {
+        if ((a.deterministic || a.causal) && !a.naive) {
             U.k = u / bh;
             r = u - U.k * bh;
         } else {

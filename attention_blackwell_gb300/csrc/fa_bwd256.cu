@@ -103,7 +103,7 @@ __device__ __forceinline__ bool unit6(const BwdArgs& a, int total, int u, Unit6&
     if (!a.varlen) {
         const int bh = a.B * a.Hkv;
         int r;
-        if (a.deterministic || a.causal) {
+        if ((a.deterministic || a.causal) && !a.naive) {
             U.k = ub / bh;
             r = ub - U.k * bh;
         } else {

@@ -115,7 +115,7 @@ __device__ __forceinline__ bool pb_unit(const BwdArgs& a, int u, PBUnit& U) {
     const int nkb = (a.N + kKeyBlock - 1) / kKeyBlock, bh = a.B * a.Hkv;
     if (u >= bh * nkb) return false;
     int r;
-    if (a.causal) {
+    if (a.causal && !a.naive) {
         U.kb = u / bh;
         r = u - U.kb * bh;
     } else {

@@ -73,13 +73,14 @@ __device__ __forceinline__ void set_blocks(const FwdArgs& a, Unit256& U) {
 }
 
 // Fixed length, unit u: one 128-row query tile of one (batch, head).
-// Non-causal: (batch, head) major; causal: query tiles from the last
-// (longest first), (batch, head) minor.
+// Non-causal (and the naive order of fa_set_schedule_order): (batch, head)
+// major; causal: query tiles from the last (longest first), (batch, head)
+// minor.
 __device__ __forceinline__ bool unit256(const FwdArgs& a, int u, Unit256& U) {
     const int nm = (a.N + kTileM - 1) / kTileM, bh_all = a.B * a.Hq;
     if (u < 0 || u >= bh_all * nm) return false;
     int bh;
-    if (a.causal) {
+    if (a.causal && !a.naive) {
         U.m = nm - 1 - u / bh_all;
         bh = u % bh_all;
     } else {
@@ -123,8 +124,32 @@ struct Walk256 {
     }
     __device__ __forceinline__ int tiles() const { return (c1 - c0 + kTileM - 1) / kTileM; }
 
+    // The naive order: (sequence, head) major, query tiles ascending.
+    __device__ bool get_naive(const FwdArgs& a, int u, Unit256& U) {
+        if (u < 0) return false;
+        if (k < 0) {
+            k = 0;
+            lvl_start = 0;
+            first(a);
+        }
+        while (u >= lvl_start + a.Hq * tiles()) {   // a later sequence
+            if (b + 1 >= a.B) return false;           // past the last one
+            lvl_start += a.Hq * tiles();
+            next(a);
+        }
+        const int i = u - lvl_start, nt = tiles();
+        U.seq = b;
+        U.h = i / nt;
+        U.m = i - U.h * nt;
+        U.tok0 = c0;
+        U.len = c1 - c0;
+        set_blocks(a, U);
+        return true;
+    }
+
     __device__ bool get(const FwdArgs& a, int u, Unit256& U) {
         if (!a.varlen) return unit256(a, u, U);
+        if (a.naive) return get_naive(a, u, U);
         if (u < 0) return false;
         while (k < 0 || u >= lvl_start + lvl_count) {
             lvl_start += lvl_count;

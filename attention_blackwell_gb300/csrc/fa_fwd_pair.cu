@@ -190,7 +190,8 @@ fwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             sh.sched.B = a.B; sh.sched.Hq = a.Hq; sh.sched.N = a.N; sh.sched.causal = a.causal;
             sh.sched.varlen = a.varlen; sh.sched.num_m = sh.maxm; sh.sched.maxm = sh.maxm;
             sh.sched.sec = a.l2_section; sh.sched.total = sh.total;
-            sh.sched.zz = a.causal && !a.varlen && sh.maxm % 2 == 0;
+            sh.sched.zz = a.causal && !a.varlen && !a.naive && sh.maxm % 2 == 0;
+            sh.sched.naive = a.naive;
             sh.sched.s_cu = s_cu; sh.sched.s_order = s_order; sh.sched.s_pref = s_pref;
         }
     }

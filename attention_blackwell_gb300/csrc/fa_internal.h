@@ -30,6 +30,7 @@ struct FwdArgs {
     int l2_section;          // causal fixed-length: (batch, head) pairs per L2 section
     float scale_log2;        // alpha * log2(e)
     float tau;               // conditional-rescale threshold (log2 units)
+    int naive;               // 1: work units in plain enumeration order (fa_set_schedule_order)
     // Debug counters (nullptr unless fa_set_debug_counters armed them):
     // visits[h * T + first row of a 128-row query tile] += 1 per finished
     // tile; rescale[0] += 1 per warp that takes the rescale branch after a
@@ -117,6 +118,7 @@ struct BwdArgs {
     long long T;
     int causal, varlen, deterministic, max_seqlen;
     float alpha, scale_log2;
+    int naive;               // 1: work units in plain enumeration order (fa_set_schedule_order)
     // Debug counters (nullptr unless fa_set_debug_counters armed them):
     // visits[hk * T + first row of a 128-key tile] += 1 per finished work
     // unit (key tile of one key/value head); inner[h * T + first row of a

@@ -29,9 +29,12 @@ struct Unit {
 //  varlen: sequences sorted by block count (descending); causal walks query
 //    block levels from the top down over the sorted sequences (longest
 //    first), non-causal walks the sorted sequences head-major.
+// naive (fa_set_schedule_order(1), for testing): every call walks
+//    (sequence, head) major, query blocks ascending, sequences in index order.
 struct Sched {
     int B, Hq, N, causal, varlen, num_m, sec, total, maxm;
     int zz;   // fixed length, causal, even num_m: zig-zag couples
+    int naive;
     const int* s_cu;
     const int* s_order;
     const int* s_pref;
@@ -51,7 +54,7 @@ struct Sched {
         if (!varlen) {
             const int BH = B * Hq;
             int bh, m;
-            if (!causal) {
+            if (!causal || naive) {
                 bh = u / num_m;
                 m = u - bh * num_m;
             } else if (zz) {
@@ -90,14 +93,15 @@ struct Sched {
             U.len = N;
             return true;
         }
-        const int n = causal ? maxm : B;
+        const bool levels = causal && !naive;
+        const int n = levels ? maxm : B;
         int lo = 0, hi = n;  // first index with pref > u, minus one
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
             if (s_pref[mid + 1] > u) hi = mid; else lo = mid + 1;
         }
         const int r = u - s_pref[lo];
-        if (causal) {
+        if (levels) {
             U.seq = s_order[r / Hq];
             U.h = r % Hq;
             U.m = maxm - 1 - lo;
@@ -133,22 +137,24 @@ __device__ __forceinline__ void build_sched_tables(const FwdArgs& a, int* s_cu, 
         for (int i = tid; i < a.B; i += nthreads) {
             const int ni = (s_cu[i + 1] - s_cu[i] + kUnitRows - 1) / kUnitRows;
             int rank = 0;
-            for (int j = 0; j < a.B; ++j) {
-                const int nj = (s_cu[j + 1] - s_cu[j] + kUnitRows - 1) / kUnitRows;
-                rank += (nj > ni) || (nj == ni && j < i);
-            }
-            s_order[rank] = i;
+            if (!a.naive)
+                for (int j = 0; j < a.B; ++j) {
+                    const int nj = (s_cu[j + 1] - s_cu[j] + kUnitRows - 1) / kUnitRows;
+                    rank += (nj > ni) || (nj == ni && j < i);
+                }
+            s_order[a.naive ? i : rank] = i;
         }
         __syncthreads();
         if (tid == 0) {
             auto nb = [&](int s) { return (s_cu[s + 1] - s_cu[s] + kUnitRows - 1) / kUnitRows; };
-            const int maxm = a.B > 0 ? nb(s_order[0]) : 0;
+            int maxm = 0;
+            for (int i = 0; i < a.B; ++i) maxm = nb(i) > maxm ? nb(i) : maxm;
             int acc = 0;
             if (maxm > kMaxUnitLevels) {
                 if (atomicCAS(&a.status->code, 0, -1) == 0) { a.status->where = 100; a.status->block = blockIdx.x; }
                 *sh_maxm = 0;
                 *sh_total = 0;
-            } else if (a.causal) {
+            } else if (a.causal && !a.naive) {
                 int p = 0;
                 for (int l = 0; l < maxm; ++l) {
                     const int m = maxm - 1 - l;

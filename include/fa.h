@@ -136,6 +136,24 @@ int fa_set_bwd_kernel(int kernel);
 int fa_bwd_pairs_resident(void);
 
 /*
+ * Process-wide order in which the kernels take their work units (affects
+ * later fa_fwd and fa_bwd calls), for testing the scheduler:
+ *   0 -- (default) the cost-ordered schedule (FlashAttention-4 blog,
+ *        "Scheduling"): longest-processing-time first under a causal mask
+ *        and for packed varlen batches (sequences sorted by length),
+ *        L2-sized (batch, head) sections, zig-zag couples of query blocks;
+ *   1 -- plain enumeration: (sequence, head) major, query tiles (forward)
+ *        or key tiles (backward) ascending, sequences in index order.
+ * Each work unit's arithmetic does not depend on the order, so the forward's
+ * O and LSE and the deterministic backward's gradients are bitwise the same
+ * under both; the atomic backward's dQ differs by the order of its fp32
+ * additions only.  Order 1 is slower under a causal mask or with unequal
+ * sequence lengths.  Not thread-safe with concurrent calls.
+ * Errors: FA_ERR_INVALID (any other value).
+ */
+int fa_set_schedule_order(int order);
+
+/*
  * Debug counters for the scheduler's exactly-once property (FlashAttention-4
  * blog, "Scheduling": every work tile is handed out once) and for the
  * conditional rescale (paper summary §3.1.4: how often tau = 8 skips).

@@ -106,6 +106,16 @@ def test_backward_kernel_selector(lib):
     assert lib.fa_set_bwd_kernel(0) == 0
 
 
+def test_schedule_order_selector(lib):
+    """Orders 0 (cost-ordered, the default) and 1 (plain enumeration) are
+    accepted, others rejected; no GPU call is made."""
+    for k in (1, 0):
+        assert lib.fa_set_schedule_order(k) == 0
+    assert lib.fa_set_schedule_order(2) == -1
+    assert lib.fa_set_schedule_order(-1) == -1
+    assert lib.fa_set_schedule_order(0) == 0
+
+
 def test_workspace_size_depends_on_head_dim(lib):
     """Host arithmetic only: the fp32 dQ accumulator scales with d."""
     f = lib.fa_bwd_workspace_size

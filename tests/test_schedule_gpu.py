@@ -37,6 +37,7 @@ def fa():
     fa.set_tuning(0, 8.0)
     fa.set_fwd_kernel(2)
     fa.set_bwd_kernel(0)
+    fa.set_schedule_order(0)
 
 
 def _dev(inp):
@@ -158,3 +159,34 @@ def test_rescale_branch_counts_on_the_causal_workload(fa, kernel):
     assert 0 < taken8 < total8
     assert counts[0.0][0] >= taken8
     assert counts[64.0][0] == 0
+
+
+# ------------------------------------------------ the naive order as well
+# (fa_set_schedule_order(1): plain enumeration instead of the cost order;
+# tests/test_schedule_order_gpu.py checks that the results do not change).
+
+@pytest.mark.parametrize("kernel,name", [(2, "causal"), (2, "varlen"), (0, "varlen")])
+def test_forward_tiles_exactly_once_naive_order(fa, kernel, name):
+    fa.set_schedule_order(1)
+    try:
+        test_forward_tiles_exactly_once(fa, kernel, name)
+    finally:
+        fa.set_schedule_order(0)
+
+
+def test_forward_d256_tiles_exactly_once_naive_order(fa):
+    fa.set_schedule_order(1)
+    try:
+        test_forward_d256_tiles_exactly_once(fa, "varlen_d256")
+    finally:
+        fa.set_schedule_order(0)
+
+
+@pytest.mark.parametrize("name,kernel,deterministic", [
+    ("causal_bwd", 0, True), ("causal_bwd", 1, False), ("varlen", 0, False)])
+def test_backward_units_and_tiles_exactly_once_naive_order(fa, name, kernel, deterministic):
+    fa.set_schedule_order(1)
+    try:
+        test_backward_units_and_tiles_exactly_once(fa, name, kernel, deterministic)
+    finally:
+        fa.set_schedule_order(0)
