@@ -111,7 +111,7 @@ def _need(t, name, dtype):
 
 def set_bwd_kernel(kernel=0):
     """Backward main kernel for later calls: 0 one CTA per 128-key tile (the
-    default), 1 CTA pairs per 256-key block (fixed length, atomic mode)."""
+    default), 1 CTA pairs per 256-key block (fixed length, d = 128)."""
     _check(lib().fa_set_bwd_kernel(int(kernel)), "fa_set_bwd_kernel")
 
 

@@ -22,8 +22,10 @@
 // adds per tile in fa_bwd.cu (blog, "2-CTA backward": exchange of half of dS,
 // halved atomic reductions).
 //
-// Fixed-length inputs, atomic dQ accumulation; packed varlen batches and
-// deterministic mode use fa_bwd.cu's kernel.
+// Fixed-length inputs; dQ accumulated atomically or, in deterministic mode,
+// in ascending key-block order at every query tile (FlashAttention-4 blog,
+// "Deterministic mode": semaphores); packed varlen batches use fa_bwd.cu's
+// kernel.
 //
 // Roles (512 threads per CTA, both CTAs): warps 0-3 and 12-15 key-row
 // warpgroups (P^T, dS^T; one thread per key row, each group half of the 128
@@ -89,7 +91,7 @@ constexpr uint32_t kColDK = 0, kColDV = 128, kColR0 = 256, kColR1 = 384;
 constexpr uint16_t kBoth = 3, kLead = 1;
 
 enum : int { kPBSiteKv = 81, kPBSiteQ, kPBSiteDo, kPBSiteS, kPBSiteP, kPBSiteDp, kPBSiteDs, kPBSiteDsFree,
-             kPBSiteDq, kPBSiteDqFree, kPBSiteDkdv, kPBSiteAcc, kPBSiteR0, kPBSiteSt };
+             kPBSiteDq, kPBSiteDqFree, kPBSiteDkdv, kPBSiteAcc, kPBSiteR0, kPBSiteSt, kPBSiteSem };
 
 struct PBShared {
     uint64_t kv_full, kv_empty, qs_full, qs_empty, q_empty[2], qd_full, do_full, do_empty, st_full[2];
@@ -108,14 +110,19 @@ struct PBUnit {
     int seq, hk, kb, tok0, len, nq, i0, n;
 };
 
-// Unit order as in fa_bwd.cu: non-causal head-major (the live Q, dO and dQ
-// accumulator of a few heads stay in L2), causal key-block-major (longest
-// first: a key block sees query tiles 2 kb .. nq-1).
+// Unit order as in fa_bwd.cu: non-causal atomic head-major (the live Q, dO
+// and dQ accumulator of a few heads stay in L2), causal and deterministic
+// key-block-major (longest first under the mask: a key block sees query
+// tiles 2 kb .. nq-1).  In deterministic mode a unit waits at its
+// semaphores only on units of smaller index (the same head's earlier key
+// blocks); every pair takes its units in increasing index, so the earliest
+// unfinished unit always runs.  The naive order (fa_set_schedule_order) is
+// head-major in every mode.
 __device__ __forceinline__ bool pb_unit(const BwdArgs& a, int u, PBUnit& U) {
     const int nkb = (a.N + kKeyBlock - 1) / kKeyBlock, bh = a.B * a.Hkv;
     if (u >= bh * nkb) return false;
     int r;
-    if (a.causal && !a.naive) {
+    if ((a.causal || a.deterministic) && !a.naive) {
         U.kb = u / bh;
         r = u - U.kb * bh;
     } else {
@@ -188,6 +195,15 @@ __device__ __forceinline__ void pb_bulk_wait_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void pb_bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void pb_fence_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+__device__ __forceinline__ int pb_ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void pb_red_release_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ void pb_named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -676,6 +692,22 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         const int qrow = r & 63, dh = r >> 6;                // dQ row of this CTA's 64 and head-dim half
         uint32_t jj = 0, uc = 0;
         bool ok = true;
+        // Deterministic mode: a query tile's semaphore counts the CTAs that
+        // have added their 64-row slice of it; key block kb adds once the
+        // count has reached 2 kb (both CTAs of every earlier block).  The
+        // release of a tile's count waits for that tile's reductions to
+        // complete; it is done at the next tile's semaphore wait (or before
+        // the unit's dK/dV epilogue), so the drain does not stall on the
+        // round trip to L2 every tile.
+        int* sem_pend = nullptr;
+        auto release_pending = [&]() {
+            if (r == 0 && sem_pend) {
+                pb_bulk_wait0();          // the tile's additions are complete
+                pb_fence_async_global();  // ... and ordered before the release
+                pb_red_release_add(sem_pend, 1);
+            }
+            sem_pend = nullptr;
+        };
         for (int u = PB_PAIR; ok; u += PB_NPAIRS) {
             PBUnit U;
             if (!pb_unit(a, u, U)) break;
@@ -692,6 +724,33 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive_remote_w(lead(&sh.dq_free[jj & 1]));
+                int* sem = a.deterministic ? a.sem + (size_t)h * a.sem_stride + U.seq + (U.tok0 + i * kTileM) / kTileN
+                                           : nullptr;
+                if (sem) {
+                    release_pending();
+                    // Wait (bounded) for the earlier key blocks' slices; the
+                    // wait runs in another warp than the releasing thread, and
+                    // the barrier below orders it before this tile's additions.
+                    bool gave_up = false;
+                    if (r == 32) {
+                        const uint64_t t0 = globaltimer_ns();
+                        uint32_t spins = 0;
+                        while (pb_ld_acquire(sem) < 2 * U.kb) {
+                            if ((++spins & 255u) == 0 &&
+                                (*(volatile int*)&sh.abort_flag || globaltimer_ns() - t0 > kWaitLimitNs)) {
+                                if (atomicCAS(&a.hdr->status.code, 0, kStatusTimeout) == 0) {
+                                    a.hdr->status.where = kPBSiteSem;
+                                    a.hdr->status.block = blockIdx.x;
+                                }
+                                *(volatile int*)&sh.abort_flag = 1;
+                                gave_up = true;
+                                break;
+                            }
+                        }
+                    }
+                    if (pb_named_bar_or(1, 128, gave_up)) { ok = false; break; }
+                    if (r == 0) pb_fence_async_global();  // our bulk reduction follows the acquire
+                }
                 // Add this CTA's 64 x 128 slice of dQ_i into the fp32
                 // accumulator: two rounds, each two 64-row x 32-column boxes
                 // (one per head-dim half), staged like a 128-B TMA box.
@@ -714,6 +773,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                         pb_bulk_commit();
                     }
                 }
+                sem_pend = sem;
                 // This CTA's key tile contributed to query tile i unless it
                 // lies past the sequence or (causal) after the tile's rows.
                 const int kt = 2 * U.kb + PB_RANK;
@@ -721,6 +781,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                     dbg_count(a.dbg_inner, (long long)h * a.T + U.tok0 + i * kTileM);
             }
             if (!ok) break;
+            release_pending();   // before the dK/dV epilogue: the next key block is waiting
             if (!(ok = mbar_wait(&sh.dkdv_done, uc & 1, wc, kPBSiteDkdv))) break;
             ++uc;
             tc_fence_after();
@@ -777,7 +838,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
 int g_bwd_pairs_resident = 0;
 
-bool bwd_pair_supported(const BwdArgs& a) { return !a.varlen && !a.deterministic; }
+bool bwd_pair_supported(const BwdArgs& a) { return !a.varlen; }
 
 cudaError_t launch_bwd_pair_main(const BwdLaunch& L, cudaStream_t stream) {
     auto kern = (L.a.dbg_visits || L.a.dbg_inner) ? bwd_pair_kernel<true> : bwd_pair_kernel<false>;

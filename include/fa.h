@@ -122,9 +122,9 @@ int fa_fwd_pairs_resident(void);
  *        dS through distributed shared memory; the dQ of a tile is computed
  *        during the next tile, in the S columns beside P^T ("2-CTA
  *        backward": the previous tile's dQ before the current dP).
- * Kernel 1 serves fixed-length d = 128 inputs in atomic mode; packed varlen
- * batches, deterministic mode and other head dims use kernel 0 (d = 256 its
- * own kernel).  Both compute the same gradients up to the order of the fp32
+ * Kernel 1 serves fixed-length d = 128 inputs, atomic or deterministic;
+ * packed varlen batches and other head dims use kernel 0 (d = 256 its own
+ * kernel).  Both compute the same gradients up to the order of the fp32
  * dQ additions; kernel 0 is the faster on GB300.  Errors: FA_ERR_INVALID.
  */
 int fa_set_bwd_kernel(int kernel);

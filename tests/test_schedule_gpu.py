@@ -109,7 +109,7 @@ def test_forward_d256_tiles_exactly_once(fa, name):
 
 @pytest.mark.parametrize("name,kernel,deterministic", [
     ("large", 0, False), ("large", 1, False), ("causal_bwd", 0, False), ("causal_bwd", 1, False),
-    ("causal_bwd", 0, True), ("varlen", 0, False)])
+    ("causal_bwd", 0, True), ("causal_bwd", 1, True), ("varlen", 0, False)])
 def test_backward_units_and_tiles_exactly_once(fa, name, kernel, deterministic):
     w, inp = FS.inputs(name)
     g = _dev(inp)
@@ -183,7 +183,7 @@ def test_forward_d256_tiles_exactly_once_naive_order(fa):
 
 
 @pytest.mark.parametrize("name,kernel,deterministic", [
-    ("causal_bwd", 0, True), ("causal_bwd", 1, False), ("varlen", 0, False)])
+    ("causal_bwd", 0, True), ("causal_bwd", 1, True), ("varlen", 0, False)])
 def test_backward_units_and_tiles_exactly_once_naive_order(fa, name, kernel, deterministic):
     fa.set_schedule_order(1)
     try:

@@ -129,15 +129,20 @@ def bwd(fa, g, causal, o, lse, deterministic, order):
     return out
 
 
-@pytest.mark.parametrize("d", [128, 64, 256])
+@pytest.mark.parametrize("d,kernel", [(128, 0), (128, 1), (64, 0), (256, 0)],
+                         ids=["d128_one_cta", "d128_pair", "d64", "d256"])
 @pytest.mark.parametrize("name", list(BWD_CASES))
-def test_deterministic_backward_bitwise_under_both_orders(fa, d, name):
+def test_deterministic_backward_bitwise_under_both_orders(fa, d, kernel, name):
     c = dict(BWD_CASES[name])
     causal = c.pop("causal")
     g = make(c.get("B", 0), c.get("N", 0), c["Hq"], c["Hkv"], d, lengths=c.get("lengths"), seed=10)
     o, lse = fwd(fa, g, causal, 0)
-    ref = bwd(fa, g, causal, o, lse, True, 0)
-    got = bwd(fa, g, causal, o, lse, True, 1)
+    fa.set_bwd_kernel(kernel)   # the pair kernel serves fixed length only
+    try:
+        ref = bwd(fa, g, causal, o, lse, True, 0)
+        got = bwd(fa, g, causal, o, lse, True, 1)
+    finally:
+        fa.set_bwd_kernel(0)
     for n, a, b in zip(("dq", "dk", "dv"), ref, got):
         assert torch.isfinite(a.float()).all(), n
         assert same_bits(a, b), (n, (a.float() - b.float()).abs().max().item())
