@@ -122,9 +122,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
 //     head major, key tiles ascending (the heads' Q and dO stay in L2 while
 //     their key tiles run).
 // The naive order (fa_set_schedule_order) lists every call like the
-// non-causal one, with the sequences in index order.
-// One CTA of 1024 threads.
-__global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a) {
+// non-causal one, with the sequences in index order.  kt: keys per unit, 128
+// (one CTA per key tile) or 256 (the CTA-pair kernel's key blocks); the
+// header records it, so that a main kernel never reads a list built for the
+// other.  One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a, int kt) {
     __shared__ int s_cu[kMaxVarlenSeqs + 1], s_order[kMaxVarlenSeqs], s_pref[kLevelsMax + 1], s_cnt[kLevelsMax];
     __shared__ int s_maxk, s_levels;
     const int tid = threadIdx.x, B = a.B;
@@ -139,7 +141,7 @@ __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a) {
     // The main kernel reads the units' bounds from this copy, so that plan
     // and main kernel agree on every sequence whatever the offsets were.
     for (int i = tid; i <= B; i += blockDim.x) a.cu_s[i] = s_cu[i];
-    auto nkv = [&](int s) { return (s_cu[s + 1] - s_cu[s] + kTileN - 1) / kTileN; };
+    auto nkv = [&](int s) { return (s_cu[s + 1] - s_cu[s] + kt - 1) / kt; };
     for (int i = tid; i < B; i += blockDim.x) {
         const int ni = nkv(i);
         int rank = 0;
@@ -180,6 +182,7 @@ __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a) {
         s_maxk = maxk;
         s_levels = levels;
         a.hdr->total_units = acc;
+        a.hdr->unit_keys = kt;
     }
     __syncthreads();
     const int maxk = s_maxk, levels = s_levels, total = s_pref[levels];
@@ -492,7 +495,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         mbar_init(&sh.r0_free, 1);
         for (int s = 0; s < 4; ++s) { mbar_init(&sh.unit_full[s], 1); mbar_init(&sh.unit_empty[s], kUnitReaders<D>); }
         sh.abort_flag = 0;
-        sh.total = a.varlen ? a.hdr->total_units : a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN);
+        int total = a.varlen ? a.hdr->total_units : a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN);
+        if (a.varlen && a.hdr->unit_keys != kTileN) {   // planned for the CTA-pair kernel
+            if (atomicCAS(&a.hdr->status.code, 0, -1) == 0) a.hdr->status.where = 202;
+            total = 0;
+        }
+        sh.total = total;
         fence_mbar_init();
     }
     if (warp == 8 && lane == 0) {
@@ -1009,7 +1017,7 @@ cudaError_t launch_bwd_d(const BwdLaunch& L, int stages, cudaStream_t stream) {
     if (stages & 1) {
         bwd_reset_status_kernel<<<1, 1, 0, stream>>>(a.hdr);
         bwd_pre_kernel<D><<<ew_grid, 256, 0, stream>>>(a);
-        if (a.varlen) bwd_plan_kernel<<<1, 1024, 0, stream>>>(a);
+        if (a.varlen) bwd_plan_kernel<<<1, 1024, 0, stream>>>(a, L.pair ? 2 * kTileN : kTileN);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -22,10 +22,9 @@
 // adds per tile in fa_bwd.cu (blog, "2-CTA backward": exchange of half of dS,
 // halved atomic reductions).
 //
-// Fixed-length inputs; dQ accumulated atomically or, in deterministic mode,
-// in ascending key-block order at every query tile (FlashAttention-4 blog,
-// "Deterministic mode": semaphores); packed varlen batches use fa_bwd.cu's
-// kernel.
+// Fixed-length and packed varlen inputs; dQ accumulated atomically or, in
+// deterministic mode, in ascending key-block order at every query tile
+// (FlashAttention-4 blog, "Deterministic mode": semaphores).
 //
 // Roles (512 threads per CTA, both CTAs): warps 0-3 and 12-15 key-row
 // warpgroups (P^T, dS^T; one thread per key row, each group half of the 128
@@ -103,6 +102,7 @@ struct PBShared {
     uint64_t dsx, dsx_ready;
     uint32_t tmem_base;
     int abort_flag;
+    int total;   // work units of this call
 };
 static_assert(sizeof(PBShared) <= 1024, "barrier block");
 
@@ -117,22 +117,49 @@ struct PBUnit {
 // semaphores only on units of smaller index (the same head's earlier key
 // blocks); every pair takes its units in increasing index, so the earliest
 // unfinished unit always runs.  The naive order (fa_set_schedule_order) is
-// head-major in every mode.
-__device__ __forceinline__ bool pb_unit(const BwdArgs& a, int u, PBUnit& U) {
-    const int nkb = (a.N + kKeyBlock - 1) / kKeyBlock, bh = a.B * a.Hkv;
-    if (u >= bh * nkb) return false;
-    int r;
-    if ((a.causal || a.deterministic) && !a.naive) {
-        U.kb = u / bh;
-        r = u - U.kb * bh;
-    } else {
-        r = u / nkb;
-        U.kb = u - r * nkb;
+// head-major in every mode.  Packed varlen batches: the plan kernel's list
+// of (sequence, key/value head, 256-key block), most expensive first (its
+// causal order lists each sequence's blocks in ascending order, as the
+// semaphores need).
+
+// Units of this call, read once per CTA; a varlen list planned for 128-key
+// units (the one-CTA kernel's) is refused: no units, FA_ERR_INVALID.
+template <bool kVar>
+__device__ __forceinline__ int pb_total(const BwdArgs& a) {
+    if constexpr (!kVar) return a.B * a.Hkv * ((a.N + kKeyBlock - 1) / kKeyBlock);
+    if (a.hdr->unit_keys != kKeyBlock) {
+        if (atomicCAS(&a.hdr->status.code, 0, -1) == 0) a.hdr->status.where = 202;
+        return 0;
     }
-    U.seq = r / a.Hkv;
-    U.hk = r - U.seq * a.Hkv;
-    U.tok0 = U.seq * a.N;
-    U.len = a.N;
+    return a.hdr->total_units;
+}
+
+// Decode unit u (false past the end; total from pb_total).
+template <bool kVar>
+__device__ __forceinline__ bool pb_unit(const BwdArgs& a, int total, int u, PBUnit& U) {
+    if (u < 0 || u >= total) return false;
+    if constexpr (kVar) {
+        const int4 e = a.units[u];
+        U.seq = e.x;
+        U.hk = e.y;
+        U.kb = e.z;
+        U.tok0 = a.cu_s[U.seq];            // sanitised by the plan kernel
+        U.len = a.cu_s[U.seq + 1] - U.tok0;
+    } else {
+        const int nkb = (a.N + kKeyBlock - 1) / kKeyBlock, bh = a.B * a.Hkv;
+        int r;
+        if ((a.causal || a.deterministic) && !a.naive) {
+            U.kb = u / bh;
+            r = u - U.kb * bh;
+        } else {
+            r = u / nkb;
+            U.kb = u - r * nkb;
+        }
+        U.seq = r / a.Hkv;
+        U.hk = r - U.seq * a.Hkv;
+        U.tok0 = U.seq * a.N;
+        U.len = a.N;
+    }
     U.nq = (U.len + kTileM - 1) / kTileM;
     U.i0 = a.causal ? 2 * U.kb : 0;
     if (U.i0 > U.nq) U.i0 = U.nq;
@@ -248,8 +275,10 @@ __device__ __forceinline__ void pb_drain_wait(uint64_t* bar, uint32_t parity) {
 #define PB_RANK ((int)(blockIdx.x & 1))
 
 // kDbg: the debug counters are armed (a separate build of the kernel, so
-// that their tests cost nothing otherwise).
-template <bool kDbg>
+// that their tests cost nothing otherwise).  kVar: packed varlen batches (a
+// separate build too: the fixed-length kernel measured 5 % slower with both
+// decodes in one body).
+template <bool kDbg, bool kVar>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPBThreads, 1)
 bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tq64,
                 const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -296,6 +325,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         mbar_init(&sh.acc_free, 8);
         mbar_init(&sh.drain, 2);       // both issuers
         sh.abort_flag = 0;
+        sh.total = pb_total<kVar>(a);
         fence_mbar_init();
     }
     if (warp == 8 && lane == 0) {
@@ -317,6 +347,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
     const WaitCtx wc{&sh.abort_flag, &a.hdr->status};
     const uint32_t tmem = sh.tmem_base;
+    const int total = sh.total;
     const int g = a.Hq / a.Hkv;
     const float scale = a.scale_log2;
     auto lead = [](uint64_t* bar) { return mapa_rank(smem_u32(bar), 0); };
@@ -331,7 +362,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             bool ok = true;
             for (int u = PB_PAIR; ok; u += PB_NPAIRS) {
                 PBUnit U;
-                if (!pb_unit(a, u, U)) break;
+                if (!pb_unit<kVar>(a, total, u, U)) break;
                 if (lane == 0) {
                     ok = mbar_wait(&sh.kv_empty, (uc & 1) ^ 1, wc, kPBSiteKv);
                     if (ok) {
@@ -371,7 +402,9 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
                         const int row = 4 * lane + e, q = i * kTileM + row;
                         float l2 = 0.f, dd = 0.f;
                         if (q < U.len) {
-                            l2 = a.lse[((size_t)U.seq * a.Hq + h) * a.N + q] * 1.4426950408889634f;
+                            const size_t li = kVar ? (size_t)h * a.T + U.tok0 + q
+                                                   : ((size_t)U.seq * a.Hq + h) * a.N + q;
+                            l2 = a.lse[li] * 1.4426950408889634f;
                             dd = a.D[(size_t)h * a.T + U.tok0 + q];
                         }
                         s_lse[st * 128 + row] = l2;
@@ -426,7 +459,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             bool ok = true;
             for (int u = PB_PAIR; ok; u += PB_NPAIRS) {
                 PBUnit U;
-                if (!pb_unit(a, u, U)) break;
+                if (!pb_unit<kVar>(a, total, u, U)) break;
                 for (int t = 0; t < U.n; ++t, ++jj) {
                     if (t + 1 < U.n) {
                         const uint32_t n1 = jj + 1;
@@ -458,7 +491,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             bool ok = true;
             for (int u = PB_PAIR; ok; u += PB_NPAIRS) {
                 PBUnit U;
-                if (!pb_unit(a, u, U)) break;
+                if (!pb_unit<kVar>(a, total, u, U)) break;
                 for (int t = 0; t < U.n; ++t, ++jj) {
                     if (!(ok = mbar_wait_w(&sh.dsx, jj & 1, wc, kPBSiteDs))) break;
                     pb_arrive_release_cluster_w(lead(&sh.dsx_ready));
@@ -471,7 +504,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
             bool ok = true;
             for (int u = PB_PAIR; ok; u += PB_NPAIRS) {
                 PBUnit U;
-                if (!pb_unit(a, u, U)) break;
+                if (!pb_unit<kVar>(a, total, u, U)) break;
                 if (U.n == 0) {   // no visible query tile: only the zero epilogue
                     if (!(ok = mbar_wait_w(&sh.kv_full, uc & 1, wc, kPBSiteKv))) break;
                     if (!(ok = mbar_wait_w(&sh.acc_free, (uc & 1) ^ 1, wc, kPBSiteAcc))) break;
@@ -546,7 +579,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         bool ok = true;
         for (int u = PB_PAIR; ok; u += PB_NPAIRS) {
             PBUnit U;
-            if (!pb_unit(a, u, U)) break;
+            if (!pb_unit<kVar>(a, total, u, U)) break;
             const int key = U.kb * kKeyBlock + PB_RANK * kTileM + r;
             const int span = U.nq - U.i0;
             for (int t = 0; t < U.n; ++t, ++jj) {
@@ -710,7 +743,7 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         };
         for (int u = PB_PAIR; ok; u += PB_NPAIRS) {
             PBUnit U;
-            if (!pb_unit(a, u, U)) break;
+            if (!pb_unit<kVar>(a, total, u, U)) break;
             const int span = U.nq - U.i0;
             for (int t = 0; t < U.n; ++t, ++jj) {
                 const int h = U.hk * g + t / span, i = U.i0 + t % span;
@@ -838,10 +871,12 @@ bwd_pair_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
 
 int g_bwd_pairs_resident = 0;
 
-bool bwd_pair_supported(const BwdArgs& a) { return !a.varlen; }
+bool bwd_pair_supported(const BwdArgs&) { return true; }
 
 cudaError_t launch_bwd_pair_main(const BwdLaunch& L, cudaStream_t stream) {
-    auto kern = (L.a.dbg_visits || L.a.dbg_inner) ? bwd_pair_kernel<true> : bwd_pair_kernel<false>;
+    const bool dbg = L.a.dbg_visits || L.a.dbg_inner;
+    auto kern = L.a.varlen ? (dbg ? bwd_pair_kernel<true, true> : bwd_pair_kernel<false, true>)
+                           : (dbg ? bwd_pair_kernel<true, false> : bwd_pair_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPBSmem);
     if (e != cudaSuccess) return e;
     int max_pairs = g_bwd_pairs_resident;
@@ -862,7 +897,8 @@ cudaError_t launch_bwd_pair_main(const BwdLaunch& L, cudaStream_t stream) {
         max_pairs = g_bwd_pairs_resident = n;
     }
     const BwdArgs& a = L.a;
-    const long long units = (long long)a.B * a.Hkv * ((a.N + kKeyBlock - 1) / kKeyBlock);
+    const long long units = a.varlen ? (long long)a.Hkv * ((a.T + kKeyBlock - 1) / kKeyBlock + a.B)
+                                     : (long long)a.B * a.Hkv * ((a.N + kKeyBlock - 1) / kKeyBlock);
     int pairs = (int)(units < max_pairs ? units : max_pairs);
     if (pairs < 1) pairs = 1;
     kern<<<2 * pairs, kPBThreads, kPBSmem, stream>>>(L.tq, L.tq64, L.tk, L.tv, L.tdo, L.tdo64, L.tdq64, a);

@@ -69,7 +69,8 @@ struct BwdHeader {
     int total_units;   // varlen: written by the plan kernel
     int next_unit;     // main kernel: units claimed past the first wave
     int done_ctas;     // main kernel: CTAs that found the list exhausted (follows next_unit)
-    int pad[57];
+    int unit_keys;     // varlen: keys per unit of the planned list (256 for the CTA-pair kernel, else 128)
+    int pad[56];
 };
 static_assert(sizeof(BwdHeader) == 256, "backward workspace header");
 static_assert(offsetof(BwdHeader, done_ctas) == offsetof(BwdHeader, next_unit) + sizeof(int), "claim counters");

@@ -229,7 +229,7 @@ def traffic_key(args, w, kernel):
     if w.d != 128:   # the records are taken at d = 128
         return "%s_d%d" % (kernel, w.d)
     if kernel == "bwd":
-        return "bwd" if (w.varlen or args.bwd_kernel == 0) else "bwd_pair"
+        return "bwd" if args.bwd_kernel == 0 else "bwd_pair"
     if kernel != "fwd":
         return kernel
     if args.fwd_kernel == 0:
@@ -487,7 +487,7 @@ def main_ours(args):
                            "CTA pairs, 256-key blocks"),
             "fwd_pairs_resident": fa_pairs_resident(),
             "bwd_kernel": ("128-key tile per head-dim half, 64-row query steps (d = 256)" if w.d == 256 else
-                           "one CTA per 128-key tile" if w.varlen or args.bwd_kernel == 0 or w.d != 128
+                           "one CTA per 128-key tile" if args.bwd_kernel == 0 or w.d != 128
                            else "CTA pairs per 256-key block"),
             "bwd_pairs_resident": bwd_pairs_resident(),
             "parallelism": "replicas" if world > 1 else "single",

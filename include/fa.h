@@ -122,9 +122,8 @@ int fa_fwd_pairs_resident(void);
  *        dS through distributed shared memory; the dQ of a tile is computed
  *        during the next tile, in the S columns beside P^T ("2-CTA
  *        backward": the previous tile's dQ before the current dP).
- * Kernel 1 serves fixed-length d = 128 inputs, atomic or deterministic;
- * packed varlen batches and other head dims use kernel 0 (d = 256 its own
- * kernel).  Both compute the same gradients up to the order of the fp32
+ * Kernel 1 serves d = 128 inputs, fixed length or packed varlen, atomic or
+ * deterministic; other head dims use kernel 0 (d = 256 its own kernel).  Both compute the same gradients up to the order of the fp32
  * dQ additions; kernel 0 is the faster on GB300.  Errors: FA_ERR_INVALID.
  */
 int fa_set_bwd_kernel(int kernel);
@@ -240,7 +239,11 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
  * them separately: stages is a bit mask, 1 = preprocess (D, zero the dQ
  * accumulator and semaphores, varlen work list), 2 = main kernel (dK, dV and
  * the dQ accumulator), 4 = dQ postprocess (dq = bf16(alpha * accumulator)).
- * Stages must run in this order on one workspace; fa_bwd == stages 7.
+ * Stages must run in this order on one workspace; fa_bwd == stages 7.  For
+ * a packed varlen batch, stage 1 plans the work list for the backward kernel
+ * selected at that time (fa_set_bwd_kernel): a stage 2 run with the other
+ * selection computes nothing and reports FA_ERR_INVALID through
+ * fa_get_device_status.
  */
 int fa_bwd_stages(int stages, const void *q, const void *k, const void *v, const void *o,
                   const float *lse, const void *dout, void *dq, void *dk, void *dv,

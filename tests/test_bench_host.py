@@ -60,7 +60,7 @@ def test_traffic_key_follows_the_kernel_that_runs():
     assert bench.traffic_key(_args(), large, "bwd") == "bwd"
     assert bench.traffic_key(_args(bwd_kernel=1), large, "bwd") == "bwd_pair"
     assert bench.traffic_key(_args(bwd_kernel=1, deterministic=True), large, "bwd") == "bwd_pair"
-    assert bench.traffic_key(_args(bwd_kernel=1), varlen, "bwd") == "bwd"   # varlen: the one-CTA kernel
+    assert bench.traffic_key(_args(bwd_kernel=1), varlen, "bwd") == "bwd_pair"
     assert bench.traffic_key(_args(), W.WORKLOADS["large_d256"], "fwd") == "fwd_d256"
     assert bench.traffic_key(_args(), W.WORKLOADS["large_d64"], "bwd") == "bwd_d64"
 

@@ -24,8 +24,8 @@ REL = 2e-2
 @pytest.fixture(scope="module", params=[0, 1], ids=["one_cta", "pair"])
 def fa(request):
     """Every backward test runs on both main kernels: 0 = one CTA per 128-key
-    tile, 1 = CTA pairs per 256-key block (fixed length, atomic or
-    deterministic; varlen calls always use kernel 0)."""
+    tile, 1 = CTA pairs per 256-key block (fixed length and packed varlen,
+    atomic or deterministic)."""
     import attention_blackwell_gb300 as fa
     fa.lib()
     fa.set_tuning(0, 8.0)

@@ -109,7 +109,8 @@ def test_forward_d256_tiles_exactly_once(fa, name):
 
 @pytest.mark.parametrize("name,kernel,deterministic", [
     ("large", 0, False), ("large", 1, False), ("causal_bwd", 0, False), ("causal_bwd", 1, False),
-    ("causal_bwd", 0, True), ("causal_bwd", 1, True), ("varlen", 0, False)])
+    ("causal_bwd", 0, True), ("causal_bwd", 1, True), ("varlen", 0, False), ("varlen", 1, False),
+    ("varlen", 1, True)])
 def test_backward_units_and_tiles_exactly_once(fa, name, kernel, deterministic):
     w, inp = FS.inputs(name)
     g = _dev(inp)

@@ -137,7 +137,7 @@ def test_deterministic_backward_bitwise_under_both_orders(fa, d, kernel, name):
     causal = c.pop("causal")
     g = make(c.get("B", 0), c.get("N", 0), c["Hq"], c["Hkv"], d, lengths=c.get("lengths"), seed=10)
     o, lse = fwd(fa, g, causal, 0)
-    fa.set_bwd_kernel(kernel)   # the pair kernel serves fixed length only
+    fa.set_bwd_kernel(kernel)
     try:
         ref = bwd(fa, g, causal, o, lse, True, 0)
         got = bwd(fa, g, causal, o, lse, True, 1)
@@ -165,3 +165,28 @@ def test_atomic_backward_within_summation_order_under_both_orders(fa, kernel, na
         a, b = a.float(), b.float()
         tol = 1e-2 * max(a.abs().max().item(), 1e-6)
         assert (a - b).abs().max().item() <= tol, n
+
+
+def test_varlen_plan_for_the_other_backward_kernel_is_refused(fa):
+    """Stage 1 of a packed batch plans the work list for the backward kernel
+    selected at that time (128-key units for the one-CTA kernel, 256-key
+    blocks for CTA pairs).  A stage 2 run under the other selection must
+    compute nothing and report FA_ERR_INVALID, never read the list with the
+    wrong unit size; a consistent pair of stages then works again."""
+    g = make(0, 0, 2, 1, 128, lengths=[300, 129, 513], seed=41)
+    o, lse = fwd(fa, g, True, 0)
+    ws = fa.bwd_workspace(g["B"], 2, g["N"], False, True)
+    dq, dk, dv = (torch.zeros_like(t) for t in (g["q"], g["k"], g["v"]))
+    kw = dict(causal=True, cu_seqlens=g["cu"], max_seqlen=g["ms"], workspace=ws, dq=dq, dk=dk, dv=dv)
+    try:
+        for first, second in ((0, 1), (1, 0)):
+            fa.set_bwd_kernel(first)
+            fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], stages=1, **kw)
+            fa.set_bwd_kernel(second)
+            fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], stages=2, **kw)
+            assert fa.device_status(ws) == -1   # FA_ERR_INVALID
+            fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], stages=1, **kw)
+            fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], stages=2, **kw)
+            assert fa.device_status(ws) == 0
+    finally:
+        fa.set_bwd_kernel(0)

@@ -8,8 +8,8 @@ outside every sequence unwritten (o, lse, dk, dv) or zero (dq), (c) give,
 on the rows they do cover, the oracle's attention for the sanitised offsets,
 and (d) report FA_OK.  Checked on every kernel that reads offsets: the
 pair and ping-pong forwards (d = 128), the ping-pong forward at d = 64, the
-d = 256 forward, and the backward (d = 128 and 64; its plan stage and main
-kernel share one sanitised copy).
+d = 256 forward, and the backward (d = 128 on both main kernels, and 64;
+the plan stage and the main kernel share one sanitised copy).
 """
 import math
 
@@ -102,9 +102,17 @@ def test_forward_malformed_offsets(fa, case, kernel, d, causal):
 
 
 @pytest.mark.parametrize("case", range(len(CASES)))
-@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("kernel,d", [(0, 128), (1, 128), (0, 64)], ids=["one_cta", "pair", "d64"])
 @pytest.mark.parametrize("causal,deterministic", [(False, False), (True, False), (True, True)])
-def test_backward_malformed_offsets(fa, case, d, causal, deterministic):
+def test_backward_malformed_offsets(fa, case, kernel, d, causal, deterministic):
+    fa.set_bwd_kernel(kernel)
+    try:
+        _backward_malformed_offsets(fa, case, d, causal, deterministic)
+    finally:
+        fa.set_bwd_kernel(0)
+
+
+def _backward_malformed_offsets(fa, case, d, causal, deterministic):
     raw, T = CASES[case]
     cs = sanitise(raw, T)
     Hq, Hkv = 4, 2
