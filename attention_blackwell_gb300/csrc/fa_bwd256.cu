@@ -92,9 +92,9 @@ struct Unit6 {
 };
 
 // Work unit u: base unit u / 2 (one 128-key tile of one key/value head, in
-// the one-CTA kernel's order: head-major for non-causal atomic runs,
-// key-tile-major otherwise, the planned list for varlen), head-dim half
-// u % 2.  The two halves of a tile are neighbours in the list, so the CTAs
+// the one-CTA kernel's order: head-major for non-causal atomic runs and in
+// the naive order of fa_set_schedule_order, key-tile-major otherwise, the
+// planned list for varlen), head-dim half u % 2.  The two halves of a tile are neighbours in the list, so the CTAs
 // running them read the same K and V from L2 at about the same time.
 __device__ __forceinline__ bool unit6(const BwdArgs& a, int total, int u, Unit6& U) {
     if (u < 0 || u >= total) return false;
