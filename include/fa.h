@@ -123,8 +123,9 @@ int fa_fwd_pairs_resident(void);
  *        during the next tile, in the S columns beside P^T ("2-CTA
  *        backward": the previous tile's dQ before the current dP).
  * Kernel 1 serves d = 128 inputs, fixed length or packed varlen, atomic or
- * deterministic; other head dims use kernel 0 (d = 256 its own kernel).  Both compute the same gradients up to the order of the fp32
- * dQ additions; kernel 0 is the faster on GB300.  Errors: FA_ERR_INVALID.
+ * deterministic; other head dims use kernel 0 (d = 256 its own kernel).
+ * Both compute the same gradients up to the order of the fp32 dQ
+ * additions; kernel 0 is the faster on GB300.  Errors: FA_ERR_INVALID.
  */
 int fa_set_bwd_kernel(int kernel);
 
