@@ -224,6 +224,33 @@ def forward_rows(q, k, v, alpha, causal, picks, cu_seqlens=None):
     return np.array(out_o), np.array(out_l)
 
 
+def dq_rows(q, k, v, do, alpha, causal, picks, cu_seqlens=None):
+    """dQ rows for sampled (sequence, query head, row) triples.
+
+    dQ_i = alpha * sum_j dS_ij k_j with dS_ij = P_ij (dP_ij - D_i),
+    dP_ij = do_i . v_j and D_i = sum_j P_ij dP_ij: every quantity belongs to
+    query row i and the keys it sees, so sampled rows are exact (the same
+    steps as ``head_backward``, for one row).  Returns dq [n, d].
+    """
+    q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(do)
+    Hq, Hkv = q.shape[-2], k.shape[-2]
+    if cu_seqlens is not None:
+        cu = [int(c) for c in np.asarray(cu_seqlens).reshape(-1)]
+    out = []
+    for (b, hq, i) in picks:
+        hk = kv_head_of(hq, Hq, Hkv)
+        if cu_seqlens is None:
+            qs, ks, vs, ds_ = q[b], k[b], v[b], do[b]
+        else:
+            o0, L = cu[b], cu[b + 1] - cu[b]
+            qs, ks, vs, ds_ = q[o0:o0 + L], k[o0:o0 + L], v[o0:o0 + L], do[o0:o0 + L]
+        p, _ = _softmax_rows(_scores(qs[i:i + 1, hq], ks[:, hk], alpha, causal, i))
+        dp = ds_[i:i + 1, hq] @ vs[:, hk].T
+        D = (p * dp).sum(axis=1, keepdims=True)
+        out.append((alpha * ((p * (dp - D)) @ ks[:, hk]))[0])
+    return np.array(out)
+
+
 def head_backward(qh, kh, vh, doh, alpha, causal=False):
     """One head: returns (dq [L,d], dk [L,d], dv [L,d]) in float64."""
     L = qh.shape[0]

@@ -122,6 +122,28 @@ def test_forward_rows_matches_full():
         assert abs(rl[n] - lse[b, h, i]) < 1e-13
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_dq_rows_match_full_backward(causal):
+    """Sampled dQ rows equal the full backward's rows (fixed length, grouped
+    heads), and the packed layout's rows equal each sequence's own."""
+    B, N, Hq, Hkv, d = 2, 40, 4, 2, 8
+    q, k, v, do = (rnd((B, N, h, d), 30 + n) for n, h in enumerate((Hq, Hkv, Hkv, Hq)))
+    dq, _, _ = A.backward(q, k, v, do, 0.3, causal)
+    picks = [(0, 0, 0), (1, 3, 39), (0, 2, 17), (1, 1, 1)]
+    rq = A.dq_rows(q, k, v, do, 0.3, causal, picks)
+    for n, (b, h, i) in enumerate(picks):
+        assert np.abs(rq[n] - dq[b, i, h]).max() < 1e-12
+    lengths = [5, 0, 1, 33]
+    cu = np.cumsum([0] + lengths).astype(np.int32)
+    T = int(cu[-1])
+    qv, kv, vv, dov = (rnd((T, h, d), 40 + n) for n, h in enumerate((Hq, Hkv, Hkv, Hq)))
+    dqv, _, _ = A.backward(qv, kv, vv, dov, 0.3, causal, cu_seqlens=cu)
+    picks = [(0, 0, 4), (2, 1, 0), (3, 3, 32), (3, 0, 0)]
+    rq = A.dq_rows(qv, kv, vv, dov, 0.3, causal, picks, cu_seqlens=cu)
+    for n, (b, h, i) in enumerate(picks):
+        assert np.abs(rq[n] - dqv[cu[b] + i, h]).max() < 1e-12
+
+
 # ---------------------------------------------------------------- backward
 
 @pytest.mark.parametrize("causal", [False, True])
