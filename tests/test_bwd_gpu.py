@@ -123,6 +123,23 @@ def test_deterministic_noncausal_many_tiles(fa):
     check([g[0, :, 0] for g in runs[0]], ref_h)
 
 
+@pytest.mark.parametrize("alpha", [0.01, 0.5])
+@pytest.mark.parametrize("causal", [False, True])
+def test_scale_extremes(fa, alpha, causal):
+    """alpha = 0.01 makes every row of P nearly uniform; alpha = 0.5 (logits
+    of standard deviation ~5.7 at d = 128) makes it nearly one-hot, so the
+    forward's row maxima jump often and the backward's P and dS are
+    dominated by a few keys per row."""
+    inp = inputs(2, 700, 4, 2, seed=47)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.fwd(q, k, v, causal=causal, alpha=alpha)
+    ws = fa.bwd_workspace(2, 4, 700, False, False)
+    got = fa.bwd(q, k, v, o, lse, do, causal=causal, alpha=alpha, workspace=ws)
+    assert fa.device_status(ws) == 0
+    ref = A.backward(inp["q"], inp["k"], inp["v"], inp["do"], alpha, causal)
+    check([t.float().cpu().numpy() for t in got], ref)
+
+
 def test_large_q_logits(fa):
     inp = inputs(1, 384, 2, 2, seed=17, q_std=3.0)
     check(gpu_grads(fa, inp, True)[0], oracle(inp, True))
