@@ -323,13 +323,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     for (int c = 0; c < 128; ++c)
                         if (c >= lim) s[c] = -INFINITY;
                 }
-                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+                // Row max: three-input max, four chains; then the exponents two
+                // at a time (packed fp32 FMA) and the row sum in two packed
+                // accumulators, so that no long chain of dependent adds sits
+                // between the exponentials (d = 64 forward 893 -> 957 TFLOP/s).
+                float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]),
+                      mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-                for (int c = 4; c < 128; c += 4) {
-                    mx0 = fmaxf(mx0, s[c]);
-                    mx1 = fmaxf(mx1, s[c + 1]);
-                    mx2 = fmaxf(mx2, s[c + 2]);
-                    mx3 = fmaxf(mx3, s[c + 3]);
+                for (int c = 8; c < 128; c += 8) {
+                    mx0 = fmax3(mx0, s[c], s[c + 1]);
+                    mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+                    mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+                    mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
                 }
                 const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale;
                 const float m_new = fmaxf(m_ref, m_blk);
@@ -356,24 +361,31 @@ fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     m_ref = m_new;
                 }
                 const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-                float l0 = 0.f, l1 = 0.f;
+                const uint64_t sc2 = f2_pack(scale, scale), nm2 = f2_pack(-m_use, -m_use);
+                uint64_t la = f2_pack(0.f, 0.f), lb = la;
 #pragma unroll
                 for (int st = 0; st < 4; ++st) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int c = st * 32 + 2 * i;
-                        const float x0 = fmaf(s[c], scale, -m_use), x1 = fmaf(s[c + 1], scale, -m_use);
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sc2, nm2), x0, x1);
                         float p0, p1;
                         if (i < kEmu16) { p0 = exp2_fma(x0); p1 = exp2_fma(x1); }   // kEmu16 of 16 pairs
                         else { p0 = ex2_mufu(x0); p1 = ex2_mufu(x1); }
-                        l0 += p0;
-                        l1 += p1;
+                        if (i & 1) lb = f2_add(lb, f2_pack(p0, p1));
+                        else la = f2_add(la, f2_pack(p0, p1));
                         pk[i] = pack_bf16x2(p0, p1);
                     }
                     tmem_st16(tS + st * 16, pk);
                 }
-                l += l0 + l1;
+                {
+                    float a0, a1, b0, b1;
+                    f2_unpack(la, a0, a1);
+                    f2_unpack(lb, b0, b1);
+                    l += (a0 + a1) + (b0 + b1);
+                }
                 tmem_wait_st();
                 tc_fence_before();
                 mbar_arrive(&sh.p_ready[x]);
