@@ -54,7 +54,8 @@ def parse():
                     help="backward main kernel: 0 one CTA per 128-key tile, 1 CTA pairs per 256-key block")
     ap.add_argument("--fwd-kernel", type=int, default=2, choices=[0, 2],
                     help="forward kernel: 0 ping-pong 128x128, 2 CTA pairs with 256-key blocks")
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=100,
+                    help="end-to-end steps timed (the first upload and the last download are not overlapped)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU baseline sample budget")
     return ap.parse_args()
 
@@ -506,7 +507,8 @@ def main_ours(args):
                      "traffic": kernel_traffic(traffic_key(args, w, dom["kernel"]), w.name)},
         "e2e": {"value": round(r["e2e_value"], 2), "unit": "TFLOP/s", "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"], "steps": r["E"],
-                "note": "public API, pinned host buffers, copies of step s overlap compute of step s-1"},
+                "note": "public API, pinned host buffers, copies of step s overlap compute of step s-1; "
+                        "the timed steps include the first upload and the last download"},
         "gpu_launches": K * sum(p["launches_per_step"] for p in per_kernel),
         "clocks": clk,
     }
