@@ -191,3 +191,49 @@ def test_backward_units_and_tiles_exactly_once_naive_order(fa, name, kernel, det
         test_backward_units_and_tiles_exactly_once(fa, name, kernel, deterministic)
     finally:
         fa.set_schedule_order(0)
+
+
+# ------------------------------------------- backward at d = 64 and d = 256
+
+def _expected_inner_steps(inp, H, causal, step):
+    """Key tiles contributing to each `step`-row query step (d = 256: 64-row
+    steps; a 128-key tile k reaches the steps from row 128 k on)."""
+    T = inp["T"]
+    e = np.zeros((H, T), dtype=np.int64)
+    row = 0
+    for L in inp["lengths"]:
+        nk = (L + 127) // 128
+        for i in range((L + step - 1) // step):
+            e[:, row + step * i] = (step * i) // 128 + 1 if causal else nk
+        row += L
+    return e
+
+
+@pytest.mark.parametrize("name,deterministic", [
+    ("large_d64", False), ("causal_bwd_d64", False), ("causal_bwd_d64", True),
+    ("large_d256", False), ("causal_d256", False), ("causal_d256", True), ("varlen_d256", False)])
+def test_backward_other_head_dims_exactly_once(fa, name, deterministic):
+    """Every 128-key unit once; every query tile (d = 64) or 64-row query
+    step (d = 256, counted on the first head-dim pass) receives one
+    contribution per key tile that sees it."""
+    w, inp = FS.inputs(name)
+    g = _dev(inp)
+    T = inp["T"]
+    o, lse = fa.fwd(g["q"], g["k"], g["v"], causal=w.causal, cu_seqlens=g["cu"], max_seqlen=g["ms"])
+    visits = torch.zeros(w.Hkv * T, dtype=torch.int32, device="cuda")
+    inner = torch.zeros(w.Hq * T, dtype=torch.int32, device="cuda")
+    fa.set_debug_counters(visits, inner, None)
+    try:
+        ws = fa.bwd_workspace(len(inp["lengths"]), w.Hq, T if g["cu"] is not None else w.N, deterministic,
+                              g["cu"] is not None, d=w.d)
+        fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal=w.causal, cu_seqlens=g["cu"], max_seqlen=g["ms"],
+               deterministic=deterministic, workspace=ws)
+        assert fa.device_status(ws) == 0
+    finally:
+        fa.set_debug_counters(None, None, None)
+    gv = visits.view(w.Hkv, T).cpu().numpy()
+    gi = inner.view(w.Hq, T).cpu().numpy()
+    assert np.array_equal(gv, _expected_visits(inp, w.Hkv)), (gv.max(), gv.sum())
+    want = (_expected_inner_steps(inp, w.Hq, w.causal, 64) if w.d == 256
+            else _expected_inner(inp, w.Hq, w.causal))
+    assert np.array_equal(gi, want), (gi.max(), gi.sum(), want.sum())
