@@ -243,8 +243,10 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 //               P^T = 2^(alpha log2e S^T - LSE log2e) -> bf16 into TMEM
 //               (operand A of dV += P^T dO); dS^T = P^T (dP^T - D) -> bf16
 //               into shared memory in the 128-B swizzled key-major layout,
-//               which the dQ UMMA reads as an MN-major A and the dK UMMA as
-//               a K-major A;
+//               which the dQ UMMA reads as an MN-major A, and at d = 128
+//               also into TMEM beside the dP^T it was computed from (operand
+//               A of dK += dS^T Q; at d = 64 dK reads the shared-memory copy
+//               as a K-major A);
 //   warps 4-7   dQ warpgroup, one thread per QUERY row: drains dQ_i from TMEM
 //               into the fp32 accumulator (vector reductions), then at the end
 //               of a unit stores dK (x alpha) and dV in bf16;
@@ -256,9 +258,13 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 // Tensor memory (512 columns): dK acc 0-127, dV acc 128-255 (d columns used),
 //   R0 256-383: S^T, then P^T (bf16; each key-row half packs its 64 queries
 //               into the first 32 of the 64 columns it read);
-//   R1 384-511: dP^T, then dQ_i (d columns) once the dS step has read dP^T (the
-//               paper's 1-CTA sharing of dP/dS/dQ columns; dS itself stays in
-//               shared memory).
+//   R1 384-511: dP^T, then at d = 128 dS^T (bf16, packed like P^T in R0),
+//               then dQ_i (d columns) once dK has read dS^T (issued first by
+//               the same thread) -- the paper's 1-CTA sharing of dP/dS/dQ
+//               columns.  Taking dK's A operand from TMEM saves 32 KB of the
+//               ~512 KB of shared-memory traffic per tile that bounds the
+//               kernel (headline backward 1183 -> 1196 TFLOP/s, bitwise the
+//               same gradients).
 // The next tile's S^T is computed while this tile's dS is (FlashAttention-4
 // blog, "Backward pass": the next tile's products overlap the elementwise
 // work).  At d = 128 one thread issues every product: dV(j), then S^T(j+1)
@@ -375,10 +381,11 @@ __device__ __forceinline__ void mma_kk(uint32_t d, uint32_t a_smem, uint32_t b_s
     });
 }
 
-// D (+)= A[tmem] B, B MN-major in shared memory (dV += P^T dO).
-// A is bf16 in the region the two key-row halves wrote: queries 0-63 in
-// columns 0-31 of the region, queries 64-127 in columns 64-95 (each half
-// packs its 64 queries at the start of the 64 columns it read).  N = D.
+// D (+)= A[tmem] B, B MN-major in shared memory (dV += P^T dO, and at
+// d = 128 dK += dS^T Q).  A is bf16 in the region the two key-row halves
+// wrote: queries 0-63 in columns 0-31 of the region, queries 64-127 in
+// columns 64-95 (each half packs its 64 queries at the start of the 64
+// columns it read).  N = D.
 template <int D>
 __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b_smem, uint32_t acc) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
@@ -389,7 +396,7 @@ __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b_s
     });
 }
 
-// D (+)= A B with A K-major and B MN-major in shared memory (dK += dS^T Q:
+// D (+)= A B with A K-major and B MN-major in shared memory (dK += dS^T Q at d = 64:
 // dS^T is stored key-major with the queries contiguous, as the K-major A of
 // this product; Q as loaded, d contiguous, is its MN-major B).  N = D.
 template <int D>
@@ -713,10 +720,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     }
                     if (!(ok = mbar_wait_w(&sh.ds_ready, jj & 1, wc, kBSiteDs))) break;
                     tc_fence_after();
-                    // dQ goes over dP^T, which the dS step has read; both dQ
-                    // and dK read dS from shared memory.
+                    // dQ goes over dP^T, which the dS step has read.  At
+                    // d = 128 dK reads dS^T from R1 and dQ, issued after it
+                    // by this thread, overwrites it; at d = 64 both read dS
+                    // from shared memory.
                     if constexpr (kIssuers<D> == 1) {
-                        mma_ks<D>(tmem + kColDK, sDS, base + kOffQ + st * kT32, t > 0);
+                        mma_tn<D>(tmem + kColDK, tmem + kColR1, base + kOffQ + st * kT32, t > 0);
                         umma_commit_w(&sh.q_empty[st]);  // Q and LSE/D of this stage are consumed
                         mma_nn<D>(tmem + kColR1, sDS, sK);
                         umma_commit_w(&sh.dq_full);
@@ -872,8 +881,12 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         *reinterpret_cast<uint4*>(ds_row + ((q ^ sw) << 4)) =
                             make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
                     }
+                    // At d = 128 also into this half's own R1 columns, which
+                    // this thread has read (dK's A operand, packed as P^T is).
+                    if constexpr (D == 128) tmem_st16(tR1 + cb + cc * 16, pk);
                 }
-                fence_async_smem();   // dS is read by the dQ and dK products
+                if constexpr (D == 128) tmem_wait_st();
+                fence_async_smem();   // dS is read by the dQ (and at d = 64 the dK) product
                 tc_fence_before();    // dP^T read: dQ may overwrite it
                 mbar_arrive(&sh.ds_ready);
             }
