@@ -243,10 +243,10 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 //               P^T = 2^(alpha log2e S^T - LSE log2e) -> bf16 into TMEM
 //               (operand A of dV += P^T dO); dS^T = P^T (dP^T - D) -> bf16
 //               into shared memory in the 128-B swizzled key-major layout,
-//               which the dQ UMMA reads as an MN-major A, and at d = 128
-//               also into TMEM beside the dP^T it was computed from (operand
-//               A of dK += dS^T Q; at d = 64 dK reads the shared-memory copy
-//               as a K-major A);
+//               which the dQ UMMA reads as an MN-major A, and also into TMEM
+//               as operand A of dK += dS^T Q (at d = 128 beside the dP^T it
+//               was computed from, at d = 64 in columns 64-127, which the
+//               64-column accumulators leave free);
 //   warps 4-7   dQ warpgroup, one thread per QUERY row: drains dQ_i from TMEM
 //               into the fp32 accumulator (vector reductions), then at the end
 //               of a unit stores dK (x alpha) and dV in bf16;
@@ -255,7 +255,9 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 //   warp  9     issues dV, dQ, dK, dP (and, at d = 128, S);  warp 10 issues S
 //               at d = 64;  warp 11 idle.
 //
-// Tensor memory (512 columns): dK acc 0-127, dV acc 128-255 (d columns used),
+// Tensor memory (512 columns): dK acc 0-127, dV acc 128-255 (d columns used;
+//   at d = 64 columns 64-127 hold dS^T, bf16, queries 0-63 in 64-95 and
+//   64-127 in 96-127),
 //   R0 256-383: S^T, then P^T (bf16; each key-row half packs its 64 queries
 //               into the first 32 of the 64 columns it read);
 //   R1 384-511: dP^T, then at d = 128 dS^T (bf16, packed like P^T in R0),
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
 //               columns.  Taking dK's A operand from TMEM saves 32 KB of the
 //               ~512 KB of shared-memory traffic per tile that bounds the
 //               kernel (headline backward 1183 -> 1196 TFLOP/s, bitwise the
-//               same gradients).
+//               same gradients; at d = 64 large_d64 782 -> 787).
 // The next tile's S^T is computed while this tile's dS is (FlashAttention-4
 // blog, "Backward pass": the next tile's products overlap the elementwise
 // work).  At d = 128 one thread issues every product: dV(j), then S^T(j+1)
@@ -309,6 +311,7 @@ struct BwdShared {
 static_assert(sizeof(BwdShared) <= 1024, "barrier block");
 
 constexpr uint32_t kColDK = 0, kColDV = 128, kColR0 = 256, kColR1 = 384;
+constexpr uint32_t kColDS64 = 64;   // dS^T at d = 64 (past the 64-column dK)
 
 enum : int { kBSiteKvEmpty = 11, kBSiteQEmpty, kBSiteKvFull, kBSiteAcc, kBSiteQFull, kBSiteP, kBSiteDs,
              kBSiteDqFree, kBSiteS, kBSiteDp, kBSiteDsFree, kBSiteDq, kBSiteDkdv, kBSiteSem, kBSiteUnit };
@@ -396,16 +399,15 @@ __device__ __forceinline__ void mma_tn(uint32_t d, uint32_t a_tmem, uint32_t b_s
     });
 }
 
-// D (+)= A B with A K-major and B MN-major in shared memory (dK += dS^T Q at d = 64:
-// dS^T is stored key-major with the queries contiguous, as the K-major A of
-// this product; Q as loaded, d contiguous, is its MN-major B).  N = D.
+// The same with A's queries in consecutive columns (dK += dS^T Q at d = 64,
+// dS^T in the columns the 64-column accumulators leave free).
 template <int D>
-__device__ __forceinline__ void mma_ks(uint32_t d, uint32_t a_smem, uint32_t b_smem, uint32_t acc) {
+__device__ __forceinline__ void mma_tl(uint32_t d, uint32_t a_tmem, uint32_t b_smem, uint32_t acc) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
-    const uint64_t ad = sdesc_sw128(a_smem, 16, 1024), bd = sdesc_sw128(b_smem, kBox, 1024);
+    const uint64_t bd = sdesc_sw128(b_smem, kBox, 1024);
     static_for<8>([&](auto kc) {
-        constexpr uint32_t k = kc, ao = ((k >> 2) * kBox + (k & 3) * 32) >> 4, bo = (k * 2048) >> 4;
-        umma_ss_k<ao, bo>(d, ad, bd, idesc, (acc | k) != 0);
+        constexpr uint32_t k = kc, col = k * 8;
+        umma_ts_k<col, ((k * 2048) >> 4)>(d, a_tmem, bd, idesc, (acc | k) != 0);
     });
 }
 
@@ -722,8 +724,8 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     tc_fence_after();
                     // dQ goes over dP^T, which the dS step has read.  At
                     // d = 128 dK reads dS^T from R1 and dQ, issued after it
-                    // by this thread, overwrites it; at d = 64 both read dS
-                    // from shared memory.
+                    // by this thread, overwrites it; at d = 64 dK reads it
+                    // from columns of its own.
                     if constexpr (kIssuers<D> == 1) {
                         mma_tn<D>(tmem + kColDK, tmem + kColR1, base + kOffQ + st * kT32, t > 0);
                         umma_commit_w(&sh.q_empty[st]);  // Q and LSE/D of this stage are consumed
@@ -732,7 +734,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     } else {
                         mma_nn<D>(tmem + kColR1, sDS, sK);
                         umma_commit_w(&sh.dq_full);
-                        mma_ks<D>(tmem + kColDK, sDS, base + kOffQ + st * kT32, t > 0);
+                        mma_tl<D>(tmem + kColDK, tmem + kColDS64, base + kOffQ + st * kT32, t > 0);
                         umma_commit_w(&sh.q_empty[st]);  // Q and LSE/D of this stage are consumed
                     }
                     umma_commit_w(&sh.ds_free);      // dS read by dQ and dK
@@ -881,12 +883,15 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                         *reinterpret_cast<uint4*>(ds_row + ((q ^ sw) << 4)) =
                             make_uint4(pk[4 * m], pk[4 * m + 1], pk[4 * m + 2], pk[4 * m + 3]);
                     }
-                    // At d = 128 also into this half's own R1 columns, which
-                    // this thread has read (dK's A operand, packed as P^T is).
+                    // And into TMEM as dK's A operand: at d = 128 into this
+                    // half's own R1 columns, which this thread has read
+                    // (packed as P^T is); at d = 64 into the free columns
+                    // 64-127, which dK of the previous tile has read (ds_free).
                     if constexpr (D == 128) tmem_st16(tR1 + cb + cc * 16, pk);
+                    else tmem_st16(tmem + lb + kColDS64 + hc * 32 + cc * 16, pk);
                 }
-                if constexpr (D == 128) tmem_wait_st();
-                fence_async_smem();   // dS is read by the dQ (and at d = 64 the dK) product
+                tmem_wait_st();
+                fence_async_smem();   // dS is read by the dQ product
                 tc_fence_before();    // dP^T read: dQ may overwrite it
                 mbar_arrive(&sh.ds_ready);
             }

@@ -180,10 +180,8 @@ def tile_budget(kind, M=128, N=128, d=128, mma_flop_per_clk=8192, exp_per_clk=16
     forward's S, V in P V; Q, dO, dO, Q, K in the backward's five products);
     the dQ tile's round trip is counted whole, as the paper summary's Table 3
     counts it.
-    tma_writes=True gives this build's one-CTA backward at d = 128 (dK reads
-    dS^T from tensor memory; the Q and dO copies land in shared memory); at
-    d = 64 it also takes ds_t_in_tmem=False (dK reads dS^T from shared
-    memory)."""
+    tma_writes=True gives this build's one-CTA backward (dK reads dS^T from
+    tensor memory; the Q and dO copies land in shared memory)."""
     b = 2  # bf16 bytes
     if kind == "fwd":
         mma = 4 * M * N * d / mma_flop_per_clk
