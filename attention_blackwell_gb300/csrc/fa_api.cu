@@ -386,6 +386,19 @@ int fa_bwd_stages(int stages, const void* q, const void* k, const void* v, const
     a.dbg_inner = g_dbg_inner;
     L.num_sms = dev->num_sms;
     L.pair = d == 128 && g_bwd_kernel == 1 && bwd_pair_supported(a) ? 1 : 0;
+    // Packed batches whose key/value heads serve many query heads (MQA-like):
+    // the one-CTA kernel's work units cover kSplitHeads query heads each and
+    // add their dK, dV into fp32 partial sums (atomic mode only, so that
+    // deterministic mode keeps one unit per key tile and its fixed order).
+    const int G = Hq / Hkv;
+    a.kv_split = varlen && !deterministic && d != 256 && !L.pair && G >= kSplitMinGroup && G % kSplitHeads == 0
+                     ? kSplitHeads : 0;
+    a.dkvacc = varlen && d != 256 ? reinterpret_cast<float*>(ws + w.kv_off) : nullptr;
+    if (a.kv_split) {
+        if ((rc = make_map_acc(&L.tdkv, ws + w.kv_off, 2LL * Hkv * T, kTileM, d)) != FA_OK) return rc;
+    } else {
+        L.tdkv = L.tdq;   // not read
+    }
     if (L.pair) {
         if ((rc = make_map(&L.tq64, q, Hq, T, 64)) != FA_OK) return rc;
         if ((rc = make_map(&L.tdo64, dout, Hq, T, 64)) != FA_OK) return rc;

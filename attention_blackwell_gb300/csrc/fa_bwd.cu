@@ -100,6 +100,13 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
             }
         }
     }
+    if (a.kv_split) {        // the fp32 dK / dV partial sums of split units
+        const long long n = 2LL * a.Hkv * a.T * D / 4;
+        float4* z4 = reinterpret_cast<float4*>(a.dkvacc);
+        for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+             i += (long long)gridDim.x * blockDim.x)
+            z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (a.deterministic) {   // d = 256: one set per head-dim half
         const long long n = (D == 256 ? 2LL : 1LL) * a.Hq * a.sem_stride;
         for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -122,7 +129,13 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
 //     head major, key tiles ascending (the heads' Q and dO stay in L2 while
 //     their key tiles run).
 // The naive order (fa_set_schedule_order) lists every call like the
-// non-causal one, with the sequences in index order.  kt: keys per unit, 128
+// non-causal one, with the sequences in index order.
+// Split units (kv_split query heads each, atomic mode, groups of at least
+// kSplitMinGroup query heads): sequence-major (longest first), then
+// key/value head, head group, key tiles ascending, so that the CTAs of a wave
+// share one group's rows of Q, dO and the fp32 dQ accumulator and their
+// reductions hit L2; each unit adds its partial dK and dV into fp32 sums.
+// kt: keys per unit, 128
 // (one CTA per key tile) or 256 (the CTA-pair kernel's key blocks); the
 // header records it, so that a main kernel never reads a list built for the
 // other.  One CTA of 1024 threads.
@@ -153,7 +166,8 @@ __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a, int kt)
         s_order[a.naive ? i : rank] = i;   // tile count descending, index ascending among equals
     }
     __syncthreads();
-    const bool levels_by_cost = a.causal && !a.naive;
+    const int gs = a.kv_split, ng = gs ? (a.Hq / a.Hkv) / gs : 1;   // query heads, groups per unit
+    const bool levels_by_cost = a.causal && !a.naive && !gs;
     if (tid == 0) {
         int maxk = 0;
         for (int i = 0; i < B; ++i) maxk = nkv(i) > maxk ? nkv(i) : maxk;
@@ -175,7 +189,7 @@ __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a, int kt)
             levels = maxk > 0 ? B : 0;
             for (int L = 0; L < levels; ++L) {
                 s_pref[L] = acc;
-                acc += nkv(s_order[L]) * a.Hkv;
+                acc += nkv(s_order[L]) * a.Hkv * ng;
             }
         }
         s_pref[levels] = acc;
@@ -183,6 +197,7 @@ __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a, int kt)
         s_levels = levels;
         a.hdr->total_units = acc;
         a.hdr->unit_keys = kt;
+        a.hdr->unit_heads = gs;
     }
     __syncthreads();
     const int maxk = s_maxk, levels = s_levels, total = s_pref[levels];
@@ -193,7 +208,7 @@ __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a, int kt)
             if (s_pref[mid + 1] > u) hi = mid; else lo = mid + 1;
         }
         const int r = u - s_pref[lo];
-        int seq, hk, k;
+        int seq, hk, k, grp = 0;
         if (levels_by_cost) {
             seq = s_order[s_cnt[lo] - 1 - r / a.Hkv];
             hk = r % a.Hkv;
@@ -201,10 +216,12 @@ __global__ void __launch_bounds__(1024) bwd_plan_kernel(const BwdArgs a, int kt)
         } else {
             seq = s_order[lo];
             const int nk = nkv(seq);
-            hk = r / nk;
-            k = r - hk * nk;
+            hk = r / (nk * ng);
+            const int r2 = r - hk * nk * ng;
+            grp = r2 / nk;
+            k = r2 - grp * nk;
         }
-        a.units[u] = make_int4(seq, hk, k, 0);
+        a.units[u] = make_int4(seq, hk, k, grp);
     }
 }
 
@@ -231,6 +248,31 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const BwdArgs a) {
             if (w < rows) {
                 const long long h = w / a.T, tok = w - h * a.T;
                 reinterpret_cast<BV*>(a.dq)[(tok * a.Hq + h) * 32 + lane] = pack_scaled(g[e], a.alpha);
+            }
+        }
+    }
+    if (a.kv_split) {   // split units: dK = bf16(alpha sum), dV = bf16(sum) of the fp32 partial sums
+        const long long kvrows = a.T * a.Hkv;   // rows per accumulator, (key/value head, token) order
+        // Only the sequences' rows: the sanitised sequences tile [cu_s[0], cu_s[B]).
+        const long long c_lo = a.cu_s[0], c_hi = a.cu_s[a.B];
+        for (long long w0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 4; w0 < 2 * kvrows;
+             w0 += nwarps * 4) {
+            FV g[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const long long w = w0 + e < 2 * kvrows ? w0 + e : 2 * kvrows - 1;
+                g[e] = reinterpret_cast<const FV*>(a.dkvacc + (size_t)w * D)[lane];
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const long long w = w0 + e;
+                if (w < 2 * kvrows) {
+                    const int which = w >= kvrows;
+                    const long long rem = w - which * kvrows, hk = rem / a.T, tok = rem - hk * a.T;
+                    if (tok >= c_lo && tok < c_hi)
+                        reinterpret_cast<BV*>(which ? a.dv : a.dk)[(tok * a.Hkv + hk) * 32 + lane] =
+                            pack_scaled(g[e], which ? 1.f : a.alpha);
+                }
             }
         }
     }
@@ -325,6 +367,7 @@ template <int D> constexpr uint32_t kUnitReaders = kIssuers<D> + 256 + 128;
 
 struct BUnit {
     int seq, hk, k, tok0, len, n, nq, i0;
+    int h0;   // first query head of the unit within its key/value head's group
 };
 
 // Decode unit u.  Fixed length, non-causal, atomic mode: (sequence,
@@ -338,7 +381,8 @@ struct BUnit {
 // ones it waits on, and CTAs claim units in list order, so the earliest
 // unfinished unit always runs.  The naive order (fa_set_schedule_order) is
 // head-major with key tiles ascending in every mode, which also lists a
-// unit after those it waits on.  Varlen: the planned work list.  u < 0 is
+// unit after those it waits on.  Varlen: the planned work list (a split
+// unit covers kv_split query heads from its group's h0).  u < 0 is
 // the end of the list.
 __device__ __forceinline__ bool bwd_unit(const BwdArgs& a, int total, int u, BUnit& U) {
     if (u < 0 || u >= total) return false;
@@ -357,18 +401,20 @@ __device__ __forceinline__ bool bwd_unit(const BwdArgs& a, int total, int u, BUn
         U.hk = r - U.seq * a.Hkv;
         U.tok0 = U.seq * a.N;
         U.len = a.N;
+        U.h0 = 0;
     } else {
         const int4 e = a.units[u];
         U.seq = e.x;
         U.hk = e.y;
         U.k = e.z;
+        U.h0 = e.w * a.kv_split;        // head group (split units), else 0
         const int c0 = a.cu_s[U.seq];   // sanitised by the plan kernel
         U.tok0 = c0;
         U.len = a.cu_s[U.seq + 1] - c0;
     }
     U.nq = (U.len + kTileM - 1) / kTileM;
     U.i0 = a.causal ? U.k : 0;
-    U.n = (a.Hq / a.Hkv) * (U.nq - U.i0);
+    U.n = (a.varlen && a.kv_split ? a.kv_split : a.Hq / a.Hkv) * (U.nq - U.i0);
     return true;
 }
 
@@ -469,7 +515,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
            const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-           const __grid_constant__ CUtensorMap tdq, const BwdArgs a) {
+           const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdkv, const BwdArgs a) {
     extern __shared__ __align__(1024) uint8_t dsm[];
     using G = BGeo<D>;
     constexpr uint32_t kOffK = G::kOffK, kOffV = G::kOffV, kOffQ = G::kOffQ, kOffDO = G::kOffDO, kOffDS = G::kOffDS,
@@ -509,6 +555,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             if (atomicCAS(&a.hdr->status.code, 0, -1) == 0) a.hdr->status.where = 202;
             total = 0;
         }
+        if (a.varlen && a.hdr->unit_heads != a.kv_split) {   // planned for the other mode
+            if (atomicCAS(&a.hdr->status.code, 0, -1) == 0) a.hdr->status.where = 203;
+            total = 0;
+        }
         sh.total = total;
         fence_mbar_init();
     }
@@ -518,6 +568,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         tma_prefetch_desc(&tv);
         tma_prefetch_desc(&tdo);
         tma_prefetch_desc(&tdq);
+        if (a.kv_split) tma_prefetch_desc(&tdkv);
     }
     if (warp == 0) {
         tmem_alloc(&sh.tmem_base, 512);
@@ -585,7 +636,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 // ring instead of delaying the tile's q_full.
                 float nl[4], nd[4];
                 auto load_stats = [&](int t) {
-                    const int h = U.hk * g + t / span, i = U.i0 + t % span;
+                    const int h = U.hk * g + U.h0 + t / span, i = U.i0 + t % span;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int q = i * kTileM + 4 * lane + e;
@@ -601,7 +652,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                 };
                 load_stats(0);
                 for (int t = 0; t < U.n; ++t, ++jj) {
-                    const int st = jj & 1, h = U.hk * g + t / span, i = U.i0 + t % span;
+                    const int st = jj & 1, h = U.hk * g + U.h0 + t / span, i = U.i0 + t % span;
                     if (lane == 0) ok = mbar_wait(&sh.q_empty[st], ((jj >> 1) & 1) ^ 1, wc, kBSiteQEmpty);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
@@ -909,6 +960,34 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
         // start of the next tile instead of waited for at the end of this one,
         // so the drain does not stall on the round trip to L2 every tile.
         int* sem_pend = nullptr;
+        // Add a 128-row tile of fp32 rows (this thread's row in v) into an
+        // accumulator with TMA bulk tensor reductions of whole 128-byte
+        // lines, staged in shared memory in D / 32 rounds of one 32-column
+        // box (128 rows x 128 B, swizzled like a 128-B TMA box) alternating
+        // between two buffers, so each round's reduction reads one buffer
+        // while the threads fill the other.
+        auto stage_add = [&](const uint32_t (&v)[D], const CUtensorMap* map, int grow) {
+            uint8_t* stage_row = dsm + kOffStage + r * 128;
+#pragma unroll
+            for (int rnd = 0; rnd < D / 32; ++rnd) {
+                const int b = rnd & 1;
+                // At most the latest group may still be reading: the one
+                // before it used this buffer.
+                if (r == 0) bulk_wait_read1();
+                named_bar(1, 128);
+                const uint32_t* src = v + rnd * 32;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<uint4*>(stage_row + b * kBox + ((q ^ (r & 7)) << 4)) =
+                        make_uint4(src[4 * q], src[4 * q + 1], src[4 * q + 2], src[4 * q + 3]);
+                fence_async_smem();
+                named_bar(1, 128);
+                if (r == 0) {
+                    tma_reduce_add_2d(map, base + kOffStage + b * kBox, rnd * 32, grow);
+                    bulk_commit();
+                }
+            }
+        };
         auto release_pending = [&]() {
             if (r == 0 && sem_pend) {
                 bulk_wait0();          // the tile's additions are complete
@@ -927,7 +1006,7 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             if (!bwd_unit(a, total, u, U)) break;
             const int span = U.nq - U.i0;
             for (int t = 0; t < U.n; ++t, ++jj) {
-                const int h = U.hk * g + t / span, i = U.i0 + t % span;
+                const int h = U.hk * g + U.h0 + t / span, i = U.i0 + t % span;
                 ok = mbar_wait(&sh.dq_full, jj & 1, wc, kBSiteDq);
                 // Named barriers follow: every thread of the warpgroup must
                 // take the same path, so the warpgroup agrees on aborts.
@@ -972,35 +1051,10 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
                     if (named_bar_or(1, 128, gave_up)) { ok = false; break; }
                     if (r == 0) fence_async_global();  // our bulk reduction follows the acquire
                 }
-                // Add dQ_i into the fp32 accumulator with TMA bulk tensor
-                // reductions of whole 128-byte lines, staged in shared memory
-                // in D / 32 rounds of one 32-column box (128 rows x 128 B,
-                // swizzled like a 128-B TMA box) alternating between two
-                // buffers, so each round's reduction reads one buffer while
-                // the threads fill the other.  Rows past the sequence end hold
-                // exact zeros (their P, hence dS, is zero), so adding them to
-                // the neighbouring rows changes nothing.
-                const int grow = h * (int)a.T + U.tok0 + i * kTileM;
-                uint8_t* stage_row = dsm + kOffStage + r * 128;
-#pragma unroll
-                for (int rnd = 0; rnd < D / 32; ++rnd) {
-                    const int b = rnd & 1;
-                    // At most the latest group may still be reading: the one
-                    // before it used this buffer.
-                    if (r == 0) bulk_wait_read1();
-                    named_bar(1, 128);
-                    const uint32_t* src = v + rnd * 32;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        *reinterpret_cast<uint4*>(stage_row + b * kBox + ((q ^ (r & 7)) << 4)) =
-                            make_uint4(src[4 * q], src[4 * q + 1], src[4 * q + 2], src[4 * q + 3]);
-                    fence_async_smem();
-                    named_bar(1, 128);
-                    if (r == 0) {
-                        tma_reduce_add_2d(&tdq, base + kOffStage + b * kBox, rnd * 32, grow);
-                        bulk_commit();
-                    }
-                }
+                // Add dQ_i into the fp32 accumulator.  Rows past the sequence
+                // end hold exact zeros (their P, hence dS, is zero), so adding
+                // them to the neighbouring rows changes nothing.
+                stage_add(v, &tdq, h * (int)a.T + U.tok0 + i * kTileM);
                 sem_pend = sem;
                 if (r == 0) dbg_count(a.dbg_inner, (long long)h * a.T + U.tok0 + i * kTileM);
             }
@@ -1010,6 +1064,28 @@ bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUten
             if (named_bar_or(1, 128, !ok)) { ok = false; break; }
             ++uc;
             tc_fence_after();
+            if (a.kv_split) {
+                // A split unit's dK and dV are partial (its head group's
+                // share): added into the fp32 sums [2][Hkv][T][d], which the
+                // last stage converts.  Key rows past the sequence end hold
+                // exact zeros, as dQ's rows do.
+#pragma unroll
+                for (int which = 0; which < 2; ++which) {
+                    uint32_t v[D];
+                    const uint32_t tacc = tmem + lb + (which ? kColDV : kColDK);
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32)
+                        tmem_ld32(tacc + c0, *reinterpret_cast<uint32_t(*)[32]>(v + c0));
+                    tmem_wait_ld();
+                    if (which == 1) {   // both accumulators read: the next unit may start
+                        if (r == 0) dbg_count(a.dbg_visits, (long long)U.hk * a.T + U.tok0 + U.k * kTileN);
+                        tc_fence_before();
+                        mbar_arrive(&sh.acc_free);
+                    }
+                    stage_add(v, &tdkv, (which * a.Hkv + U.hk) * (int)a.T + U.tok0 + U.k * kTileN);
+                }
+                continue;
+            }
             const int key = U.k * kTileN + r;
             const bool kvalid = key < U.len;
             const size_t orow = ((size_t)(U.tok0 + key) * a.Hkv + U.hk) * D;
@@ -1081,9 +1157,10 @@ cudaError_t launch_bwd_d(const BwdLaunch& L, int stages, cudaStream_t stream) {
         if (e0 != cudaSuccess) return e0;
         long long units = a.varlen ? (long long)a.Hkv * ((a.T + kTileN - 1) / kTileN + a.B)
                                    : (long long)a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN);
+        if (a.kv_split) units *= (a.Hq / a.Hkv) / a.kv_split;
         int grid = (int)(units < L.num_sms ? units : L.num_sms);
         if (grid < 1) grid = 1;
-        bwd_kernel<D><<<grid, kBwdThreads, smem, stream>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, a);
+        bwd_kernel<D><<<grid, kBwdThreads, smem, stream>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, L.tdkv, a);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

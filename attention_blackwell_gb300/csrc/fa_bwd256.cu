@@ -267,7 +267,7 @@ bwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CU
         for (int s = 0; s < 4; ++s) { mbar_init(&sh.unit_full[s], 1); mbar_init(&sh.unit_empty[s], kUnitReaders6); }
         sh.abort_flag = 0;
         int total = 2 * (a.varlen ? a.hdr->total_units : a.B * a.Hkv * ((a.N + kTileN - 1) / kTileN));
-        if (a.varlen && a.hdr->unit_keys != kTileN) {   // a list planned for other units
+        if (a.varlen && (a.hdr->unit_keys != kTileN || a.hdr->unit_heads != 0)) {   // a list planned for other units
             if (atomicCAS(&a.hdr->status.code, 0, -1) == 0) a.hdr->status.where = 202;
             total = 0;
         }

@@ -123,11 +123,12 @@ struct PBUnit {
 // semaphores need).
 
 // Units of this call, read once per CTA; a varlen list planned for 128-key
-// units (the one-CTA kernel's) is refused: no units, FA_ERR_INVALID.
+// units or split by query-head group (the one-CTA kernel's) is refused: no
+// units, FA_ERR_INVALID.
 template <bool kVar>
 __device__ __forceinline__ int pb_total(const BwdArgs& a) {
     if constexpr (!kVar) return a.B * a.Hkv * ((a.N + kKeyBlock - 1) / kKeyBlock);
-    if (a.hdr->unit_keys != kKeyBlock) {
+    if (a.hdr->unit_keys != kKeyBlock || a.hdr->unit_heads != 0) {
         if (atomicCAS(&a.hdr->status.code, 0, -1) == 0) a.hdr->status.where = 202;
         return 0;
     }

@@ -16,6 +16,10 @@ constexpr int kTileN = 128;             // keys per K/V tile
 constexpr int kUnitRows = 2 * kTileM;   // two Q tiles (ping-pong) per forward work unit
 constexpr int kMaxVarlenSeqs = 1024;    // sequences a varlen call may pack
 constexpr int kMaxUnitLevels = 512;     // ceil(max_seqlen / 256) limit (max_seqlen <= 131072)
+// Varlen backward: units of kSplitHeads query heads when a key/value head's
+// group has at least kSplitMinGroup of them (a multiple of kSplitHeads).
+constexpr int kSplitHeads = 8;
+constexpr int kSplitMinGroup = 16;
 
 // Forward arguments that are not tensor maps.
 struct FwdArgs {
@@ -70,13 +74,14 @@ struct BwdHeader {
     int next_unit;     // main kernel: units claimed past the first wave
     int done_ctas;     // main kernel: CTAs that found the list exhausted (follows next_unit)
     int unit_keys;     // varlen: keys per unit of the planned list (256 for the CTA-pair kernel, else 128)
-    int pad[56];
+    int unit_heads;    // varlen: query heads per unit of the planned list (0: the whole group)
+    int pad[55];
 };
 static_assert(sizeof(BwdHeader) == 256, "backward workspace header");
 static_assert(offsetof(BwdHeader, done_ctas) == offsetof(BwdHeader, next_unit) + sizeof(int), "claim counters");
 
 struct WsLayout {
-    size_t d_off, dq_off, sem_off, unit_off, cu_off, total;
+    size_t d_off, dq_off, sem_off, unit_off, cu_off, kv_off, total;
     long long sem_stride;  // semaphores per query head
 };
 
@@ -95,7 +100,11 @@ inline WsLayout ws_layout(long long T, int B, int Hq, int deterministic, int var
     w.sem_off = align256(w.dq_off + (size_t)Hq * T * d * 4);
     w.unit_off = align256(w.sem_off + (deterministic ? sem_sets * Hq * w.sem_stride * 4 : 0));
     w.cu_off = align256(w.unit_off + (varlen ? (size_t)Hq * (tiles + B) * 16 : 0));
-    w.total = align256(w.cu_off + (varlen ? (size_t)(B + 1) * 4 : 0));
+    // Varlen at d = 64 / 128: fp32 dK and dV partial sums [2][Hkv][T][d] for
+    // work units split by query-head group, which needs Hq >= kSplitMinGroup
+    // * Hkv, so Hq * T * d / 2 bytes always hold them.
+    w.kv_off = align256(w.cu_off + (varlen ? (size_t)(B + 1) * 4 : 0));
+    w.total = align256(w.kv_off + (varlen && d != 256 ? (size_t)Hq * T * d / 2 : 0));
     return w;
 }
 
@@ -113,6 +122,9 @@ struct BwdArgs {
     int* sem;
     int4* units;
     int* cu_s;               // varlen: sanitised offsets [B+1], written by the plan kernel
+    float* dkvacc;           // varlen: fp32 dK, dV partial sums [2][Hkv][T][d] (split units)
+    int kv_split;            // varlen: query heads per work unit when a unit covers part of
+                             // its key/value head's group (its dK, dV then partial), else 0
     long long sem_stride;
     int B, Hq, Hkv;
     int N;                   // fixed: sequence length; varlen: T
@@ -122,7 +134,8 @@ struct BwdArgs {
     int naive;               // 1: work units in plain enumeration order (fa_set_schedule_order)
     // Debug counters (nullptr unless fa_set_debug_counters armed them):
     // visits[hk * T + first row of a 128-key tile] += 1 per finished work
-    // unit (key tile of one key/value head); inner[h * T + first row of a
+    // unit (key tile of one key/value head, or of one query-head group of it
+    // for split units); inner[h * T + first row of a
     // 128-row query tile] += 1 per (key tile, query tile) product chain.
     int* dbg_visits;
     int* dbg_inner;
@@ -131,6 +144,7 @@ struct BwdArgs {
 struct BwdLaunch {
     CUtensorMap tq, tk, tv, tdo;
     CUtensorMap tdq;         // dQacc as fp32 [Hq*T, d], box {32, 128}, 128-B swizzle
+    CUtensorMap tdkv;        // dkvacc as fp32 [2*Hkv*T, d], box {32, 128} (split units)
     // CTA-pair main kernel only: Q and dO with 64-row boxes, dQacc with 64-row boxes.
     CUtensorMap tq64, tdo64, tdq64;
     BwdArgs a;

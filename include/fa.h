@@ -165,7 +165,8 @@ int fa_set_schedule_order(int order);
  *     fa_fwd adds 1 at [h * T + r] when it finishes the 128-row query tile
  *     of head h starting at token row r; fa_bwd adds 1 at [hk * T + r] when
  *     it finishes the work unit of key/value head hk whose 128-key tile
- *     starts at row r (its dK, dV written);
+ *     starts at row r (its dK, dV written; units split by query-head group
+ *     count once per group);
  *   inner (int [Hq * T], fa_bwd; may be NULL): 1 at [h * T + r] each time a
  *     128-key tile's dQ contribution to the query tile of head h starting at
  *     row r has been added (so the count is the number of key tiles that see
@@ -205,9 +206,12 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
 /*
  * Bytes of device workspace fa_bwd needs (the library allocates none):
  * D (rowsum(dO*O), fp32), the fp32 dQ accumulator, the deterministic-mode
- * semaphores and the varlen work list.  N is the sequence length (fixed
- * length) or the total token count T (varlen = 1).  Returns 0 for invalid
- * sizes (d not 64, 128 or 256 among them).  About (4 d + 4) * Hq * T bytes.
+ * semaphores, the varlen work list and, for varlen at d = 64 or 128, room
+ * for fp32 dK and dV partial sums (Hq * T * d / 2 bytes; used when the work
+ * is split by query-head group, see fa_bwd).  N is the sequence length
+ * (fixed length) or the total token count T (varlen = 1).  Returns 0 for
+ * invalid sizes (d not 64, 128 or 256 among them).  About (4 d + 4) * Hq * T
+ * bytes (varlen at d = 64 / 128: (4.5 d + 4) * Hq * T).
  */
 size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, int deterministic, int varlen);
 
@@ -226,6 +230,13 @@ size_t fa_bwd_workspace_size(int B, int Hq, int N, int d, int deterministic, int
  * 128-key tile would fill all of tensor memory, so each tile is processed
  * once per head-dim half of the gradients (recomputing S and dP for each),
  * with queries in 64-row steps (fa_set_bwd_kernel does not apply).
+ * Packed varlen batches in atomic mode whose key/value heads each serve at
+ * least 16 query heads (a multiple of 8; MQA-like) run, on the one-CTA
+ * kernel at d = 64 or 128, as work units of 8 query heads each: the CTAs of
+ * a wave then share one head group's rows of Q, dO and the dQ accumulator
+ * in L2 (FlashAttention-4 blog, "Scheduling": L2-sized sections), and each
+ * unit adds its group's share of dK and dV into fp32 sums in the workspace
+ * that the last stage converts to bf16 (dK times alpha).
  * Errors: as fa_fwd, plus FA_ERR_WORKSPACE (NULL, misaligned or too small)
  * and FA_ERR_UNSUPPORTED (varlen with max_seqlen > 131072 or B > 1024).
  */
@@ -242,9 +253,11 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
  * the dQ accumulator), 4 = dQ postprocess (dq = bf16(alpha * accumulator)).
  * Stages must run in this order on one workspace; fa_bwd == stages 7.  For
  * a packed varlen batch, stage 1 plans the work list for the backward kernel
- * selected at that time (fa_set_bwd_kernel): a stage 2 run with the other
- * selection computes nothing and reports FA_ERR_INVALID through
- * fa_get_device_status.
+ * selected at that time (fa_set_bwd_kernel) and for the call's mode (units
+ * split by query-head group or not, see fa_bwd): a stage 2 run with the
+ * other selection or the other mode computes nothing and reports
+ * FA_ERR_INVALID through fa_get_device_status.  With split units, stage 4
+ * also writes dk and dv.
  */
 int fa_bwd_stages(int stages, const void *q, const void *k, const void *v, const void *o,
                   const float *lse, const void *dout, void *dq, void *dk, void *dv,

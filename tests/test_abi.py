@@ -130,6 +130,20 @@ def test_workspace_size_depends_on_head_dim(lib):
     assert f(2, 4, 1000, 96, 0, 0) == 0 and f(2, 4, 1000, 512, 0, 0) == 0
 
 
+def test_varlen_workspace_holds_the_head_group_partial_sums(lib):
+    """Host arithmetic only: at d = 64 / 128 a varlen workspace also holds
+    fp32 dK and dV partial sums, [2][Hkv][T][d] with Hkv <= Hq / 16 when the
+    work is split by query-head group: Hq * T * d / 2 bytes."""
+    f = lib.fa_bwd_workspace_size
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int] * 6
+    for d in (64, 128):
+        fixed, packed = f(1, 32, 5000, d, 0, 0), f(4, 32, 5000, d, 0, 1)   # T = 5000 both
+        assert packed - fixed >= 32 * 5000 * d // 2 >= 2 * (32 // 16) * 5000 * d * 4
+    # d = 256 never splits: only the work list and offsets are added
+    assert f(4, 32, 5000, 256, 0, 1) - f(1, 32, 5000, 256, 0, 0) < 32 * 5000 * 256 // 2
+
+
 def test_noalloc_returns_fa_bwd_codes_on_the_host(lib):
     """fa_bwd_noalloc runs fa_bwd's argument checks first, so both entry
     points give the same code for the same bad arguments (unbuilt head dims:

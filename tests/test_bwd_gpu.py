@@ -250,6 +250,32 @@ def test_varlen_many_short_sequences(fa):
     check(got, oracle(inp, True))
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(16, 1), (32, 2), (24, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_head_group_units(fa, Hq, Hkv, causal):
+    """Packed batches whose key/value heads serve 16 or more query heads
+    (a multiple of 8): in atomic mode the one-CTA kernel's units cover 8
+    query heads each and add partial dK and dV into fp32 sums that the last
+    stage converts -- two groups per key/value head, on one and on two
+    key/value heads, and three groups -- with empty, one-token and ragged
+    sequences.  The CTA-pair kernel keeps whole groups."""
+    inp = inputs(0, 0, Hq, Hkv, seed=61, lengths=[700, 0, 1, 300, 129, 257])
+    check(gpu_grads(fa, inp, causal)[0], oracle(inp, causal))
+
+
+def test_varlen_head_group_units_match_whole_groups(fa):
+    """The same packed MQA batch (32 query heads on one key/value head,
+    9 sequences, more than a wave of split units) in atomic mode and in
+    deterministic mode, which keeps one unit per key tile: the gradients
+    agree to within the order of the fp32 additions."""
+    lengths = [4100, 2500, 2000, 1500, 700, 300, 129, 0, 1]
+    inp = inputs(0, 0, 32, 1, seed=62, lengths=lengths)
+    got = gpu_grads(fa, inp, True)[0]
+    ref = gpu_grads(fa, inp, True, deterministic=True)[0]
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert np.abs(g - r).max() <= 1e-2 * np.abs(r).max(), name
+
+
 # ------------------------------------------ races that only show sometimes
 
 @pytest.mark.parametrize("name", ["large", "causal_bwd"])

@@ -165,6 +165,15 @@ def test_bwd_many_tiles_one_head(fa):
 
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_varlen_head_group_units(fa, causal):
+    """16 query heads on one key/value head, packed: atomic-mode units of 8
+    query heads with fp32 partial dK and dV, as at d = 128."""
+    inp = inputs(0, 0, 16, 1, seed=63, lengths=[700, 0, 1, 300, 129, 257])
+    check_bwd(gpu_grads(fa, inp, causal)[0],
+              A.backward(inp["q"], inp["k"], inp["v"], inp["do"], ALPHA, causal, cu_seqlens=inp["cu_seqlens"]))
+
+
 def test_varlen_many_short_sequences_d64(fa):
     rng = np.random.default_rng(78)
     lengths = [int(x) for x in rng.integers(0, 301, size=1000)]

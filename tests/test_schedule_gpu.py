@@ -13,7 +13,9 @@ was finished:
   sees it (all key tiles of its sequence, or under the causal mask the tiles
   at or before it) -- on the headline workload, whose 2048 units are claimed
   from the workspace counter over more than ten waves of CTAs, on the causal
-  one in both modes, and on the packed MQA one;
+  one in both modes, and on the packed MQA one (whose atomic units on the
+  one-CTA kernel cover 8 of the 32 query heads each: one visit per head
+  group);
 * the conditional rescale's branch counter (paper summary §3.1.4): on the
   causal workload (Q ~ N(0, 9)) tau = 8 takes the rescale branch on some
   but not all warp decisions, tau = 0 on at least as many, tau = 64 on none.
@@ -65,6 +67,16 @@ def _expected_visits(inp, H):
     for r, _, _ in _tile_starts(inp):
         e[:, r] = 1
     return e
+
+
+def _split_groups(w, kernel, deterministic):
+    """Head groups per key tile of a packed batch's backward: in atomic mode
+    the one-CTA kernel (d = 64 or 128) splits a key/value head's query heads
+    into units of 8 when there are at least 16 of them, a multiple of 8
+    (include/fa.h, fa_bwd_workspace_size); each unit counts one visit."""
+    G = w.Hq // w.Hkv
+    split = w.varlen and not deterministic and kernel == 0 and w.d != 256 and G >= 16 and G % 8 == 0
+    return G // 8 if split else 1
 
 
 def _expected_inner(inp, H, causal):
@@ -132,7 +144,8 @@ def test_backward_units_and_tiles_exactly_once(fa, name, kernel, deterministic):
         fa.set_bwd_kernel(0)
     gv = visits.view(w.Hkv, T).cpu().numpy()
     gi = inner.view(w.Hq, T).cpu().numpy()
-    assert np.array_equal(gv, _expected_visits(inp, w.Hkv)), (gv.max(), gv.sum())
+    want_v = _expected_visits(inp, w.Hkv) * _split_groups(w, kernel, deterministic)
+    assert np.array_equal(gv, want_v), (gv.max(), gv.sum())
     assert np.array_equal(gi, _expected_inner(inp, w.Hq, w.causal)), (gi.max(), gi.sum())
 
 

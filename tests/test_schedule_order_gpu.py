@@ -190,3 +190,23 @@ def test_varlen_plan_for_the_other_backward_kernel_is_refused(fa):
             assert fa.device_status(ws) == 0
     finally:
         fa.set_bwd_kernel(0)
+
+
+def test_varlen_plan_for_the_other_mode_is_refused(fa):
+    """With 16 query heads per key/value head, stage 1 in atomic mode plans
+    units of 8 query heads (their dK and dV partial sums in fp32) and in
+    deterministic mode one unit per key tile.  A stage 2 in the other mode
+    must compute nothing and report FA_ERR_INVALID; a consistent pair of
+    stages then works again."""
+    g = make(0, 0, 16, 1, 128, lengths=[300, 129, 513], seed=42)
+    o, lse = fwd(fa, g, True, 0)
+    ws = fa.bwd_workspace(g["B"], 16, g["N"], True, True)   # sized for both modes
+    dq, dk, dv = (torch.zeros_like(t) for t in (g["q"], g["k"], g["v"]))
+    kw = dict(causal=True, cu_seqlens=g["cu"], max_seqlen=g["ms"], workspace=ws, dq=dq, dk=dk, dv=dv)
+    for first, second in ((False, True), (True, False)):
+        fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], stages=1, deterministic=first, **kw)
+        fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], stages=2, deterministic=second, **kw)
+        assert fa.device_status(ws) == -1   # FA_ERR_INVALID
+        fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], stages=1, deterministic=second, **kw)
+        fa.bwd(g["q"], g["k"], g["v"], o, lse, g["do"], stages=2, deterministic=second, **kw)
+        assert fa.device_status(ws) == 0

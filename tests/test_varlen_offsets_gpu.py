@@ -102,20 +102,24 @@ def test_forward_malformed_offsets(fa, case, kernel, d, causal):
 
 
 @pytest.mark.parametrize("case", range(len(CASES)))
-@pytest.mark.parametrize("kernel,d", [(0, 128), (1, 128), (0, 64)], ids=["one_cta", "pair", "d64"])
+@pytest.mark.parametrize("kernel,d,heads", [(0, 128, (4, 2)), (1, 128, (4, 2)), (0, 64, (4, 2)), (0, 128, (16, 1))],
+                         ids=["one_cta", "pair", "d64", "one_cta_head_groups"])
 @pytest.mark.parametrize("causal,deterministic", [(False, False), (True, False), (True, True)])
-def test_backward_malformed_offsets(fa, case, kernel, d, causal, deterministic):
+def test_backward_malformed_offsets(fa, case, kernel, d, heads, causal, deterministic):
+    """16 query heads on one key/value head: in atomic mode units of 8
+    query heads whose fp32 partial dK and dV the last stage converts, for
+    the sequences' rows only."""
     fa.set_bwd_kernel(kernel)
     try:
-        _backward_malformed_offsets(fa, case, d, causal, deterministic)
+        _backward_malformed_offsets(fa, case, d, causal, deterministic, heads)
     finally:
         fa.set_bwd_kernel(0)
 
 
-def _backward_malformed_offsets(fa, case, d, causal, deterministic):
+def _backward_malformed_offsets(fa, case, d, causal, deterministic, heads=(4, 2)):
     raw, T = CASES[case]
     cs = sanitise(raw, T)
-    Hq, Hkv = 4, 2
+    Hq, Hkv = heads
     q, k, v = (W.normal_bf16((T, h, d), 80 + i) for i, h in enumerate((Hq, Hkv, Hkv)))
     do = W.normal_bf16((T, Hq, d), 83)
     qg, kg, vg, dog = q.cuda(), k.cuda(), v.cuda(), do.cuda()
